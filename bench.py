@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Throughput of the Sparse Delta Memory write/read op on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload layer] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input, as a
+layer call runs it: the per-stream copy of the learned bank, product-key scoring and
+exact top-k of both queries, the chunk plan and the fused gather / gated delta-rule
+update / read (sdm_write_read with bank_init).  The default workload is the README
+layer call (B=2, T=4096, 2 heads of 1024, 65536 slots from two factors of 256, W=R=64,
+chunk 64, bf16 activations, fp32 bank).  Prints one JSON line (rank 0).
+
+Multi-GPU (torchrun): every rank runs its own streams (weak scaling, no collective on
+the data path); the timed region is bracketed by barriers and the slowest rank's time
+is reported.  --impl reference times the CPU oracle on the host instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import sdm_inputs  # noqa: E402
+
+METRIC = "SDM write/read tokens/s per layer on 1 GB300; achieved HBM GB/s vs roofline"
+UNIT = "tokens/s"
+WORKLOADS = {"layer": "layer", "train_fwd": "train_fwd", "three_factor": "three_factor",
+             "decode": "decode", "tiny": "tiny"}
+KERNEL_SOURCES = ("sdm_write_read.cu", "sdm_delta.cuh", "sdm_common.cuh", "sdm_internal.h")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_desc(cfg) -> str:
+    dims = "x".join(str(n) for n in cfg.factor_dims)
+    return (f"{cfg.name}: B={cfg.B} T={cfg.T} H={cfg.H} d_v={cfg.d_v} factors={dims} "
+            f"(N={cfg.N}/head) d_sub={cfg.d_sub} W={cfg.W} R={cfg.R} chunk={cfg.chunk_size} "
+            f"acts={cfg.act_dtype} bank={cfg.bank_dtype}")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gated_delta_rule_factor_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per write/read launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"write_read_{workload}_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+_ORACLE_TIMER = r"""
+import json, sys, time
+sys.path.insert(0, %(root)r)
+import numpy as np
+import sdm_inputs, oracle
+cfg = sdm_inputs.CONFIGS[%(workload)r]
+budget = %(budget)f
+T_max = min(cfg.T, %(t_max)d)
+d = sdm_inputs.make_inputs(cfg, T=T_max)
+f64 = lambda t: t.float().double().numpy()
+q_w, q_r, k_val, gates, subkeys = (f64(d[k]) for k in ("q_w", "q_r", "k_val", "gates", "subkeys"))
+banks = [f64(d["bank_init"][h]).copy() for h in range(cfg.H)]    # batch element 0, every head
+kw = dict(factor_dims=cfg.factor_dims, d_sub=cfg.d_sub, W=cfg.W, R=cfg.R,
+          act_dtype=cfg.act_dtype, bank_dtype=cfg.bank_dtype)
+done, spent, per, chunks = 0, 0.0, %(per)d, []
+while done + per <= T_max and (spent < budget or done == 0):
+    t0 = time.perf_counter()
+    for h in range(cfg.H):
+        sl = slice(done, done + per)
+        oracle.run_stream(banks[h], q_w[0, sl, h], q_r[0, sl, h], k_val[0, sl, h], gates[0, sl, h],
+                          subkeys[h], **kw)
+    chunks.append(time.perf_counter() - t0)
+    spent += chunks[-1]
+    done += per
+print(json.dumps({"tokens": done, "seconds": spent, "heads": cfg.H, "chunk_seconds": chunks}))
+"""
+
+
+def _time_oracle(workload: str, budget_s: float, t_max: int, per: int) -> dict:
+    code = _ORACLE_TIMER % {"root": ROOT, "workload": workload, "budget": budget_s, "t_max": t_max,
+                            "per": per}
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(workload: str, budget_s: float = 15.0) -> dict:
+    """Time the CPU oracle (one thread, fresh process) on a bounded sample of the workload."""
+    try:
+        res = _time_oracle(workload, budget_s, t_max=4096, per=8)
+    except Exception as e:  # reported, not fatal
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"[:300]}
+    return {"value": res["tokens"] / res["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"the first {res['tokens']} tokens of batch element 0 through every head "
+                       f"({res['heads']}), state carried token to token from the learned table; "
+                       f"{res['seconds']:.1f} s of CPU work, single-threaded numpy (BLAS threads = 1)")}
+
+
+def reference_arm(args, cfg, rank, world):
+    """--impl reference: the CPU oracle on the host cores, same metric, unit and config.
+
+    Each step runs a bounded sample (a few tokens of batch element 0 through every head,
+    the state carried from step to step); the whole run stays within a few minutes."""
+    if rank != 0:
+        return 0
+    per = 2 if cfg.N >= 65536 else 8
+    n_steps = min(args.warmup + args.steps, cfg.T // per)
+    res = _time_oracle(WORKLOADS[args.workload], budget_s=1e30, t_max=n_steps * per, per=per)
+    timed = res["chunk_seconds"][args.warmup:]
+    tokens = per * len(timed)
+    dt = max(sum(timed), 1e-9)
+    value = tokens / dt
+    steps = tokens // per
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_desc(cfg)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{per} tokens of batch element 0 through all {cfg.H} heads per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="layer", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = dist_env()
+    cfg = sdm_inputs.CONFIGS[WORKLOADS[args.workload]]
+
+    if args.impl == "reference":
+        return reference_arm(args, cfg, rank, world)
+
+    import gated_delta_rule_factor_gb300 as sdm
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    if cfg.T == 1:
+        return bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg)
+
+    d = sdm_inputs.make_inputs(cfg, seed=cfg.seed + 7919 * rank)
+    g = {k: v.to(dev) for k, v in d.items()}
+    B, T, H = cfg.B, cfg.T, cfg.H
+    bank = torch.empty((B, H, cfg.N, cfg.d_v), dtype=g["bank_init"].dtype, device=dev)
+    y = torch.empty_like(g["k_val"])
+    shape = sdm.make_shape(B=B, T=T, H=H, factor_dims=cfg.factor_dims, d_sub=cfg.d_sub, d_v=cfg.d_v,
+                           W=cfg.W, R=cfg.R, chunk_size=cfg.chunk_size,
+                           act_dtype=0 if cfg.act_dtype == "f32" else 1,
+                           bank_dtype=0 if cfg.bank_dtype == "f32" else 1)
+    ws = torch.empty(sdm.write_read_workspace_size(shape), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        sdm.sdm_write_read(g["q_w"], g["q_r"], g["k_val"], g["gates"], g["subkeys"], bank, cfg.chunk_size,
+                           cfg.W, cfg.R, factor_dims=cfg.factor_dims, bank_init=g["bank_init"], y=y,
+                           workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    assert sdm.last_device_error(ws) == 0
+
+    # ---- device-resident timed region
+    launches0 = sdm.launch_count()
+    sdm.profile_begin()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+    kt = sdm.profile_end()
+    launches = sdm.launch_count() - launches0
+    ms = ev0.elapsed_time(ev1)
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_rank = B * T * args.steps
+    value = tokens_per_rank * world / (ms / 1e3)
+
+    # ---- roofline of the dominant kernel (fused gather / update / read)
+    sb = 4 if cfg.bank_dtype == "f32" else 2
+    wr_launches, wr_ms = kt["write_read"]
+    wr_avg_s = wr_ms / max(wr_launches, 1) / 1e3
+    alg_bytes = B * T * H * (cfg.W + cfg.R) * cfg.d_v * sb
+    peak, peak_kind = peaks()
+    achieved = alg_bytes / wr_avg_s / 1e9
+    traffic = recorded_traffic(args.workload)
+    copy_bytes = 2 * B * H * cfg.N * cfg.d_v * sb
+    step_alg = alg_bytes + copy_bytes
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: d[k].pin_memory() for k in ("q_w", "q_r", "k_val", "gates")}
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = y_host.numel() * y_host.element_size()
+        bufs = {k: torch.empty_like(g[k]) for k in host}
+
+        def e2e_step():
+            for k, v in host.items():
+                bufs[k].copy_(v, non_blocking=True)
+            sdm.sdm_write_read(bufs["q_w"], bufs["q_r"], bufs["k_val"], bufs["gates"], g["subkeys"], bank,
+                               cfg.chunk_size, cfg.W, cfg.R, factor_dims=cfg.factor_dims,
+                               bank_init=g["bank_init"], y=y, workspace=ws, stream=stream)
+            y_host.copy_(y, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        e_steps = max(10, args.steps // 3)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if pg is not None:
+            t = torch.tensor([ems], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": B * T * e_steps * world / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "parallelism": f"streams sharded, {world} independent ranks",
+                   "l2": "inputs larger than L2: the 1 GiB bank is rewritten from the learned table every step",
+                   "step": "bank copy + scoring/top-k + chunk plan + fused write/read"},
+        "roofline": {"bound": "hbm", "kernel": "write_read", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "launch_ms": wr_avg_s * 1e3},
+        "step_roofline": {"algorithmic_bytes": step_alg, "achieved_gbs": step_alg / (ms / args.steps / 1e3) / 1e9,
+                          "frac": step_alg / (ms / args.steps / 1e3) / 1e9 / peak},
+        "kernels_ms_per_step": {k: v[1] / max(v[0], 1) * (v[0] / args.steps) for k, v in kt.items() if v[0]},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg):
+    """Decode workload: B streams, one token per step, donated (in place) state."""
+    steps_total = args.warmup + args.steps
+    d = sdm_inputs.make_decode_inputs(cfg, steps=min(steps_total, 64), seed=cfg.seed + 7919 * rank)
+    g = {k: v.to(dev) for k, v in d.items()}
+    state = g["bank"].clone()
+    donate = os.environ.get("SDM_DECODE_COPY", "0") != "1"
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(g["k_val"][:, 0])
+    nT = g["q_w"].shape[1]
+
+    def step(i):
+        nonlocal state
+        t = i % nT
+        _, state = sdm.sdm_decode_step(g["q_w"][:, t], g["q_r"][:, t], g["k_val"][:, t], g["gates"][:, t],
+                                       g["subkeys"], state, cfg.W, cfg.R, factor_dims=cfg.factor_dims,
+                                       donate=donate, y=y, workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    launches0 = sdm.launch_count()
+    sdm.profile_begin()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        ev1.record(stream)
+        barrier()
+    kt = sdm.profile_end()
+    ms = ev0.elapsed_time(ev1)
+    value = cfg.B * args.steps * world / (ms / 1e3)
+    sb = 4 if cfg.bank_dtype == "f32" else 2
+    alg = cfg.B * cfg.H * (cfg.W + cfg.R) * cfg.d_v * sb + (0 if donate else 2 * cfg.B * cfg.H * cfg.N * cfg.d_v * sb)
+    n, kms = kt["decode"]
+    achieved = alg / (kms / max(n, 1) / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "donate": donate},
+            "roofline": {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind},
+            "gpu_launches": sdm.launch_count() - launches0, "clocks": clk.summary()}), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,22 @@
+"""GB300-native Sparse Delta Memory (SDM) hot path.
+
+The chunked write/read op and the single-token decode step run as hand-written
+sm_103a CUDA kernels in libsdm_gb300.so behind the C ABI of include/sdm.h.  This
+package is the thin Python binding: ``sdm_write_read`` and ``sdm_decode_step`` take
+torch CUDA tensors and pass their pointers through.  Importing it loads the library
+and fails loudly if it has not been built (``python -m gated_delta_rule_factor_gb300.build``).
+"""
+
+from . import _abi
+from ._abi import SdmError, SdmShape
+from .ops import (decode_workspace_size, last_device_error, launch_count, make_shape,
+                  profile_begin, profile_end, sdm_decode_step, sdm_write_read,
+                  write_read_workspace_size)
+
+lib = _abi.load()
+
+__all__ = [
+    "SdmError", "SdmShape", "decode_workspace_size", "last_device_error", "launch_count",
+    "make_shape", "profile_begin", "profile_end", "sdm_decode_step", "sdm_write_read",
+    "write_read_workspace_size", "lib",
+]

@@ -1,0 +1,110 @@
+"""ctypes declarations of the C ABI in include/sdm.h (argument marshalling only)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+MAX_FACTORS = 4
+MAX_K = 128
+MAX_CANDIDATES = 1024
+MAX_CHUNK = 256
+ABI_VERSION = 1
+
+SDM_OK, SDM_ERR_INVALID_ARG, SDM_ERR_UNSUPPORTED, SDM_ERR_ALIAS, SDM_ERR_WORKSPACE, \
+    SDM_ERR_CUDA, SDM_ERR_DEVICE = range(7)
+SDM_F32, SDM_BF16, SDM_F16 = 0, 1, 2
+KERNEL_KINDS = ("bank_copy", "topk", "plan_sort", "plan_link", "write_read", "decode")
+
+# Every function include/sdm.h declares, in header order.
+EXPORTS = (
+    "sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
+    "sdm_decode_step", "sdm_last_device_error", "sdm_status_string", "sdm_last_error_message",
+    "sdm_abi_version", "sdm_launch_count", "sdm_profile_begin", "sdm_profile_end",
+    "sdm_kernel_name",
+)
+
+
+class SdmShape(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
+        ("d_sub", ctypes.c_int64), ("d_v", ctypes.c_int64),
+        ("F", ctypes.c_int32), ("factor_dims", ctypes.c_int32 * MAX_FACTORS),
+        ("W", ctypes.c_int32), ("R", ctypes.c_int32), ("chunk_size", ctypes.c_int32),
+        ("act_dtype", ctypes.c_int32), ("bank_dtype", ctypes.c_int32),
+    ]
+
+
+class KernelTimes(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int64 * len(KERNEL_KINDS)),
+                ("ms", ctypes.c_double * len(KERNEL_KINDS))]
+
+
+class SdmError(RuntimeError):
+    """A non-OK status from the library; .status holds the code."""
+
+    def __init__(self, status: int, func: str, message: str):
+        self.status = status
+        super().__init__(f"{func}: {STATUS_NAMES.get(status, status)}: {message}")
+
+
+STATUS_NAMES = {
+    SDM_OK: "ok", SDM_ERR_INVALID_ARG: "invalid argument", SDM_ERR_UNSUPPORTED: "unsupported",
+    SDM_ERR_ALIAS: "alias", SDM_ERR_WORKSPACE: "workspace", SDM_ERR_CUDA: "cuda",
+    SDM_ERR_DEVICE: "device",
+}
+
+_P = ctypes.c_void_p
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libsdm_gb300.so.  Raises ImportError when it is not built (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise ImportError(f"SDM CUDA library not built ({path}); run "
+                              "`python -m gated_delta_rule_factor_gb300.build`")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    sp = ctypes.POINTER(SdmShape)
+    szp = ctypes.POINTER(ctypes.c_size_t)
+    lib.sdm_write_read_workspace_size.argtypes = [sp, szp]
+    lib.sdm_decode_workspace_size.argtypes = [sp, szp]
+    lib.sdm_write_read.argtypes = [sp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   ctypes.c_size_t, _P]
+    lib.sdm_decode_step.argtypes = [sp, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _P,
+                                    _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    lib.sdm_last_device_error.argtypes = [_P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int32), _P]
+    lib.sdm_status_string.argtypes = [ctypes.c_int]
+    lib.sdm_status_string.restype = ctypes.c_char_p
+    lib.sdm_last_error_message.argtypes = []
+    lib.sdm_last_error_message.restype = ctypes.c_char_p
+    lib.sdm_abi_version.restype = ctypes.c_int32
+    lib.sdm_launch_count.restype = ctypes.c_uint64
+    lib.sdm_profile_begin.argtypes = []
+    lib.sdm_profile_end.argtypes = [ctypes.POINTER(KernelTimes)]
+    lib.sdm_kernel_name.argtypes = [ctypes.c_int32]
+    lib.sdm_kernel_name.restype = ctypes.c_char_p
+    for name in ("sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
+                 "sdm_decode_step", "sdm_last_device_error", "sdm_profile_begin", "sdm_profile_end"):
+        getattr(lib, name).restype = ctypes.c_int
+    if lib.sdm_abi_version() != ABI_VERSION:
+        raise ImportError(f"SDM library ABI {lib.sdm_abi_version()} != binding ABI {ABI_VERSION}")
+    _lib = lib
+    return lib
+
+
+def check(status: int, func: str) -> None:
+    if status != SDM_OK:
+        msg = load().sdm_last_error_message().decode(errors="replace")
+        raise SdmError(status, func, msg)

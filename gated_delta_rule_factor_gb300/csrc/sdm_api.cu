@@ -1,0 +1,724 @@
+// Host side of the SDM C ABI: argument checks, configuration, workspace layout,
+// launches, kernel-side error read-back and per-kernel timing.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/sdm.h"
+#include "sdm_internal.h"
+
+namespace sdm {
+int64_t topk_scratch_bytes();
+}
+
+using namespace sdm;
+
+namespace {
+
+// ---------------------------------------------------------------- error reporting
+
+thread_local char g_msg[512] = "";
+
+sdm_status fail(sdm_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+sdm_status ok() {
+  g_msg[0] = '\0';
+  return SDM_OK;
+}
+
+std::atomic<uint64_t> g_launches{0};
+
+// ---------------------------------------------------------------- profiling
+
+constexpr int kProfSlots = 4096;
+struct ProfState {
+  std::mutex mu;
+  bool active = false;
+  bool created = false;
+  std::vector<cudaEvent_t> start, stop;
+  std::vector<int> kind;
+  int used = 0;
+} g_prof;
+
+bool prof_acquire(int kind, cudaEvent_t *start, cudaEvent_t *stop) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.active || g_prof.used >= kProfSlots) return false;
+  const int i = g_prof.used++;
+  g_prof.kind[i] = kind;
+  *start = g_prof.start[i];
+  *stop = g_prof.stop[i];
+  return true;
+}
+
+template <class Launch>
+sdm_status run_kernel(int kind, cudaStream_t st, const char *name, Launch &&launch) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  const bool prof = prof_acquire(kind, &e0, &e1);
+  if (prof) cudaEventRecord(e0, st);
+  const cudaError_t e = launch();
+  if (prof) cudaEventRecord(e1, st);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return fail(SDM_ERR_CUDA, "%s launch failed: %s", name, cudaGetErrorString(e));
+  return SDM_OK;
+}
+
+// ---------------------------------------------------------------- shape checks
+
+int64_t elem_bytes(int32_t dt) { return dt == SDM_BF16 ? 2 : 4; }
+
+sdm_status check_dtype(int32_t dt, const char *what) {
+  if (dt == SDM_F16) return fail(SDM_ERR_UNSUPPORTED, "%s: float16 is not supported", what);
+  if (dt != SDM_F32 && dt != SDM_BF16) return fail(SDM_ERR_INVALID_ARG, "%s: unknown dtype %d", what, dt);
+  return SDM_OK;
+}
+
+// Position tuples (p_1..p_F), p_f < kf_f, prod(p_f + 1) <= k, lexicographic.
+void enumerate_candidates(int F, const int32_t *kf, int k, std::vector<uint32_t> &out) {
+  out.clear();
+  int p[SDM_MAX_FACTORS] = {0, 0, 0, 0};
+  // iterative odometer with pruning on the product
+  std::vector<uint32_t> tmp;
+  struct Rec {
+    static void go(int f, int F, const int32_t *kf, int k, int64_t prod, int *p, std::vector<uint32_t> &o) {
+      if (f == F) {
+        uint32_t t = 0;
+        for (int i = 0; i < F; ++i) t |= (uint32_t)p[i] << (8 * i);
+        o.push_back(t);
+        return;
+      }
+      for (int x = 0; x < kf[f]; ++x) {
+        if (prod * (x + 1) > k) break;
+        p[f] = x;
+        go(f + 1, F, kf, k, prod * (x + 1), p, o);
+        if (o.size() > (size_t)SDM_MAX_CANDIDATES) return;
+      }
+      p[f] = 0;
+    }
+  };
+  Rec::go(0, F, kf, k, 1, p, out);
+}
+
+struct Derived {
+  int64_t N = 0;
+  int32_t ntot = 0;
+  KeyGeometry g{};
+  CandidateList *cl = nullptr;  // filled on demand
+};
+
+sdm_status check_shape(const sdm_shape *sh, bool decode, Derived *d) {
+  if (!sh) return fail(SDM_ERR_INVALID_ARG, "shape is NULL");
+  if (sh->B < 0 || sh->T < 0 || sh->H < 0) return fail(SDM_ERR_INVALID_ARG, "B, T, H must be >= 0");
+  if (decode && sh->T != 1) return fail(SDM_ERR_INVALID_ARG, "decode step needs T == 1 (got %lld)", (long long)sh->T);
+  if (!decode && sh->B * sh->H > 65535)
+    return fail(SDM_ERR_UNSUPPORTED, "B*H = %lld streams exceeds 65535", (long long)(sh->B * sh->H));
+  sdm_status st;
+  if ((st = check_dtype(sh->act_dtype, "act_dtype")) != SDM_OK) return st;
+  if ((st = check_dtype(sh->bank_dtype, "bank_dtype")) != SDM_OK) return st;
+  if (sh->F < 1) return fail(SDM_ERR_INVALID_ARG, "F must be >= 1");
+  if (sh->F > SDM_MAX_FACTORS) return fail(SDM_ERR_UNSUPPORTED, "F = %d > %d factors", sh->F, SDM_MAX_FACTORS);
+  int64_t N = 1;
+  int32_t ntot = 0;
+  for (int f = 0; f < sh->F; ++f) {
+    const int32_t n = sh->factor_dims[f];
+    if (n < 1) return fail(SDM_ERR_INVALID_ARG, "factor_dims[%d] = %d < 1", f, n);
+    if (n > SDM_MAX_FACTOR_DIM) return fail(SDM_ERR_UNSUPPORTED, "factor_dims[%d] = %d > %d", f, n, SDM_MAX_FACTOR_DIM);
+    N *= n;
+    ntot += n;
+  }
+  if (N > 0x7fffffffLL) return fail(SDM_ERR_UNSUPPORTED, "N = %lld slots exceeds 2^31 - 1", (long long)N);
+  if (sh->d_sub < 1) return fail(SDM_ERR_INVALID_ARG, "d_sub must be >= 1");
+  if (sh->d_sub > SDM_MAX_SUBKEY_DIM) return fail(SDM_ERR_UNSUPPORTED, "d_sub = %lld > %d", (long long)sh->d_sub, SDM_MAX_SUBKEY_DIM);
+  if (sh->d_v < 1) return fail(SDM_ERR_INVALID_ARG, "d_v must be >= 1");
+  if (sh->d_v > SDM_MAX_HEAD_DIM) return fail(SDM_ERR_UNSUPPORTED, "head dim d_v = %lld > 2^20", (long long)sh->d_v);
+  if (sh->d_v % 8 != 0) return fail(SDM_ERR_UNSUPPORTED, "d_v = %lld is not a multiple of 8 (16-byte rows)", (long long)sh->d_v);
+  if (sh->W < 1 || sh->R < 1) return fail(SDM_ERR_INVALID_ARG, "W and R must be >= 1");
+  if (sh->W > N || sh->R > N)
+    return fail(SDM_ERR_INVALID_ARG, "more writes or reads per token (W=%d, R=%d) than slots (N=%lld)", sh->W, sh->R, (long long)N);
+  if (sh->W > SDM_MAX_K || sh->R > SDM_MAX_K)
+    return fail(SDM_ERR_UNSUPPORTED, "W=%d or R=%d above the compiled limit %d", sh->W, sh->R, SDM_MAX_K);
+  if (!decode && (sh->chunk_size < 1 || sh->chunk_size > SDM_MAX_CHUNK))
+    return fail(SDM_ERR_INVALID_ARG, "chunk_size = %d outside [1, %d]", sh->chunk_size, SDM_MAX_CHUNK);
+  if (d) {
+    d->N = N;
+    d->ntot = ntot;
+    KeyGeometry &g = d->g;
+    g.F = sh->F;
+    g.d_sub = (int32_t)sh->d_sub;
+    g.ntot = ntot;
+    int off = 0;
+    for (int f = 0; f < SDM_MAX_FACTORS; ++f) {
+      g.nf[f] = f < sh->F ? sh->factor_dims[f] : 1;
+      g.off[f] = off;
+      if (f < sh->F) off += sh->factor_dims[f];
+    }
+    g.k[0] = sh->W;
+    g.k[1] = sh->R;
+    for (int q = 0; q < 2; ++q)
+      for (int f = 0; f < SDM_MAX_FACTORS; ++f) g.kf[q][f] = f < sh->F ? std::min(g.k[q], g.nf[f]) : 1;
+  }
+  return SDM_OK;
+}
+
+sdm_status build_candidates(const Derived &d, CandidateList *cl) {
+  std::vector<uint32_t> v;
+  for (int q = 0; q < 2; ++q) {
+    enumerate_candidates(d.g.F, d.g.kf[q], d.g.k[q], v);
+    if (v.size() > (size_t)SDM_MAX_CANDIDATES)
+      return fail(SDM_ERR_UNSUPPORTED, "k = %d has more than %d product-key candidates", d.g.k[q], SDM_MAX_CANDIDATES);
+    cl->n[q] = (int32_t)v.size();
+    std::copy(v.begin(), v.end(), cl->tup[q]);
+  }
+  return SDM_OK;
+}
+
+int pow2_at_least(int64_t x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// Sort width of a factor (EF) and of the candidate list (EC), in keys per lane.
+void sort_widths(const Derived &d, const CandidateList &cl, int *EF, int *EC) {
+  int maxnf = 0;
+  for (int f = 0; f < d.g.F; ++f) maxnf = std::max(maxnf, d.g.nf[f]);
+  *EF = maxnf <= 64 ? 2 : 8;
+  const int nc = std::max(cl.n[0], cl.n[1]);
+  *EC = std::max(4, pow2_at_least(nc) / 32);
+}
+
+// ---------------------------------------------------------------- plan / kernel config
+
+constexpr int kMaxStageRefs = 4096;
+
+int64_t a16(int64_t x) { return (x + 15) & ~int64_t(15); }
+
+PlanLayout plan_layout(int G, int W, int R, int64_t T) {
+  PlanLayout p{};
+  p.G = G;
+  p.L = G * (W + R);
+  p.n_stages = (int32_t)((T + G - 1) / G);
+  const int64_t L = p.L;
+  int64_t o = 16;
+  p.off_load_slot = o; o = a16(o + 4 * L);
+  p.off_load_u = o;    o = a16(o + 2 * L);
+  p.off_carry = o;     o = a16(o + 4 * L);
+  p.off_wb_slot = o;   o = a16(o + 4 * L);
+  p.off_wb_u = o;      o = a16(o + 2 * L);
+  p.off_refmap = o;    o = a16(o + 2 * L);
+  p.rec_bytes = o;
+  return p;
+}
+
+struct WrChoice {
+  int CW = 0;
+  PlanLayout lay{};
+  int64_t smem = 0;
+};
+
+// Column slices the write/read kernel is compiled for: 16..128 bytes of a row.
+void cw_candidates(const sdm_shape *sh, std::vector<int> &out) {
+  out.clear();
+  const int sb = (int)elem_bytes(sh->bank_dtype), ab = (int)elem_bytes(sh->act_dtype);
+  for (int bytes = 128; bytes >= 16; bytes >>= 1) {
+    const int cw = bytes / sb;
+    if (cw * ab < 16) continue;            // value slice must be a whole 16-byte chunk
+    if (sh->d_v % cw != 0) continue;
+    out.push_back(cw);
+  }
+}
+
+// Largest stage length (tokens) whose buffers fit `budget` bytes of shared memory.
+WrChoice stage_for(const sdm_shape *sh, int cw, int64_t budget) {
+  WrChoice c;
+  c.CW = cw;
+  const int WR = sh->W + sh->R;
+  int gmax = std::min<int64_t>(sh->chunk_size, std::max<int64_t>(sh->T, 1));
+  gmax = std::min(gmax, kMaxStageRefs / WR);
+  gmax = std::max(gmax, 1);
+  int G = gmax;
+  for (; G > 1; --G) {
+    const PlanLayout lay = plan_layout(G, sh->W, sh->R, sh->T);
+    if (write_read_smem_bytes(cw, (int)elem_bytes(sh->bank_dtype), (int)elem_bytes(sh->act_dtype), G,
+                              sh->W, sh->R, lay.rec_bytes) <= budget)
+      break;
+  }
+  c.lay = plan_layout(G, sh->W, sh->R, sh->T);
+  c.smem = write_read_smem_bytes(cw, (int)elem_bytes(sh->bank_dtype), (int)elem_bytes(sh->act_dtype), G,
+                                 sh->W, sh->R, c.lay.rec_bytes);
+  return c;
+}
+
+constexpr int64_t kSmemOneCta = 220 * 1024;
+constexpr int64_t kSmemTwoCta = 110 * 1024;
+
+int env_int(const char *name, int dflt) {
+  const char *v = getenv(name);
+  return (v && *v) ? atoi(v) : dflt;
+}
+
+WrChoice choose_write_read(const sdm_shape *sh, int sm_count) {
+  std::vector<int> cands;
+  cw_candidates(sh, cands);
+  const int64_t streams = sh->B * sh->H;
+  int cw = cands.empty() ? 0 : cands.back();
+  const int forced = env_int("SDM_WR_CW", 0);
+  bool picked = false;
+  for (int c : cands) {
+    if (forced > 0 && c == forced) { cw = c; picked = true; break; }
+  }
+  if (!picked) {
+    for (int c : cands) {
+      if (streams * (sh->d_v / c) * 10 >= (int64_t)sm_count * 8) { cw = c; break; }
+    }
+  }
+  const int64_t ctas = streams * (sh->d_v / std::max(cw, 1));
+  const int64_t budget = ctas > sm_count ? kSmemTwoCta : kSmemOneCta;
+  WrChoice c = stage_for(sh, cw, budget);
+  const int forced_g = env_int("SDM_WR_G", 0);
+  if (forced_g > 0 && forced_g < c.lay.G) {
+    c.lay = plan_layout(forced_g, sh->W, sh->R, sh->T);
+    c.smem = write_read_smem_bytes(cw, (int)elem_bytes(sh->bank_dtype), (int)elem_bytes(sh->act_dtype),
+                                   forced_g, sh->W, sh->R, c.lay.rec_bytes);
+  }
+  return c;
+}
+
+// ---------------------------------------------------------------- workspace layout
+
+constexpr int64_t kHeaderBytes = 256;
+
+int64_t a256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+struct WsLayout {
+  int64_t idx_w, wt_w, idx_r, wt_r;  // selection outputs kept here when the caller passes NULL
+  int64_t uniq, nuniq, written, records;
+  int64_t total;
+};
+
+WsLayout ws_layout(const sdm_shape *sh, const PlanLayout &lay) {
+  WsLayout w{};
+  const int64_t rows = sh->B * sh->T * sh->H;
+  const int64_t stages = sh->B * sh->H * (int64_t)lay.n_stages;
+  int64_t o = kHeaderBytes;
+  w.idx_w = o; o = a256(o + rows * sh->W * 4);
+  w.wt_w = o;  o = a256(o + rows * sh->W * 4);
+  w.idx_r = o; o = a256(o + rows * sh->R * 4);
+  w.wt_r = o;  o = a256(o + rows * sh->R * 4);
+  w.uniq = o;  o = a256(o + stages * lay.L * 4);
+  w.nuniq = o; o = a256(o + stages * 4);
+  w.written = o; o = a256(o + stages * lay.L);
+  w.records = o; o = a256(o + stages * lay.rec_bytes);
+  w.total = o;
+  return w;
+}
+
+// The size depends only on the shape: the maximum over every slice and stage length the
+// launch may pick on any device.
+int64_t write_read_ws_bytes(const sdm_shape *sh) {
+  std::vector<int> cands;
+  cw_candidates(sh, cands);
+  int64_t best = kHeaderBytes;
+  for (int cw : cands)
+    for (int64_t budget : {kSmemOneCta, kSmemTwoCta}) {
+      const WrChoice c = stage_for(sh, cw, budget);
+      best = std::max(best, ws_layout(sh, c.lay).total);
+      for (int g = 1; g <= c.lay.G; ++g)   // stage lengths forced down for tuning
+        best = std::max(best, ws_layout(sh, plan_layout(g, sh->W, sh->R, sh->T)).total);
+    }
+  return best;
+}
+
+// ---------------------------------------------------------------- pointer checks
+
+bool aligned(const void *p, int64_t a) { return ((uintptr_t)p % (uintptr_t)a) == 0; }
+
+struct Range {
+  const void *p;
+  int64_t n;
+  const char *name;
+};
+
+bool overlap(const Range &a, const Range &b) {
+  if (!a.p || !b.p || a.n <= 0 || b.n <= 0) return false;
+  const uintptr_t a0 = (uintptr_t)a.p, a1 = a0 + (uintptr_t)a.n;
+  const uintptr_t b0 = (uintptr_t)b.p, b1 = b0 + (uintptr_t)b.n;
+  return a0 < b1 && b0 < a1;
+}
+
+int g_sm_count_cache[64] = {0};
+
+sdm_status sm_count(int *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev >= 0 && dev < 64 && g_sm_count_cache[dev] > 0) {
+    *out = g_sm_count_cache[dev];
+    return SDM_OK;
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+  if (dev >= 0 && dev < 64) g_sm_count_cache[dev] = n;
+  *out = n;
+  return SDM_OK;
+}
+
+int64_t topk_tokens_per_cta(int32_t ntot) {
+  int64_t t = (96 * 1024) / (8 * (int64_t)ntot);
+  return std::max<int64_t>(1, std::min<int64_t>(16, t));
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+sdm_status sdm_write_read_workspace_size(const sdm_shape *shape, size_t *bytes) {
+  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
+  Derived d;
+  sdm_status st = check_shape(shape, false, &d);
+  if (st != SDM_OK) return st;
+  *bytes = (size_t)write_read_ws_bytes(shape);
+  return ok();
+}
+
+sdm_status sdm_decode_workspace_size(const sdm_shape *shape, size_t *bytes) {
+  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
+  sdm_status st = check_shape(shape, true, nullptr);
+  if (st != SDM_OK) return st;
+  *bytes = (size_t)kHeaderBytes;
+  return ok();
+}
+
+sdm_status sdm_write_read(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
+                          const float *gates, const void *subkeys, const void *bank_init, void *bank,
+                          void *y, int32_t *idx_w, float *wt_w, int32_t *idx_r, float *wt_r,
+                          void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+  Derived d;
+  sdm_status st = check_shape(sh, false, &d);
+  if (st != SDM_OK) return st;
+  static thread_local CandidateList cl;
+  if ((st = build_candidates(d, &cl)) != SDM_OK) return st;
+
+  const int64_t ab = elem_bytes(sh->act_dtype), sb = elem_bytes(sh->bank_dtype);
+  const int64_t rows = sh->B * sh->T * sh->H;
+  const int64_t qbytes = rows * sh->F * sh->d_sub * ab;
+  const Range r_qw{q_w, qbytes, "q_w"}, r_qr{q_r, qbytes, "q_r"}, r_kv{k_val, rows * sh->d_v * ab, "k_val"};
+  const Range r_g{gates, rows * 2 * 4, "gates"}, r_sk{subkeys, sh->H * d.ntot * sh->d_sub * ab, "subkeys"};
+  const Range r_bi{bank_init, sh->H * d.N * sh->d_v * sb, "bank_init"};
+  const Range r_b{bank, sh->B * sh->H * d.N * sh->d_v * sb, "bank"};
+  const Range r_y{y, rows * sh->d_v * ab, "y"};
+  const Range r_iw{idx_w, rows * sh->W * 4, "idx_w"}, r_ww{wt_w, rows * sh->W * 4, "wt_w"};
+  const Range r_ir{idx_r, rows * sh->R * 4, "idx_r"}, r_wr{wt_r, rows * sh->R * 4, "wt_r"};
+  const int64_t need_ws = write_read_ws_bytes(sh);
+  const Range r_ws{workspace, (int64_t)workspace_bytes, "workspace"};
+
+  if (rows > 0) {
+    const Range req[] = {r_qw, r_qr, r_kv, r_g, r_sk, r_b, r_y};
+    for (const Range &r : req)
+      if (!r.p) return fail(SDM_ERR_INVALID_ARG, "%s is NULL", r.name);
+  } else if (!bank && sh->B * sh->H > 0) {
+    return fail(SDM_ERR_INVALID_ARG, "bank is NULL");
+  }
+  const Range al16[] = {r_qw, r_qr, r_kv, r_sk, r_bi, r_b, r_y};
+  for (const Range &r : al16)
+    if (r.p && !aligned(r.p, 16)) return fail(SDM_ERR_INVALID_ARG, "%s is not 16-byte aligned", r.name);
+  if (gates && !aligned(gates, 8)) return fail(SDM_ERR_INVALID_ARG, "gates is not 8-byte aligned");
+  const Range al4[] = {r_iw, r_ww, r_ir, r_wr};
+  for (const Range &r : al4)
+    if (r.p && !aligned(r.p, 4)) return fail(SDM_ERR_INVALID_ARG, "%s is not 4-byte aligned", r.name);
+  if (!workspace) return fail(SDM_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 16)) return fail(SDM_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+  if ((int64_t)workspace_bytes < need_ws)
+    return fail(SDM_ERR_WORKSPACE, "workspace has %zu bytes, needs %lld", workspace_bytes, (long long)need_ws);
+
+  // outputs must not overlap inputs or each other
+  const Range ins[] = {r_qw, r_qr, r_kv, r_g, r_sk, r_bi};
+  const Range outs[] = {r_b, r_y, r_iw, r_ww, r_ir, r_wr, r_ws};
+  for (const Range &o : outs)
+    for (const Range &i : ins)
+      if (overlap(o, i)) return fail(SDM_ERR_ALIAS, "%s overlaps %s", o.name, i.name);
+  for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i)
+    for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+      if (overlap(outs[i], outs[j])) return fail(SDM_ERR_ALIAS, "%s overlaps %s", outs[i].name, outs[j].name);
+
+  int sms = 0;
+  if ((st = sm_count(&sms)) != SDM_OK) return st;
+  const WrChoice wc = choose_write_read(sh, sms);
+  const WsLayout wl = ws_layout(sh, wc.lay);
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  int32_t *err = reinterpret_cast<int32_t *>(ws);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+
+  cudaError_t ce = cudaMemsetAsync(err, 0, sizeof(int32_t), cs);
+  if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
+
+  const int64_t streams = sh->B * sh->H;
+  if (bank_init && streams > 0) {
+    BankCopyArgs bc{bank_init, bank, sh->B, d.N * sh->d_v * sb, sh->H};
+    if ((st = run_kernel(SDM_KERNEL_BANK_COPY, cs, "bank_copy", [&] { return launch_bank_copy(bc, sms, cs); })) != SDM_OK)
+      return st;
+  }
+  if (rows == 0) return ok();
+
+  int32_t *iw = idx_w ? idx_w : reinterpret_cast<int32_t *>(ws + wl.idx_w);
+  float *ww = wt_w ? wt_w : reinterpret_cast<float *>(ws + wl.wt_w);
+  int32_t *ir = idx_r ? idx_r : reinterpret_cast<int32_t *>(ws + wl.idx_r);
+  float *wr = wt_r ? wt_r : reinterpret_cast<float *>(ws + wl.wt_r);
+
+  // 1. scoring + exact top-k of both queries
+  int EF, EC;
+  sort_widths(d, cl, &EF, &EC);
+  TopkArgs ta{};
+  ta.q[0] = q_w;
+  ta.q[1] = q_r;
+  ta.subkeys = subkeys;
+  ta.idx[0] = iw;
+  ta.idx[1] = ir;
+  ta.wt[0] = ww;
+  ta.wt[1] = wr;
+  ta.err = err;
+  ta.BT = sh->B * sh->T;
+  ta.H = (int32_t)sh->H;
+  ta.tok_per_cta = (int32_t)topk_tokens_per_cta(d.ntot);
+  ta.g = d.g;
+  const int64_t topk_smem = a16((int64_t)2 * ta.tok_per_cta * d.ntot * 4 + (int64_t)(cl.n[0] + cl.n[1]) * 4) +
+                            topk_scratch_bytes();
+  if ((st = run_kernel(SDM_KERNEL_TOPK, cs, "topk",
+                       [&] { return launch_topk(ta, cl, sh->act_dtype, EF, EC, topk_smem, cs); })) != SDM_OK)
+    return st;
+
+  // 2. chunk plan
+  PlanArgs pa{};
+  pa.idx[0] = iw;
+  pa.idx[1] = ir;
+  pa.uniq = reinterpret_cast<int32_t *>(ws + wl.uniq);
+  pa.nuniq = reinterpret_cast<int32_t *>(ws + wl.nuniq);
+  pa.written = ws + wl.written;
+  pa.records = ws + wl.records;
+  pa.err = err;
+  pa.T = sh->T;
+  pa.H = (int32_t)sh->H;
+  pa.W = sh->W;
+  pa.R = sh->R;
+  pa.N = d.N;
+  pa.lay = wc.lay;
+  const int P = pow2_at_least(wc.lay.L);
+  if ((st = run_kernel(SDM_KERNEL_PLAN_SORT, cs, "plan_sort", [&] { return launch_plan_sort(pa, streams, P, cs); })) != SDM_OK)
+    return st;
+  if ((st = run_kernel(SDM_KERNEL_PLAN_LINK, cs, "plan_link", [&] { return launch_plan_link(pa, streams, cs); })) != SDM_OK)
+    return st;
+
+  // 3. fused gather / delta update / read
+  WriteReadArgs wa{};
+  wa.k_val = k_val;
+  wa.gates = gates;
+  wa.wt[0] = ww;
+  wa.wt[1] = wr;
+  wa.records = ws + wl.records;
+  wa.bank = bank;
+  wa.y = y;
+  wa.err = err;
+  wa.T = sh->T;
+  wa.N = d.N;
+  wa.d_v = sh->d_v;
+  wa.H = (int32_t)sh->H;
+  wa.W = sh->W;
+  wa.R = sh->R;
+  wa.slices = (int32_t)(sh->d_v / wc.CW);
+  wa.lay = wc.lay;
+  if ((st = run_kernel(SDM_KERNEL_WRITE_READ, cs, "write_read", [&] {
+         return launch_write_read(wa, streams, sh->bank_dtype, sh->act_dtype, wc.CW, wc.smem, cs);
+       })) != SDM_OK)
+    return st;
+  return ok();
+}
+
+sdm_status sdm_decode_step(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
+                           const float *gates, const void *subkeys, const void *bank_in, int bank_in_shared,
+                           void *bank_out, int donate, void *y, int32_t *idx_w, float *wt_w, int32_t *idx_r,
+                           float *wt_r, void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+  Derived d;
+  sdm_status st = check_shape(sh, true, &d);
+  if (st != SDM_OK) return st;
+  static thread_local CandidateList cl;
+  if ((st = build_candidates(d, &cl)) != SDM_OK) return st;
+  if (donate) {
+    if (bank_in_shared) return fail(SDM_ERR_INVALID_ARG, "a shared (broadcast) bank cannot be donated");
+    if (bank_out == nullptr) bank_out = const_cast<void *>(bank_in);
+    if (bank_out != bank_in) return fail(SDM_ERR_ALIAS, "donate needs bank_out == bank_in");
+  }
+  const int64_t ab = elem_bytes(sh->act_dtype), sb = elem_bytes(sh->bank_dtype);
+  const int64_t rows = sh->B * sh->H;
+  const int64_t qbytes = rows * sh->F * sh->d_sub * ab;
+  const Range r_qw{q_w, qbytes, "q_w"}, r_qr{q_r, qbytes, "q_r"}, r_kv{k_val, rows * sh->d_v * ab, "k_val"};
+  const Range r_g{gates, rows * 2 * 4, "gates"}, r_sk{subkeys, sh->H * d.ntot * sh->d_sub * ab, "subkeys"};
+  const int64_t table = d.N * sh->d_v * sb;
+  const Range r_bi{bank_in, (bank_in_shared ? sh->H : rows) * table, "bank_in"};
+  const Range r_bo{bank_out, rows * table, "bank_out"};
+  const Range r_y{y, rows * sh->d_v * ab, "y"};
+  const Range r_iw{idx_w, rows * sh->W * 4, "idx_w"}, r_ww{wt_w, rows * sh->W * 4, "wt_w"};
+  const Range r_ir{idx_r, rows * sh->R * 4, "idx_r"}, r_wr{wt_r, rows * sh->R * 4, "wt_r"};
+  const Range r_ws{workspace, (int64_t)workspace_bytes, "workspace"};
+  if (rows > 0) {
+    const Range req[] = {r_qw, r_qr, r_kv, r_g, r_sk, r_bi, r_bo, r_y};
+    for (const Range &r : req)
+      if (!r.p) return fail(SDM_ERR_INVALID_ARG, "%s is NULL", r.name);
+  }
+  const Range al16[] = {r_qw, r_qr, r_kv, r_sk, r_bi, r_bo, r_y};
+  for (const Range &r : al16)
+    if (r.p && !aligned(r.p, 16)) return fail(SDM_ERR_INVALID_ARG, "%s is not 16-byte aligned", r.name);
+  if (gates && !aligned(gates, 8)) return fail(SDM_ERR_INVALID_ARG, "gates is not 8-byte aligned");
+  const Range al4[] = {r_iw, r_ww, r_ir, r_wr};
+  for (const Range &r : al4)
+    if (r.p && !aligned(r.p, 4)) return fail(SDM_ERR_INVALID_ARG, "%s is not 4-byte aligned", r.name);
+  if (!workspace) return fail(SDM_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 16)) return fail(SDM_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+  if ((int64_t)workspace_bytes < kHeaderBytes)
+    return fail(SDM_ERR_WORKSPACE, "workspace has %zu bytes, needs %lld", workspace_bytes, (long long)kHeaderBytes);
+  const Range ins[] = {r_qw, r_qr, r_kv, r_g, r_sk};
+  const Range outs[] = {r_bo, r_y, r_iw, r_ww, r_ir, r_wr, r_ws};
+  for (const Range &o : outs)
+    for (const Range &i : ins)
+      if (overlap(o, i)) return fail(SDM_ERR_ALIAS, "%s overlaps %s", o.name, i.name);
+  for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i)
+    for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+      if (overlap(outs[i], outs[j])) return fail(SDM_ERR_ALIAS, "%s overlaps %s", outs[i].name, outs[j].name);
+  const Range bin_others[] = {r_y, r_iw, r_ww, r_ir, r_wr, r_ws};
+  for (const Range &o : bin_others)
+    if (overlap(o, r_bi)) return fail(SDM_ERR_ALIAS, "%s overlaps bank_in", o.name);
+  if (!donate && overlap(r_bi, r_bo)) return fail(SDM_ERR_ALIAS, "bank_out overlaps bank_in (use donate)");
+
+  const int64_t smem = (int64_t)2 * sh->F * sh->d_sub * 4 + (int64_t)2 * d.ntot * 4 + (int64_t)(cl.n[0] + cl.n[1]) * 4;
+  if (smem > 160 * 1024) return fail(SDM_ERR_UNSUPPORTED, "decode needs %lld bytes of shared memory", (long long)smem);
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int32_t *err = static_cast<int32_t *>(workspace);
+  cudaError_t ce = cudaMemsetAsync(err, 0, sizeof(int32_t), cs);
+  if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
+  if (rows == 0) return ok();
+
+  int EF, EC;
+  sort_widths(d, cl, &EF, &EC);
+  DecodeArgs da{};
+  da.q[0] = q_w;
+  da.q[1] = q_r;
+  da.k_val = k_val;
+  da.gates = gates;
+  da.subkeys = subkeys;
+  da.bank_in = bank_in;
+  da.bank_out = bank_out;
+  da.y = y;
+  da.idx[0] = idx_w;
+  da.idx[1] = idx_r;
+  da.wt[0] = wt_w;
+  da.wt[1] = wt_r;
+  da.err = err;
+  da.B = sh->B;
+  da.N = d.N;
+  da.d_v = sh->d_v;
+  da.H = (int32_t)sh->H;
+  da.bank_in_shared = bank_in_shared ? 1 : 0;
+  da.copy_rest = donate ? 0 : 1;
+  da.g = d.g;
+  if ((st = run_kernel(SDM_KERNEL_DECODE, cs, "decode",
+                       [&] { return launch_decode(da, cl, sh->act_dtype, sh->bank_dtype, EF, EC, smem, cs); })) != SDM_OK)
+    return st;
+  return ok();
+}
+
+sdm_status sdm_last_device_error(const void *workspace, size_t workspace_bytes, int32_t *code,
+                                 sdm_stream_t stream) {
+  if (!code) return fail(SDM_ERR_INVALID_ARG, "code is NULL");
+  if (!workspace || workspace_bytes < sizeof(int32_t)) return fail(SDM_ERR_WORKSPACE, "workspace too small");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return fail(SDM_ERR_CUDA, "reading the device flag: %s", cudaGetErrorString(e));
+  *code = v;
+  if (v != 0) return fail(SDM_ERR_DEVICE, "kernel-side error code %d", v);
+  return ok();
+}
+
+const char *sdm_status_string(sdm_status s) {
+  switch (s) {
+    case SDM_OK: return "ok";
+    case SDM_ERR_INVALID_ARG: return "invalid argument";
+    case SDM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SDM_ERR_ALIAS: return "buffers overlap";
+    case SDM_ERR_WORKSPACE: return "workspace missing or too small";
+    case SDM_ERR_CUDA: return "CUDA error";
+    case SDM_ERR_DEVICE: return "kernel-side error";
+  }
+  return "unknown status";
+}
+
+const char *sdm_last_error_message(void) { return g_msg; }
+
+int32_t sdm_abi_version(void) { return SDM_ABI_VERSION; }
+
+uint64_t sdm_launch_count(void) { return g_launches.load(); }
+
+sdm_status sdm_profile_begin(void) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.created) {
+    g_prof.start.resize(kProfSlots);
+    g_prof.stop.resize(kProfSlots);
+    g_prof.kind.resize(kProfSlots);
+    for (int i = 0; i < kProfSlots; ++i) {
+      if (cudaEventCreate(&g_prof.start[i]) != cudaSuccess || cudaEventCreate(&g_prof.stop[i]) != cudaSuccess)
+        return fail(SDM_ERR_CUDA, "cudaEventCreate failed");
+    }
+    g_prof.created = true;
+  }
+  g_prof.used = 0;
+  g_prof.active = true;
+  return ok();
+}
+
+sdm_status sdm_profile_end(sdm_kernel_times *out) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!out) return fail(SDM_ERR_INVALID_ARG, "out is NULL");
+  memset(out, 0, sizeof(*out));
+  if (!g_prof.active) return fail(SDM_ERR_INVALID_ARG, "profiling was not started");
+  g_prof.active = false;
+  for (int i = 0; i < g_prof.used; ++i) {
+    cudaError_t e = cudaEventSynchronize(g_prof.stop[i]);
+    float ms = 0.0f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, g_prof.start[i], g_prof.stop[i]);
+    if (e != cudaSuccess) return fail(SDM_ERR_CUDA, "event timing: %s", cudaGetErrorString(e));
+    const int k = g_prof.kind[i];
+    out->launches[k] += 1;
+    out->ms[k] += ms;
+  }
+  return ok();
+}
+
+const char *sdm_kernel_name(int32_t kind) {
+  switch (kind) {
+    case SDM_KERNEL_BANK_COPY: return "bank_copy";
+    case SDM_KERNEL_TOPK: return "topk";
+    case SDM_KERNEL_PLAN_SORT: return "plan_sort";
+    case SDM_KERNEL_PLAN_LINK: return "plan_link";
+    case SDM_KERNEL_WRITE_READ: return "write_read";
+    case SDM_KERNEL_DECODE: return "decode";
+  }
+  return "unknown";
+}
+
+}  // extern "C"

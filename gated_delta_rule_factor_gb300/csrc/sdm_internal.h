@@ -1,0 +1,137 @@
+// Host <-> kernel interface of the SDM library (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sdm.h"
+
+namespace sdm {
+
+constexpr int kThreads = 256;
+
+// Position tuples (p_1..p_F), p_f < min(k, n_f), with prod(p_f + 1) <= k, in
+// lexicographic order; byte f of an entry holds p_f.  Index 0 = write query (k = W),
+// 1 = read query (k = R).  Passed to kernels by value.
+struct CandidateList {
+  int32_t n[2];
+  uint32_t tup[2][SDM_MAX_CANDIDATES];
+};
+
+// Geometry of the product keys, shared by the top-k and decode kernels.
+struct KeyGeometry {
+  int32_t F, d_sub, ntot;            // factors, sub-key dim, sum of n_f
+  int32_t nf[SDM_MAX_FACTORS];       // n_f
+  int32_t off[SDM_MAX_FACTORS];      // row offset of factor f in the sub-key table
+  int32_t k[2];                      // W, R
+  int32_t kf[2][SDM_MAX_FACTORS];    // min(k, n_f)
+};
+
+struct TopkArgs {
+  const void *q[2];      // q_w, q_r [BT, H, F*d_sub]
+  const void *subkeys;   // [H, ntot, d_sub]
+  int32_t *idx[2];       // [BT, H, k]
+  float *wt[2];
+  int32_t *err;
+  int64_t BT;            // B*T tokens
+  int32_t H;
+  int32_t tok_per_cta;
+  KeyGeometry g;
+};
+
+struct BankCopyArgs {
+  const void *src;       // [H, N, d_v]
+  void *dst;             // [B, H, N, d_v]
+  int64_t B;
+  int64_t head_bytes;    // N * d_v * elem bytes (multiple of 16)
+  int64_t H;
+};
+
+// Chunk plan (per stream s = b*H + h and stage g of G tokens, L = G*(W+R) refs):
+//   uniq[s][g][u]    sorted unique slot ids of the stage      (int32, L per stage)
+//   nuniq[s][g]      number of unique rows
+//   written[s][g][u] 1 if a write ref of the stage hits row u (uint8, L per stage)
+//   record[s][g]     the stage record read by the write/read kernel:
+//     int32 n_u, n_load, n_carry, n_wb
+//     int32  load_slot[L]; uint16 load_u[L]      rows fetched from the bank
+//     uint32 carry[L]      (u | src_u << 16)      rows copied from the previous stage
+//     int32  wb_slot[L];   uint16 wb_u[L]         rows written back after the stage
+//     uint16 refmap[L]     row u of ref (t_local*(W+R) + j)
+struct PlanLayout {
+  int32_t G;             // tokens per stage
+  int32_t L;             // refs per full stage = G*(W+R)
+  int32_t n_stages;      // ceil(T / G)
+  int64_t rec_bytes;     // bytes per stage record (multiple of 16)
+  int64_t off_load_slot, off_load_u, off_carry, off_wb_slot, off_wb_u, off_refmap;
+};
+
+struct PlanArgs {
+  const int32_t *idx[2];  // idx_w [B,T,H,W], idx_r [B,T,H,R]
+  int32_t *uniq;
+  int32_t *nuniq;
+  uint8_t *written;
+  unsigned char *records;
+  int32_t *err;
+  int64_t T;
+  int32_t H, W, R;
+  int64_t N;
+  PlanLayout lay;
+};
+
+struct WriteReadArgs {
+  const void *k_val;      // [B,T,H,d_v]
+  const float *gates;     // [B,T,H,2]
+  const float *wt[2];     // [B,T,H,W], [B,T,H,R]
+  const unsigned char *records;
+  void *bank;             // [B,H,N,d_v]
+  void *y;                // [B,T,H,d_v]
+  int32_t *err;
+  int64_t T, N, d_v;
+  int32_t H, W, R;
+  int32_t slices;         // d_v / CW
+  PlanLayout lay;
+};
+
+struct DecodeArgs {
+  const void *q[2];       // [B, H, F*d_sub]
+  const void *k_val;      // [B, H, d_v]
+  const float *gates;     // [B, H, 2]
+  const void *subkeys;
+  const void *bank_in;    // [B,H,N,d_v] or [H,N,d_v] when shared
+  void *bank_out;
+  void *y;
+  int32_t *idx[2];        // nullable
+  float *wt[2];           // nullable
+  int32_t *err;
+  int64_t B, N, d_v;
+  int32_t H;
+  int32_t bank_in_shared; // bank_in is one [H,N,d_v] table for all streams
+  int32_t copy_rest;      // copy the unwritten rows bank_in -> bank_out
+  KeyGeometry g;
+};
+
+// Column slice of the write/read kernel and its stage length.
+struct WriteReadConfig {
+  int32_t CW;             // bank columns per CTA
+  int32_t G;              // tokens per stage
+  int64_t smem_bytes;
+};
+
+// Launchers, defined next to their kernels.  Each returns the launch error.
+cudaError_t launch_topk(const TopkArgs &a, const CandidateList &cl, int act_dtype, int EF,
+                        int EC, int64_t smem_bytes, cudaStream_t st);
+cudaError_t launch_bank_copy(const BankCopyArgs &a, int sm_count, cudaStream_t st);
+cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int sort_pow2,
+                             cudaStream_t st);
+cudaError_t launch_plan_link(const PlanArgs &a, int64_t streams, cudaStream_t st);
+cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_dtype,
+                              int act_dtype, int CW, int64_t smem_bytes, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs &a, const CandidateList &cl, int act_dtype,
+                          int bank_dtype, int EF, int EC, int64_t smem_bytes,
+                          cudaStream_t st);
+
+// Dynamic shared memory needed by the write/read kernel for a column slice and stage.
+int64_t write_read_smem_bytes(int CW, int bank_elem, int act_elem, int G, int W, int R,
+                              int64_t rec_bytes);
+
+}  // namespace sdm

@@ -1,0 +1,157 @@
+// Exact product-key top-k of one query row, by one warp (shared by the sequence
+// top-k kernel and the decode kernel so that both select identically).
+//
+// Product-key memory (Lample et al., cited in the sparse-delta-memory README) scores
+// each factor's sub-keys separately; the slot score is the float32 sum of the factor
+// scores, and ties go to the larger rank sum, then the larger first rank
+// (sparse-delta-memory CHANGELOG, 2.0.0 > Upgrading from v1).  A factor's rank is its
+// ascending score rank, equal scores ordered by index, so "larger rank" means
+// "earlier in the factor's best-first order".
+//
+// Exactness of the pruning: let each factor be sorted best first and describe a slot
+// by its positions (p_1..p_F) in those orders.  Any tuple p' <= p position-wise scores
+// at least as high (float addition is monotone in each operand) and, if the scores
+// tie, has the larger rank sum.  The prod(p_f + 1) - 1 tuples below p therefore all
+// beat p, so p can only be among the top k if prod(p_f + 1) <= k.  The surviving
+// candidates are ranked with one 64-bit key:
+//   bits 63..32  slot score (order-preserving bits)
+//   bits 31..24  255 - sum_f p_f      (larger rank sum first)
+//   bits 23..16  255 - p_1            (larger first rank first)
+//   bits 15..8   255 - p_2, bits 7..0  255 - p_3   (then the next ranks)
+// Distinct tuples get distinct keys (p_4 = sum - p_1 - p_2 - p_3), so the order is
+// total and the selection unique.  Every p_f and sum_f p_f is <= k - 1 <= 255.
+#pragma once
+
+#include "sdm_common.cuh"
+#include "sdm_internal.h"
+
+namespace sdm {
+
+// Per-warp scratch: best-first factor scores and indices, [F][SDM_MAX_K] each.
+struct RowScratch {
+  float fs[SDM_MAX_FACTORS * SDM_MAX_K];
+  int32_t fi[SDM_MAX_FACTORS * SDM_MAX_K];
+};
+
+// scores: the row's ntot factor scores (shared memory), factor f at g.off[f].
+// qsel: 0 = write query (k = W), 1 = read query (k = R).
+// cand: the candidate tuples of this query kind (shared memory), ncand entries.
+// Writes k slot ids (best first) to idx_out and their softmax weights to wt_out.
+template <int EF, int EC>
+__device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry &g, int qsel,
+                                         const uint32_t *cand, int ncand, RowScratch &sc,
+                                         int32_t *idx_out, float *wt_out) {
+  const int lane = threadIdx.x & 31;
+  const int k = g.k[qsel];
+  constexpr int P = 32 * EF;
+
+  // 1. best-first order of each factor, kept to its first min(k, n_f) positions
+  for (int f = 0; f < g.F; ++f) {
+    const int nf = g.nf[f];
+    const float *s = scores + g.off[f];
+    uint64_t best[EF];
+    for (int c0 = 0; c0 < nf; c0 += P) {
+      uint64_t key[EF];
+#pragma unroll
+      for (int e = 0; e < EF; ++e) {
+        const int a = c0 + lane * EF + e;
+        key[e] = (a < nf) ? ((uint64_t)ordered_bits(s[a]) << 32) | (uint32_t)a : 0ull;
+      }
+      warp_sort_desc<EF>(key);
+      if (c0 == 0) {
+#pragma unroll
+        for (int e = 0; e < EF; ++e) best[e] = key[e];
+      } else {
+        warp_merge_top_desc<EF>(best, key);
+      }
+    }
+    const int kf = g.kf[qsel][f];
+#pragma unroll
+    for (int e = 0; e < EF; ++e) {
+      const int pos = lane * EF + e;
+      if (pos < kf) {
+        sc.fs[f * SDM_MAX_K + pos] = from_ordered_bits((uint32_t)(best[e] >> 32));
+        sc.fi[f * SDM_MAX_K + pos] = (int32_t)(uint32_t)(best[e] & 0xffffffffu);
+      }
+    }
+  }
+  __syncwarp();
+
+  // 2. candidate tuples, keyed and sorted best first
+  uint64_t ck[EC];
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    const int c = lane * EC + e;
+    if (c < ncand) {
+      const uint32_t t = cand[c];
+      const int p0 = t & 255, p1 = (t >> 8) & 255, p2 = (t >> 16) & 255, p3 = t >> 24;
+      float S = sc.fs[p0];
+      if (g.F > 1) S = __fadd_rn(S, sc.fs[SDM_MAX_K + p1]);
+      if (g.F > 2) S = __fadd_rn(S, sc.fs[2 * SDM_MAX_K + p2]);
+      if (g.F > 3) S = __fadd_rn(S, sc.fs[3 * SDM_MAX_K + p3]);
+      const uint32_t sum = p0 + p1 + p2 + p3;
+      const uint32_t low = ((255u - sum) << 24) | ((255u - p0) << 16) | ((255u - p1) << 8) |
+                           (255u - p2);
+      ck[e] = ((uint64_t)ordered_bits(S) << 32) | low;
+    } else {
+      ck[e] = 0ull;
+    }
+  }
+  warp_sort_desc<EC>(ck);
+
+  // 3. softmax weights of the k best (fixed summation order) and slot ids
+  const float S0 = from_ordered_bits((uint32_t)(__shfl_sync(0xffffffffu, ck[0], 0) >> 32));
+  float ex[EC];
+  float part = 0.0f;
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    const int pos = lane * EC + e;
+    ex[e] = 0.0f;
+    if (pos < k) {
+      const float S = from_ordered_bits((uint32_t)(ck[e] >> 32));
+      ex[e] = expf(__fsub_rn(S, S0));
+      part = __fadd_rn(part, ex[e]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    const int pos = lane * EC + e;
+    if (pos < k) {
+      const uint32_t low = (uint32_t)(ck[e] & 0xffffffffu);
+      const int sum = 255 - (int)(low >> 24);
+      const int p0 = 255 - (int)((low >> 16) & 255);
+      const int p1 = 255 - (int)((low >> 8) & 255);
+      const int p2 = 255 - (int)(low & 255);
+      const int p3 = sum - p0 - p1 - p2;
+      int64_t slot = sc.fi[p0];
+      if (g.F > 1) slot = slot * g.nf[1] + sc.fi[SDM_MAX_K + p1];
+      if (g.F > 2) slot = slot * g.nf[2] + sc.fi[2 * SDM_MAX_K + p2];
+      if (g.F > 3) slot = slot * g.nf[3] + sc.fi[3 * SDM_MAX_K + p3];
+      idx_out[pos] = (int32_t)slot;
+      wt_out[pos] = __fdiv_rn(ex[e], part);
+    }
+  }
+  __syncwarp();
+}
+
+// One factor score: <q, k> over d_sub terms with the accurate accumulation described
+// in sdm_common.cuh.  q is float32 (shared memory), k of the activation type.
+template <typename ACT>
+__device__ __forceinline__ float score_dot(const float *q, const ACT *k, int d_sub) {
+  Acc2 acc{0.0f, 0.0f};
+  if constexpr (sizeof(ACT) == 2) {
+    for (int d0 = 0; d0 < d_sub; d0 += kBf16Block) {
+      const int d1 = min(d_sub, d0 + kBf16Block);
+      float blk = 0.0f;
+      for (int d = d0; d < d1; ++d) blk = __fmaf_rn(q[d], to_f32(k[d]), blk);
+      two_sum_into(acc, blk);
+    }
+  } else {
+    for (int d = 0; d < d_sub; ++d) dot2_step(acc, q[d], to_f32(k[d]));
+  }
+  return acc2_value(acc);
+}
+
+}  // namespace sdm

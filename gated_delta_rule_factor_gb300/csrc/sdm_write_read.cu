@@ -1,0 +1,297 @@
+// The fused gather / gated delta-rule update / read kernel of sdm_write_read, and the
+// per-call bank copy (learned table -> per-stream banks).
+//
+// Parallel axes: streams (b, h) are independent, and so is every bank column (the
+// update of a column reads only that column, see sdm_delta.cuh).  One CTA owns one
+// stream and a slice of CW columns (CW * elem = 32..128 bytes of every row) and runs
+// the stream's tokens in order.  Tokens are staged G at a time; the chunk plan
+// (sdm_plan.cu) lists the distinct rows of each stage.
+//
+// Warp roles (one CTA):
+//   warp 0      compute: the tokens of the current stage on the shared-memory rows;
+//   warps 1..4  loaders: write back the previous stage's dirty rows, then fetch the next
+//               stage's rows (cp.async, 16 B per request) and token data, and the stage
+//               record after it.
+// Two row buffers alternate between stages; rows shared by consecutive stages are
+// copied across buffers instead of re-read, because the bank copy may be stale.  Stage
+// records use three buffers (in use / rows being fetched / record being fetched).
+#include "sdm_common.cuh"
+#include "sdm_delta.cuh"
+#include "sdm_internal.h"
+
+namespace sdm {
+
+namespace {
+
+constexpr int kLoaderWarps = 4;
+constexpr int kLoaderThreads = 32 * kLoaderWarps;
+
+struct TokLayout {
+  int64_t wts, gates, v, bytes;  // offsets inside one token-data buffer
+};
+
+__host__ __device__ inline int64_t align16(int64_t x) { return (x + 15) & ~int64_t(15); }
+
+__host__ __device__ inline TokLayout tok_layout(int G, int W, int R, int CW, int act_elem) {
+  TokLayout t;
+  t.wts = 0;
+  t.gates = align16((int64_t)G * (W + R) * 4);
+  t.v = t.gates + align16((int64_t)G * 2 * 4);
+  t.bytes = t.v + align16((int64_t)G * CW * act_elem);
+  return t;
+}
+
+template <typename BANK, typename ACT, int CW>
+__global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
+    write_read_kernel(const __grid_constant__ WriteReadArgs a) {
+  constexpr int VEC = Vec16<BANK>::N;                 // elements per 16 B
+  constexpr int NCG = CW / VEC;                       // 16-byte column groups
+  static_assert(NCG >= 1 && NCG <= 8 && (NCG & (NCG - 1)) == 0, "column slice");
+  constexpr int RB = CW * (int)sizeof(BANK);          // row slice bytes in smem
+  constexpr int CPR = RB / 16;                        // 16-byte chunks per row slice
+  constexpr int NTHR = 32 * (1 + kLoaderWarps);
+
+  extern __shared__ __align__(16) unsigned char smem[];
+  const PlanLayout &lay = a.lay;
+  const int L = lay.L, G = lay.G, S = lay.n_stages;
+  const int W = a.W, R = a.R, WR = W + R;
+  const int64_t s = blockIdx.y;
+  const int slice = blockIdx.x;
+  const int64_t b = s / a.H, h = s % a.H;
+  const int64_t c0 = (int64_t)slice * CW;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  unsigned char *rowbuf[2] = {smem, smem + (int64_t)L * RB};
+  unsigned char *plans = smem + 2 * (int64_t)L * RB;
+  const TokLayout tl = tok_layout(G, W, R, CW, (int)sizeof(ACT));
+  unsigned char *tokbuf[2] = {plans + 3 * lay.rec_bytes, plans + 3 * lay.rec_bytes + tl.bytes};
+
+  BANK *bank = static_cast<BANK *>(a.bank) + s * a.N * a.d_v;   // this stream's table
+  const ACT *kv = static_cast<const ACT *>(a.k_val);
+  ACT *y = static_cast<ACT *>(a.y);
+  const unsigned char *records = a.records + s * (int64_t)S * lay.rec_bytes;
+
+  auto plan_of = [&](int g) -> unsigned char * { return plans + (int64_t)(g % 3) * lay.rec_bytes; };
+  auto hdr_ok = [&](const int32_t *hdr) -> bool {
+    return hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[1] <= L && hdr[2] >= 0 && hdr[2] <= L &&
+           hdr[3] >= 0 && hdr[3] <= L;
+  };
+
+  // ---- loader helpers (threads of warps 1..4)
+  const int ltid = tid - 32;
+  auto fetch_record = [&](int g) {
+    const unsigned char *src = records + (int64_t)g * lay.rec_bytes;
+    unsigned char *dst = plan_of(g);
+    for (int64_t i = ltid; i < lay.rec_bytes / 16; i += kLoaderThreads) cp_async16(dst + i * 16, src + i * 16);
+  };
+  auto fetch_stage = [&](int g) {
+    const unsigned char *rec = plan_of(g);
+    const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+    const int n_load = hdr_ok(hdr) ? hdr[1] : 0;
+    const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
+    const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
+    unsigned char *dst = rowbuf[g & 1];
+    for (int i = ltid; i < n_load * CPR; i += kLoaderThreads) {
+      const int e = i / CPR, c = i % CPR;
+      const int32_t slot = load_slot[e];
+      const int u = load_u[e];
+      if (u >= L || slot < 0 || slot >= a.N) {
+        raise_error(a.err, SDM_DEVERR_PLAN);
+        continue;
+      }
+      cp_async16(dst + (int64_t)u * RB + c * 16,
+                 reinterpret_cast<const unsigned char *>(bank + (int64_t)slot * a.d_v + c0) + c * 16);
+    }
+    // token data of the stage
+    const int64_t t0 = (int64_t)g * G;
+    const int nt = (int)min((int64_t)G, a.T - t0);
+    unsigned char *tb = tokbuf[g & 1];
+    float *wts = reinterpret_cast<float *>(tb + tl.wts);
+    for (int i = ltid; i < nt * WR; i += kLoaderThreads) {
+      const int t = i / WR, j = i % WR;
+      const int64_t row = (b * a.T + t0 + t) * a.H + h;
+      const float *src = (j < W) ? a.wt[0] + row * W + j : a.wt[1] + row * R + (j - W);
+      cp_async4(wts + i, src);
+    }
+    float *gt = reinterpret_cast<float *>(tb + tl.gates);
+    for (int i = ltid; i < nt; i += kLoaderThreads) {
+      const int64_t row = (b * a.T + t0 + i) * a.H + h;
+      cp_async8(gt + 2 * i, a.gates + row * 2);
+    }
+    constexpr int VB = CW * (int)sizeof(ACT);          // value bytes per token (>= 16)
+    unsigned char *vb = tb + tl.v;
+    for (int i = ltid; i < nt * (VB / 16); i += kLoaderThreads) {
+      const int t = i / (VB / 16), c = i % (VB / 16);
+      const int64_t row = (b * a.T + t0 + t) * a.H + h;
+      cp_async16(vb + (int64_t)t * VB + c * 16,
+                 reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
+    }
+  };
+  auto write_back = [&](int g, int t_begin, int t_stride) {
+    const unsigned char *rec = plan_of(g);
+    const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+    const int n_wb = hdr_ok(hdr) ? hdr[3] : 0;
+    const int32_t *wb_slot = reinterpret_cast<const int32_t *>(rec + lay.off_wb_slot);
+    const uint16_t *wb_u = reinterpret_cast<const uint16_t *>(rec + lay.off_wb_u);
+    const unsigned char *src = rowbuf[g & 1];
+    for (int i = t_begin; i < n_wb * CPR; i += t_stride) {
+      const int e = i / CPR, c = i % CPR;
+      const int32_t slot = wb_slot[e];
+      const int u = wb_u[e];
+      if (u >= L || slot < 0 || slot >= a.N) {
+        raise_error(a.err, SDM_DEVERR_PLAN);
+        continue;
+      }
+      const uint4 val = *reinterpret_cast<const uint4 *>(src + (int64_t)u * RB + c * 16);
+      *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(bank + (int64_t)slot * a.d_v + c0) + c * 16) = val;
+    }
+  };
+
+  // ---- prologue: record 0, then stage 0 and record 1
+  if (warp >= 1) {
+    fetch_record(0);
+    cp_async_commit();
+    cp_async_wait_all();
+    named_barrier(1, kLoaderThreads);
+    fetch_stage(0);
+    if (S > 1) fetch_record(1);
+    cp_async_commit();
+  }
+
+  for (int g = 0; g < S; ++g) {
+    if (warp >= 1) cp_async_wait_all();
+    __syncthreads();                                             // stage g resident
+    {
+      const unsigned char *rec = plan_of(g);
+      const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+      const bool ok = hdr_ok(hdr);
+      if (!ok && tid == 0) raise_error(a.err, SDM_DEVERR_PLAN);
+      const int n_carry = ok ? hdr[2] : 0;
+      const uint32_t *carry = reinterpret_cast<const uint32_t *>(rec + lay.off_carry);
+      const unsigned char *from = rowbuf[(g + 1) & 1];
+      unsigned char *to = rowbuf[g & 1];
+      for (int i = tid; i < n_carry * CPR; i += NTHR) {
+        const int e = i / CPR, c = i % CPR;
+        const int u = carry[e] & 0xffff, src = carry[e] >> 16;
+        if (u >= L || src >= L) {
+          raise_error(a.err, SDM_DEVERR_PLAN);
+          continue;
+        }
+        *reinterpret_cast<uint4 *>(to + (int64_t)u * RB + c * 16) =
+            *reinterpret_cast<const uint4 *>(from + (int64_t)src * RB + c * 16);
+      }
+    }
+    __syncthreads();                                             // carries in place
+
+    if (warp == 0) {
+      // ---- compute: tokens of stage g in order
+      const unsigned char *rec = plan_of(g);
+      const uint16_t *refmap = reinterpret_cast<const uint16_t *>(rec + lay.off_refmap);
+      const unsigned char *tb = tokbuf[g & 1];
+      const float *wts = reinterpret_cast<const float *>(tb + tl.wts);
+      const float *gt = reinterpret_cast<const float *>(tb + tl.gates);
+      const ACT *vv = reinterpret_cast<const ACT *>(tb + tl.v);
+      unsigned char *rows = rowbuf[g & 1];
+      const int cg = lane % NCG;
+      const int64_t t0 = (int64_t)g * G;
+      const int nt = (int)min((int64_t)G, a.T - t0);
+      for (int t = 0; t < nt; ++t) {
+        const uint16_t *rm = refmap + t * WR;
+        const float *w = wts + t * WR;
+        auto row_ptr = [&](int j) -> BANK * {
+          int u = rm[j];
+          if (u >= L) u = 0;                           // plan_sort never emits these
+          return reinterpret_cast<BANK *>(rows + (int64_t)u * RB) + cg * VEC;
+        };
+        auto wrow = [&](int j) { return row_ptr(j); };
+        auto rrow = [&](int j) { return row_ptr(W + j); };
+        float v[VEC];
+        load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
+        delta_write_cols<BANK, NCG>(W, w, gt[2 * t], gt[2 * t + 1], v, wrow, wrow);
+        __syncwarp();
+        float out[VEC];
+        weighted_read_cols<BANK, NCG>(R, w + W, rrow, out);
+        if (lane < NCG) {
+          const int64_t row = (b * a.T + t0 + t) * a.H + h;
+          store_vec<ACT, VEC>(y + row * a.d_v + c0 + cg * VEC, out);
+        }
+        __syncwarp();
+      }
+    } else {
+      // ---- loaders: retire stage g-1, fetch stage g+1 and record g+2
+      if (g >= 1) write_back(g - 1, ltid, kLoaderThreads);
+      named_barrier(1, kLoaderThreads);
+      if (g + 1 < S) fetch_stage(g + 1);
+      if (g + 2 < S) fetch_record(g + 2);
+      cp_async_commit();
+    }
+  }
+  __syncthreads();
+  if (S > 0) write_back(S - 1, tid, NTHR);
+}
+
+template <typename BANK, typename ACT>
+cudaError_t launch_wr_t(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem, cudaStream_t st) {
+  dim3 grid((unsigned)a.slices, (unsigned)streams);
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 32 * (1 + kLoaderWarps), smem, st>>>(a);
+    return cudaGetLastError();
+  };
+  constexpr int V = Vec16<BANK>::N;
+  switch (CW / V) {
+    case 1: return go(write_read_kernel<BANK, ACT, V * 1>);
+    case 2: return go(write_read_kernel<BANK, ACT, V * 2>);
+    case 4: return go(write_read_kernel<BANK, ACT, V * 4>);
+    case 8: return go(write_read_kernel<BANK, ACT, V * 8>);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Learned table [H, N, d_v] -> every stream's bank [B, H, N, d_v]: each 16-byte chunk
+// of the source is read once and written B times.
+__global__ void __launch_bounds__(kThreads) bank_copy_kernel(const __grid_constant__ BankCopyArgs a) {
+  const int64_t chunks_per_head = a.head_bytes / 16;
+  const int64_t total = chunks_per_head * a.H;
+  const uint4 *src = static_cast<const uint4 *>(a.src);
+  uint4 *dst = static_cast<uint4 *>(a.dst);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const uint4 v = src[i];
+    const int64_t h = i / chunks_per_head, c = i % chunks_per_head;
+    for (int64_t bb = 0; bb < a.B; ++bb) dst[(bb * a.H + h) * chunks_per_head + c] = v;
+  }
+}
+
+}  // namespace
+
+int64_t write_read_smem_bytes(int CW, int bank_elem, int act_elem, int G, int W, int R,
+                              int64_t rec_bytes) {
+  const int64_t L = (int64_t)G * (W + R);
+  const TokLayout t = tok_layout(G, W, R, CW, act_elem);
+  return 2 * L * CW * bank_elem + 3 * rec_bytes + 2 * t.bytes;
+}
+
+cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_dtype,
+                              int act_dtype, int CW, int64_t smem, cudaStream_t st) {
+  if (streams == 0 || a.slices == 0) return cudaSuccess;
+  if (bank_dtype == SDM_F32) {
+    if (act_dtype == SDM_F32) return launch_wr_t<float, float>(a, streams, CW, smem, st);
+    return launch_wr_t<float, __nv_bfloat16>(a, streams, CW, smem, st);
+  }
+  if (act_dtype == SDM_F32) return launch_wr_t<__nv_bfloat16, float>(a, streams, CW, smem, st);
+  return launch_wr_t<__nv_bfloat16, __nv_bfloat16>(a, streams, CW, smem, st);
+}
+
+cudaError_t launch_bank_copy(const BankCopyArgs &a, int sm_count, cudaStream_t st) {
+  if (a.B == 0 || a.H == 0 || a.head_bytes == 0) return cudaSuccess;
+  const int64_t total = a.head_bytes / 16 * a.H;
+  int64_t blocks = (total + kThreads - 1) / kThreads;
+  const int64_t cap = (int64_t)sm_count * 8;
+  if (blocks > cap) blocks = cap;
+  bank_copy_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace sdm

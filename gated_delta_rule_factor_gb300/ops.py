@@ -1,0 +1,219 @@
+"""Torch-tensor front end of the C ABI: sdm_write_read and sdm_decode_step.
+
+Argument marshalling only.  Every step of the op runs in the CUDA library
+(libsdm_gb300.so); PyTorch only supplies device memory and the current stream.
+There is no CPU path: without the library, importing the package fails.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _abi
+
+_DT = {torch.float32: _abi.SDM_F32, torch.bfloat16: _abi.SDM_BF16, torch.float16: _abi.SDM_F16}
+
+
+def _dtype_code(t: torch.Tensor, name: str) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"{name}: dtype {t.dtype} is not float32 or bfloat16")
+    return _DT[t.dtype]
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _require_cuda_contig(name: str, t: Optional[torch.Tensor], device) -> None:
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_shape(*, B: int, T: int, H: int, factor_dims: Sequence[int], d_sub: int, d_v: int,
+               W: int, R: int, chunk_size: int, act_dtype: int, bank_dtype: int) -> _abi.SdmShape:
+    if len(factor_dims) > _abi.MAX_FACTORS:
+        # let the library refuse it with its own status
+        dims = list(factor_dims)[:_abi.MAX_FACTORS]
+        F = len(factor_dims)
+    else:
+        dims = list(factor_dims) + [1] * (_abi.MAX_FACTORS - len(factor_dims))
+        F = len(factor_dims)
+    sh = _abi.SdmShape()
+    sh.B, sh.T, sh.H, sh.d_sub, sh.d_v = int(B), int(T), int(H), int(d_sub), int(d_v)
+    sh.F = F
+    for i, n in enumerate(dims):
+        sh.factor_dims[i] = int(n)
+    sh.W, sh.R, sh.chunk_size = int(W), int(R), int(chunk_size)
+    sh.act_dtype, sh.bank_dtype = int(act_dtype), int(bank_dtype)
+    return sh
+
+
+def write_read_workspace_size(shape: _abi.SdmShape) -> int:
+    n = ctypes.c_size_t(0)
+    _abi.check(_abi.load().sdm_write_read_workspace_size(ctypes.byref(shape), ctypes.byref(n)),
+               "sdm_write_read_workspace_size")
+    return int(n.value)
+
+
+def decode_workspace_size(shape: _abi.SdmShape) -> int:
+    n = ctypes.c_size_t(0)
+    _abi.check(_abi.load().sdm_decode_workspace_size(ctypes.byref(shape), ctypes.byref(n)),
+               "sdm_decode_workspace_size")
+    return int(n.value)
+
+
+def _shape_of(q_w, k_val, bank_dtype_t, factor_dims, W, R, chunk_size, T=None) -> _abi.SdmShape:
+    F = len(factor_dims)
+    if q_w.dim() != 4 and T is None:
+        raise ValueError("q_w must be [B, T, H, F*d_sub]")
+    B, Tq, H, D = q_w.shape if T is None else (q_w.shape[0], 1, q_w.shape[1], q_w.shape[2])
+    if F == 0 or D % F != 0:
+        raise ValueError(f"query width {D} is not a multiple of F={F}")
+    return make_shape(B=B, T=Tq, H=H, factor_dims=factor_dims, d_sub=D // F, d_v=k_val.shape[-1],
+                      W=W, R=R, chunk_size=chunk_size, act_dtype=_dtype_code(q_w, "q_w"),
+                      bank_dtype=_dtype_code(bank_dtype_t, "bank"))
+
+
+def sdm_write_read(q_w: torch.Tensor, q_r: torch.Tensor, k_val: torch.Tensor, gates: torch.Tensor,
+                   subkeys: torch.Tensor, bank: torch.Tensor, chunk_size: int, W: int, R: int, *,
+                   factor_dims: Sequence[int], bank_init: Optional[torch.Tensor] = None,
+                   y: Optional[torch.Tensor] = None, idx_w: Optional[torch.Tensor] = None,
+                   wt_w: Optional[torch.Tensor] = None, idx_r: Optional[torch.Tensor] = None,
+                   wt_r: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The chunked write/read op; the bank advances in place.  Returns y [B, T, H, d_v].
+
+    q_w, q_r [B,T,H,F*d_sub]; k_val [B,T,H,d_v]; gates [B,T,H,2] float32 (alpha, beta);
+    subkeys [H, sum(factor_dims), d_sub]; bank [B,H,N,d_v] (float32 or bfloat16).
+    bank_init: optional learned table [H,N,d_v] copied into every stream's bank first.
+    idx_w/wt_w/idx_r/wt_r: optional output buffers for the selections.
+    """
+    dev = q_w.device
+    for name, t in (("q_w", q_w), ("q_r", q_r), ("k_val", k_val), ("gates", gates),
+                    ("subkeys", subkeys), ("bank", bank), ("bank_init", bank_init), ("y", y),
+                    ("idx_w", idx_w), ("wt_w", wt_w), ("idx_r", idx_r), ("wt_r", wt_r),
+                    ("workspace", workspace)):
+        _require_cuda_contig(name, t, dev)
+    if gates.dtype != torch.float32:
+        raise TypeError("gates must be float32")
+    shape = _shape_of(q_w, k_val, bank, factor_dims, W, R, chunk_size)
+    if y is None:
+        y = torch.empty_like(k_val)
+    if workspace is None:
+        workspace = torch.empty(write_read_workspace_size(shape), dtype=torch.uint8, device=dev)
+    st = _abi.load().sdm_write_read(
+        ctypes.byref(shape), _ptr(q_w), _ptr(q_r), _ptr(k_val), _ptr(gates), _ptr(subkeys),
+        _ptr(bank_init), _ptr(bank), _ptr(y), _ptr(idx_w), _ptr(wt_w), _ptr(idx_r), _ptr(wt_r),
+        _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    _abi.check(st, "sdm_write_read")
+    return y
+
+
+def _owns_storage(t: torch.Tensor) -> bool:
+    """True when writing into t cannot reach another tensor's data (the donate guards).
+
+    A view (including a broadcast with a zero stride) may share its storage with a table
+    that is not the stream's own, and a tensor autograd records must not change under
+    it (lumen PR #29, Donating is a permission).
+    """
+    if t._base is not None:
+        return False
+    if any(s == 0 for s, n in zip(t.stride(), t.shape) if n > 1):
+        return False
+    if t.requires_grad:
+        return False
+    return t.is_contiguous()
+
+
+def sdm_decode_step(q_w: torch.Tensor, q_r: torch.Tensor, k_val: torch.Tensor, gates: torch.Tensor,
+                    subkeys: torch.Tensor, bank: torch.Tensor, W: int, R: int, *,
+                    factor_dims: Sequence[int], donate: bool = False,
+                    bank_out: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                    idx_w: Optional[torch.Tensor] = None, wt_w: Optional[torch.Tensor] = None,
+                    idx_r: Optional[torch.Tensor] = None, wt_r: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None):
+    """One decode step for every stream.  Returns (y [B,H,d_v], successor bank).
+
+    q_w, q_r [B,H,F*d_sub]; k_val [B,H,d_v]; gates [B,H,2]; bank [B,H,N,d_v], or a
+    learned table [H,N,d_v] / its broadcast view that every stream starts from.
+    donate=True lets the step write the successor into `bank` itself; it is honoured only
+    when `bank` owns its storage (not a view, not a broadcast, not recorded by autograd),
+    otherwise the step copies, as a permission and not a demand.
+    """
+    dev = q_w.device
+    B, H = q_w.shape[0], q_w.shape[1]
+    shared = False
+    bank_in = bank
+    if bank.dim() == 3:
+        shared = True
+    elif bank.dim() == 4 and bank.shape[0] == B and bank.stride(0) == 0 and B > 1:
+        bank_in = bank[0]               # a broadcast of one [H,N,d_v] table
+        shared = True
+    if shared:
+        if not bank_in.is_contiguous():
+            bank_in = bank_in.contiguous()
+        donate = False
+    elif donate and not _owns_storage(bank):
+        donate = False
+    for name, t in (("q_w", q_w), ("q_r", q_r), ("k_val", k_val), ("gates", gates),
+                    ("subkeys", subkeys), ("bank", bank_in), ("bank_out", bank_out), ("y", y),
+                    ("idx_w", idx_w), ("wt_w", wt_w), ("idx_r", idx_r), ("wt_r", wt_r),
+                    ("workspace", workspace)):
+        _require_cuda_contig(name, t, dev)
+    shape = _shape_of(q_w, k_val, bank_in, factor_dims, W, R, 1, T=1)
+    N = int(torch.tensor(list(factor_dims)).prod().item())
+    if donate:
+        bank_out = bank
+    elif bank_out is None:
+        bank_out = torch.empty((B, H, N, k_val.shape[-1]), dtype=bank_in.dtype, device=dev)
+    if y is None:
+        y = torch.empty_like(k_val)
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_size(shape), dtype=torch.uint8, device=dev)
+    st = _abi.load().sdm_decode_step(
+        ctypes.byref(shape), _ptr(q_w), _ptr(q_r), _ptr(k_val), _ptr(gates), _ptr(subkeys),
+        _ptr(bank_in), 1 if shared else 0, _ptr(bank_out), 1 if donate else 0, _ptr(y),
+        _ptr(idx_w), _ptr(wt_w), _ptr(idx_r), _ptr(wt_r), _ptr(workspace), workspace.numel(),
+        _stream_handle(stream, dev))
+    _abi.check(st, "sdm_decode_step")
+    return y, bank_out
+
+
+def last_device_error(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Kernel-side error code of the last call that used `workspace` (0 = none); syncs."""
+    code = ctypes.c_int32(0)
+    st = _abi.load().sdm_last_device_error(_ptr(workspace), workspace.numel(), ctypes.byref(code),
+                                           _stream_handle(stream, workspace.device))
+    if st not in (_abi.SDM_OK, _abi.SDM_ERR_DEVICE):
+        _abi.check(st, "sdm_last_device_error")
+    return int(code.value)
+
+
+def launch_count() -> int:
+    return int(_abi.load().sdm_launch_count())
+
+
+def profile_begin() -> None:
+    _abi.check(_abi.load().sdm_profile_begin(), "sdm_profile_begin")
+
+
+def profile_end() -> dict:
+    """{kernel name: (launches, total ms)} of the launches since profile_begin."""
+    out = _abi.KernelTimes()
+    _abi.check(_abi.load().sdm_profile_end(ctypes.byref(out)), "sdm_profile_end")
+    return {name: (int(out.launches[i]), float(out.ms[i])) for i, name in enumerate(_abi.KERNEL_KINDS)}

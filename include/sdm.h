@@ -1,0 +1,209 @@
+/*
+ * sdm.h - C ABI of the GB300 (sm_103a) Sparse Delta Memory hot path.
+ *
+ * Sparse Delta Memory (SDM) is a sequence mixer that reads from and writes to a
+ * large memory bank addressed by product keys, with gated (forget/input)
+ * delta-rule updates (sparse-delta-memory README, introduction).  This library
+ * runs its data-parallel hot path on one GPU:
+ *
+ *   sdm_write_read   the chunked write/read op over a sequence
+ *                    (CHANGELOG 2.0.0 > Removed: sdm_write_read is the one op;
+ *                     reads happen inside the write/read call)
+ *   sdm_decode_step  the single-token decode step, copying or in place
+ *                    (CHANGELOG 2.0.0 > New: a single-token decode kernel;
+ *                     lumen PR #29 > Donating is a permission)
+ *
+ * What one token of one stream (batch element b, head h) computes, in token order:
+ *   1. factor scores  s_f[a] = <q[f*d_sub:(f+1)*d_sub], K_f[a]>  for q in {q_w, q_r}
+ *      (product-key memory, README > prior ideas);
+ *   2. the exact top-k slots (k = W for q_w, R for q_r) over all factor
+ *      combinations: slot score = the float32 sum of the factor scores, ties to the
+ *      larger rank sum, then the larger first rank, then the second, ...
+ *      (CHANGELOG 2.0.0 > Upgrading from v1; "rank" is a factor's ascending score
+ *      rank, equal factor scores ordered by index);  slot id = mixed radix of the
+ *      factor indices, first factor most significant;
+ *   3. weights w_j = softmax over the selected slot scores (the same for reads, r_j);
+ *   4. gated delta-rule write of the W selected rows of the stream's bank M:
+ *        m_j = alpha M[i_j];  p = sum_j w_j m_j;  M[i_j] <- m_j + beta w_j (v - p)
+ *      with (alpha, beta) = gates[b,t,h] and v = k_val[b,t,h];  the row is rounded to
+ *      the bank type after every token;
+ *   5. the read after the write: y[b,t,h] = sum_j r_j M[i^r_j].
+ * Results do not depend on chunk_size at all (bitwise), which the CHANGELOG allows
+ * ("the chunk size changes outputs only through floating-point rounding").
+ * Outputs, the final bank and the selections are bitwise identical across runs.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, row-major and contiguous, with the
+ *     shapes given below, and 16-byte aligned unless marked otherwise.
+ *   - The caller owns every buffer.  The library allocates no device memory and
+ *     never synchronises the stream, except sdm_last_device_error (it reads back a
+ *     flag) and sdm_profile_end.  All work is enqueued on `stream`.
+ *   - Every argument check runs on the host before any work is enqueued; a call that
+ *     returns an error has enqueued nothing.  sdm_last_error_message() then gives
+ *     the reason.
+ *   - Kernel-side anomalies (a corrupt plan, an out-of-range slot) never fault: the
+ *     kernel skips the access and records a code in the workspace, read back with
+ *     sdm_last_device_error.
+ */
+#ifndef SDM_GB300_H
+#define SDM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SDM_ABI_VERSION 1
+
+/* Compiled limits.  Shapes beyond them are refused with SDM_ERR_UNSUPPORTED. */
+#define SDM_MAX_FACTORS 4          /* product-key factors F                          */
+#define SDM_MAX_FACTOR_DIM 1024    /* sub-keys per factor n_f                        */
+#define SDM_MAX_K 128              /* writes W and reads R per token                 */
+#define SDM_MAX_CANDIDATES 1024    /* position tuples with prod(p_f+1) <= k          */
+#define SDM_MAX_CHUNK 256          /* chunk_size                                     */
+#define SDM_MAX_HEAD_DIM (1 << 20) /* d_v (CHANGELOG 2.0.0 > Behavior changes)       */
+#define SDM_MAX_SUBKEY_DIM 4096    /* d_sub                                          */
+
+typedef struct CUstream_st *sdm_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  SDM_OK = 0,
+  SDM_ERR_INVALID_ARG = 1, /* malformed shape, NULL/misaligned pointer, W or R > N     */
+  SDM_ERR_UNSUPPORTED = 2, /* float16, or a shape beyond the compiled limits           */
+  SDM_ERR_ALIAS = 3,       /* an output overlaps an input it must not overlap          */
+  SDM_ERR_WORKSPACE = 4,   /* workspace NULL, misaligned or smaller than required      */
+  SDM_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed                     */
+  SDM_ERR_DEVICE = 6       /* sdm_last_device_error found a kernel-side error code     */
+} sdm_status;
+
+typedef enum { SDM_F32 = 0, SDM_BF16 = 1, SDM_F16 = 2 /* always refused */ } sdm_dtype;
+
+/* Kernel-side codes written to the workspace flag (see sdm_last_device_error). */
+#define SDM_DEVERR_NONE 0
+#define SDM_DEVERR_SLOT_RANGE 1    /* a selected slot id outside [0, N)                */
+#define SDM_DEVERR_PLAN 2          /* a chunk plan count or row index out of range     */
+
+/*
+ * Shape of one call.  Tensors (row-major, contiguous):
+ *   q_w, q_r  [B, T, H, F*d_sub]   act_dtype   write / read queries
+ *   k_val     [B, T, H, d_v]       act_dtype   values
+ *   gates     [B, T, H, 2]         float32     (alpha = forget, beta = input), in [0, 1]
+ *   subkeys   [H, sum_f n_f, d_sub] act_dtype  factor f at row offset sum_{g<f} n_g
+ *   bank      [B, H, N, d_v]       bank_dtype  N = prod_f n_f slots per head
+ *   y         [B, T, H, d_v]       act_dtype
+ *   idx_w/wt_w [B, T, H, W] int32 / float32, idx_r/wt_r [B, T, H, R]: selected slot
+ *             ids (best first) and their softmax weights.
+ * Field order avoids padding: five int64 then ten int32 (80 bytes).
+ */
+typedef struct {
+  int64_t B, T, H;       /* streams = B*H; T tokens per stream (decode: T == 1)      */
+  int64_t d_sub, d_v;    /* sub-key dim, head (value) dim; d_v % 8 == 0              */
+  int32_t F;             /* number of product-key factors, 1..SDM_MAX_FACTORS         */
+  int32_t factor_dims[SDM_MAX_FACTORS]; /* n_f; entries >= F ignored                 */
+  int32_t W, R;          /* writes / reads per token, 1..min(N, SDM_MAX_K)            */
+  int32_t chunk_size;    /* 1..SDM_MAX_CHUNK; caps the tokens planned together         */
+  int32_t act_dtype;     /* sdm_dtype of q_w, q_r, k_val, subkeys, y                  */
+  int32_t bank_dtype;    /* sdm_dtype of the bank                                     */
+} sdm_shape;
+
+/* Device bytes of workspace sdm_write_read needs for `shape` (16-byte aligned buffer).
+ * Depends only on the shape.  Errors as for sdm_write_read's shape checks. */
+sdm_status sdm_write_read_workspace_size(const sdm_shape *shape, size_t *bytes);
+
+/* Device bytes of workspace sdm_decode_step needs (a few hundred bytes). */
+sdm_status sdm_decode_workspace_size(const sdm_shape *shape, size_t *bytes);
+
+/*
+ * The chunked write/read op (CHANGELOG 2.0.0 > Removed: sdm_write_read), all B*H
+ * streams, T tokens each, in token order.  The bank advances in place
+ * (README usage example: "the bank advances in place").
+ *   bank_init  NULL, or a learned initial table [H, N, d_v] (bank_dtype) that is first
+ *              copied into every stream's bank (the per-call bank copy of a layer
+ *              call, CHANGELOG 2.0.0 > Behavior changes).  Must not overlap `bank`.
+ *   bank       [B, H, N, d_v] in/out.
+ *   y          [B, T, H, d_v] out; must not overlap any input or the bank.
+ *   idx_w, wt_w, idx_r, wt_r  outputs, each NULL or a buffer of the shape above (4-byte
+ *              aligned); NULL ones are kept in the workspace instead.
+ *   workspace  device scratch of >= sdm_write_read_workspace_size bytes; its contents
+ *              need not be initialised and are overwritten.  Calls sharing one
+ *              workspace must be ordered on one stream.
+ * Refusals (nothing enqueued): float16 (UNSUPPORTED; CHANGELOG > Behavior changes);
+ * W or R > N (INVALID); d_v > 2^20 (UNSUPPORTED); limits above (UNSUPPORTED);
+ * NULL/misaligned pointers (INVALID); overlaps (ALIAS); short workspace (WORKSPACE).
+ */
+sdm_status sdm_write_read(const sdm_shape *shape, const void *q_w, const void *q_r,
+                          const void *k_val, const float *gates, const void *subkeys,
+                          const void *bank_init, void *bank, void *y, int32_t *idx_w,
+                          float *wt_w, int32_t *idx_r, float *wt_r, void *workspace,
+                          size_t workspace_bytes, sdm_stream_t stream);
+
+/*
+ * One decode step (shape->T must be 1; chunk_size is ignored) for all B*H streams.
+ * Tensors as above with T = 1.
+ *   bank_in         the state's tables: [B, H, N, d_v], or, with bank_in_shared != 0,
+ *                   one [H, N, d_v] table every stream starts from (a learned initial
+ *                   table; only with donate == 0).
+ *   bank_out        [B, H, N, d_v], receives the successor tables.
+ *   donate != 0     in place: bank_out must equal bank_in (or be NULL); only the W
+ *                   written rows are touched (lumen PR #29 > Donating is a permission).
+ *   donate == 0     copy: bank_out must not overlap bank_in; every row is written
+ *                   (the unselected ones copied).  Both forms run the same arithmetic
+ *                   and give bit-identical y and successor tables.
+ * A decode bank smaller than the configured slots cannot be expressed here: N is
+ * derived from factor_dims (CHANGELOG 2.0.0 > Behavior changes: decoding with a
+ * smaller bank raises).
+ */
+sdm_status sdm_decode_step(const sdm_shape *shape, const void *q_w, const void *q_r,
+                           const void *k_val, const float *gates, const void *subkeys,
+                           const void *bank_in, int bank_in_shared, void *bank_out,
+                           int donate, void *y, int32_t *idx_w, float *wt_w, int32_t *idx_r,
+                           float *wt_r, void *workspace, size_t workspace_bytes,
+                           sdm_stream_t stream);
+
+/* Synchronises `stream`, reads the kernel-side error code of the last call that used
+ * `workspace` into *code (SDM_DEVERR_*), and returns SDM_ERR_DEVICE if it is nonzero. */
+sdm_status sdm_last_device_error(const void *workspace, size_t workspace_bytes,
+                                 int32_t *code, sdm_stream_t stream);
+
+/* Static English name of a status. */
+const char *sdm_status_string(sdm_status status);
+
+/* Reason for the last non-OK status returned on this host thread ("" if none). */
+const char *sdm_last_error_message(void);
+
+/* SDM_ABI_VERSION of the loaded library. */
+int32_t sdm_abi_version(void);
+
+/* Number of kernels this library has launched in this process (monotonic). */
+uint64_t sdm_launch_count(void);
+
+/* Per-kernel timing with CUDA events recorded on the launch stream around each of
+ * this library's launches between sdm_profile_begin and sdm_profile_end.  begin
+ * creates its events on first use (not inside a CUDA-graph capture); end synchronises
+ * the recorded events and returns, per kernel kind, the number of launches and the
+ * summed milliseconds.  Up to 4096 launches are recorded per session. */
+enum {
+  SDM_KERNEL_BANK_COPY = 0,
+  SDM_KERNEL_TOPK = 1,
+  SDM_KERNEL_PLAN_SORT = 2,
+  SDM_KERNEL_PLAN_LINK = 3,
+  SDM_KERNEL_WRITE_READ = 4,
+  SDM_KERNEL_DECODE = 5,
+  SDM_NUM_KERNEL_KINDS = 6
+};
+typedef struct {
+  int64_t launches[SDM_NUM_KERNEL_KINDS];
+  double ms[SDM_NUM_KERNEL_KINDS];
+} sdm_kernel_times;
+sdm_status sdm_profile_begin(void);
+sdm_status sdm_profile_end(sdm_kernel_times *out);
+
+/* Name of a kernel kind ("write_read", ...). */
+const char *sdm_kernel_name(int32_t kind);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDM_GB300_H */

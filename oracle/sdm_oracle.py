@@ -130,23 +130,18 @@ def slot_scores(s_list: list) -> np.ndarray:
     return S
 
 
-def slot_tie_keys(rank_list: list) -> tuple:
-    """Per-slot rank sum and per-factor ranks, laid out like ``slot_scores``."""
-    F = len(rank_list)
+def slot_tie_keys(rank_list: list, slots: np.ndarray) -> tuple:
+    """Rank sum and per-factor ranks of the given slots (slot layout of ``slot_scores``)."""
     dims = [r.shape[0] for r in rank_list]
-    per_factor = []
-    for f in range(F):
-        shape = [1] * F
-        shape[f] = dims[f]
-        per_factor.append(np.broadcast_to(rank_list[f].reshape(shape), dims).reshape(-1))
-    rank_sum = np.zeros_like(per_factor[0])
+    digits = np.unravel_index(np.asarray(slots, dtype=np.int64), dims)   # (a_1, ..., a_F)
+    per_factor = [rank_list[f][digits[f]] for f in range(len(dims))]
+    rank_sum = np.zeros(len(slots), dtype=np.int64)
     for r in per_factor:
         rank_sum = rank_sum + r
     return rank_sum, per_factor
 
 
-def topk_slots(S: np.ndarray, rank_sum: np.ndarray, ranks: list, k: int,
-               prefilter: bool = True) -> np.ndarray:
+def topk_slots(S: np.ndarray, ranks: list, k: int, prefilter: bool = True) -> np.ndarray:
     """Exact top-k slot ids, best first.
 
     Order (CHANGELOG > Upgrading from v1): larger slot score; on equal score the
@@ -161,7 +156,8 @@ def topk_slots(S: np.ndarray, rank_sum: np.ndarray, ranks: list, k: int,
         cand = np.nonzero(S >= kth)[0]
     else:
         cand = np.arange(N)
-    keys = [-r[cand] for r in reversed(ranks)] + [-rank_sum[cand], -S[cand].astype(np.float64)]
+    rank_sum, per_factor = slot_tie_keys(ranks, cand)
+    keys = [-r for r in reversed(per_factor)] + [-rank_sum, -S[cand].astype(np.float64)]
     order = np.lexsort(tuple(keys))             # last key primary, all ascending
     return cand[order[:k]]
 
@@ -179,8 +175,7 @@ def select(q: np.ndarray, subkeys: np.ndarray, factor_dims, d_sub: int, k: int,
     s_list = factor_scores(q, subkeys, factor_dims, d_sub)
     ranks = [factor_ranks(s) for s in s_list]
     S = slot_scores(s_list)
-    rank_sum, per_factor = slot_tie_keys(ranks)
-    idx = topk_slots(S, rank_sum, per_factor, k, prefilter=prefilter)
+    idx = topk_slots(S, ranks, k, prefilter=prefilter)
     w = softmax_weights(S[idx])
     return idx, w, S[idx]
 
@@ -263,7 +258,6 @@ def sdm_write_read(q_w, q_r, k_val, gates, subkeys, bank, *, factor_dims, W: int
     del chunk_size
     q_w, q_r, k_val, gates = _f64(q_w), _f64(q_r), _f64(k_val), _f64(gates)
     subkeys = _f64(subkeys)
-    bank = _f64(bank)
     B, T, H, _ = q_w.shape
     d_sub = subkeys.shape[2]
     if T_limit is not None:
@@ -272,7 +266,7 @@ def sdm_write_read(q_w, q_r, k_val, gates, subkeys, bank, *, factor_dims, W: int
         streams = [(b, h) for b in range(B) for h in range(H)]
     out = {}
     for (b, h) in streams:
-        M = (bank[h] if bank.ndim == 3 else bank[b, h]).copy()
+        M = _f64(bank[h] if bank.ndim == 3 else bank[b, h]).copy()   # one stream at a time
         res = run_stream(M, q_w[b, :T, h], q_r[b, :T, h], k_val[b, :T, h], gates[b, :T, h],
                          subkeys[h], factor_dims=factor_dims, d_sub=d_sub, W=W, R=R,
                          act_dtype=act_dtype, bank_dtype=bank_dtype, prefilter=prefilter)

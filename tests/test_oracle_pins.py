@@ -139,8 +139,7 @@ def test_slot_score_is_float32_sum_left_to_right():
 def _select_from_scores(s_list, k):
     ranks = [oracle.factor_ranks(np.asarray(s, np.float32)) for s in s_list]
     S = oracle.slot_scores([np.asarray(s, np.float32) for s in s_list])
-    rank_sum, per = oracle.slot_tie_keys(ranks)
-    return list(oracle.topk_slots(S, rank_sum, per, k, prefilter=False))
+    return list(oracle.topk_slots(S, ranks, k, prefilter=False))
 
 
 def test_tie_rule_equal_scores_two_factors():
