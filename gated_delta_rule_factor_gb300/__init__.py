@@ -4,7 +4,7 @@ The chunked write/read op and the single-token decode step run as hand-written
 sm_103a CUDA kernels in libsdm_gb300.so behind the C ABI of include/sdm.h.  This
 package is the thin Python binding: ``sdm_write_read`` and ``sdm_decode_step`` take
 torch CUDA tensors and pass their pointers through.  Importing it loads the library
-and fails loudly if it has not been built (``python -m gated_delta_rule_factor_gb300.build``).
+and fails loudly if it has not been built (``python gated_delta_rule_factor_gb300/build.py``).
 """
 
 from . import _abi

@@ -73,7 +73,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     if not os.path.exists(path):
         if not build_if_missing:
             raise ImportError(f"SDM CUDA library not built ({path}); run "
-                              "`python -m gated_delta_rule_factor_gb300.build`")
+                              "`python gated_delta_rule_factor_gb300/build.py`")
         _build.build()
     lib = ctypes.CDLL(path)
     sp = ctypes.POINTER(SdmShape)

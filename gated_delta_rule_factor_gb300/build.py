@@ -1,6 +1,6 @@
 """Build the SDM CUDA library (sm_103a) in-tree: gated_delta_rule_factor_gb300/_build/.
 
-    python -m gated_delta_rule_factor_gb300.build [--force] [--jobs N]
+    python gated_delta_rule_factor_gb300/build.py [--force] [--jobs N] [--ptxas-info]
 
 Each translation unit under csrc/ is compiled by nvcc in parallel, then linked into
 one shared library, libsdm_gb300.so, with the CUDA runtime linked statically (the
