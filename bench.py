@@ -389,13 +389,13 @@ def bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg):
     ws = torch.empty(256, dtype=torch.uint8, device=dev)
     y = torch.empty_like(g["k_val"][:, 0])
     nT = g["q_w"].shape[1]
+    per_step = [tuple(g[k][:, t].contiguous() for k in ("q_w", "q_r", "k_val", "gates")) for t in range(nT)]
 
     def step(i):
         nonlocal state
-        t = i % nT
-        _, state = sdm.sdm_decode_step(g["q_w"][:, t], g["q_r"][:, t], g["k_val"][:, t], g["gates"][:, t],
-                                       g["subkeys"], state, cfg.W, cfg.R, factor_dims=cfg.factor_dims,
-                                       donate=donate, y=y, workspace=ws, stream=stream)
+        _, state = sdm.sdm_decode_step(*per_step[i % nT], g["subkeys"], state, cfg.W, cfg.R,
+                                       factor_dims=cfg.factor_dims, donate=donate, y=y, workspace=ws,
+                                       stream=stream)
 
     for i in range(args.warmup):
         step(i)

@@ -16,7 +16,7 @@ ABI_VERSION = 1
 SDM_OK, SDM_ERR_INVALID_ARG, SDM_ERR_UNSUPPORTED, SDM_ERR_ALIAS, SDM_ERR_WORKSPACE, \
     SDM_ERR_CUDA, SDM_ERR_DEVICE = range(7)
 SDM_F32, SDM_BF16, SDM_F16 = 0, 1, 2
-KERNEL_KINDS = ("bank_copy", "topk", "plan_sort", "plan_link", "write_read", "decode")
+KERNEL_KINDS = ("bank_copy", "score", "select", "plan_sort", "plan_link", "write_read", "decode")
 
 # Every function include/sdm.h declares, in header order.
 EXPORTS = (

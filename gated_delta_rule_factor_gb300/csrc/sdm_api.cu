@@ -14,10 +14,6 @@
 #include "../../include/sdm.h"
 #include "sdm_internal.h"
 
-namespace sdm {
-int64_t topk_scratch_bytes();
-}
-
 using namespace sdm;
 
 namespace {
@@ -304,6 +300,7 @@ int64_t a256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
 struct WsLayout {
   int64_t idx_w, wt_w, idx_r, wt_r;  // selection outputs kept here when the caller passes NULL
+  int64_t scores;                    // factor scores [2, B*T*H, sum n_f] float32
   int64_t uniq, nuniq, written, records;
   int64_t total;
 };
@@ -317,6 +314,9 @@ WsLayout ws_layout(const sdm_shape *sh, const PlanLayout &lay) {
   w.wt_w = o;  o = a256(o + rows * sh->W * 4);
   w.idx_r = o; o = a256(o + rows * sh->R * 4);
   w.wt_r = o;  o = a256(o + rows * sh->R * 4);
+  int64_t ntot = 0;
+  for (int f = 0; f < sh->F && f < SDM_MAX_FACTORS; ++f) ntot += sh->factor_dims[f];
+  w.scores = o; o = a256(o + 2 * rows * ntot * 4);
   w.uniq = o;  o = a256(o + stages * lay.L * 4);
   w.nuniq = o; o = a256(o + stages * 4);
   w.written = o; o = a256(o + stages * lay.L);
@@ -376,9 +376,15 @@ sdm_status sm_count(int *out) {
   return SDM_OK;
 }
 
-int64_t topk_tokens_per_cta(int32_t ntot) {
-  int64_t t = (96 * 1024) / (8 * (int64_t)ntot);
-  return std::max<int64_t>(1, std::min<int64_t>(16, t));
+// The tensor-core scorer takes bfloat16 inputs whose d_sub is a multiple of 64 and whose
+// factor widths are multiples of 16; SDM_SCORE_SIMT=1 forces the CUDA-core scorer.
+bool use_tensor_cores(const Derived &d, const sdm_shape *sh) {
+  if (env_int("SDM_SCORE_SIMT", 0)) return false;
+  int maxnf = 0;
+  for (int f = 0; f < d.g.F; ++f) maxnf = std::max(maxnf, d.g.nf[f]);
+  const int64_t n_tiles = (maxnf + 255) / 256;
+  if (2 * sh->H * d.g.F * n_tiles > 65535) return false;
+  return score_tc_supported(d.g, sh->act_dtype);
 }
 
 }  // namespace
@@ -480,26 +486,35 @@ sdm_status sdm_write_read(const sdm_shape *sh, const void *q_w, const void *q_r,
   int32_t *ir = idx_r ? idx_r : reinterpret_cast<int32_t *>(ws + wl.idx_r);
   float *wr = wt_r ? wt_r : reinterpret_cast<float *>(ws + wl.wt_r);
 
-  // 1. scoring + exact top-k of both queries
+  // 1. factor scores of both queries, then the exact top-k of every row
   int EF, EC;
   sort_widths(d, cl, &EF, &EC);
-  TopkArgs ta{};
-  ta.q[0] = q_w;
-  ta.q[1] = q_r;
-  ta.subkeys = subkeys;
-  ta.idx[0] = iw;
-  ta.idx[1] = ir;
-  ta.wt[0] = ww;
-  ta.wt[1] = wr;
-  ta.err = err;
-  ta.BT = sh->B * sh->T;
-  ta.H = (int32_t)sh->H;
-  ta.tok_per_cta = (int32_t)topk_tokens_per_cta(d.ntot);
-  ta.g = d.g;
-  const int64_t topk_smem = a16((int64_t)2 * ta.tok_per_cta * d.ntot * 4 + (int64_t)(cl.n[0] + cl.n[1]) * 4) +
-                            topk_scratch_bytes();
-  if ((st = run_kernel(SDM_KERNEL_TOPK, cs, "topk",
-                       [&] { return launch_topk(ta, cl, sh->act_dtype, EF, EC, topk_smem, cs); })) != SDM_OK)
+  float *scores = reinterpret_cast<float *>(ws + wl.scores);
+  ScoreArgs sa{};
+  sa.q[0] = q_w;
+  sa.q[1] = q_r;
+  sa.subkeys = subkeys;
+  sa.scores = scores;
+  sa.err = err;
+  sa.BT = sh->B * sh->T;
+  sa.H = (int32_t)sh->H;
+  sa.g = d.g;
+  const bool tc = use_tensor_cores(d, sh);
+  if ((st = run_kernel(SDM_KERNEL_SCORE, cs, tc ? "score_tc" : "score_simt", [&] {
+         return tc ? launch_score_tc(sa, cs) : launch_score_simt(sa, sh->act_dtype, cs);
+       })) != SDM_OK)
+    return st;
+  SelectArgs se{};
+  se.scores = scores;
+  se.idx[0] = iw;
+  se.idx[1] = ir;
+  se.wt[0] = ww;
+  se.wt[1] = wr;
+  se.err = err;
+  se.rows = rows;
+  se.g = d.g;
+  if ((st = run_kernel(SDM_KERNEL_SELECT, cs, "select", [&] { return launch_select(se, cl, EF, EC, sms, cs); })) !=
+      SDM_OK)
     return st;
 
   // 2. chunk plan
@@ -712,7 +727,8 @@ sdm_status sdm_profile_end(sdm_kernel_times *out) {
 const char *sdm_kernel_name(int32_t kind) {
   switch (kind) {
     case SDM_KERNEL_BANK_COPY: return "bank_copy";
-    case SDM_KERNEL_TOPK: return "topk";
+    case SDM_KERNEL_SCORE: return "score";
+    case SDM_KERNEL_SELECT: return "select";
     case SDM_KERNEL_PLAN_SORT: return "plan_sort";
     case SDM_KERNEL_PLAN_LINK: return "plan_link";
     case SDM_KERNEL_WRITE_READ: return "write_read";

@@ -14,11 +14,16 @@
 // belongs to row group j % RG and is accumulated in increasing j; the RG partial sums
 // are combined by an xor butterfly.  All of it is float32 with fixed operation order,
 // so results are bitwise repeatable and independent of how tokens are staged.
+//
+// Rows are fetched kJB at a time per lane (independent loads in flight) because the
+// token chain is latency-bound: one warp walks the tokens of a stream in order.
 #pragma once
 
 #include "sdm_common.cuh"
 
 namespace sdm {
+
+constexpr int kJB = 8;  // rows in flight per lane
 
 template <typename BANK, int NCG, class SrcRow, class DstRow>
 __device__ __forceinline__ void delta_write_cols(int W, const float *w, float alpha, float beta,
@@ -29,12 +34,22 @@ __device__ __forceinline__ void delta_write_cols(int W, const float *w, float al
   float acc[VEC];
 #pragma unroll
   for (int c = 0; c < VEC; ++c) acc[c] = 0.0f;
-  for (int j = rg; j < W; j += RG) {
-    float r[VEC];
-    load_vec16<BANK>(src(j), r);
-    const float wj = w[j];
+  for (int j0 = rg; j0 < W; j0 += RG * kJB) {
+    float r[kJB][VEC];
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) acc[c] = __fmaf_rn(wj, __fmul_rn(alpha, r[c]), acc[c]);
+    for (int b = 0; b < kJB; ++b) {
+      const int j = j0 + b * RG;
+      if (j < W) load_vec16<BANK>(src(j), r[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < kJB; ++b) {
+      const int j = j0 + b * RG;
+      if (j < W) {
+        const float wj = w[j];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) acc[c] = __fmaf_rn(wj, __fmul_rn(alpha, r[b][c]), acc[c]);
+      }
+    }
   }
 #pragma unroll
   for (int o = NCG; o < 32; o <<= 1)
@@ -43,13 +58,23 @@ __device__ __forceinline__ void delta_write_cols(int W, const float *w, float al
   float d[VEC];
 #pragma unroll
   for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], acc[c]));
-  for (int j = rg; j < W; j += RG) {
-    float r[VEC];
-    load_vec16<BANK>(src(j), r);
-    const float wj = w[j];
+  for (int j0 = rg; j0 < W; j0 += RG * kJB) {
+    float r[kJB][VEC];
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) r[c] = __fmaf_rn(wj, d[c], __fmul_rn(alpha, r[c]));
-    store_vec16<BANK>(dst(j), r);
+    for (int b = 0; b < kJB; ++b) {
+      const int j = j0 + b * RG;
+      if (j < W) load_vec16<BANK>(src(j), r[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < kJB; ++b) {
+      const int j = j0 + b * RG;
+      if (j < W) {
+        const float wj = w[j];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) r[b][c] = __fmaf_rn(wj, d[c], __fmul_rn(alpha, r[b][c]));
+        store_vec16<BANK>(dst(j), r[b]);
+      }
+    }
   }
 }
 
@@ -60,12 +85,22 @@ __device__ __forceinline__ void weighted_read_cols(int R, const float *r, SrcRow
   const int rg = (threadIdx.x & 31) / NCG;
 #pragma unroll
   for (int c = 0; c < VEC; ++c) y[c] = 0.0f;
-  for (int j = rg; j < R; j += RG) {
-    float m[VEC];
-    load_vec16<BANK>(src(j), m);
-    const float rj = r[j];
+  for (int j0 = rg; j0 < R; j0 += RG * kJB) {
+    float m[kJB][VEC];
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) y[c] = __fmaf_rn(rj, m[c], y[c]);
+    for (int b = 0; b < kJB; ++b) {
+      const int j = j0 + b * RG;
+      if (j < R) load_vec16<BANK>(src(j), m[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < kJB; ++b) {
+      const int j = j0 + b * RG;
+      if (j < R) {
+        const float rj = r[j];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) y[c] = __fmaf_rn(rj, m[b][c], y[c]);
+      }
+    }
   }
 #pragma unroll
   for (int o = NCG; o < 32; o <<= 1)

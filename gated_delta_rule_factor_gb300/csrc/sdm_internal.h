@@ -27,15 +27,24 @@ struct KeyGeometry {
   int32_t kf[2][SDM_MAX_FACTORS];    // min(k, n_f)
 };
 
-struct TopkArgs {
+// Factor scores of every query row: scores[qsel][(b*T + t)*H + h][ntot] (float32).
+struct ScoreArgs {
   const void *q[2];      // q_w, q_r [BT, H, F*d_sub]
   const void *subkeys;   // [H, ntot, d_sub]
-  int32_t *idx[2];       // [BT, H, k]
-  float *wt[2];
+  float *scores;         // [2, BT*H, ntot]
   int32_t *err;
   int64_t BT;            // B*T tokens
   int32_t H;
-  int32_t tok_per_cta;
+  KeyGeometry g;
+};
+
+// Exact top-k of every query row from its factor scores.
+struct SelectArgs {
+  const float *scores;   // [2, rows, ntot]
+  int32_t *idx[2];       // [rows, k]
+  float *wt[2];
+  int32_t *err;
+  int64_t rows;          // B*T*H rows per query kind
   KeyGeometry g;
 };
 
@@ -118,8 +127,11 @@ struct WriteReadConfig {
 };
 
 // Launchers, defined next to their kernels.  Each returns the launch error.
-cudaError_t launch_topk(const TopkArgs &a, const CandidateList &cl, int act_dtype, int EF,
-                        int EC, int64_t smem_bytes, cudaStream_t st);
+cudaError_t launch_score_simt(const ScoreArgs &a, int act_dtype, cudaStream_t st);
+cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t st);   // bf16, tensor cores
+bool score_tc_supported(const KeyGeometry &g, int act_dtype);
+cudaError_t launch_select(const SelectArgs &a, const CandidateList &cl, int EF, int EC,
+                          int sm_count, cudaStream_t st);
 cudaError_t launch_bank_copy(const BankCopyArgs &a, int sm_count, cudaStream_t st);
 cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int sort_pow2,
                              cudaStream_t st);

@@ -8,10 +8,12 @@
 // (sdm_plan.cu) lists the distinct rows of each stage.
 //
 // Warp roles (one CTA):
-//   warp 0      compute: the tokens of the current stage on the shared-memory rows;
-//   warps 1..4  loaders: write back the previous stage's dirty rows, then fetch the next
-//               stage's rows (cp.async, 16 B per request) and token data, and the stage
-//               record after it.
+//   compute warps (1 or 2, each owning up to four 16-byte column groups of the slice):
+//               the tokens of the current stage on the shared-memory rows;
+//   4 loader warps: write back the previous stage's dirty rows, then fetch the next
+//               stage's rows (cp.async, 16 B per request, one row slice per group of
+//               lanes so that every request batch covers whole 128-byte lines) and token
+//               data, and the stage record after it.
 // Two row buffers alternate between stages; rows shared by consecutive stages are
 // copied across buffers instead of re-read, because the bank copy may be stale.  Stage
 // records use three buffers (in use / rows being fetched / record being fetched).
@@ -41,15 +43,24 @@ __host__ __device__ inline TokLayout tok_layout(int G, int W, int R, int CW, int
   return t;
 }
 
+template <typename BANK, int CW>
+struct WrGeometry {
+  static constexpr int VEC = Vec16<BANK>::N;          // elements per 16 B
+  static constexpr int NCGT = CW / VEC;               // 16-byte column groups of the slice
+  static constexpr int NCG = NCGT < 4 ? NCGT : 4;     // column groups per compute warp
+  static constexpr int NCW = NCGT / NCG;              // compute warps
+  static constexpr int NTHR = 32 * (NCW + kLoaderWarps);
+};
+
 template <typename BANK, typename ACT, int CW>
-__global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
+__global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
     write_read_kernel(const __grid_constant__ WriteReadArgs a) {
-  constexpr int VEC = Vec16<BANK>::N;                 // elements per 16 B
-  constexpr int NCG = CW / VEC;                       // 16-byte column groups
-  static_assert(NCG >= 1 && NCG <= 8 && (NCG & (NCG - 1)) == 0, "column slice");
+  using Geo = WrGeometry<BANK, CW>;
+  constexpr int VEC = Geo::VEC, NCG = Geo::NCG, NCW = Geo::NCW, NTHR = Geo::NTHR;
+  static_assert(Geo::NCGT >= 1 && Geo::NCGT <= 8 && (Geo::NCGT & (Geo::NCGT - 1)) == 0, "column slice");
   constexpr int RB = CW * (int)sizeof(BANK);          // row slice bytes in smem
   constexpr int CPR = RB / 16;                        // 16-byte chunks per row slice
-  constexpr int NTHR = 32 * (1 + kLoaderWarps);
+  constexpr int GRP = kLoaderThreads / CPR;           // rows handled per loader pass
 
   extern __shared__ __align__(16) unsigned char smem[];
   const PlanLayout &lay = a.lay;
@@ -60,6 +71,7 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
   const int64_t b = s / a.H, h = s % a.H;
   const int64_t c0 = (int64_t)slice * CW;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool is_loader = warp >= NCW;
 
   unsigned char *rowbuf[2] = {smem, smem + (int64_t)L * RB};
   unsigned char *plans = smem + 2 * (int64_t)L * RB;
@@ -77,8 +89,9 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
            hdr[3] >= 0 && hdr[3] <= L;
   };
 
-  // ---- loader helpers (threads of warps 1..4)
-  const int ltid = tid - 32;
+  // ---- loader helpers (threads of the loader warps)
+  const int ltid = tid - 32 * NCW;
+  const int sub = ltid % CPR, grp = ltid / CPR;       // chunk of a row, row group
   auto fetch_record = [&](int g) {
     const unsigned char *src = records + (int64_t)g * lay.rec_bytes;
     unsigned char *dst = plan_of(g);
@@ -90,17 +103,16 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
     const int n_load = hdr_ok(hdr) ? hdr[1] : 0;
     const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
     const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
-    unsigned char *dst = rowbuf[g & 1];
-    for (int i = ltid; i < n_load * CPR; i += kLoaderThreads) {
-      const int e = i / CPR, c = i % CPR;
+    unsigned char *dst = rowbuf[g & 1] + sub * 16;
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0) + sub * 16;
+    for (int e = grp; e < n_load; e += GRP) {
       const int32_t slot = load_slot[e];
       const int u = load_u[e];
       if (u >= L || slot < 0 || slot >= a.N) {
         raise_error(a.err, SDM_DEVERR_PLAN);
         continue;
       }
-      cp_async16(dst + (int64_t)u * RB + c * 16,
-                 reinterpret_cast<const unsigned char *>(bank + (int64_t)slot * a.d_v + c0) + c * 16);
+      cp_async16(dst + (int64_t)u * RB, src + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK));
     }
     // token data of the stage
     const int64_t t0 = (int64_t)g * G;
@@ -110,8 +122,8 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
     for (int i = ltid; i < nt * WR; i += kLoaderThreads) {
       const int t = i / WR, j = i % WR;
       const int64_t row = (b * a.T + t0 + t) * a.H + h;
-      const float *src = (j < W) ? a.wt[0] + row * W + j : a.wt[1] + row * R + (j - W);
-      cp_async4(wts + i, src);
+      const float *src_w = (j < W) ? a.wt[0] + row * W + j : a.wt[1] + row * R + (j - W);
+      cp_async4(wts + i, src_w);
     }
     float *gt = reinterpret_cast<float *>(tb + tl.gates);
     for (int i = ltid; i < nt; i += kLoaderThreads) {
@@ -127,28 +139,28 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
                  reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
     }
   };
-  auto write_back = [&](int g, int t_begin, int t_stride) {
+  auto write_back = [&](int g, int row0, int row_step, int chunk) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
     const int n_wb = hdr_ok(hdr) ? hdr[3] : 0;
     const int32_t *wb_slot = reinterpret_cast<const int32_t *>(rec + lay.off_wb_slot);
     const uint16_t *wb_u = reinterpret_cast<const uint16_t *>(rec + lay.off_wb_u);
-    const unsigned char *src = rowbuf[g & 1];
-    for (int i = t_begin; i < n_wb * CPR; i += t_stride) {
-      const int e = i / CPR, c = i % CPR;
+    const unsigned char *src = rowbuf[g & 1] + chunk * 16;
+    unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + chunk * 16;
+    for (int e = row0; e < n_wb; e += row_step) {
       const int32_t slot = wb_slot[e];
       const int u = wb_u[e];
       if (u >= L || slot < 0 || slot >= a.N) {
         raise_error(a.err, SDM_DEVERR_PLAN);
         continue;
       }
-      const uint4 val = *reinterpret_cast<const uint4 *>(src + (int64_t)u * RB + c * 16);
-      *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(bank + (int64_t)slot * a.d_v + c0) + c * 16) = val;
+      *reinterpret_cast<uint4 *>(dst + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK)) =
+          *reinterpret_cast<const uint4 *>(src + (int64_t)u * RB);
     }
   };
 
   // ---- prologue: record 0, then stage 0 and record 1
-  if (warp >= 1) {
+  if (is_loader) {
     fetch_record(0);
     cp_async_commit();
     cp_async_wait_all();
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
   }
 
   for (int g = 0; g < S; ++g) {
-    if (warp >= 1) cp_async_wait_all();
+    if (is_loader) cp_async_wait_all();
     __syncthreads();                                             // stage g resident
     {
       const unsigned char *rec = plan_of(g);
@@ -183,16 +195,16 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
     }
     __syncthreads();                                             // carries in place
 
-    if (warp == 0) {
-      // ---- compute: tokens of stage g in order
+    if (!is_loader) {
+      // ---- compute: tokens of stage g in order; warp w owns column groups [w*NCG, w*NCG+NCG)
       const unsigned char *rec = plan_of(g);
       const uint16_t *refmap = reinterpret_cast<const uint16_t *>(rec + lay.off_refmap);
       const unsigned char *tb = tokbuf[g & 1];
       const float *wts = reinterpret_cast<const float *>(tb + tl.wts);
       const float *gt = reinterpret_cast<const float *>(tb + tl.gates);
       const ACT *vv = reinterpret_cast<const ACT *>(tb + tl.v);
-      unsigned char *rows = rowbuf[g & 1];
-      const int cg = lane % NCG;
+      const int cg = warp * NCG + lane % NCG;                 // column group in the slice
+      unsigned char *rows = rowbuf[g & 1] + cg * 16;
       const int64_t t0 = (int64_t)g * G;
       const int nt = (int)min((int64_t)G, a.T - t0);
       for (int t = 0; t < nt; ++t) {
@@ -201,7 +213,7 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
         auto row_ptr = [&](int j) -> BANK * {
           int u = rm[j];
           if (u >= L) u = 0;                           // plan_sort never emits these
-          return reinterpret_cast<BANK *>(rows + (int64_t)u * RB) + cg * VEC;
+          return reinterpret_cast<BANK *>(rows + (int64_t)u * RB);
         };
         auto wrow = [&](int j) { return row_ptr(j); };
         auto rrow = [&](int j) { return row_ptr(W + j); };
@@ -219,7 +231,7 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
       }
     } else {
       // ---- loaders: retire stage g-1, fetch stage g+1 and record g+2
-      if (g >= 1) write_back(g - 1, ltid, kLoaderThreads);
+      if (g >= 1) write_back(g - 1, grp, GRP, sub);
       named_barrier(1, kLoaderThreads);
       if (g + 1 < S) fetch_stage(g + 1);
       if (g + 2 < S) fetch_record(g + 2);
@@ -227,24 +239,24 @@ __global__ void __launch_bounds__(32 * (1 + kLoaderWarps))
     }
   }
   __syncthreads();
-  if (S > 0) write_back(S - 1, tid, NTHR);
+  if (S > 0) write_back(S - 1, tid / CPR, NTHR / CPR, tid % CPR);
 }
 
 template <typename BANK, typename ACT>
 cudaError_t launch_wr_t(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem, cudaStream_t st) {
   dim3 grid((unsigned)a.slices, (unsigned)streams);
-  auto go = [&](auto kern) -> cudaError_t {
+  auto go = [&](auto kern, int threads) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 32 * (1 + kLoaderWarps), smem, st>>>(a);
+    kern<<<grid, threads, smem, st>>>(a);
     return cudaGetLastError();
   };
   constexpr int V = Vec16<BANK>::N;
   switch (CW / V) {
-    case 1: return go(write_read_kernel<BANK, ACT, V * 1>);
-    case 2: return go(write_read_kernel<BANK, ACT, V * 2>);
-    case 4: return go(write_read_kernel<BANK, ACT, V * 4>);
-    case 8: return go(write_read_kernel<BANK, ACT, V * 8>);
+    case 1: return go(write_read_kernel<BANK, ACT, V * 1>, WrGeometry<BANK, V * 1>::NTHR);
+    case 2: return go(write_read_kernel<BANK, ACT, V * 2>, WrGeometry<BANK, V * 2>::NTHR);
+    case 4: return go(write_read_kernel<BANK, ACT, V * 4>, WrGeometry<BANK, V * 4>::NTHR);
+    case 8: return go(write_read_kernel<BANK, ACT, V * 8>, WrGeometry<BANK, V * 8>::NTHR);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -84,6 +84,7 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1, SDM_F16 = 2 /* always refused */ } sdm
 #define SDM_DEVERR_NONE 0
 #define SDM_DEVERR_SLOT_RANGE 1    /* a selected slot id outside [0, N)                */
 #define SDM_DEVERR_PLAN 2          /* a chunk plan count or row index out of range     */
+#define SDM_DEVERR_TIMEOUT 3       /* a bounded wait inside a kernel gave up             */
 
 /*
  * Shape of one call.  Tensors (row-major, contiguous):
@@ -186,12 +187,13 @@ uint64_t sdm_launch_count(void);
  * summed milliseconds.  Up to 4096 launches are recorded per session. */
 enum {
   SDM_KERNEL_BANK_COPY = 0,
-  SDM_KERNEL_TOPK = 1,
-  SDM_KERNEL_PLAN_SORT = 2,
-  SDM_KERNEL_PLAN_LINK = 3,
-  SDM_KERNEL_WRITE_READ = 4,
-  SDM_KERNEL_DECODE = 5,
-  SDM_NUM_KERNEL_KINDS = 6
+  SDM_KERNEL_SCORE = 1,      /* factor scores (tensor cores for bf16, else CUDA cores) */
+  SDM_KERNEL_SELECT = 2,     /* exact product-key top-k and weights                   */
+  SDM_KERNEL_PLAN_SORT = 3,
+  SDM_KERNEL_PLAN_LINK = 4,
+  SDM_KERNEL_WRITE_READ = 5,
+  SDM_KERNEL_DECODE = 6,
+  SDM_NUM_KERNEL_KINDS = 7
 };
 typedef struct {
   int64_t launches[SDM_NUM_KERNEL_KINDS];

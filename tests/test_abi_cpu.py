@@ -63,7 +63,7 @@ def test_status_strings(lib):
     for s in range(7):
         assert lib.sdm_status_string(s)
     assert lib.sdm_status_string(99) == b"unknown status"
-    assert lib.sdm_kernel_name(4) == b"write_read"
+    assert lib.sdm_kernel_name(5) == b"write_read"
 
 
 def shape(**kw):

@@ -107,8 +107,8 @@ def test_launch_count_and_kernel_timing(sdm):
         sdm.sdm_write_read(g["q_w"], g["q_r"], g["k_val"], g["gates"], g["subkeys"], bank, 64, 8, 8,
                            factor_dims=cfg.factor_dims, bank_init=g["bank_init"])
     times = sdm.profile_end()
-    assert sdm.launch_count() - before == 15    # copy, top-k, 2 plan kernels, write/read
-    for k in ("bank_copy", "topk", "plan_sort", "plan_link", "write_read"):
+    assert sdm.launch_count() - before == 18    # copy, score, select, 2 plan kernels, write/read
+    for k in ("bank_copy", "score", "select", "plan_sort", "plan_link", "write_read"):
         assert times[k][0] == 3 and times[k][1] > 0
 
 
@@ -128,14 +128,18 @@ def test_non_default_stream(sdm):
 
 # --------------------------------------------------------------------------- decode
 
+def _step_inputs(g, t):
+    """Token t of every stream, as contiguous [B, H, ...] tensors."""
+    return tuple(g[k][:, t].contiguous() for k in ("q_w", "q_r", "k_val", "gates"))
+
+
 def _decode_steps(sdm, cfg, d, steps, donate):
     g = to_device(d)
     state = g["bank"].clone()
     ys = []
     for t in range(steps):
-        y, new = sdm.sdm_decode_step(g["q_w"][:, t], g["q_r"][:, t], g["k_val"][:, t], g["gates"][:, t],
-                                     g["subkeys"], state, cfg.W, cfg.R, factor_dims=cfg.factor_dims,
-                                     donate=donate)
+        y, new = sdm.sdm_decode_step(*_step_inputs(g, t), g["subkeys"], state, cfg.W, cfg.R,
+                                     factor_dims=cfg.factor_dims, donate=donate)
         assert (new.data_ptr() == state.data_ptr()) == donate   # in place exactly when donating
         ys.append(y.clone())
         state = new
@@ -157,12 +161,11 @@ def test_decode_copy_leaves_the_old_state_and_donate_reuses_it(sdm):
     g = to_device(d)
     bank = g["bank"].clone()
     keep = bank.clone()
-    y, new = sdm.sdm_decode_step(g["q_w"][:, 0], g["q_r"][:, 0], g["k_val"][:, 0], g["gates"][:, 0],
-                                 g["subkeys"], bank, cfg.W, cfg.R, factor_dims=cfg.factor_dims)
+    y, new = sdm.sdm_decode_step(*_step_inputs(g, 0), g["subkeys"], bank, cfg.W, cfg.R,
+                                 factor_dims=cfg.factor_dims)
     assert new.data_ptr() != bank.data_ptr() and torch.equal(bank, keep)
-    y2, same = sdm.sdm_decode_step(g["q_w"][:, 0], g["q_r"][:, 0], g["k_val"][:, 0], g["gates"][:, 0],
-                                   g["subkeys"], bank, cfg.W, cfg.R, factor_dims=cfg.factor_dims,
-                                   donate=True)
+    y2, same = sdm.sdm_decode_step(*_step_inputs(g, 0), g["subkeys"], bank, cfg.W, cfg.R,
+                                   factor_dims=cfg.factor_dims, donate=True)
     assert same.data_ptr() == bank.data_ptr()
     assert torch.equal(same, new) and torch.equal(y, y2)
     assert not torch.equal(bank, keep)              # the predecessor really was overwritten
@@ -176,9 +179,8 @@ def test_decode_from_a_learned_table_never_writes_it(sdm):
     table_keep = table.clone()
     state = table.unsqueeze(0).expand(cfg.B, *table.shape)   # init_state's broadcast
     for t in range(3):
-        y, state = sdm.sdm_decode_step(g["q_w"][:, t], g["q_r"][:, t], g["k_val"][:, t], g["gates"][:, t],
-                                       g["subkeys"], state, cfg.W, cfg.R, factor_dims=cfg.factor_dims,
-                                       donate=True)
+        y, state = sdm.sdm_decode_step(*_step_inputs(g, t), g["subkeys"], state, cfg.W, cfg.R,
+                                       factor_dims=cfg.factor_dims, donate=True)
     assert torch.equal(table, table_keep)
     # and the result equals stepping from materialised tables
     y_ref, b_ref = _decode_steps(sdm, cfg, d, 3, donate=False)
