@@ -32,7 +32,6 @@ constexpr int kTcK = 64;          // bf16 per k-block = one 128-byte swizzle row
 constexpr int kTcStages = 4;
 constexpr int kTcMaxN = 256;
 constexpr int kTcThreads = 128;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // give up on an mbarrier after 2 s
 
 struct TcArgs {
   CUtensorMap tq[2];   // q_w, q_r viewed as [BT rows][H*F*d_sub] bf16
@@ -45,37 +44,6 @@ struct TcArgs {
   int32_t n_tile;      // MMA N (multiple of 16, <= 256)
   int32_t n_tiles;     // N tiles per factor (max over factors)
 };
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-  return t;
-}
-
-// Bounded wait for the phase with the given parity; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  const uint32_t addr = smem_addr(bar);
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 0;; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if ((i & 255) == 255 && global_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int32_t x, int32_t y, uint64_t *bar) {
   asm volatile(
@@ -166,7 +134,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
     }
     mbar_init(done, 1);
     *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    mbar_init_fence();
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(tmem_slot)),

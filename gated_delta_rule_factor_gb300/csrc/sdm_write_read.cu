@@ -10,10 +10,9 @@
 // Warp roles (one CTA):
 //   compute warps (1 or 2, each owning up to four 16-byte column groups of the slice):
 //               the tokens of the current stage on the shared-memory rows;
-//   4 loader warps: write back the previous stage's dirty rows, then fetch the next
-//               stage's rows (cp.async, 16 B per request, one row slice per group of
-//               lanes so that every request batch covers whole 128-byte lines) and token
-//               data, and the stage record after it.
+//   4 loader warps: fetch the next stage's rows (one bulk copy per row slice, completing
+//               on an mbarrier), its token data (cp.async) and the stage record after it.
+// After each stage every thread writes the stage's dirty rows back to the bank.
 // Two row buffers alternate between stages; rows shared by consecutive stages are
 // copied across buffers instead of re-read, because the bank copy may be stale.  Stage
 // records use three buffers (in use / rows being fetched / record being fetched).
@@ -60,7 +59,6 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
   static_assert(Geo::NCGT >= 1 && Geo::NCGT <= 8 && (Geo::NCGT & (Geo::NCGT - 1)) == 0, "column slice");
   constexpr int RB = CW * (int)sizeof(BANK);          // row slice bytes in smem
   constexpr int CPR = RB / 16;                        // 16-byte chunks per row slice
-  constexpr int GRP = kLoaderThreads / CPR;           // rows handled per loader pass
 
   extern __shared__ __align__(16) unsigned char smem[];
   const PlanLayout &lay = a.lay;
@@ -89,32 +87,40 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
            hdr[3] >= 0 && hdr[3] <= L;
   };
 
+  uint64_t *full = reinterpret_cast<uint64_t *>(tokbuf[1] + tl.bytes);   // [2], one per row buffer
+
   // ---- loader helpers (threads of the loader warps)
   const int ltid = tid - 32 * NCW;
-  const int sub = ltid % CPR, grp = ltid / CPR;       // chunk of a row, row group
   auto fetch_record = [&](int g) {
     const unsigned char *src = records + (int64_t)g * lay.rec_bytes;
     unsigned char *dst = plan_of(g);
     for (int64_t i = ltid; i < lay.rec_bytes / 16; i += kLoaderThreads) cp_async16(dst + i * 16, src + i * 16);
   };
-  auto fetch_stage = [&](int g) {
+  // Rows of stage g: one bulk copy per row slice, completing on full[g & 1].
+  auto fetch_rows = [&](int g) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
     const int n_load = hdr_ok(hdr) ? hdr[1] : 0;
     const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
     const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
-    unsigned char *dst = rowbuf[g & 1] + sub * 16;
-    const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0) + sub * 16;
-    for (int e = grp; e < n_load; e += GRP) {
-      const int32_t slot = load_slot[e];
-      const int u = load_u[e];
+    unsigned char *dst = rowbuf[g & 1];
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0);
+    uint64_t *bar = &full[g & 1];
+    if (ltid == 0) mbar_expect_tx(bar, (uint32_t)(n_load * RB));
+#pragma unroll 4
+    for (int e = ltid; e < n_load; e += kLoaderThreads) {
+      int32_t slot = load_slot[e];
+      int u = load_u[e];
       if (u >= L || slot < 0 || slot >= a.N) {
+        // corrupt plan: flag it and still deliver the counted bytes, inside the buffer
         raise_error(a.err, SDM_DEVERR_PLAN);
-        continue;
+        u = 0;
+        slot = 0;
       }
-      cp_async16(dst + (int64_t)u * RB, src + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK));
+      bulk_load(dst + (int64_t)u * RB, src + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK), RB, bar);
     }
-    // token data of the stage
+  };
+  auto fetch_tokens = [&](int g) {
     const int64_t t0 = (int64_t)g * G;
     const int nt = (int)min((int64_t)G, a.T - t0);
     unsigned char *tb = tokbuf[g & 1];
@@ -139,15 +145,18 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
                  reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
     }
   };
-  auto write_back = [&](int g, int row0, int row_step, int chunk) {
+  // Dirty rows of stage g back to the bank, by every thread (CPR lanes per row).
+  auto write_back = [&](int g) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
     const int n_wb = hdr_ok(hdr) ? hdr[3] : 0;
     const int32_t *wb_slot = reinterpret_cast<const int32_t *>(rec + lay.off_wb_slot);
     const uint16_t *wb_u = reinterpret_cast<const uint16_t *>(rec + lay.off_wb_u);
+    const int chunk = tid % CPR;
     const unsigned char *src = rowbuf[g & 1] + chunk * 16;
     unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + chunk * 16;
-    for (int e = row0; e < n_wb; e += row_step) {
+#pragma unroll 4
+    for (int e = tid / CPR; e < n_wb; e += NTHR / CPR) {
       const int32_t slot = wb_slot[e];
       const int u = wb_u[e];
       if (u >= L || slot < 0 || slot >= a.N) {
@@ -159,19 +168,32 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
     }
   };
 
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+
   // ---- prologue: record 0, then stage 0 and record 1
   if (is_loader) {
     fetch_record(0);
     cp_async_commit();
     cp_async_wait_all();
     named_barrier(1, kLoaderThreads);
-    fetch_stage(0);
+    fetch_rows(0);
+    fetch_tokens(0);
     if (S > 1) fetch_record(1);
     cp_async_commit();
   }
 
+  bool failed = false;
   for (int g = 0; g < S; ++g) {
     if (is_loader) cp_async_wait_all();
+    if (!failed && !mbar_wait(&full[g & 1], (g >> 1) & 1)) {
+      failed = true;
+      raise_error(a.err, SDM_DEVERR_TIMEOUT);
+    }
     __syncthreads();                                             // stage g resident
     {
       const unsigned char *rec = plan_of(g);
@@ -193,6 +215,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
             *reinterpret_cast<const uint4 *>(from + (int64_t)src * RB + c * 16);
       }
     }
+    fence_proxy_async_shared();                                  // before bulk copies reuse the buffer
     __syncthreads();                                             // carries in place
 
     if (!is_loader) {
@@ -229,17 +252,21 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
         }
         __syncwarp();
       }
+      fence_proxy_async_shared();
     } else {
-      // ---- loaders: retire stage g-1, fetch stage g+1 and record g+2
-      if (g >= 1) write_back(g - 1, grp, GRP, sub);
-      named_barrier(1, kLoaderThreads);
-      if (g + 1 < S) fetch_stage(g + 1);
+      // ---- loaders: fetch stage g+1 (its rows are not in stage g, and stage g-1's
+      // write-back finished before the barriers above) and record g+2
+      if (g + 1 < S) {
+        fetch_rows(g + 1);
+        fetch_tokens(g + 1);
+      }
       if (g + 2 < S) fetch_record(g + 2);
       cp_async_commit();
     }
+    __syncthreads();                                             // stage g computed
+    write_back(g);
+    fence_proxy_async_global();                                  // before later bulk reads of these rows
   }
-  __syncthreads();
-  if (S > 0) write_back(S - 1, tid / CPR, NTHR / CPR, tid % CPR);
 }
 
 template <typename BANK, typename ACT>
@@ -282,7 +309,7 @@ int64_t write_read_smem_bytes(int CW, int bank_elem, int act_elem, int G, int W,
                               int64_t rec_bytes) {
   const int64_t L = (int64_t)G * (W + R);
   const TokLayout t = tok_layout(G, W, R, CW, act_elem);
-  return 2 * L * CW * bank_elem + 3 * rec_bytes + 2 * t.bytes;
+  return 2 * L * CW * bank_elem + 3 * rec_bytes + 2 * t.bytes + 64;   // + 2 mbarriers
 }
 
 cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_dtype,
