@@ -214,6 +214,7 @@ PlanLayout plan_layout(int G, int W, int R, int64_t T) {
   p.off_wb_slot = o;   o = a16(o + 4 * L);
   p.off_wb_u = o;      o = a16(o + 2 * L);
   p.off_refmap = o;    o = a16(o + 2 * L);
+  p.off_tokflag = o;   o = a16(o + G);
   p.rec_bytes = o;
   return p;
 }
@@ -555,6 +556,7 @@ sdm_status sdm_write_read(const sdm_shape *sh, const void *q_w, const void *q_r,
   wa.W = sh->W;
   wa.R = sh->R;
   wa.slices = (int32_t)(sh->d_v / wc.CW);
+  wa.tok_bulk = (sh->W % 4 == 0 && sh->R % 4 == 0 && aligned(ww, 16) && aligned(wr, 16)) ? 1 : 0;
   wa.lay = wc.lay;
   if ((st = run_kernel(SDM_KERNEL_WRITE_READ, cs, "write_read", [&] {
          return launch_write_read(wa, streams, sh->bank_dtype, sh->act_dtype, wc.CW, wc.smem, cs);

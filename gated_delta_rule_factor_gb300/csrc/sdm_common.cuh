@@ -291,6 +291,16 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, 
       : "memory");
 }
 
+// Shared -> global bulk copy in the calling thread's current bulk group.
+__device__ __forceinline__ void bulk_store(void *dst_gmem, const void *src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst_gmem),
+               "r"(smem_addr(src_smem)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Waits until this thread's bulk stores are complete (their writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // Orders this thread's earlier generic-proxy accesses before later async-proxy (bulk
 // copy / TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_shared() {

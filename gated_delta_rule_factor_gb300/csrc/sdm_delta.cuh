@@ -25,6 +25,14 @@ namespace sdm {
 
 constexpr int kJB = 8;  // rows in flight per lane
 
+// 16-byte raw row chunk <-> float32 lanes.
+template <typename BANK>
+__device__ __forceinline__ void unpack16(const uint4 &u, float (&out)[Vec16<BANK>::N]) {
+  const BANK *e = reinterpret_cast<const BANK *>(&u);
+#pragma unroll
+  for (int i = 0; i < Vec16<BANK>::N; ++i) out[i] = to_f32(e[i]);
+}
+
 template <typename BANK, int NCG, class SrcRow, class DstRow>
 __device__ __forceinline__ void delta_write_cols(int W, const float *w, float alpha, float beta,
                                                  const float (&v)[Vec16<BANK>::N], SrcRow src,
@@ -35,19 +43,21 @@ __device__ __forceinline__ void delta_write_cols(int W, const float *w, float al
 #pragma unroll
   for (int c = 0; c < VEC; ++c) acc[c] = 0.0f;
   for (int j0 = rg; j0 < W; j0 += RG * kJB) {
-    float r[kJB][VEC];
+    uint4 raw[kJB];
 #pragma unroll
     for (int b = 0; b < kJB; ++b) {
       const int j = j0 + b * RG;
-      if (j < W) load_vec16<BANK>(src(j), r[b]);
+      if (j < W) raw[b] = *reinterpret_cast<const uint4 *>(src(j));
     }
 #pragma unroll
     for (int b = 0; b < kJB; ++b) {
       const int j = j0 + b * RG;
       if (j < W) {
         const float wj = w[j];
+        float r[VEC];
+        unpack16<BANK>(raw[b], r);
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) acc[c] = __fmaf_rn(wj, __fmul_rn(alpha, r[b][c]), acc[c]);
+        for (int c = 0; c < VEC; ++c) acc[c] = __fmaf_rn(wj, __fmul_rn(alpha, r[c]), acc[c]);
       }
     }
   }
@@ -59,20 +69,22 @@ __device__ __forceinline__ void delta_write_cols(int W, const float *w, float al
 #pragma unroll
   for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], acc[c]));
   for (int j0 = rg; j0 < W; j0 += RG * kJB) {
-    float r[kJB][VEC];
+    uint4 raw[kJB];
 #pragma unroll
     for (int b = 0; b < kJB; ++b) {
       const int j = j0 + b * RG;
-      if (j < W) load_vec16<BANK>(src(j), r[b]);
+      if (j < W) raw[b] = *reinterpret_cast<const uint4 *>(src(j));
     }
 #pragma unroll
     for (int b = 0; b < kJB; ++b) {
       const int j = j0 + b * RG;
       if (j < W) {
         const float wj = w[j];
+        float r[VEC];
+        unpack16<BANK>(raw[b], r);
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) r[b][c] = __fmaf_rn(wj, d[c], __fmul_rn(alpha, r[b][c]));
-        store_vec16<BANK>(dst(j), r[b]);
+        for (int c = 0; c < VEC; ++c) r[c] = __fmaf_rn(wj, d[c], __fmul_rn(alpha, r[c]));
+        store_vec16<BANK>(dst(j), r);
       }
     }
   }
@@ -86,19 +98,21 @@ __device__ __forceinline__ void weighted_read_cols(int R, const float *r, SrcRow
 #pragma unroll
   for (int c = 0; c < VEC; ++c) y[c] = 0.0f;
   for (int j0 = rg; j0 < R; j0 += RG * kJB) {
-    float m[kJB][VEC];
+    uint4 raw[kJB];
 #pragma unroll
     for (int b = 0; b < kJB; ++b) {
       const int j = j0 + b * RG;
-      if (j < R) load_vec16<BANK>(src(j), m[b]);
+      if (j < R) raw[b] = *reinterpret_cast<const uint4 *>(src(j));
     }
 #pragma unroll
     for (int b = 0; b < kJB; ++b) {
       const int j = j0 + b * RG;
       if (j < R) {
         const float rj = r[j];
+        float m[VEC];
+        unpack16<BANK>(raw[b], m);
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) y[c] = __fmaf_rn(rj, m[b][c], y[c]);
+        for (int c = 0; c < VEC; ++c) y[c] = __fmaf_rn(rj, m[c], y[c]);
       }
     }
   }
@@ -106,6 +120,112 @@ __device__ __forceinline__ void weighted_read_cols(int R, const float *r, SrcRow
   for (int o = NCG; o < 32; o <<= 1)
 #pragma unroll
     for (int c = 0; c < VEC; ++c) y[c] = __fadd_rn(y[c], __shfl_xor_sync(0xffffffffu, y[c], o));
+}
+
+// The row references of one token that one lane handles: row group rg takes the refs
+// j = rg + b*RG, b < kJB (valid while j < W, resp. j < R).
+struct LaneRefs {
+  int uw[kJB], ur[kJB];      // row byte offsets in the stage buffer
+};
+
+// One token, when each lane holds at most kJB write rows and kJB read rows (W, R <=
+// RG*kJB).  Same arithmetic, in the same order, as delta_write_cols followed by
+// weighted_read_cols.  When the token reads no row it writes (overlap == false) its
+// read rows are fetched together with the write rows and both reductions run side by
+// side: the rows it reads hold the same values before and after its write.
+template <typename BANK, int NCG>
+__device__ __forceinline__ void token_write_read(int W, int R, const LaneRefs &ref, const float *w,
+                                                 float alpha, float beta, const float (&v)[Vec16<BANK>::N],
+                                                 unsigned char *rows, bool overlap, float (&y)[Vec16<BANK>::N]) {
+  constexpr int VEC = Vec16<BANK>::N, RG = 32 / NCG;
+  const int rg = (threadIdx.x & 31) / NCG;
+  uint4 rw[kJB], rr[kJB];
+  struct {
+    float ww[kJB], wr[kJB];
+  } wt;
+#pragma unroll
+  for (int b = 0; b < kJB; ++b) {
+    const int j = rg + b * RG;
+    wt.ww[b] = j < W ? w[j] : 0.0f;
+    wt.wr[b] = j < R ? w[W + j] : 0.0f;
+  }
+#pragma unroll
+  for (int b = 0; b < kJB; ++b)
+    if (rg + b * RG < W) rw[b] = *reinterpret_cast<const uint4 *>(rows + ref.uw[b]);
+  if (!overlap) {
+#pragma unroll
+    for (int b = 0; b < kJB; ++b)
+      if (rg + b * RG < R) rr[b] = *reinterpret_cast<const uint4 *>(rows + ref.ur[b]);
+  }
+  float acc[VEC], ya[VEC];
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) acc[c] = ya[c] = 0.0f;
+#pragma unroll
+  for (int b = 0; b < kJB; ++b) {
+    if (rg + b * RG < W) {
+      float r[VEC];
+      unpack16<BANK>(rw[b], r);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) acc[c] = __fmaf_rn(wt.ww[b], __fmul_rn(alpha, r[c]), acc[c]);
+    }
+  }
+  if (!overlap) {
+#pragma unroll
+    for (int b = 0; b < kJB; ++b) {
+      if (rg + b * RG < R) {
+        float m[VEC];
+        unpack16<BANK>(rr[b], m);
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) ya[c] = __fmaf_rn(wt.wr[b], m[c], ya[c]);
+      }
+    }
+#pragma unroll
+    for (int o = NCG; o < 32; o <<= 1)
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        acc[c] = __fadd_rn(acc[c], __shfl_xor_sync(0xffffffffu, acc[c], o));
+        ya[c] = __fadd_rn(ya[c], __shfl_xor_sync(0xffffffffu, ya[c], o));
+      }
+  } else {
+#pragma unroll
+    for (int o = NCG; o < 32; o <<= 1)
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) acc[c] = __fadd_rn(acc[c], __shfl_xor_sync(0xffffffffu, acc[c], o));
+  }
+  float d[VEC];
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], acc[c]));
+#pragma unroll
+  for (int b = 0; b < kJB; ++b) {
+    if (rg + b * RG < W) {
+      float r[VEC];
+      unpack16<BANK>(rw[b], r);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) r[c] = __fmaf_rn(wt.ww[b], d[c], __fmul_rn(alpha, r[c]));
+      store_vec16<BANK>(reinterpret_cast<BANK *>(rows + ref.uw[b]), r);
+    }
+  }
+  if (overlap) {
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < kJB; ++b)
+      if (rg + b * RG < R) rr[b] = *reinterpret_cast<const uint4 *>(rows + ref.ur[b]);
+#pragma unroll
+    for (int b = 0; b < kJB; ++b) {
+      if (rg + b * RG < R) {
+        float m[VEC];
+        unpack16<BANK>(rr[b], m);
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) ya[c] = __fmaf_rn(wt.wr[b], m[c], ya[c]);
+      }
+    }
+#pragma unroll
+    for (int o = NCG; o < 32; o <<= 1)
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) ya[c] = __fadd_rn(ya[c], __shfl_xor_sync(0xffffffffu, ya[c], o));
+  }
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) y[c] = ya[c];
 }
 
 }  // namespace sdm

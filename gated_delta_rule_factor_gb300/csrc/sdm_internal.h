@@ -66,12 +66,13 @@ struct BankCopyArgs {
 //     uint32 carry[L]      (u | src_u << 16)      rows copied from the previous stage
 //     int32  wb_slot[L];   uint16 wb_u[L]         rows written back after the stage
 //     uint16 refmap[L]     row u of ref (t_local*(W+R) + j)
+//     uint8  tokflag[G]    1 if the token reads a row it also writes
 struct PlanLayout {
   int32_t G;             // tokens per stage
   int32_t L;             // refs per full stage = G*(W+R)
   int32_t n_stages;      // ceil(T / G)
   int64_t rec_bytes;     // bytes per stage record (multiple of 16)
-  int64_t off_load_slot, off_load_u, off_carry, off_wb_slot, off_wb_u, off_refmap;
+  int64_t off_load_slot, off_load_u, off_carry, off_wb_slot, off_wb_u, off_refmap, off_tokflag;
 };
 
 struct PlanArgs {
@@ -98,6 +99,7 @@ struct WriteReadArgs {
   int64_t T, N, d_v;
   int32_t H, W, R;
   int32_t slices;         // d_v / CW
+  int32_t tok_bulk;       // weights and values of a token fetched by bulk copies (16-byte aligned)
   PlanLayout lay;
 };
 

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
   extern __shared__ __align__(16) unsigned char smem[];
   uint64_t *keys = reinterpret_cast<uint64_t *>(smem);            // [P]
   uint8_t *wr = reinterpret_cast<uint8_t *>(keys + P);              // [P]
+  uint8_t *tokflag = wr + P;                                        // [G]
   __shared__ int warp_sums[kThreads / 32];
 
   const PlanLayout &lay = a.lay;
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
     keys[i] = key;
     wr[i] = 0;
   }
+  for (int i = tid; i < lay.G; i += kThreads) tokflag[i] = 0;
   __syncthreads();
   for (int k = 2; k <= P; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
@@ -123,9 +125,19 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
     }
     const int ref = (int)(keys[i] & 0xffffu);
     refmap[ref] = (uint16_t)u;
-    if (ref % WR < a.W) wr[u] = 1;
+    if (ref % WR < a.W) {
+      wr[u] = 1;
+      // a token's refs to one row are adjacent in (slot, ref) order, its write before its
+      // read: a read ref of the same token right after this write ref means overlap
+      if (i + 1 < L && (keys[i + 1] >> 16) == slot) {
+        const int ref2 = (int)(keys[i + 1] & 0xffffu);
+        if (ref2 / WR == ref / WR) tokflag[ref / WR] = 1;
+      }
+    }
   }
   __syncthreads();
+  uint8_t *tf = a.records + stage * lay.rec_bytes + lay.off_tokflag;
+  for (int i = tid; i < nt; i += kThreads) tf[i] = tokflag[i];
   uint8_t *written = a.written + stage * lay.L;
   for (int i = tid; i < n_u; i += kThreads) written[i] = wr[i];
   if (tid == 0) a.nuniq[stage] = n_u;
@@ -205,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
 
 cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int P, cudaStream_t st) {
   if (streams == 0 || a.lay.n_stages == 0) return cudaSuccess;
-  const int64_t smem = (int64_t)P * 9;
+  const int64_t smem = (int64_t)P * 9 + a.lay.G;
   cudaError_t e = cudaFuncSetAttribute(plan_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

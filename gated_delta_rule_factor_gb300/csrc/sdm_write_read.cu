@@ -10,9 +10,9 @@
 // Warp roles (one CTA):
 //   compute warps (1 or 2, each owning up to four 16-byte column groups of the slice):
 //               the tokens of the current stage on the shared-memory rows;
-//   4 loader warps: fetch the next stage's rows (one bulk copy per row slice, completing
-//               on an mbarrier), its token data (cp.async) and the stage record after it.
-// After each stage every thread writes the stage's dirty rows back to the bank.
+//   4 loader warps: after each stage, write its dirty rows back (one bulk store per row
+//               slice); fetch the next stage's rows and token data (bulk copies completing
+//               on an mbarrier) and the stage record after it (one bulk copy).
 // Two row buffers alternate between stages; rows shared by consecutive stages are
 // copied across buffers instead of re-read, because the bank copy may be stale.  Stage
 // records use three buffers (in use / rows being fetched / record being fetched).
@@ -87,26 +87,38 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
            hdr[3] >= 0 && hdr[3] <= L;
   };
 
-  uint64_t *full = reinterpret_cast<uint64_t *>(tokbuf[1] + tl.bytes);   // [2], one per row buffer
+  uint64_t *full = reinterpret_cast<uint64_t *>(tokbuf[1] + tl.bytes);   // [2]: rows + token data of a stage
+  uint64_t *recb = full + 2;                                                // [3]: stage records
+  constexpr int VB = CW * (int)sizeof(ACT);                                 // value bytes per token (>= 16)
 
   // ---- loader helpers (threads of the loader warps)
   const int ltid = tid - 32 * NCW;
+  // Stage record g: one bulk copy into record buffer g % 3.
   auto fetch_record = [&](int g) {
-    const unsigned char *src = records + (int64_t)g * lay.rec_bytes;
-    unsigned char *dst = plan_of(g);
-    for (int64_t i = ltid; i < lay.rec_bytes / 16; i += kLoaderThreads) cp_async16(dst + i * 16, src + i * 16);
+    if (ltid == 0) {
+      uint64_t *bar = &recb[g % 3];
+      mbar_expect_tx(bar, (uint32_t)lay.rec_bytes);
+      bulk_load(plan_of(g), records + (int64_t)g * lay.rec_bytes, (uint32_t)lay.rec_bytes, bar);
+    }
   };
-  // Rows of stage g: one bulk copy per row slice, completing on full[g & 1].
-  auto fetch_rows = [&](int g) {
+  // Rows and token data of stage g (record g resident): bulk copies completing on
+  // full[g & 1]; the gates (8 bytes a token) and, for unaligned weights, the token data
+  // go by cp.async.
+  auto fetch_stage = [&](int g) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
     const int n_load = hdr_ok(hdr) ? hdr[1] : 0;
     const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
     const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
+    const int64_t t0 = (int64_t)g * G;
+    const int nt = (int)min((int64_t)G, a.T - t0);
+    uint64_t *bar = &full[g & 1];
+    if (ltid == 0) {
+      const int64_t tok_bytes = a.tok_bulk ? (int64_t)nt * (4 * WR + VB) : 0;
+      mbar_expect_tx(bar, (uint32_t)(n_load * RB + tok_bytes));
+    }
     unsigned char *dst = rowbuf[g & 1];
     const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0);
-    uint64_t *bar = &full[g & 1];
-    if (ltid == 0) mbar_expect_tx(bar, (uint32_t)(n_load * RB));
 #pragma unroll 4
     for (int e = ltid; e < n_load; e += kLoaderThreads) {
       int32_t slot = load_slot[e];
@@ -119,81 +131,88 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
       }
       bulk_load(dst + (int64_t)u * RB, src + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK), RB, bar);
     }
-  };
-  auto fetch_tokens = [&](int g) {
-    const int64_t t0 = (int64_t)g * G;
-    const int nt = (int)min((int64_t)G, a.T - t0);
     unsigned char *tb = tokbuf[g & 1];
     float *wts = reinterpret_cast<float *>(tb + tl.wts);
-    for (int i = ltid; i < nt * WR; i += kLoaderThreads) {
-      const int t = i / WR, j = i % WR;
-      const int64_t row = (b * a.T + t0 + t) * a.H + h;
-      const float *src_w = (j < W) ? a.wt[0] + row * W + j : a.wt[1] + row * R + (j - W);
-      cp_async4(wts + i, src_w);
+    unsigned char *vb = tb + tl.v;
+    if (a.tok_bulk) {
+      for (int i = ltid; i < 3 * nt; i += kLoaderThreads) {
+        const int t = i / 3, kind = i % 3;
+        const int64_t row = (b * a.T + t0 + t) * a.H + h;
+        if (kind == 0) bulk_load(wts + t * WR, a.wt[0] + row * W, 4 * W, bar);
+        else if (kind == 1) bulk_load(wts + t * WR + W, a.wt[1] + row * R, 4 * R, bar);
+        else bulk_load(vb + (int64_t)t * VB, kv + row * a.d_v + c0, VB, bar);
+      }
+    } else {
+      for (int i = ltid; i < nt * WR; i += kLoaderThreads) {
+        const int t = i / WR, j = i % WR;
+        const int64_t row = (b * a.T + t0 + t) * a.H + h;
+        const float *src_w = (j < W) ? a.wt[0] + row * W + j : a.wt[1] + row * R + (j - W);
+        cp_async4(wts + i, src_w);
+      }
+      for (int i = ltid; i < nt * (VB / 16); i += kLoaderThreads) {
+        const int t = i / (VB / 16), c = i % (VB / 16);
+        const int64_t row = (b * a.T + t0 + t) * a.H + h;
+        cp_async16(vb + (int64_t)t * VB + c * 16,
+                   reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
+      }
     }
     float *gt = reinterpret_cast<float *>(tb + tl.gates);
     for (int i = ltid; i < nt; i += kLoaderThreads) {
       const int64_t row = (b * a.T + t0 + i) * a.H + h;
       cp_async8(gt + 2 * i, a.gates + row * 2);
     }
-    constexpr int VB = CW * (int)sizeof(ACT);          // value bytes per token (>= 16)
-    unsigned char *vb = tb + tl.v;
-    for (int i = ltid; i < nt * (VB / 16); i += kLoaderThreads) {
-      const int t = i / (VB / 16), c = i % (VB / 16);
-      const int64_t row = (b * a.T + t0 + t) * a.H + h;
-      cp_async16(vb + (int64_t)t * VB + c * 16,
-                 reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
-    }
   };
-  // Dirty rows of stage g back to the bank, by every thread (CPR lanes per row).
+  // Dirty rows of stage g back to the bank: one bulk store per row slice.
   auto write_back = [&](int g) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
     const int n_wb = hdr_ok(hdr) ? hdr[3] : 0;
     const int32_t *wb_slot = reinterpret_cast<const int32_t *>(rec + lay.off_wb_slot);
     const uint16_t *wb_u = reinterpret_cast<const uint16_t *>(rec + lay.off_wb_u);
-    const int chunk = tid % CPR;
-    const unsigned char *src = rowbuf[g & 1] + chunk * 16;
-    unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + chunk * 16;
+    const unsigned char *src = rowbuf[g & 1];
+    unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0);
 #pragma unroll 4
-    for (int e = tid / CPR; e < n_wb; e += NTHR / CPR) {
+    for (int e = ltid; e < n_wb; e += kLoaderThreads) {
       const int32_t slot = wb_slot[e];
       const int u = wb_u[e];
       if (u >= L || slot < 0 || slot >= a.N) {
         raise_error(a.err, SDM_DEVERR_PLAN);
         continue;
       }
-      *reinterpret_cast<uint4 *>(dst + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK)) =
-          *reinterpret_cast<const uint4 *>(src + (int64_t)u * RB);
+      bulk_store(dst + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK), src + (int64_t)u * RB, RB);
     }
+    bulk_commit();
   };
 
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int i = 0; i < 5; ++i) mbar_init(&full[i], 1);
     mbar_init_fence();
   }
   __syncthreads();
 
-  // ---- prologue: record 0, then stage 0 and record 1
-  if (is_loader) {
-    fetch_record(0);
-    cp_async_commit();
-    cp_async_wait_all();
-    named_barrier(1, kLoaderThreads);
-    fetch_rows(0);
-    fetch_tokens(0);
-    if (S > 1) fetch_record(1);
-    cp_async_commit();
-  }
-
   bool failed = false;
-  for (int g = 0; g < S; ++g) {
-    if (is_loader) cp_async_wait_all();
-    if (!failed && !mbar_wait(&full[g & 1], (g >> 1) & 1)) {
+  auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
+    if (!failed && !mbar_wait(bar, parity)) {
       failed = true;
       raise_error(a.err, SDM_DEVERR_TIMEOUT);
     }
+  };
+
+  // ---- prologue: records 0 and 1, then stage 0
+  if (is_loader) {
+    fetch_record(0);
+    if (S > 1) fetch_record(1);
+    wait_bar(&recb[0], 0);
+    fetch_stage(0);
+    cp_async_commit();
+  }
+
+  constexpr int RG = 32 / NCG;
+  const bool fast = W <= RG * kJB && R <= RG * kJB;
+  for (int g = 0; g < S; ++g) {
+    if (is_loader) cp_async_wait_all();                          // gates (and cp.async token data)
+    wait_bar(&full[g & 1], (g >> 1) & 1);                        // rows + bulk token data of stage g
+    wait_bar(&recb[g % 3], (g / 3) & 1);                         // record g
     __syncthreads();                                             // stage g resident
     {
       const unsigned char *rec = plan_of(g);
@@ -215,58 +234,92 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
             *reinterpret_cast<const uint4 *>(from + (int64_t)src * RB + c * 16);
       }
     }
-    fence_proxy_async_shared();                                  // before bulk copies reuse the buffer
+    fence_proxy_async_shared();                                  // before bulk copies touch these buffers
     __syncthreads();                                             // carries in place
 
     if (!is_loader) {
       // ---- compute: tokens of stage g in order; warp w owns column groups [w*NCG, w*NCG+NCG)
       const unsigned char *rec = plan_of(g);
       const uint16_t *refmap = reinterpret_cast<const uint16_t *>(rec + lay.off_refmap);
+      const uint8_t *tokflag = rec + lay.off_tokflag;
       const unsigned char *tb = tokbuf[g & 1];
       const float *wts = reinterpret_cast<const float *>(tb + tl.wts);
       const float *gt = reinterpret_cast<const float *>(tb + tl.gates);
       const ACT *vv = reinterpret_cast<const ACT *>(tb + tl.v);
       const int cg = warp * NCG + lane % NCG;                 // column group in the slice
+      const int rg = lane / NCG;
       unsigned char *rows = rowbuf[g & 1] + cg * 16;
       const int64_t t0 = (int64_t)g * G;
       const int nt = (int)min((int64_t)G, a.T - t0);
-      for (int t = 0; t < nt; ++t) {
-        const uint16_t *rm = refmap + t * WR;
-        const float *w = wts + t * WR;
-        auto row_ptr = [&](int j) -> BANK * {
-          int u = rm[j];
-          if (u >= L) u = 0;                           // plan_sort never emits these
-          return reinterpret_cast<BANK *>(rows + (int64_t)u * RB);
+      if (fast) {
+        auto load_refs = [&](int t, LaneRefs &r) {
+          const uint16_t *rm = refmap + t * WR;
+#pragma unroll
+          for (int bb = 0; bb < kJB; ++bb) {
+            const int j = rg + bb * RG;
+            int uw = j < W ? rm[j] : 0, ur = j < R ? rm[W + j] : 0;
+            r.uw[bb] = (uw < L ? uw : 0) * RB;
+            r.ur[bb] = (ur < L ? ur : 0) * RB;
+          }
         };
-        auto wrow = [&](int j) { return row_ptr(j); };
-        auto rrow = [&](int j) { return row_ptr(W + j); };
-        float v[VEC];
-        load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
-        delta_write_cols<BANK, NCG>(W, w, gt[2 * t], gt[2 * t + 1], v, wrow, wrow);
-        __syncwarp();
-        float out[VEC];
-        weighted_read_cols<BANK, NCG>(R, w + W, rrow, out);
-        if (lane < NCG) {
-          const int64_t row = (b * a.T + t0 + t) * a.H + h;
-          store_vec<ACT, VEC>(y + row * a.d_v + c0 + cg * VEC, out);
+        LaneRefs cur, nxt;
+        if (nt > 0) load_refs(0, cur);
+        for (int t = 0; t < nt; ++t) {
+          if (t + 1 < nt) load_refs(t + 1, nxt);
+          float v[VEC], out[VEC];
+          load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
+          token_write_read<BANK, NCG>(W, R, cur, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, rows, tokflag[t] != 0,
+                                      out);
+          if (lane < NCG) {
+            const int64_t row = (b * a.T + t0 + t) * a.H + h;
+            store_vec<ACT, VEC>(y + row * a.d_v + c0 + cg * VEC, out);
+          }
+          __syncwarp();
+          cur = nxt;
         }
-        __syncwarp();
+      } else {
+        for (int t = 0; t < nt; ++t) {
+          const uint16_t *rm = refmap + t * WR;
+          const float *w = wts + t * WR;
+          auto row_ptr = [&](int j) -> BANK * {
+            int u = rm[j];
+            if (u >= L) u = 0;                         // plan_sort never emits these
+            return reinterpret_cast<BANK *>(rows + (int64_t)u * RB);
+          };
+          auto wrow = [&](int j) { return row_ptr(j); };
+          auto rrow = [&](int j) { return row_ptr(W + j); };
+          float v[VEC];
+          load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
+          delta_write_cols<BANK, NCG>(W, w, gt[2 * t], gt[2 * t + 1], v, wrow, wrow);
+          __syncwarp();
+          float out[VEC];
+          weighted_read_cols<BANK, NCG>(R, w + W, rrow, out);
+          if (lane < NCG) {
+            const int64_t row = (b * a.T + t0 + t) * a.H + h;
+            store_vec<ACT, VEC>(y + row * a.d_v + c0 + cg * VEC, out);
+          }
+          __syncwarp();
+        }
       }
-      fence_proxy_async_shared();
+      fence_proxy_async_shared();                              // row updates before the bulk stores
     } else {
-      // ---- loaders: fetch stage g+1 (its rows are not in stage g, and stage g-1's
-      // write-back finished before the barriers above) and record g+2
+      // ---- loaders: stage g+1 goes into the buffer stage g-1 used, once the bulk stores
+      // of stage g-1 are complete (their smem reads done, their global writes visible to
+      // the loads below); then record g+2
+      fence_proxy_async_shared();
+      bulk_wait_all();
+      named_barrier(1, kLoaderThreads);
       if (g + 1 < S) {
-        fetch_rows(g + 1);
-        fetch_tokens(g + 1);
+        wait_bar(&recb[(g + 1) % 3], ((g + 1) / 3) & 1);
+        fetch_stage(g + 1);
       }
       if (g + 2 < S) fetch_record(g + 2);
       cp_async_commit();
     }
     __syncthreads();                                             // stage g computed
-    write_back(g);
-    fence_proxy_async_global();                                  // before later bulk reads of these rows
+    if (is_loader) write_back(g);
   }
+  if (is_loader) bulk_wait_all();                                // smem must outlive the stores
 }
 
 template <typename BANK, typename ACT>
@@ -309,7 +362,7 @@ int64_t write_read_smem_bytes(int CW, int bank_elem, int act_elem, int G, int W,
                               int64_t rec_bytes) {
   const int64_t L = (int64_t)G * (W + R);
   const TokLayout t = tok_layout(G, W, R, CW, act_elem);
-  return 2 * L * CW * bank_elem + 3 * rec_bytes + 2 * t.bytes + 64;   // + 2 mbarriers
+  return 2 * L * CW * bank_elem + 3 * rec_bytes + 2 * t.bytes + 64;   // + 5 mbarriers
 }
 
 cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_dtype,
