@@ -28,7 +28,7 @@ constexpr int kLoaderWarps = 4;
 constexpr int kLoaderThreads = 32 * kLoaderWarps;
 
 struct TokLayout {
-  int64_t wts, gates, v, bytes;  // offsets inside one token-data buffer
+  int64_t wts, gates, v, y, bytes;  // offsets inside one token-data buffer
 };
 
 __host__ __device__ inline int64_t align16(int64_t x) { return (x + 15) & ~int64_t(15); }
@@ -38,7 +38,8 @@ __host__ __device__ inline TokLayout tok_layout(int G, int W, int R, int CW, int
   t.wts = 0;
   t.gates = align16((int64_t)G * (W + R) * 4);
   t.v = t.gates + align16((int64_t)G * 2 * 4);
-  t.bytes = t.v + align16((int64_t)G * CW * act_elem);
+  t.y = t.v + align16((int64_t)G * CW * act_elem);
+  t.bytes = t.y + align16((int64_t)G * CW * act_elem);
   return t;
 }
 
@@ -162,7 +163,8 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
       cp_async8(gt + 2 * i, a.gates + row * 2);
     }
   };
-  // Dirty rows of stage g back to the bank: one bulk store per row slice.
+  // Dirty rows of stage g back to the bank (one bulk store per row slice) and the
+  // stage's outputs y (one bulk store per token).
   auto write_back = [&](int g) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
@@ -180,6 +182,13 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
         continue;
       }
       bulk_store(dst + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK), src + (int64_t)u * RB, RB);
+    }
+    const int64_t t0 = (int64_t)g * G;
+    const int nt = (int)min((int64_t)G, a.T - t0);
+    const unsigned char *ys = tokbuf[g & 1] + tl.y;
+    for (int t = ltid; t < nt; t += kLoaderThreads) {
+      const int64_t row = (b * a.T + t0 + t) * a.H + h;
+      bulk_store(y + row * a.d_v + c0, ys + (int64_t)t * VB, VB);
     }
     bulk_commit();
   };
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
       const uint32_t *carry = reinterpret_cast<const uint32_t *>(rec + lay.off_carry);
       const unsigned char *from = rowbuf[(g + 1) & 1];
       unsigned char *to = rowbuf[g & 1];
-      for (int i = tid; i < n_carry * CPR; i += NTHR) {
+      for (int i = is_loader ? ltid : n_carry * CPR; i < n_carry * CPR; i += kLoaderThreads) {
         const int e = i / CPR, c = i % CPR;
         const int u = carry[e] & 0xffff, src = carry[e] >> 16;
         if (u >= L || src >= L) {
@@ -234,7 +243,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
             *reinterpret_cast<const uint4 *>(from + (int64_t)src * RB + c * 16);
       }
     }
-    fence_proxy_async_shared();                                  // before bulk copies touch these buffers
+    if (is_loader) fence_proxy_async_shared();                   // before bulk copies touch these buffers
     __syncthreads();                                             // carries in place
 
     if (!is_loader) {
@@ -246,6 +255,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
       const float *wts = reinterpret_cast<const float *>(tb + tl.wts);
       const float *gt = reinterpret_cast<const float *>(tb + tl.gates);
       const ACT *vv = reinterpret_cast<const ACT *>(tb + tl.v);
+      ACT *ys = reinterpret_cast<ACT *>(tokbuf[g & 1] + tl.y);  // y of the stage, stored by the loaders
       const int cg = warp * NCG + lane % NCG;                 // column group in the slice
       const int rg = lane / NCG;
       unsigned char *rows = rowbuf[g & 1] + cg * 16;
@@ -270,10 +280,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
           load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
           token_write_read<BANK, NCG>(W, R, cur, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, rows, tokflag[t] != 0,
                                       out);
-          if (lane < NCG) {
-            const int64_t row = (b * a.T + t0 + t) * a.H + h;
-            store_vec<ACT, VEC>(y + row * a.d_v + c0 + cg * VEC, out);
-          }
+          if (lane < NCG) store_vec<ACT, VEC>(ys + t * CW + cg * VEC, out);
           __syncwarp();
           cur = nxt;
         }
@@ -294,10 +301,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
           __syncwarp();
           float out[VEC];
           weighted_read_cols<BANK, NCG>(R, w + W, rrow, out);
-          if (lane < NCG) {
-            const int64_t row = (b * a.T + t0 + t) * a.H + h;
-            store_vec<ACT, VEC>(y + row * a.d_v + c0 + cg * VEC, out);
-          }
+          if (lane < NCG) store_vec<ACT, VEC>(ys + t * CW + cg * VEC, out);
           __syncwarp();
         }
       }
