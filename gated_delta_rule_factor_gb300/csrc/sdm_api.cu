@@ -207,7 +207,7 @@ PlanLayout plan_layout(int G, int W, int R, int64_t T) {
   p.L = G * (W + R);
   p.n_stages = (int32_t)((T + G - 1) / G);
   const int64_t L = p.L;
-  int64_t o = 16;
+  int64_t o = 32;                                    // header: n_u, n_load, n_carry, n_wb, n_late
   p.off_load_slot = o; o = a16(o + 4 * L);
   p.off_load_u = o;    o = a16(o + 2 * L);
   p.off_carry = o;     o = a16(o + 4 * L);

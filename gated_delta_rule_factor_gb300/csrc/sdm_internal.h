@@ -61,7 +61,8 @@ struct BankCopyArgs {
 //   nuniq[s][g]      number of unique rows
 //   written[s][g][u] 1 if a write ref of the stage hits row u (uint8, L per stage)
 //   record[s][g]     the stage record read by the write/read kernel:
-//     int32 n_u, n_load, n_carry, n_wb
+//     int32 n_u, n_load, n_carry, n_wb, n_late, 3 x pad   (32 bytes)
+//       the last n_late loads re-read rows stage g-2 held (possibly written back late)
 //     int32  load_slot[L]; uint16 load_u[L]      rows fetched from the bank
 //     uint32 carry[L]      (u | src_u << 16)      rows copied from the previous stage
 //     int32  wb_slot[L];   uint16 wb_u[L]         rows written back after the stage

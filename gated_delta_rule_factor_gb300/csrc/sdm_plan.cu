@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
   const PlanLayout &lay = a.lay;
   int32_t *prev = reinterpret_cast<int32_t *>(smem);       // [L]
   int32_t *next = prev + lay.L;                             // [L]
+  int32_t *prev2 = next + lay.L;                            // [L]
   __shared__ int warp_sums[kThreads / 32];
 
   const int g = blockIdx.x;
@@ -158,6 +159,8 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
   const int n_prev = g > 0 ? a.nuniq[stage - 1] : 0;
   const int n_cur = a.nuniq[stage];
   const int n_next = g + 1 < S ? a.nuniq[stage + 1] : 0;
+  const int n_prev2 = g > 1 ? a.nuniq[stage - 2] : 0;
+  for (int i = tid; i < n_prev2; i += kThreads) prev2[i] = a.uniq[(stage - 2) * lay.L + i];
   for (int i = tid; i < n_prev; i += kThreads) prev[i] = a.uniq[(stage - 1) * lay.L + i];
   for (int i = tid; i < n_next; i += kThreads) next[i] = a.uniq[(stage + 1) * lay.L + i];
   __syncthreads();
@@ -166,17 +169,22 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
   const uint8_t *written = a.written + stage * lay.L;
   const int ept = (n_cur + kThreads - 1) / kThreads;
   const int u0 = min(n_cur, tid * ept), u1 = min(n_cur, u0 + ept);
-  int c_load = 0, c_carry = 0, c_wb = 0;
+  // A row loaded here that stage g-2 also held may have been written back at the end of
+  // stage g-2, which the write/read kernel only waits for late: such loads go last.
+  int c_load = 0, c_late = 0, c_carry = 0, c_wb = 0;
   for (int u = u0; u < u1; ++u) {
     const int32_t slot = cur[u];
     const int src = find_sorted(prev, n_prev, slot);
     const bool out = find_sorted(next, n_next, slot) >= 0;
-    c_load += src < 0;
+    const bool late = src < 0 && find_sorted(prev2, n_prev2, slot) >= 0;
+    c_load += src < 0 && !late;
+    c_late += late;
     c_carry += src >= 0;
     c_wb += ((written[u] || src >= 0) && !out);
   }
-  int n_load, n_carry, n_wb;
+  int n_load, n_late, n_carry, n_wb;
   int o_load = block_scan_exclusive(c_load, warp_sums, &n_load);
+  int o_late = n_load + block_scan_exclusive(c_late, warp_sums, &n_late);
   int o_carry = block_scan_exclusive(c_carry, warp_sums, &n_carry);
   int o_wb = block_scan_exclusive(c_wb, warp_sums, &n_wb);
 
@@ -191,9 +199,11 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
     const int src = find_sorted(prev, n_prev, slot);
     const bool out = find_sorted(next, n_next, slot) >= 0;
     if (src < 0) {
-      load_slot[o_load] = slot;
-      load_u[o_load] = (uint16_t)u;
-      ++o_load;
+      const bool late = find_sorted(prev2, n_prev2, slot) >= 0;
+      int &o = late ? o_late : o_load;
+      load_slot[o] = slot;
+      load_u[o] = (uint16_t)u;
+      ++o;
     } else {
       carry[o_carry] = (uint32_t)u | ((uint32_t)src << 16);
       ++o_carry;
@@ -207,9 +217,10 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
   if (tid == 0) {
     int32_t *hdr = reinterpret_cast<int32_t *>(rec);
     hdr[0] = n_cur;
-    hdr[1] = n_load;
+    hdr[1] = n_load + n_late;
     hdr[2] = n_carry;
     hdr[3] = n_wb;
+    hdr[4] = n_late;
   }
 }
 
@@ -227,7 +238,7 @@ cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int P, cudaStre
 
 cudaError_t launch_plan_link(const PlanArgs &a, int64_t streams, cudaStream_t st) {
   if (streams == 0 || a.lay.n_stages == 0) return cudaSuccess;
-  const int64_t smem = (int64_t)a.lay.L * 8;
+  const int64_t smem = (int64_t)a.lay.L * 12;
   cudaError_t e = cudaFuncSetAttribute(plan_link_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
   auto plan_of = [&](int g) -> unsigned char * { return plans + (int64_t)(g % 3) * lay.rec_bytes; };
   auto hdr_ok = [&](const int32_t *hdr) -> bool {
     return hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[1] <= L && hdr[2] >= 0 && hdr[2] <= L &&
-           hdr[3] >= 0 && hdr[3] <= L;
+           hdr[3] >= 0 && hdr[3] <= L && hdr[4] >= 0 && hdr[4] <= hdr[1];
   };
 
   uint64_t *full = reinterpret_cast<uint64_t *>(tokbuf[1] + tl.bytes);   // [2]: rows + token data of a stage
@@ -104,11 +104,12 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
   };
   // Rows and token data of stage g (record g resident): bulk copies completing on
   // full[g & 1]; the gates (8 bytes a token) and, for unaligned weights, the token data
-  // go by cp.async.
+  // go by cp.async.  The last n_late rows are left for fetch_late.
   auto fetch_stage = [&](int g) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
     const int n_load = hdr_ok(hdr) ? hdr[1] : 0;
+    const int n_early = hdr_ok(hdr) ? hdr[1] - hdr[4] : 0;
     const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
     const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
     const int64_t t0 = (int64_t)g * G;
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
     unsigned char *dst = rowbuf[g & 1];
     const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0);
 #pragma unroll 4
-    for (int e = ltid; e < n_load; e += kLoaderThreads) {
+    for (int e = ltid; e < n_early; e += kLoaderThreads) {
       int32_t slot = load_slot[e];
       int u = load_u[e];
       if (u >= L || slot < 0 || slot >= a.N) {
@@ -161,6 +162,27 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
     for (int i = ltid; i < nt; i += kLoaderThreads) {
       const int64_t row = (b * a.T + t0 + i) * a.H + h;
       cp_async8(gt + 2 * i, a.gates + row * 2);
+    }
+  };
+  // Rows of stage g that stage g-2 also held, once that stage's write-back is complete.
+  auto fetch_late = [&](int g) {
+    const unsigned char *rec = plan_of(g);
+    const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+    if (!hdr_ok(hdr)) return;
+    const int n_load = hdr[1], n_early = hdr[1] - hdr[4];
+    const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
+    const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
+    unsigned char *dst = rowbuf[g & 1];
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0);
+    for (int e = n_early + ltid; e < n_load; e += kLoaderThreads) {
+      int32_t slot = load_slot[e];
+      int u = load_u[e];
+      if (u >= L || slot < 0 || slot >= a.N) {
+        raise_error(a.err, SDM_DEVERR_PLAN);
+        u = 0;
+        slot = 0;
+      }
+      bulk_load(dst + (int64_t)u * RB, src + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK), RB, &full[g & 1]);
     }
   };
   // Dirty rows of stage g back to the bank (one bulk store per row slice) and the
@@ -213,6 +235,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
     if (S > 1) fetch_record(1);
     wait_bar(&recb[0], 0);
     fetch_stage(0);
+    fetch_late(0);
     cp_async_commit();
   }
 
@@ -232,7 +255,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
       const uint32_t *carry = reinterpret_cast<const uint32_t *>(rec + lay.off_carry);
       const unsigned char *from = rowbuf[(g + 1) & 1];
       unsigned char *to = rowbuf[g & 1];
-      for (int i = is_loader ? ltid : n_carry * CPR; i < n_carry * CPR; i += kLoaderThreads) {
+      for (int i = is_loader ? n_carry * CPR : tid; i < n_carry * CPR; i += 32 * NCW) {
         const int e = i / CPR, c = i % CPR;
         const int u = carry[e] & 0xffff, src = carry[e] >> 16;
         if (u >= L || src >= L) {
@@ -243,7 +266,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
             *reinterpret_cast<const uint4 *>(from + (int64_t)src * RB + c * 16);
       }
     }
-    if (is_loader) fence_proxy_async_shared();                   // before bulk copies touch these buffers
+    if (!is_loader) fence_proxy_async_shared();                  // carried rows before bulk stores read them
     __syncthreads();                                             // carries in place
 
     if (!is_loader) {
@@ -307,17 +330,22 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
       }
       fence_proxy_async_shared();                              // row updates before the bulk stores
     } else {
-      // ---- loaders: stage g+1 goes into the buffer stage g-1 used, once the bulk stores
-      // of stage g-1 are complete (their smem reads done, their global writes visible to
-      // the loads below); then record g+2
-      fence_proxy_async_shared();
-      bulk_wait_all();
+      // ---- loaders: stage g+1 goes into the buffer stage g-1 used once stage g-1's bulk
+      // stores have read it; rows stage g-1 held (the planner's late rows) only once those
+      // stores' writes are performed; then record g+2
+      bulk_wait_read();                                        // stage g-1's bulk stores read their rows
       named_barrier(1, kLoaderThreads);
       if (g + 1 < S) {
         wait_bar(&recb[(g + 1) % 3], ((g + 1) / 3) & 1);
         fetch_stage(g + 1);
       }
-      if (g + 2 < S) fetch_record(g + 2);
+      bulk_wait_all();                                         // ... and their writes are performed
+      named_barrier(1, kLoaderThreads);
+      if (g + 1 < S) fetch_late(g + 1);
+      if (g + 2 < S) {
+        if (ltid == 0) fence_proxy_async_shared();
+        fetch_record(g + 2);
+      }
       cp_async_commit();
     }
     __syncthreads();                                             // stage g computed
