@@ -9,10 +9,12 @@
 //
 // Warp roles (one CTA):
 //   compute warps (1 or 2, each owning up to four 16-byte column groups of the slice):
-//               the tokens of the current stage on the shared-memory rows;
-//   4 loader warps: after each stage, write its dirty rows back (one bulk store per row
-//               slice); fetch the next stage's rows and token data (bulk copies completing
-//               on an mbarrier) and the stage record after it (one bulk copy).
+//               the tokens of the current stage on the shared-memory rows, and the rows
+//               carried over from the previous stage;
+//   4 loader warps: write back the previous stage's dirty rows, then fetch the next
+//               stage's rows and token data and the stage record after it, all with
+//               16-byte cp.async on the LSU path (a bulk/TMA copy per 128-byte row costs
+//               more than it saves at this granularity).
 // Two row buffers alternate between stages; rows shared by consecutive stages are
 // copied across buffers instead of re-read, because the bank copy may be stale.  Stage
 // records use three buffers (in use / rows being fetched / record being fetched).
@@ -28,7 +30,7 @@ constexpr int kLoaderWarps = 4;
 constexpr int kLoaderThreads = 32 * kLoaderWarps;
 
 struct TokLayout {
-  int64_t wts, gates, v, y, bytes;  // offsets inside one token-data buffer
+  int64_t wts, gates, v, bytes;  // offsets inside one token-data buffer
 };
 
 __host__ __device__ inline int64_t align16(int64_t x) { return (x + 15) & ~int64_t(15); }
@@ -38,8 +40,7 @@ __host__ __device__ inline TokLayout tok_layout(int G, int W, int R, int CW, int
   t.wts = 0;
   t.gates = align16((int64_t)G * (W + R) * 4);
   t.v = t.gates + align16((int64_t)G * 2 * 4);
-  t.y = t.v + align16((int64_t)G * CW * act_elem);
-  t.bytes = t.y + align16((int64_t)G * CW * act_elem);
+  t.bytes = t.v + align16((int64_t)G * CW * act_elem);
   return t;
 }
 
@@ -88,61 +89,49 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
            hdr[3] >= 0 && hdr[3] <= L && hdr[4] >= 0 && hdr[4] <= hdr[1];
   };
 
-  uint64_t *full = reinterpret_cast<uint64_t *>(tokbuf[1] + tl.bytes);   // [2]: rows + token data of a stage
-  uint64_t *recb = full + 2;                                                // [3]: stage records
-  constexpr int VB = CW * (int)sizeof(ACT);                                 // value bytes per token (>= 16)
+  constexpr int VB = CW * (int)sizeof(ACT);          // value bytes per token (>= 16)
+  constexpr int RG = 32 / NCG;
 
-  // ---- loader helpers (threads of the loader warps)
+  // ---- loader helpers (threads of the loader warps).  Every copy is a 16-byte cp.async
+  // (or 8/4-byte for the gates and unaligned weights) on the LSU path: CPR lanes take
+  // one row slice, so one warp request covers whole 128-byte lines.
   const int ltid = tid - 32 * NCW;
-  // Stage record g: one bulk copy into record buffer g % 3.
+  const int sub = ltid % CPR, grp = ltid / CPR;       // chunk of a row, row group
+  constexpr int GRP = kLoaderThreads / CPR;           // row slices per loader pass
   auto fetch_record = [&](int g) {
-    if (ltid == 0) {
-      uint64_t *bar = &recb[g % 3];
-      mbar_expect_tx(bar, (uint32_t)lay.rec_bytes);
-      bulk_load(plan_of(g), records + (int64_t)g * lay.rec_bytes, (uint32_t)lay.rec_bytes, bar);
-    }
+    const unsigned char *src = records + (int64_t)g * lay.rec_bytes;
+    unsigned char *dst = plan_of(g);
+    for (int64_t i = ltid; i < lay.rec_bytes / 16; i += kLoaderThreads) cp_async16(dst + i * 16, src + i * 16);
   };
-  // Rows and token data of stage g (record g resident): bulk copies completing on
-  // full[g & 1]; the gates (8 bytes a token) and, for unaligned weights, the token data
-  // go by cp.async.  The last n_late rows are left for fetch_late.
   auto fetch_stage = [&](int g) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
     const int n_load = hdr_ok(hdr) ? hdr[1] : 0;
-    const int n_early = hdr_ok(hdr) ? hdr[1] - hdr[4] : 0;
     const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
     const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
+    unsigned char *dst = rowbuf[g & 1] + sub * 16;
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0) + sub * 16;
+#pragma unroll 4
+    for (int e = grp; e < n_load; e += GRP) {
+      const int32_t slot = load_slot[e];
+      const int u = load_u[e];
+      if (u >= L || slot < 0 || slot >= a.N) {
+        raise_error(a.err, SDM_DEVERR_PLAN);
+        continue;
+      }
+      cp_async16(dst + (int64_t)u * RB, src + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK));
+    }
     const int64_t t0 = (int64_t)g * G;
     const int nt = (int)min((int64_t)G, a.T - t0);
-    uint64_t *bar = &full[g & 1];
-    if (ltid == 0) {
-      const int64_t tok_bytes = a.tok_bulk ? (int64_t)nt * (4 * WR + VB) : 0;
-      mbar_expect_tx(bar, (uint32_t)(n_load * RB + tok_bytes));
-    }
-    unsigned char *dst = rowbuf[g & 1];
-    const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0);
-#pragma unroll 4
-    for (int e = ltid; e < n_early; e += kLoaderThreads) {
-      int32_t slot = load_slot[e];
-      int u = load_u[e];
-      if (u >= L || slot < 0 || slot >= a.N) {
-        // corrupt plan: flag it and still deliver the counted bytes, inside the buffer
-        raise_error(a.err, SDM_DEVERR_PLAN);
-        u = 0;
-        slot = 0;
-      }
-      bulk_load(dst + (int64_t)u * RB, src + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK), RB, bar);
-    }
     unsigned char *tb = tokbuf[g & 1];
     float *wts = reinterpret_cast<float *>(tb + tl.wts);
-    unsigned char *vb = tb + tl.v;
-    if (a.tok_bulk) {
-      for (int i = ltid; i < 3 * nt; i += kLoaderThreads) {
-        const int t = i / 3, kind = i % 3;
+    if (a.tok_bulk) {                                  // weights in 16-byte pieces
+      const int wq = W / 4, rq = R / 4;
+      for (int i = ltid; i < nt * (wq + rq); i += kLoaderThreads) {
+        const int t = i / (wq + rq), q = i % (wq + rq);
         const int64_t row = (b * a.T + t0 + t) * a.H + h;
-        if (kind == 0) bulk_load(wts + t * WR, a.wt[0] + row * W, 4 * W, bar);
-        else if (kind == 1) bulk_load(wts + t * WR + W, a.wt[1] + row * R, 4 * R, bar);
-        else bulk_load(vb + (int64_t)t * VB, kv + row * a.d_v + c0, VB, bar);
+        if (q < wq) cp_async16(wts + t * WR + 4 * q, a.wt[0] + row * W + 4 * q);
+        else cp_async16(wts + t * WR + W + 4 * (q - wq), a.wt[1] + row * R + 4 * (q - wq));
       }
     } else {
       for (int i = ltid; i < nt * WR; i += kLoaderThreads) {
@@ -151,103 +140,60 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
         const float *src_w = (j < W) ? a.wt[0] + row * W + j : a.wt[1] + row * R + (j - W);
         cp_async4(wts + i, src_w);
       }
-      for (int i = ltid; i < nt * (VB / 16); i += kLoaderThreads) {
-        const int t = i / (VB / 16), c = i % (VB / 16);
-        const int64_t row = (b * a.T + t0 + t) * a.H + h;
-        cp_async16(vb + (int64_t)t * VB + c * 16,
-                   reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
-      }
     }
     float *gt = reinterpret_cast<float *>(tb + tl.gates);
     for (int i = ltid; i < nt; i += kLoaderThreads) {
       const int64_t row = (b * a.T + t0 + i) * a.H + h;
       cp_async8(gt + 2 * i, a.gates + row * 2);
     }
-  };
-  // Rows of stage g that stage g-2 also held, once that stage's write-back is complete.
-  auto fetch_late = [&](int g) {
-    const unsigned char *rec = plan_of(g);
-    const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
-    if (!hdr_ok(hdr)) return;
-    const int n_load = hdr[1], n_early = hdr[1] - hdr[4];
-    const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
-    const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
-    unsigned char *dst = rowbuf[g & 1];
-    const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0);
-    for (int e = n_early + ltid; e < n_load; e += kLoaderThreads) {
-      int32_t slot = load_slot[e];
-      int u = load_u[e];
-      if (u >= L || slot < 0 || slot >= a.N) {
-        raise_error(a.err, SDM_DEVERR_PLAN);
-        u = 0;
-        slot = 0;
-      }
-      bulk_load(dst + (int64_t)u * RB, src + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK), RB, &full[g & 1]);
+    unsigned char *vb = tb + tl.v;
+    for (int i = ltid; i < nt * (VB / 16); i += kLoaderThreads) {
+      const int t = i / (VB / 16), c = i % (VB / 16);
+      const int64_t row = (b * a.T + t0 + t) * a.H + h;
+      cp_async16(vb + (int64_t)t * VB + c * 16,
+                 reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
     }
   };
-  // Dirty rows of stage g back to the bank (one bulk store per row slice) and the
-  // stage's outputs y (one bulk store per token).
+  // Dirty rows of stage g back to the bank (CPR lanes per row slice, 16-byte stores).
   auto write_back = [&](int g) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
     const int n_wb = hdr_ok(hdr) ? hdr[3] : 0;
     const int32_t *wb_slot = reinterpret_cast<const int32_t *>(rec + lay.off_wb_slot);
     const uint16_t *wb_u = reinterpret_cast<const uint16_t *>(rec + lay.off_wb_u);
-    const unsigned char *src = rowbuf[g & 1];
-    unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0);
+    const unsigned char *src = rowbuf[g & 1] + sub * 16;
+    unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + sub * 16;
 #pragma unroll 4
-    for (int e = ltid; e < n_wb; e += kLoaderThreads) {
+    for (int e = grp; e < n_wb; e += GRP) {
       const int32_t slot = wb_slot[e];
       const int u = wb_u[e];
       if (u >= L || slot < 0 || slot >= a.N) {
         raise_error(a.err, SDM_DEVERR_PLAN);
         continue;
       }
-      bulk_store(dst + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK), src + (int64_t)u * RB, RB);
-    }
-    const int64_t t0 = (int64_t)g * G;
-    const int nt = (int)min((int64_t)G, a.T - t0);
-    const unsigned char *ys = tokbuf[g & 1] + tl.y;
-    for (int t = ltid; t < nt; t += kLoaderThreads) {
-      const int64_t row = (b * a.T + t0 + t) * a.H + h;
-      bulk_store(y + row * a.d_v + c0, ys + (int64_t)t * VB, VB);
-    }
-    bulk_commit();
-  };
-
-  if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(&full[i], 1);
-    mbar_init_fence();
-  }
-  __syncthreads();
-
-  bool failed = false;
-  auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
-    if (!failed && !mbar_wait(bar, parity)) {
-      failed = true;
-      raise_error(a.err, SDM_DEVERR_TIMEOUT);
+      *reinterpret_cast<uint4 *>(dst + (int64_t)slot * a.d_v * (int64_t)sizeof(BANK)) =
+          *reinterpret_cast<const uint4 *>(src + (int64_t)u * RB);
     }
   };
 
-  // ---- prologue: records 0 and 1, then stage 0
+  // ---- prologue: record 0, then stage 0 and record 1
   if (is_loader) {
     fetch_record(0);
-    if (S > 1) fetch_record(1);
-    wait_bar(&recb[0], 0);
+    cp_async_commit();
+    cp_async_wait_all();
+    named_barrier(1, kLoaderThreads);
     fetch_stage(0);
-    fetch_late(0);
+    if (S > 1) fetch_record(1);
     cp_async_commit();
   }
 
-  constexpr int RG = 32 / NCG;
   const bool fast = W <= RG * kJB && R <= RG * kJB;
   for (int g = 0; g < S; ++g) {
-    if (is_loader) cp_async_wait_all();                          // gates (and cp.async token data)
-    wait_bar(&full[g & 1], (g >> 1) & 1);                        // rows + bulk token data of stage g
-    wait_bar(&recb[g % 3], (g / 3) & 1);                         // record g
-    __syncthreads();                                             // stage g resident
-    {
-      const unsigned char *rec = plan_of(g);
+    if (is_loader) cp_async_wait_all();
+    named_barrier(2, NTHR);                                      // stage g resident
+    const unsigned char *rec = plan_of(g);
+    if (!is_loader) {
+      // rows shared with stage g-1 come from its buffer (the bank may still be stale)
       const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
       const bool ok = hdr_ok(hdr);
       if (!ok && tid == 0) raise_error(a.err, SDM_DEVERR_PLAN);
@@ -255,7 +201,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
       const uint32_t *carry = reinterpret_cast<const uint32_t *>(rec + lay.off_carry);
       const unsigned char *from = rowbuf[(g + 1) & 1];
       unsigned char *to = rowbuf[g & 1];
-      for (int i = is_loader ? n_carry * CPR : tid; i < n_carry * CPR; i += 32 * NCW) {
+      for (int i = tid; i < n_carry * CPR; i += 32 * NCW) {
         const int e = i / CPR, c = i % CPR;
         const int u = carry[e] & 0xffff, src = carry[e] >> 16;
         if (u >= L || src >= L) {
@@ -266,31 +212,30 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
             *reinterpret_cast<const uint4 *>(from + (int64_t)src * RB + c * 16);
       }
     }
-    if (!is_loader) fence_proxy_async_shared();                  // carried rows before bulk stores read them
-    __syncthreads();                                             // carries in place
+    named_barrier(3, NTHR);                                      // carries in place
 
     if (!is_loader) {
       // ---- compute: tokens of stage g in order; warp w owns column groups [w*NCG, w*NCG+NCG)
-      const unsigned char *rec = plan_of(g);
       const uint16_t *refmap = reinterpret_cast<const uint16_t *>(rec + lay.off_refmap);
       const uint8_t *tokflag = rec + lay.off_tokflag;
       const unsigned char *tb = tokbuf[g & 1];
       const float *wts = reinterpret_cast<const float *>(tb + tl.wts);
       const float *gt = reinterpret_cast<const float *>(tb + tl.gates);
       const ACT *vv = reinterpret_cast<const ACT *>(tb + tl.v);
-      ACT *ys = reinterpret_cast<ACT *>(tokbuf[g & 1] + tl.y);  // y of the stage, stored by the loaders
       const int cg = warp * NCG + lane % NCG;                 // column group in the slice
       const int rg = lane / NCG;
       unsigned char *rows = rowbuf[g & 1] + cg * 16;
       const int64_t t0 = (int64_t)g * G;
       const int nt = (int)min((int64_t)G, a.T - t0);
+      ACT *yrow = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + cg * VEC;
+      const int64_t ystep = (int64_t)a.H * a.d_v;
       if (fast) {
         auto load_refs = [&](int t, LaneRefs &r) {
           const uint16_t *rm = refmap + t * WR;
 #pragma unroll
           for (int bb = 0; bb < kJB; ++bb) {
             const int j = rg + bb * RG;
-            int uw = j < W ? rm[j] : 0, ur = j < R ? rm[W + j] : 0;
+            const int uw = j < W ? rm[j] : 0, ur = j < R ? rm[W + j] : 0;
             r.uw[bb] = (uw < L ? uw : 0) * RB;
             r.ur[bb] = (ur < L ? ur : 0) * RB;
           }
@@ -303,7 +248,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
           load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
           token_write_read<BANK, NCG>(W, R, cur, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, rows, tokflag[t] != 0,
                                       out);
-          if (lane < NCG) store_vec<ACT, VEC>(ys + t * CW + cg * VEC, out);
+          if (lane < NCG) store_vec<ACT, VEC>(yrow + t * ystep, out);
           __syncwarp();
           cur = nxt;
         }
@@ -324,34 +269,21 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
           __syncwarp();
           float out[VEC];
           weighted_read_cols<BANK, NCG>(R, w + W, rrow, out);
-          if (lane < NCG) store_vec<ACT, VEC>(ys + t * CW + cg * VEC, out);
+          if (lane < NCG) store_vec<ACT, VEC>(yrow + t * ystep, out);
           __syncwarp();
         }
       }
-      fence_proxy_async_shared();                              // row updates before the bulk stores
     } else {
-      // ---- loaders: stage g+1 goes into the buffer stage g-1 used once stage g-1's bulk
-      // stores have read it; rows stage g-1 held (the planner's late rows) only once those
-      // stores' writes are performed; then record g+2
-      bulk_wait_read();                                        // stage g-1's bulk stores read their rows
+      // ---- loaders: retire stage g-1, then fetch stage g+1 into its buffer and record g+2
+      if (g >= 1) write_back(g - 1);
       named_barrier(1, kLoaderThreads);
-      if (g + 1 < S) {
-        wait_bar(&recb[(g + 1) % 3], ((g + 1) / 3) & 1);
-        fetch_stage(g + 1);
-      }
-      bulk_wait_all();                                         // ... and their writes are performed
-      named_barrier(1, kLoaderThreads);
-      if (g + 1 < S) fetch_late(g + 1);
-      if (g + 2 < S) {
-        if (ltid == 0) fence_proxy_async_shared();
-        fetch_record(g + 2);
-      }
+      if (g + 1 < S) fetch_stage(g + 1);
+      if (g + 2 < S) fetch_record(g + 2);
       cp_async_commit();
     }
-    __syncthreads();                                             // stage g computed
-    if (is_loader) write_back(g);
+    named_barrier(4, NTHR);                                      // stage g computed
   }
-  if (is_loader) bulk_wait_all();                                // smem must outlive the stores
+  if (is_loader && S > 0) write_back(S - 1);
 }
 
 template <typename BANK, typename ACT>
@@ -394,7 +326,7 @@ int64_t write_read_smem_bytes(int CW, int bank_elem, int act_elem, int G, int W,
                               int64_t rec_bytes) {
   const int64_t L = (int64_t)G * (W + R);
   const TokLayout t = tok_layout(G, W, R, CW, act_elem);
-  return 2 * L * CW * bank_elem + 3 * rec_bytes + 2 * t.bytes + 64;   // + 5 mbarriers
+  return 2 * L * CW * bank_elem + 3 * rec_bytes + 2 * t.bytes;
 }
 
 cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_dtype,
