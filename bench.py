@@ -18,6 +18,7 @@ is reported.  --impl reference times the CPU oracle on the host instead (rank 0 
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -230,10 +231,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override the workload's T (smaller cases for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_env()
     cfg = sdm_inputs.CONFIGS[WORKLOADS[args.workload]]
+    if args.seq_len > 0 and cfg.T > 1:
+        cfg = dataclasses.replace(cfg, T=args.seq_len)
 
     if args.impl == "reference":
         return reference_arm(args, cfg, rank, world)
