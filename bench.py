@@ -75,15 +75,22 @@ def kernel_source_hash() -> str:
 def recorded_traffic(workload: str):
     """DRAM bytes per write/read launch from a committed ncu summary, if it was taken on
     the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"write_read_{workload}_traffic.json")
+    path = os.path.join(ROOT, "profiles", f"write_read_{workload}_traffic.txt")
+    rec = {}
     try:
         with open(path) as f:
-            rec = json.load(f)
-    except Exception:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+    except OSError:
         return None
     if rec.get("kernel_source_sha") != kernel_source_hash():
         return None
-    return rec.get("dram_bytes_per_launch")
+    try:
+        return int(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 class ClockSampler:
