@@ -23,8 +23,9 @@ EXPORTS = (
     "sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
     "sdm_decode_step", "sdm_last_device_error", "sdm_status_string", "sdm_last_error_message",
     "sdm_abi_version", "sdm_launch_count", "sdm_profile_begin", "sdm_profile_end",
-    "sdm_kernel_name",
+    "sdm_kernel_name", "sdm_write_read_static",
 )
+STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class SdmShape(ctypes.Structure):
@@ -82,6 +83,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.sdm_decode_workspace_size.argtypes = [sp, szp]
     lib.sdm_write_read.argtypes = [sp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    ctypes.c_size_t, _P]
+    lib.sdm_write_read_static.argtypes = [sp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.sdm_decode_step.argtypes = [sp, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _P,
                                     _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     lib.sdm_last_device_error.argtypes = [_P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int32), _P]
@@ -96,7 +98,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.sdm_kernel_name.argtypes = [ctypes.c_int32]
     lib.sdm_kernel_name.restype = ctypes.c_char_p
     for name in ("sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
-                 "sdm_decode_step", "sdm_last_device_error", "sdm_profile_begin", "sdm_profile_end"):
+                 "sdm_write_read_static", "sdm_decode_step", "sdm_last_device_error", "sdm_profile_begin", "sdm_profile_end"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.sdm_abi_version() != ABI_VERSION:
         raise ImportError(f"SDM library ABI {lib.sdm_abi_version()} != binding ABI {ABI_VERSION}")

@@ -740,3 +740,43 @@ const char *sdm_kernel_name(int32_t kind) {
 }
 
 }  // extern "C"
+
+// ============================================== write/read with the library's own scratch
+
+namespace {
+
+// Scratch of sdm_write_read_static: one array per device, never allocated at run time.
+static __device__ __align__(256) unsigned char g_static_scratch[SDM_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mu;
+void *g_static_ptr[64] = {nullptr};
+
+}  // namespace
+
+extern "C" sdm_status sdm_write_read_static(const sdm_shape *shape, const void *q_w, const void *q_r,
+                                            const void *k_val, const float *gates, const void *subkeys,
+                                            const void *bank_init, void *bank, void *y, int32_t *idx_w,
+                                            float *wt_w, int32_t *idx_r, float *wt_r, sdm_stream_t stream) {
+  size_t need = 0;
+  sdm_status st = sdm_write_read_workspace_size(shape, &need);
+  if (st != SDM_OK) return st;
+  if (need > SDM_STATIC_SCRATCH_BYTES)
+    return fail(SDM_ERR_WORKSPACE, "shape needs %zu bytes of scratch; the static array holds %zu", need,
+                (size_t)SDM_STATIC_SCRATCH_BYTES);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(SDM_ERR_UNSUPPORTED, "device ordinal %d is not supported", dev);
+  void *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      e = cudaGetSymbolAddress(&scratch, g_static_scratch);
+      if (e != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      g_static_ptr[dev] = scratch;
+    }
+    scratch = g_static_ptr[dev];
+  }
+  return sdm_write_read(shape, q_w, q_r, k_val, gates, subkeys, bank_init, bank, y, idx_w, wt_w, idx_r, wt_r,
+                        scratch, SDM_STATIC_SCRATCH_BYTES, stream);
+}

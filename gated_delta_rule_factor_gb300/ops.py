@@ -123,6 +123,32 @@ def sdm_write_read(q_w: torch.Tensor, q_r: torch.Tensor, k_val: torch.Tensor, ga
     return y
 
 
+def sdm_write_read_static(q_w: torch.Tensor, q_r: torch.Tensor, k_val: torch.Tensor, gates: torch.Tensor,
+                          subkeys: torch.Tensor, bank: torch.Tensor, chunk_size: int, W: int, R: int, *,
+                          factor_dims: Sequence[int], bank_init: Optional[torch.Tensor] = None,
+                          y: torch.Tensor, idx_w: Optional[torch.Tensor] = None,
+                          wt_w: Optional[torch.Tensor] = None, idx_r: Optional[torch.Tensor] = None,
+                          wt_r: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """sdm_write_read on the library's own fixed scratch array: allocates nothing, so the
+    caller passes every output buffer, y included.  Shapes needing more scratch than
+    _abi.STATIC_SCRATCH_BYTES are refused; calls must be ordered on one stream."""
+    dev = q_w.device
+    for name, t in (("q_w", q_w), ("q_r", q_r), ("k_val", k_val), ("gates", gates),
+                    ("subkeys", subkeys), ("bank", bank), ("bank_init", bank_init), ("y", y),
+                    ("idx_w", idx_w), ("wt_w", wt_w), ("idx_r", idx_r), ("wt_r", wt_r)):
+        _require_cuda_contig(name, t, dev)
+    if gates.dtype != torch.float32:
+        raise TypeError("gates must be float32")
+    shape = _shape_of(q_w, k_val, bank, factor_dims, W, R, chunk_size)
+    st = _abi.load().sdm_write_read_static(
+        ctypes.byref(shape), _ptr(q_w), _ptr(q_r), _ptr(k_val), _ptr(gates), _ptr(subkeys),
+        _ptr(bank_init), _ptr(bank), _ptr(y), _ptr(idx_w), _ptr(wt_w), _ptr(idx_r), _ptr(wt_r),
+        _stream_handle(stream, dev))
+    _abi.check(st, "sdm_write_read_static")
+    return y
+
+
 def _owns_storage(t: torch.Tensor) -> bool:
     """True when writing into t cannot reach another tensor's data (the donate guards).
 

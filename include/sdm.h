@@ -141,6 +141,35 @@ sdm_status sdm_write_read(const sdm_shape *shape, const void *q_w, const void *q
                           size_t workspace_bytes, sdm_stream_t stream);
 
 /*
+ * sdm_write_read without a caller-provided workspace.  The method itself has no
+ * counterpart to this: it exists for callers that cannot allocate device memory, such
+ * as a C host that links this library without any allocator, or a framework whose
+ * allocator has reserved the device's memory up front and grants no buffer to a
+ * library call.  Arguments and results are those of sdm_write_read, and so are the
+ * kernels it enqueues; this entry allocates nothing (no cudaMalloc, cudaFree or
+ * allocating routine of any library).
+ *   scratch    a fixed device array of SDM_STATIC_SCRATCH_BYTES (16 MiB) that this
+ *              library defines; shapes whose sdm_write_read_workspace_size exceeds it
+ *              are refused with SDM_ERR_WORKSPACE, nothing enqueued.  Nothing in it
+ *              has to start at zero: the one word the kernels read before writing (the
+ *              device error code) is cleared on `stream` at the start of every call.
+ *   set-up     the first call on a device, with that device current, looks up the
+ *              array's address (cudaGetSymbolAddress) and keeps it; make that first
+ *              call before any stream capture begins.  A failed lookup returns
+ *              SDM_ERR_CUDA.
+ *   races      every call on a device shares the one array: calls whose work may
+ *              overlap on the device (other streams, other host threads) corrupt each
+ *              other's scratch.  Order them on one stream.
+ *   errors     kernel-side codes (SDM_DEVERR_*) land in the array and are not readable
+ *              through sdm_last_device_error; use sdm_write_read to read them.
+ */
+#define SDM_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+sdm_status sdm_write_read_static(const sdm_shape *shape, const void *q_w, const void *q_r,
+                                 const void *k_val, const float *gates, const void *subkeys,
+                                 const void *bank_init, void *bank, void *y, int32_t *idx_w,
+                                 float *wt_w, int32_t *idx_r, float *wt_r, sdm_stream_t stream);
+
+/*
  * One decode step (shape->T must be 1; chunk_size is ignored) for all B*H streams.
  * Tensors as above with T = 1.
  *   bank_in         the state's tables: [B, H, N, d_v], or, with bank_in_shared != 0,
