@@ -228,4 +228,138 @@ __device__ __forceinline__ void token_write_read(int W, int R, const LaneRefs &r
   for (int c = 0; c < VEC; ++c) y[c] = ya[c];
 }
 
+// ------------------------------------------------------------------------------------
+// Block-ordered token step of the write/read kernel on a 128-byte row slice (one warp).
+//
+// Summation order.  The n rows of a sum (n = W for the prediction p, n = R for the
+// read y) are cut into 8 consecutive blocks of B8 = ceil(n / 8) rows; block k is summed
+// in increasing j into a_k and the block sums are combined as
+//   ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)).
+// The order depends on n alone: not on the stage length, nor on the column slicing.
+//
+// Lane layout.  Lane % 8 is a 16-byte column group of the slice (8 x 16 = 128 bytes)
+// and lane / 8 = rg a row group that owns blocks 2rg and 2rg+1, so a lane adds its own
+// pair and two xor steps (8 and 16 lanes apart) finish the tree; IEEE addition is
+// commutative, so both partners of a step hold the same bits afterwards.
+//
+// JB = the most rows one lane holds, >= 2 * B8 for both sums.  Register slot s < JB/2
+// holds row 2rg*B8 + s (block 2rg), slot JB/2 + s holds row 2rg*B8 + B8 + s (block
+// 2rg+1); slots past the block or past n hold nothing.
+template <int JB>
+struct BlockSlots {
+  static constexpr int H = JB / 2;
+  int b8, j0, n;
+  __device__ __forceinline__ BlockSlots(int n_, int rg) : b8((n_ + 7) >> 3), j0(2 * rg * ((n_ + 7) >> 3)), n(n_) {}
+  __device__ __forceinline__ int ref(int s) const { return j0 + (s < H ? s : b8 + s - H); }
+  __device__ __forceinline__ bool has(int s) const { return (s < H ? s : s - H) < b8 && ref(s) < n; }
+};
+
+template <int VEC>
+__device__ __forceinline__ void block_tree(const float (&a0)[VEC], const float (&a1)[VEC], float (&out)[VEC]) {
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) {
+    float x = __fadd_rn(a0[c], a1[c]);
+    x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, 8));
+    out[c] = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, 16));
+  }
+}
+
+// Accumulates the read rows of the token (slots of `rs`) into b0 / b1.
+template <typename BANK, int JB>
+__device__ __forceinline__ void block_read(const BlockSlots<JB> &rs, const uint16_t *rm_r, const float *wt_r,
+                                           const unsigned char *rows, float (&b0)[Vec16<BANK>::N],
+                                           float (&b1)[Vec16<BANK>::N]) {
+  constexpr int VEC = Vec16<BANK>::N, H = JB / 2, RB = 128;
+#pragma unroll
+  for (int s0 = 0; s0 < JB; s0 += 4) {
+    uint4 raw[4];
+    float wr[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int s = s0 + q;
+      if (rs.has(s)) {
+        raw[q] = *reinterpret_cast<const uint4 *>(rows + (int)rm_r[rs.ref(s)] * RB);
+        wr[q] = wt_r[rs.ref(s)];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int s = s0 + q;
+      if (rs.has(s)) {
+        float m[VEC];
+        unpack16<BANK>(raw[q], m);
+        float(&b)[VEC] = s < H ? b0 : b1;
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) b[c] = __fmaf_rn(wr[q], m[c], b[c]);
+      }
+    }
+  }
+}
+
+// One token: the gated delta-rule write of its W rows, then the read of its R rows,
+// with the arithmetic of delta_write_cols / weighted_read_cols per element and the
+// block order above for both sums.  rm / wt: the token's row references (stage-buffer
+// row indices) and weights, W write entries then R read entries; rows: the stage
+// buffer offset by this lane's 16-byte column group.  When the token reads none of the
+// rows it writes (overlap == false) the read runs before the write: those rows hold
+// the same values before and after it.
+// FULL: W == R == 4 * JB, every slot of every lane holds a row (no predicates).
+template <typename BANK, int JB, bool FULL = false>
+__device__ __forceinline__ void token_blocks(int W, int R, const uint16_t *rm, const float *wt, float alpha,
+                                             float beta, const float (&v)[Vec16<BANK>::N], unsigned char *rows,
+                                             bool overlap, float (&y)[Vec16<BANK>::N]) {
+  constexpr int VEC = Vec16<BANK>::N, H = JB / 2, RB = 128;
+  if constexpr (FULL) W = R = 4 * JB;
+  const int rg = (threadIdx.x & 31) >> 3;
+  const BlockSlots<JB> ws(W, rg), rs(R, rg);
+  int ow[JB];
+  float ww[JB];
+  uint4 rw[JB];
+#pragma unroll
+  for (int s = 0; s < JB; ++s) {
+    ow[s] = ws.has(s) ? (int)rm[ws.ref(s)] * RB : 0;
+    ww[s] = ws.has(s) ? wt[ws.ref(s)] : 0.0f;
+  }
+#pragma unroll
+  for (int s = 0; s < JB; ++s)
+    if (ws.has(s)) rw[s] = *reinterpret_cast<const uint4 *>(rows + ow[s]);
+  float b0[VEC], b1[VEC];
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) b0[c] = b1[c] = 0.0f;
+  if (!overlap) block_read<BANK, JB>(rs, rm + W, wt + W, rows, b0, b1);
+
+  float a0[VEC], a1[VEC];
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) a0[c] = a1[c] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < JB; ++s) {
+    if (ws.has(s)) {
+      float m[VEC];
+      unpack16<BANK>(rw[s], m);
+      float(&a)[VEC] = s < H ? a0 : a1;
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) a[c] = __fmaf_rn(ww[s], __fmul_rn(alpha, m[c]), a[c]);
+    }
+  }
+  float p[VEC], d[VEC];
+  block_tree<VEC>(a0, a1, p);
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], p[c]));
+#pragma unroll
+  for (int s = 0; s < JB; ++s) {
+    if (ws.has(s)) {
+      float m[VEC];
+      unpack16<BANK>(rw[s], m);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) m[c] = __fmaf_rn(ww[s], d[c], __fmul_rn(alpha, m[c]));
+      store_vec16<BANK>(reinterpret_cast<BANK *>(rows + ow[s]), m);
+    }
+  }
+  if (overlap) {
+    __syncwarp();
+    block_read<BANK, JB>(rs, rm + W, wt + W, rows, b0, b1);
+  }
+  block_tree<VEC>(b0, b1, y);
+}
+
 }  // namespace sdm

@@ -1,0 +1,307 @@
+// The write/read kernel template (included by the translation units that instantiate
+// it).
+//
+// Parallel axes: streams (b, h) are independent, and so is every bank column (the
+// update of a column reads only that column, see sdm_delta.cuh).  One CTA owns one
+// stream and a slice of CW columns (CW * elem = 32..128 bytes of every row) and runs
+// the stream's tokens in order.  Tokens are staged G at a time; the chunk plan
+// (sdm_plan.cu) lists the distinct rows of each stage.
+//
+// Warp roles (one CTA):
+//   compute warps (1 or 2, each owning up to four 16-byte column groups of the slice):
+//               the tokens of the current stage on the shared-memory rows, and the rows
+//               carried over from the previous stage;
+//   4 loader warps: write back the previous stage's dirty rows, then fetch the next
+//               stage's rows and token data and the stage record after it, all with
+//               16-byte cp.async on the LSU path (a bulk/TMA copy per 128-byte row costs
+//               more than it saves at this granularity).
+// Two row buffers alternate between stages; rows shared by consecutive stages are
+// copied across buffers instead of re-read, because the bank copy may be stale.  Stage
+// records use three buffers (in use / rows being fetched / record being fetched).
+#pragma once
+
+#include "sdm_common.cuh"
+#include "sdm_delta.cuh"
+#include "sdm_internal.h"
+
+namespace sdm {
+namespace wr {
+
+constexpr int kLoaderWarps = 4;
+constexpr int kLoaderThreads = 32 * kLoaderWarps;
+
+struct TokLayout {
+  int64_t wts, gates, v, bytes;  // offsets inside one token-data buffer
+};
+
+__host__ __device__ inline int64_t align16(int64_t x) { return (x + 15) & ~int64_t(15); }
+
+__host__ __device__ inline TokLayout tok_layout(int G, int W, int R, int CW, int act_elem) {
+  TokLayout t;
+  t.wts = 0;
+  t.gates = align16((int64_t)G * (W + R) * 4);
+  t.v = t.gates + align16((int64_t)G * 2 * 4);
+  t.bytes = t.v + align16((int64_t)G * CW * act_elem);
+  return t;
+}
+
+// JB == 0: row-group layout (sdm_delta.cuh token_write_read / delta_write_cols), up to
+// four column groups per compute warp.  JB > 0: the block-ordered layout
+// (token_blocks) on a 128-byte slice, one compute warp, at most JB rows per lane.
+template <typename BANK, int CW, int JB>
+struct WrGeometry {
+  static constexpr int VEC = Vec16<BANK>::N;          // elements per 16 B
+  static constexpr int NCGT = CW / VEC;               // 16-byte column groups of the slice
+  static constexpr int NCG = JB > 0 ? 8 : (NCGT < 4 ? NCGT : 4);  // column groups per compute warp
+  static constexpr int NCW = NCGT / NCG;              // compute warps
+  static constexpr int NTHR = 32 * (NCW + kLoaderWarps);
+  static_assert(JB == 0 || NCGT == 8, "the block-ordered layout takes 128-byte slices");
+};
+
+// FULL (block layout only): W == R == 4 * JB, fixed at compile time.
+template <typename BANK, typename ACT, int CW, int JB, bool FULL = false>
+__global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
+    write_read_kernel(const __grid_constant__ WriteReadArgs a) {
+  using Geo = WrGeometry<BANK, CW, JB>;
+  constexpr int VEC = Geo::VEC, NCG = Geo::NCG, NCW = Geo::NCW, NTHR = Geo::NTHR;
+  static_assert(Geo::NCGT >= 1 && Geo::NCGT <= 8 && (Geo::NCGT & (Geo::NCGT - 1)) == 0, "column slice");
+  constexpr int RB = CW * (int)sizeof(BANK);          // row slice bytes in smem
+  constexpr int CPR = RB / 16;                        // 16-byte chunks per row slice
+
+  extern __shared__ __align__(16) unsigned char smem[];
+  const PlanLayout &lay = a.lay;
+  const int L = lay.L, G = lay.G, S = lay.n_stages;
+  const int W = a.W, R = a.R, WR = W + R;
+  const int64_t s = blockIdx.y;
+  const int slice = blockIdx.x;
+  const int64_t b = s / a.H, h = s % a.H;
+  const int64_t c0 = (int64_t)slice * CW;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool is_loader = warp >= NCW;
+
+  unsigned char *rowbuf[2] = {smem, smem + (int64_t)L * RB};
+  unsigned char *plans = smem + 2 * (int64_t)L * RB;
+  const TokLayout tl = tok_layout(G, W, R, CW, (int)sizeof(ACT));
+  unsigned char *tokbuf[2] = {plans + 3 * lay.rec_bytes, plans + 3 * lay.rec_bytes + tl.bytes};
+
+  BANK *bank = static_cast<BANK *>(a.bank) + s * a.N * a.d_v;   // this stream's table
+  const ACT *kv = static_cast<const ACT *>(a.k_val);
+  ACT *y = static_cast<ACT *>(a.y);
+  const unsigned char *records = a.records + s * (int64_t)S * lay.rec_bytes;
+
+  auto plan_of = [&](int g) -> unsigned char * { return plans + (int64_t)(g % 3) * lay.rec_bytes; };
+  auto hdr_ok = [&](const int32_t *hdr) -> bool {
+    return hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[1] <= L && hdr[2] >= 0 && hdr[2] <= L &&
+           hdr[3] >= 0 && hdr[3] <= L && hdr[4] >= 0 && hdr[4] <= hdr[1];
+  };
+
+  constexpr int VB = CW * (int)sizeof(ACT);          // value bytes per token (>= 16)
+  constexpr int RG = 32 / NCG;
+
+  // ---- loader helpers (threads of the loader warps).  Every copy is a 16-byte cp.async
+  // (or 8/4-byte for the gates and unaligned weights) on the LSU path: CPR lanes take
+  // one row slice, so one warp request covers whole 128-byte lines.
+  const int ltid = tid - 32 * NCW;
+  const int sub = ltid % CPR, grp = ltid / CPR;       // chunk of a row, row group
+  constexpr int GRP = kLoaderThreads / CPR;           // row slices per loader pass
+  const int64_t row_pitch = a.d_v * (int64_t)sizeof(BANK);
+  auto fetch_record = [&](int g) {
+    const unsigned char *src = records + (int64_t)g * lay.rec_bytes;
+    unsigned char *dst = plan_of(g);
+    for (int64_t i = ltid; i < lay.rec_bytes / 16; i += kLoaderThreads) cp_async16(dst + i * 16, src + i * 16);
+  };
+  auto fetch_stage = [&](int g) {
+    const unsigned char *rec = plan_of(g);
+    const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+    const int n_load = hdr_ok(hdr) ? hdr[1] : 0;
+    const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
+    const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
+    unsigned char *dst = rowbuf[g & 1] + sub * 16;
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0) + sub * 16;
+#pragma unroll 4
+    for (int e = grp; e < n_load; e += GRP) {
+      const int32_t slot = load_slot[e];
+      const int u = load_u[e];
+      if (u >= L || slot < 0 || slot >= a.N) {
+        raise_error(a.err, SDM_DEVERR_PLAN);
+        continue;
+      }
+      cp_async16(dst + (int64_t)u * RB, src + (int64_t)slot * row_pitch);
+    }
+    const int64_t t0 = (int64_t)g * G;
+    const int nt = (int)min((int64_t)G, a.T - t0);
+    unsigned char *tb = tokbuf[g & 1];
+    float *wts = reinterpret_cast<float *>(tb + tl.wts);
+    if (a.tok_bulk) {                                  // weights in 16-byte pieces
+      const int wq = W / 4, rq = R / 4;
+      for (int i = ltid; i < nt * (wq + rq); i += kLoaderThreads) {
+        const int t = i / (wq + rq), q = i % (wq + rq);
+        const int64_t row = (b * a.T + t0 + t) * a.H + h;
+        if (q < wq) cp_async16(wts + t * WR + 4 * q, a.wt[0] + row * W + 4 * q);
+        else cp_async16(wts + t * WR + W + 4 * (q - wq), a.wt[1] + row * R + 4 * (q - wq));
+      }
+    } else {
+      for (int i = ltid; i < nt * WR; i += kLoaderThreads) {
+        const int t = i / WR, j = i % WR;
+        const int64_t row = (b * a.T + t0 + t) * a.H + h;
+        const float *src_w = (j < W) ? a.wt[0] + row * W + j : a.wt[1] + row * R + (j - W);
+        cp_async4(wts + i, src_w);
+      }
+    }
+    float *gt = reinterpret_cast<float *>(tb + tl.gates);
+    for (int i = ltid; i < nt; i += kLoaderThreads) {
+      const int64_t row = (b * a.T + t0 + i) * a.H + h;
+      cp_async8(gt + 2 * i, a.gates + row * 2);
+    }
+    unsigned char *vb = tb + tl.v;
+    for (int i = ltid; i < nt * (VB / 16); i += kLoaderThreads) {
+      const int t = i / (VB / 16), c = i % (VB / 16);
+      const int64_t row = (b * a.T + t0 + t) * a.H + h;
+      cp_async16(vb + (int64_t)t * VB + c * 16,
+                 reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
+    }
+  };
+  // Dirty rows of stage g back to the bank (CPR lanes per row slice, 16-byte stores).
+  auto write_back = [&](int g) {
+    const unsigned char *rec = plan_of(g);
+    const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+    const int n_wb = hdr_ok(hdr) ? hdr[3] : 0;
+    const int32_t *wb_slot = reinterpret_cast<const int32_t *>(rec + lay.off_wb_slot);
+    const uint16_t *wb_u = reinterpret_cast<const uint16_t *>(rec + lay.off_wb_u);
+    const unsigned char *src = rowbuf[g & 1] + sub * 16;
+    unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + sub * 16;
+#pragma unroll 4
+    for (int e = grp; e < n_wb; e += GRP) {
+      const int32_t slot = wb_slot[e];
+      const int u = wb_u[e];
+      if (u >= L || slot < 0 || slot >= a.N) {
+        raise_error(a.err, SDM_DEVERR_PLAN);
+        continue;
+      }
+      *reinterpret_cast<uint4 *>(dst + (int64_t)slot * row_pitch) = *reinterpret_cast<const uint4 *>(src + (int64_t)u * RB);
+    }
+  };
+
+  // ---- prologue: record 0, then stage 0 and record 1
+  if (is_loader) {
+    fetch_record(0);
+    cp_async_commit();
+    cp_async_wait_all();
+    named_barrier(1, kLoaderThreads);
+    fetch_stage(0);
+    if (S > 1) fetch_record(1);
+    cp_async_commit();
+  }
+
+  const bool fast = W <= RG * kJB && R <= RG * kJB;
+  for (int g = 0; g < S; ++g) {
+    if (is_loader) cp_async_wait_all();
+    named_barrier(2, NTHR);                                      // stage g resident
+    const unsigned char *rec = plan_of(g);
+    if (!is_loader) {
+      // rows shared with stage g-1 come from its buffer (the bank may still be stale)
+      const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+      const bool ok = hdr_ok(hdr);
+      if (!ok && tid == 0) raise_error(a.err, SDM_DEVERR_PLAN);
+      const int n_carry = ok ? hdr[2] : 0;
+      const uint32_t *carry = reinterpret_cast<const uint32_t *>(rec + lay.off_carry);
+      const unsigned char *from = rowbuf[(g + 1) & 1];
+      unsigned char *to = rowbuf[g & 1];
+      for (int i = tid; i < n_carry * CPR; i += 32 * NCW) {
+        const int e = i / CPR, c = i % CPR;
+        const int u = carry[e] & 0xffff, src = carry[e] >> 16;
+        if (u >= L || src >= L) {
+          raise_error(a.err, SDM_DEVERR_PLAN);
+          continue;
+        }
+        *reinterpret_cast<uint4 *>(to + (int64_t)u * RB + c * 16) =
+            *reinterpret_cast<const uint4 *>(from + (int64_t)src * RB + c * 16);
+      }
+    }
+    named_barrier(3, NTHR);                                      // carries in place
+
+    if (!is_loader) {
+      // ---- compute: tokens of stage g in order; warp w owns column groups [w*NCG, w*NCG+NCG)
+      const uint16_t *refmap = reinterpret_cast<const uint16_t *>(rec + lay.off_refmap);
+      const uint8_t *tokflag = rec + lay.off_tokflag;
+      const unsigned char *tb = tokbuf[g & 1];
+      const float *wts = reinterpret_cast<const float *>(tb + tl.wts);
+      const float *gt = reinterpret_cast<const float *>(tb + tl.gates);
+      const ACT *vv = reinterpret_cast<const ACT *>(tb + tl.v);
+      const int cg = warp * NCG + lane % NCG;                 // column group in the slice
+      const int rg = lane / NCG;
+      unsigned char *rows = rowbuf[g & 1] + cg * 16;
+      const int64_t t0 = (int64_t)g * G;
+      const int nt = (int)min((int64_t)G, a.T - t0);
+      ACT *yrow = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + cg * VEC;
+      const int64_t ystep = (int64_t)a.H * a.d_v;
+      if constexpr (JB > 0) {
+        unsigned char *brows = rowbuf[g & 1] + (lane & 7) * 16;
+        ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + (lane & 7) * VEC;
+        for (int t = 0; t < nt; ++t) {
+          float v[VEC], out[VEC];
+          load_vec<ACT, VEC>(vv + t * CW + (lane & 7) * VEC, v);
+          token_blocks<BANK, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, brows,
+                                       tokflag[t] != 0, out);
+          if (lane < 8) store_vec<ACT, VEC>(ybase + t * ystep, out);
+          __syncwarp();
+        }
+      } else if (fast) {
+        auto load_refs = [&](int t, LaneRefs &r) {
+          const uint16_t *rm = refmap + t * WR;
+#pragma unroll
+          for (int bb = 0; bb < kJB; ++bb) {
+            const int j = rg + bb * RG;
+            const int uw = j < W ? rm[j] : 0, ur = j < R ? rm[W + j] : 0;
+            r.uw[bb] = (uw < L ? uw : 0) * RB;
+            r.ur[bb] = (ur < L ? ur : 0) * RB;
+          }
+        };
+        LaneRefs cur, nxt;
+        if (nt > 0) load_refs(0, cur);
+        for (int t = 0; t < nt; ++t) {
+          if (t + 1 < nt) load_refs(t + 1, nxt);
+          float v[VEC], out[VEC];
+          load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
+          token_write_read<BANK, NCG>(W, R, cur, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, rows, tokflag[t] != 0,
+                                      out);
+          if (lane < NCG) store_vec<ACT, VEC>(yrow + t * ystep, out);
+          __syncwarp();
+          cur = nxt;
+        }
+      } else {
+        for (int t = 0; t < nt; ++t) {
+          const uint16_t *rm = refmap + t * WR;
+          const float *w = wts + t * WR;
+          auto row_ptr = [&](int j) -> BANK * {
+            int u = rm[j];
+            if (u >= L) u = 0;                         // plan_sort never emits these
+            return reinterpret_cast<BANK *>(rows + (int64_t)u * RB);
+          };
+          auto wrow = [&](int j) { return row_ptr(j); };
+          auto rrow = [&](int j) { return row_ptr(W + j); };
+          float v[VEC];
+          load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
+          delta_write_cols<BANK, NCG>(W, w, gt[2 * t], gt[2 * t + 1], v, wrow, wrow);
+          __syncwarp();
+          float out[VEC];
+          weighted_read_cols<BANK, NCG>(R, w + W, rrow, out);
+          if (lane < NCG) store_vec<ACT, VEC>(yrow + t * ystep, out);
+          __syncwarp();
+        }
+      }
+    } else {
+      // ---- loaders: retire stage g-1, then fetch stage g+1 into its buffer and record g+2
+      if (g >= 1) write_back(g - 1);
+      named_barrier(1, kLoaderThreads);
+      if (g + 1 < S) fetch_stage(g + 1);
+      if (g + 2 < S) fetch_record(g + 2);
+      cp_async_commit();
+    }
+    named_barrier(4, NTHR);                                      // stage g computed
+  }
+  if (is_loader && S > 0) write_back(S - 1);
+}
+
+}  // namespace wr
+}  // namespace sdm

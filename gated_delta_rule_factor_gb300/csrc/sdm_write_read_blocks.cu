@@ -1,0 +1,44 @@
+// Instances of the write/read kernel on 128-byte row slices with the block-ordered
+// token step (sdm_delta.cuh token_blocks): one compute warp per slice, JB = the most
+// rows a lane holds (8, 16 or 32: W and R up to 32, 64 or 128), and W = R = 64 with the
+// row counts fixed at compile time.
+#include "sdm_wr_kernel.cuh"
+
+namespace sdm {
+
+namespace {
+
+template <typename BANK, typename ACT>
+cudaError_t launch_blocks_t(const WriteReadArgs &a, int64_t streams, int64_t smem, cudaStream_t st) {
+  constexpr int CW = 128 / (int)sizeof(BANK);
+  dim3 grid((unsigned)a.slices, (unsigned)streams);
+  auto go = [&](auto kern, int threads) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, threads, smem, st>>>(a);
+    return cudaGetLastError();
+  };
+  // rows per lane: 2 * ceil(n / 8) for the larger of W and R
+  const int n = a.W > a.R ? a.W : a.R;
+  const int per_lane = 2 * ((n + 7) / 8);
+  if (a.W == 64 && a.R == 64)
+    return go(wr::write_read_kernel<BANK, ACT, CW, 16, true>, wr::WrGeometry<BANK, CW, 16>::NTHR);
+  if (per_lane <= 8) return go(wr::write_read_kernel<BANK, ACT, CW, 8>, wr::WrGeometry<BANK, CW, 8>::NTHR);
+  if (per_lane <= 16) return go(wr::write_read_kernel<BANK, ACT, CW, 16>, wr::WrGeometry<BANK, CW, 16>::NTHR);
+  if (per_lane <= 32) return go(wr::write_read_kernel<BANK, ACT, CW, 32>, wr::WrGeometry<BANK, CW, 32>::NTHR);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_write_read_blocks(const WriteReadArgs &a, int64_t streams, int bank_dtype, int act_dtype,
+                                     int64_t smem, cudaStream_t st) {
+  if (bank_dtype == SDM_F32) {
+    if (act_dtype == SDM_F32) return launch_blocks_t<float, float>(a, streams, smem, st);
+    return launch_blocks_t<float, __nv_bfloat16>(a, streams, smem, st);
+  }
+  if (act_dtype == SDM_F32) return launch_blocks_t<__nv_bfloat16, float>(a, streams, smem, st);
+  return launch_blocks_t<__nv_bfloat16, __nv_bfloat16>(a, streams, smem, st);
+}
+
+}  // namespace sdm
