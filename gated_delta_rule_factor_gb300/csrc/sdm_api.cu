@@ -186,13 +186,12 @@ int pow2_at_least(int64_t x) {
   return p;
 }
 
-// Sort width of a factor (EF) and of the candidate list (EC), in keys per lane.
-void sort_widths(const Derived &d, const CandidateList &cl, int *EF, int *EC) {
-  int maxnf = 0;
-  for (int f = 0; f < d.g.F; ++f) maxnf = std::max(maxnf, d.g.nf[f]);
-  *EF = maxnf <= 64 ? 2 : 8;
-  const int nc = std::max(cl.n[0], cl.n[1]);
-  *EC = std::max(4, pow2_at_least(nc) / 32);
+// Sort width of a factor (EF) and of the candidate list (EC), in keys per lane: both are
+// sorted in chunks of 128 keys merged into a running best 128 (k <= SDM_MAX_K = 128),
+// which keeps the selection kernels' register use low enough for several CTAs per SM.
+void sort_widths(const Derived &, const CandidateList &, int *EF, int *EC) {
+  *EF = 4;
+  *EC = 4;
 }
 
 // ---------------------------------------------------------------- plan / kernel config
@@ -388,33 +387,46 @@ bool use_tensor_cores(const Derived &d, const sdm_shape *sh) {
   return score_tc_supported(d.g, sh->act_dtype);
 }
 
-}  // namespace
+// Per-device side stream and fork / join events of write_read_impl, created on first use
+// and kept for the life of the process.  A call holds `mu` from recording the fork to
+// recording the join.  If another call re-records the join before this call's main
+// stream waits on it, the wait also covers that later copy (the side stream runs the
+// copies in order): it can only wait longer, never too little.
+struct SideStream {
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+SideStream g_side[64];
+std::mutex g_side_mu;
 
-// =================================================================== C ABI
-
-extern "C" {
-
-sdm_status sdm_write_read_workspace_size(const sdm_shape *shape, size_t *bytes) {
-  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
-  Derived d;
-  sdm_status st = check_shape(shape, false, &d);
-  if (st != SDM_OK) return st;
-  *bytes = (size_t)write_read_ws_bytes(shape);
-  return ok();
+sdm_status side_stream(SideStream **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(SDM_ERR_UNSUPPORTED, "device ordinal %d is not supported", dev);
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream &s = g_side[dev];
+  if (!s.st) {
+    e = cudaStreamCreateWithFlags(&s.st, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      s.st = nullptr;
+      return fail(SDM_ERR_CUDA, "side stream set-up: %s", cudaGetErrorString(e));
+    }
+  }
+  *out = &s;
+  return SDM_OK;
 }
 
-sdm_status sdm_decode_workspace_size(const sdm_shape *shape, size_t *bytes) {
-  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
-  sdm_status st = check_shape(shape, true, nullptr);
-  if (st != SDM_OK) return st;
-  *bytes = (size_t)kHeaderBytes;
-  return ok();
-}
-
-sdm_status sdm_write_read(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
-                          const float *gates, const void *subkeys, const void *bank_init, void *bank,
-                          void *y, int32_t *idx_w, float *wt_w, int32_t *idx_r, float *wt_r,
-                          void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+// The write/read op.  side_copy: run the learned-table copy on the library's side stream
+// of the device, concurrently with scoring, selection and planning (they touch no bank
+// row), and join it before the write/read kernel.
+sdm_status write_read_impl(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
+                           const float *gates, const void *subkeys, const void *bank_init, void *bank,
+                           void *y, int32_t *idx_w, float *wt_w, int32_t *idx_r, float *wt_r,
+                           void *workspace, size_t workspace_bytes, sdm_stream_t stream, bool side_copy) {
   Derived d;
   sdm_status st = check_shape(sh, false, &d);
   if (st != SDM_OK) return st;
@@ -475,10 +487,28 @@ sdm_status sdm_write_read(const sdm_shape *sh, const void *q_w, const void *q_r,
   if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
 
   const int64_t streams = sh->B * sh->H;
+  SideStream *side = nullptr;
   if (bank_init && streams > 0) {
     BankCopyArgs bc{bank_init, bank, sh->B, d.N * sh->d_v * sb, sh->H};
-    if ((st = run_kernel(SDM_KERNEL_BANK_COPY, cs, "bank_copy", [&] { return launch_bank_copy(bc, sms, cs); })) != SDM_OK)
-      return st;
+    cudaStream_t copy_st = cs;
+    if (side_copy && rows > 0) {
+      if ((st = side_stream(&side)) != SDM_OK) return st;
+      side->mu.lock();
+      ce = cudaEventRecord(side->fork, cs);
+      if (ce == cudaSuccess) ce = cudaStreamWaitEvent(side->st, side->fork, 0);
+      if (ce != cudaSuccess) {
+        side->mu.unlock();
+        return fail(SDM_ERR_CUDA, "side stream fork: %s", cudaGetErrorString(ce));
+      }
+      copy_st = side->st;
+    }
+    st = run_kernel(SDM_KERNEL_BANK_COPY, copy_st, "bank_copy", [&] { return launch_bank_copy(bc, sms, copy_st); });
+    if (side) {
+      ce = cudaEventRecord(side->join, side->st);
+      side->mu.unlock();
+      if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "side stream join: %s", cudaGetErrorString(ce));
+    }
+    if (st != SDM_OK) return st;
   }
   if (rows == 0) return ok();
 
@@ -558,11 +588,46 @@ sdm_status sdm_write_read(const sdm_shape *sh, const void *q_w, const void *q_r,
   wa.slices = (int32_t)(sh->d_v / wc.CW);
   wa.tok_bulk = (sh->W % 4 == 0 && sh->R % 4 == 0 && aligned(ww, 16) && aligned(wr, 16)) ? 1 : 0;
   wa.lay = wc.lay;
+  if (side) {                                          // the bank copy must land first
+    ce = cudaStreamWaitEvent(cs, side->join, 0);
+    if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "side stream join: %s", cudaGetErrorString(ce));
+  }
   if ((st = run_kernel(SDM_KERNEL_WRITE_READ, cs, "write_read", [&] {
          return launch_write_read(wa, streams, sh->bank_dtype, sh->act_dtype, wc.CW, wc.smem, cs);
        })) != SDM_OK)
     return st;
   return ok();
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+sdm_status sdm_write_read_workspace_size(const sdm_shape *shape, size_t *bytes) {
+  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
+  Derived d;
+  sdm_status st = check_shape(shape, false, &d);
+  if (st != SDM_OK) return st;
+  *bytes = (size_t)write_read_ws_bytes(shape);
+  return ok();
+}
+
+sdm_status sdm_decode_workspace_size(const sdm_shape *shape, size_t *bytes) {
+  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
+  sdm_status st = check_shape(shape, true, nullptr);
+  if (st != SDM_OK) return st;
+  *bytes = (size_t)kHeaderBytes;
+  return ok();
+}
+
+sdm_status sdm_write_read(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
+                          const float *gates, const void *subkeys, const void *bank_init, void *bank,
+                          void *y, int32_t *idx_w, float *wt_w, int32_t *idx_r, float *wt_r,
+                          void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+  return write_read_impl(sh, q_w, q_r, k_val, gates, subkeys, bank_init, bank, y, idx_w, wt_w, idx_r, wt_r,
+                         workspace, workspace_bytes, stream, true);
 }
 
 sdm_status sdm_decode_step(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
@@ -777,6 +842,6 @@ extern "C" sdm_status sdm_write_read_static(const sdm_shape *shape, const void *
     }
     scratch = g_static_ptr[dev];
   }
-  return sdm_write_read(shape, q_w, q_r, k_val, gates, subkeys, bank_init, bank, y, idx_w, wt_w, idx_r, wt_r,
-                        scratch, SDM_STATIC_SCRATCH_BYTES, stream);
+  return write_read_impl(shape, q_w, q_r, k_val, gates, subkeys, bank_init, bank, y, idx_w, wt_w, idx_r, wt_r,
+                         scratch, SDM_STATIC_SCRATCH_BYTES, stream, false);
 }

@@ -160,11 +160,7 @@ cudaError_t launch_decode_dt(const DecodeArgs &a, const CandidateList &cl, int E
     kern<<<(unsigned)(a.B * a.H), kThreads, smem, st>>>(a, cl);
     return cudaGetLastError();
   };
-#define SDM_DEC_CASE(ef, ec) \
-  if (EF == ef && EC == ec) return go(decode_kernel<ef, ec, ACT, BANK>);
-  SDM_DEC_CASE(2, 4) SDM_DEC_CASE(2, 8) SDM_DEC_CASE(2, 16) SDM_DEC_CASE(2, 32)
-  SDM_DEC_CASE(8, 4) SDM_DEC_CASE(8, 8) SDM_DEC_CASE(8, 16) SDM_DEC_CASE(8, 32)
-#undef SDM_DEC_CASE
+  if (EF == 4 && EC == 4) return go(decode_kernel<4, 4, ACT, BANK>);
   return cudaErrorInvalidValue;
 }
 

@@ -34,7 +34,12 @@ template <int EF, int EC>
 cudaError_t launch_select_t(const SelectArgs &a, const CandidateList &cl, int sm_count, cudaStream_t st) {
   const int64_t warps_needed = 2 * a.rows;
   int64_t blocks = (warps_needed + kThreads / 32 - 1) / (kThreads / 32);
-  const int64_t cap = (int64_t)sm_count * 4;
+  // one wave of resident CTAs, each warp looping over rows
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_kernel<EF, EC>, kThreads, 0) != cudaSuccess)
+    per_sm = 0;
+  const int64_t cap = (int64_t)sm_count * (per_sm > 0 ? per_sm : 2);
   if (blocks > cap) blocks = cap;
   select_kernel<EF, EC><<<(unsigned)blocks, kThreads, 0, st>>>(a, cl);
   return cudaGetLastError();
@@ -45,11 +50,7 @@ cudaError_t launch_select_t(const SelectArgs &a, const CandidateList &cl, int sm
 cudaError_t launch_select(const SelectArgs &a, const CandidateList &cl, int EF, int EC, int sm_count,
                           cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
-#define SDM_SEL_CASE(ef, ec) \
-  if (EF == ef && EC == ec) return launch_select_t<ef, ec>(a, cl, sm_count, st);
-  SDM_SEL_CASE(2, 4) SDM_SEL_CASE(2, 8) SDM_SEL_CASE(2, 16) SDM_SEL_CASE(2, 32)
-  SDM_SEL_CASE(8, 4) SDM_SEL_CASE(8, 8) SDM_SEL_CASE(8, 16) SDM_SEL_CASE(8, 32)
-#undef SDM_SEL_CASE
+  if (EF == 4 && EC == 4) return launch_select_t<4, 4>(a, cl, sm_count, st);
   return cudaErrorInvalidValue;
 }
 

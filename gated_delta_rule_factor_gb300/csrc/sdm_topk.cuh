@@ -77,27 +77,37 @@ __device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry 
   }
   __syncwarp();
 
-  // 2. candidate tuples, keyed and sorted best first
+  // 2. candidate tuples, keyed and kept best first: chunks of 32*EC keys are sorted and
+  // merged into the running 32*EC best (k <= 32*EC)
   uint64_t ck[EC];
+  for (int c0 = 0; c0 < ncand; c0 += 32 * EC) {
+    uint64_t kk[EC];
 #pragma unroll
-  for (int e = 0; e < EC; ++e) {
-    const int c = lane * EC + e;
-    if (c < ncand) {
-      const uint32_t t = cand[c];
-      const int p0 = t & 255, p1 = (t >> 8) & 255, p2 = (t >> 16) & 255, p3 = t >> 24;
-      float S = sc.fs[p0];
-      if (g.F > 1) S = __fadd_rn(S, sc.fs[SDM_MAX_K + p1]);
-      if (g.F > 2) S = __fadd_rn(S, sc.fs[2 * SDM_MAX_K + p2]);
-      if (g.F > 3) S = __fadd_rn(S, sc.fs[3 * SDM_MAX_K + p3]);
-      const uint32_t sum = p0 + p1 + p2 + p3;
-      const uint32_t low = ((255u - sum) << 24) | ((255u - p0) << 16) | ((255u - p1) << 8) |
-                           (255u - p2);
-      ck[e] = ((uint64_t)ordered_bits(S) << 32) | low;
+    for (int e = 0; e < EC; ++e) {
+      const int c = c0 + lane * EC + e;
+      if (c < ncand) {
+        const uint32_t t = cand[c];
+        const int p0 = t & 255, p1 = (t >> 8) & 255, p2 = (t >> 16) & 255, p3 = t >> 24;
+        float S = sc.fs[p0];
+        if (g.F > 1) S = __fadd_rn(S, sc.fs[SDM_MAX_K + p1]);
+        if (g.F > 2) S = __fadd_rn(S, sc.fs[2 * SDM_MAX_K + p2]);
+        if (g.F > 3) S = __fadd_rn(S, sc.fs[3 * SDM_MAX_K + p3]);
+        const uint32_t sum = p0 + p1 + p2 + p3;
+        const uint32_t low = ((255u - sum) << 24) | ((255u - p0) << 16) | ((255u - p1) << 8) |
+                             (255u - p2);
+        kk[e] = ((uint64_t)ordered_bits(S) << 32) | low;
+      } else {
+        kk[e] = 0ull;
+      }
+    }
+    warp_sort_desc<EC>(kk);
+    if (c0 == 0) {
+#pragma unroll
+      for (int e = 0; e < EC; ++e) ck[e] = kk[e];
     } else {
-      ck[e] = 0ull;
+      warp_merge_top_desc<EC>(ck, kk);
     }
   }
-  warp_sort_desc<EC>(ck);
 
   // 3. softmax weights of the k best (fixed summation order) and slot ids
   const float S0 = from_ordered_bits((uint32_t)(__shfl_sync(0xffffffffu, ck[0], 0) >> 32));
