@@ -79,10 +79,12 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool is_loader = warp >= NCW;
 
-  unsigned char *rowbuf[2] = {smem, smem + (int64_t)L * RB};
+  // Buffer addresses are computed, not kept in an indexed array, so that they stay
+  // shared-memory addresses for the compiler.
+  auto rowbuf = [&](int i) -> unsigned char * { return smem + (int64_t)(i & 1) * L * RB; };
   unsigned char *plans = smem + 2 * (int64_t)L * RB;
   const TokLayout tl = tok_layout(G, W, R, CW, (int)sizeof(ACT));
-  unsigned char *tokbuf[2] = {plans + 3 * lay.rec_bytes, plans + 3 * lay.rec_bytes + tl.bytes};
+  auto tokbuf = [&](int i) -> unsigned char * { return plans + 3 * lay.rec_bytes + (int64_t)(i & 1) * tl.bytes; };
 
   BANK *bank = static_cast<BANK *>(a.bank) + s * a.N * a.d_v;   // this stream's table
   const ACT *kv = static_cast<const ACT *>(a.k_val);
@@ -110,16 +112,20 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
     unsigned char *dst = plan_of(g);
     for (int64_t i = ltid; i < lay.rec_bytes / 16; i += kLoaderThreads) cp_async16(dst + i * 16, src + i * 16);
   };
-  auto fetch_stage = [&](int g) {
+  // Rows of stage g's load list with index in [lo, hi) (the last hdr[4] entries are the
+  // rows of stage g-2, which must wait for that stage's write-back).
+  auto fetch_rows = [&](int g, bool early, bool late) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
     const int n_load = hdr_ok(hdr) ? hdr[1] : 0;
+    const int n_late = hdr_ok(hdr) ? hdr[4] : 0;
+    const int lo = early ? 0 : n_load - n_late, hi = late ? n_load : n_load - n_late;
     const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
     const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
-    unsigned char *dst = rowbuf[g & 1] + sub * 16;
+    unsigned char *dst = rowbuf(g & 1) + sub * 16;
     const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0) + sub * 16;
 #pragma unroll 4
-    for (int e = grp; e < n_load; e += GRP) {
+    for (int e = lo + grp; e < hi; e += GRP) {
       const int32_t slot = load_slot[e];
       const int u = load_u[e];
       if (u >= L || slot < 0 || slot >= a.N) {
@@ -128,9 +134,11 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
       }
       cp_async16(dst + (int64_t)u * RB, src + (int64_t)slot * row_pitch);
     }
+  };
+  auto fetch_tokens = [&](int g) {
     const int64_t t0 = (int64_t)g * G;
     const int nt = (int)min((int64_t)G, a.T - t0);
-    unsigned char *tb = tokbuf[g & 1];
+    unsigned char *tb = tokbuf(g & 1);
     float *wts = reinterpret_cast<float *>(tb + tl.wts);
     if (a.tok_bulk) {                                  // weights in 16-byte pieces
       const int wq = W / 4, rq = R / 4;
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
     const int n_wb = hdr_ok(hdr) ? hdr[3] : 0;
     const int32_t *wb_slot = reinterpret_cast<const int32_t *>(rec + lay.off_wb_slot);
     const uint16_t *wb_u = reinterpret_cast<const uint16_t *>(rec + lay.off_wb_u);
-    const unsigned char *src = rowbuf[g & 1] + sub * 16;
+    const unsigned char *src = rowbuf(g & 1) + sub * 16;
     unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + sub * 16;
 #pragma unroll 4
     for (int e = grp; e < n_wb; e += GRP) {
@@ -182,6 +190,10 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
     }
   };
 
+  auto fetch_stage = [&](int g) {
+    fetch_rows(g, true, true);
+    fetch_tokens(g);
+  };
   // ---- prologue: record 0, then stage 0 and record 1
   if (is_loader) {
     fetch_record(0);
@@ -205,8 +217,8 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
       if (!ok && tid == 0) raise_error(a.err, SDM_DEVERR_PLAN);
       const int n_carry = ok ? hdr[2] : 0;
       const uint32_t *carry = reinterpret_cast<const uint32_t *>(rec + lay.off_carry);
-      const unsigned char *from = rowbuf[(g + 1) & 1];
-      unsigned char *to = rowbuf[g & 1];
+      const unsigned char *from = rowbuf((g + 1) & 1);
+      unsigned char *to = rowbuf(g & 1);
       for (int i = tid; i < n_carry * CPR; i += 32 * NCW) {
         const int e = i / CPR, c = i % CPR;
         const int u = carry[e] & 0xffff, src = carry[e] >> 16;
@@ -224,19 +236,19 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
       // ---- compute: tokens of stage g in order; warp w owns column groups [w*NCG, w*NCG+NCG)
       const uint16_t *refmap = reinterpret_cast<const uint16_t *>(rec + lay.off_refmap);
       const uint8_t *tokflag = rec + lay.off_tokflag;
-      const unsigned char *tb = tokbuf[g & 1];
+      const unsigned char *tb = tokbuf(g & 1);
       const float *wts = reinterpret_cast<const float *>(tb + tl.wts);
       const float *gt = reinterpret_cast<const float *>(tb + tl.gates);
       const ACT *vv = reinterpret_cast<const ACT *>(tb + tl.v);
       const int cg = warp * NCG + lane % NCG;                 // column group in the slice
       const int rg = lane / NCG;
-      unsigned char *rows = rowbuf[g & 1] + cg * 16;
+      unsigned char *rows = rowbuf(g & 1) + cg * 16;
       const int64_t t0 = (int64_t)g * G;
       const int nt = (int)min((int64_t)G, a.T - t0);
       ACT *yrow = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + cg * VEC;
       const int64_t ystep = (int64_t)a.H * a.d_v;
       if constexpr (JB > 0) {
-        unsigned char *brows = rowbuf[g & 1] + (lane & 7) * 16;
+        unsigned char *brows = rowbuf(g & 1) + (lane & 7) * 16;
         ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + (lane & 7) * VEC;
         for (int t = 0; t < nt; ++t) {
           float v[VEC], out[VEC];
