@@ -317,4 +317,10 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrives at named barrier `id` without waiting (a producer's signal to threads that
+// bar.sync on it); the arriving threads' earlier memory accesses are ordered before it.
+__device__ __forceinline__ void named_barrier_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
 }  // namespace sdm

@@ -61,8 +61,9 @@ __device__ __forceinline__ int find_sorted(const int32_t *a, int n, int32_t key)
 __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_constant__ PlanArgs a, int P) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint64_t *keys = reinterpret_cast<uint64_t *>(smem);            // [P]
-  uint8_t *wr = reinterpret_cast<uint8_t *>(keys + P);              // [P]
-  uint8_t *tokflag = wr + P;                                        // [G]
+  uint8_t *wr = reinterpret_cast<uint8_t *>(keys + P);              // [P], 4-byte aligned
+  const int P4 = (P + 3) & ~3;                                      // wr is updated by words
+  uint8_t *tokflag = wr + P4;                                       // [G]
   __shared__ int warp_sums[kThreads / 32];
 
   const PlanLayout &lay = a.lay;
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
   const int L = nt * WR;
   const int tid = threadIdx.x;
 
+  for (int i = tid; i < P4; i += kThreads) wr[i] = 0;
   for (int i = tid; i < P; i += kThreads) {
     uint64_t key = ~0ull;
     if (i < L) {
@@ -89,7 +91,6 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
       key = ((uint64_t)(uint32_t)slot << 16) | (uint32_t)i;
     }
     keys[i] = key;
-    wr[i] = 0;
   }
   for (int i = tid; i < lay.G; i += kThreads) tokflag[i] = 0;
   __syncthreads();
@@ -126,7 +127,11 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
     const int ref = (int)(keys[i] & 0xffffu);
     refmap[ref] = (uint16_t)u;
     if (ref % WR < a.W) {
-      wr[u] = 1;
+      // bit 0: written in this stage; bit 1: written by the stage's last token (such rows
+      // can only be written back once the whole stage is done).  A row's refs may be
+      // split between threads, hence the word-wide atomic OR.
+      const uint32_t bits = (ref / WR == nt - 1) ? 3u : 1u;
+      atomicOr(reinterpret_cast<unsigned int *>(wr + (u & ~3)), bits << (8 * (u & 3)));
       // a token's refs to one row are adjacent in (slot, ref) order, its write before its
       // read: a read ref of the same token right after this write ref means overlap
       if (i + 1 < L && (keys[i + 1] >> 16) == slot) {
@@ -171,7 +176,9 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
   const int u0 = min(n_cur, tid * ept), u1 = min(n_cur, u0 + ept);
   // A row loaded here that stage g-2 also held may have been written back at the end of
   // stage g-2, which the write/read kernel only waits for late: such loads go last.
-  int c_load = 0, c_late = 0, c_carry = 0, c_wb = 0;
+  // Write-backs are listed rows-the-last-token-did-not-write first: the kernel stores
+  // those while the stage's last token still runs, the rest ("wb late") after it.
+  int c_load = 0, c_late = 0, c_carry = 0, c_wb = 0, c_wbl = 0;
   for (int u = u0; u < u1; ++u) {
     const int32_t slot = cur[u];
     const int src = find_sorted(prev, n_prev, slot);
@@ -180,13 +187,17 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
     c_load += src < 0 && !late;
     c_late += late;
     c_carry += src >= 0;
-    c_wb += ((written[u] || src >= 0) && !out);
+    const bool wb = (written[u] || src >= 0) && !out;
+    c_wb += wb && !(written[u] & 2);
+    c_wbl += wb && (written[u] & 2);
   }
-  int n_load, n_late, n_carry, n_wb;
+  int n_load, n_late, n_carry, n_wb_early, n_wb_late;
   int o_load = block_scan_exclusive(c_load, warp_sums, &n_load);
   int o_late = n_load + block_scan_exclusive(c_late, warp_sums, &n_late);
   int o_carry = block_scan_exclusive(c_carry, warp_sums, &n_carry);
-  int o_wb = block_scan_exclusive(c_wb, warp_sums, &n_wb);
+  int o_wb = block_scan_exclusive(c_wb, warp_sums, &n_wb_early);
+  int o_wbl = n_wb_early + block_scan_exclusive(c_wbl, warp_sums, &n_wb_late);
+  const int n_wb = n_wb_early + n_wb_late;
 
   unsigned char *rec = a.records + stage * lay.rec_bytes;
   int32_t *load_slot = reinterpret_cast<int32_t *>(rec + lay.off_load_slot);
@@ -209,9 +220,10 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
       ++o_carry;
     }
     if ((written[u] || src >= 0) && !out) {
-      wb_slot[o_wb] = slot;
-      wb_u[o_wb] = (uint16_t)u;
-      ++o_wb;
+      int &o = (written[u] & 2) ? o_wbl : o_wb;
+      wb_slot[o] = slot;
+      wb_u[o] = (uint16_t)u;
+      ++o;
     }
   }
   if (tid == 0) {
@@ -221,6 +233,7 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
     hdr[2] = n_carry;
     hdr[3] = n_wb;
     hdr[4] = n_late;
+    hdr[5] = n_wb_late;
   }
 }
 
@@ -228,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
 
 cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int P, cudaStream_t st) {
   if (streams == 0 || a.lay.n_stages == 0) return cudaSuccess;
-  const int64_t smem = (int64_t)P * 9 + a.lay.G;
+  const int64_t smem = (int64_t)P * 8 + ((P + 3) & ~3) + a.lay.G;
   cudaError_t e = cudaFuncSetAttribute(plan_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

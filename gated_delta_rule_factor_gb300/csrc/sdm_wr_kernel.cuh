@@ -8,13 +8,18 @@
 // (sdm_plan.cu) lists the distinct rows of each stage.
 //
 // Warp roles (one CTA):
-//   compute warps (1 or 2, each owning up to four 16-byte column groups of the slice):
-//               the tokens of the current stage on the shared-memory rows, and the rows
-//               carried over from the previous stage;
-//   4 loader warps: write back the previous stage's dirty rows, then fetch the next
-//               stage's rows and token data and the stage record after it, all with
+//   compute warps: 128-byte slices, one warp (block-ordered token step); narrower slices,
+//               1 or 2 warps of up to four 16-byte column groups (row-group step).  They
+//               run the tokens of the current stage on the shared-memory rows;
+//   loader warps (8 for 128-byte slices, 4 otherwise): write back the previous stage's
+//               remaining dirty rows (the ones its last token wrote), fetch the next
+//               stage's rows, its token data and the stage record after it, all with
 //               16-byte cp.async on the LSU path (a bulk/TMA copy per 128-byte row costs
-//               more than it saves at this granularity).
+//               more than it saves at this granularity), then, once the compute warps
+//               signal (barrier 5) that the current stage's next-to-last token is done,
+//               write back the current stage's dirty rows its last token leaves alone.
+//               More loader warps keep more row requests in flight.
+//   every warp copies the rows carried over from the previous stage.
 // Two row buffers alternate between stages; rows shared by consecutive stages are
 // copied across buffers instead of re-read, because the bank copy may be stale.  Stage
 // records use three buffers (in use / rows being fetched / record being fetched).
@@ -27,8 +32,6 @@
 namespace sdm {
 namespace wr {
 
-constexpr int kLoaderWarps = 4;
-constexpr int kLoaderThreads = 32 * kLoaderWarps;
 
 struct TokLayout {
   int64_t wts, gates, v, bytes;  // offsets inside one token-data buffer
@@ -54,7 +57,8 @@ struct WrGeometry {
   static constexpr int NCGT = CW / VEC;               // 16-byte column groups of the slice
   static constexpr int NCG = JB > 0 ? 8 : (NCGT < 4 ? NCGT : 4);  // column groups per compute warp
   static constexpr int NCW = NCGT / NCG;              // compute warps
-  static constexpr int NTHR = 32 * (NCW + kLoaderWarps);
+  static constexpr int LW = JB > 0 ? 8 : 4;           // loader warps
+  static constexpr int NTHR = 32 * (NCW + LW);
   static_assert(JB == 0 || NCGT == 8, "the block-ordered layout takes 128-byte slices");
 };
 
@@ -63,6 +67,7 @@ template <typename BANK, typename ACT, int CW, int JB, bool FULL = false>
 __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
     write_read_kernel(const __grid_constant__ WriteReadArgs a) {
   using Geo = WrGeometry<BANK, CW, JB>;
+  constexpr int kLoaderThreads = 32 * Geo::LW;
   constexpr int VEC = Geo::VEC, NCG = Geo::NCG, NCW = Geo::NCW, NTHR = Geo::NTHR;
   static_assert(Geo::NCGT >= 1 && Geo::NCGT <= 8 && (Geo::NCGT & (Geo::NCGT - 1)) == 0, "column slice");
   constexpr int RB = CW * (int)sizeof(BANK);          // row slice bytes in smem
@@ -94,7 +99,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
   auto plan_of = [&](int g) -> unsigned char * { return plans + (int64_t)(g % 3) * lay.rec_bytes; };
   auto hdr_ok = [&](const int32_t *hdr) -> bool {
     return hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[1] <= L && hdr[2] >= 0 && hdr[2] <= L &&
-           hdr[3] >= 0 && hdr[3] <= L && hdr[4] >= 0 && hdr[4] <= hdr[1];
+           hdr[3] >= 0 && hdr[3] <= L && hdr[4] >= 0 && hdr[4] <= hdr[1] && hdr[5] >= 0 && hdr[5] <= hdr[3];
   };
 
   constexpr int VB = CW * (int)sizeof(ACT);          // value bytes per token (>= 16)
@@ -170,16 +175,20 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
     }
   };
   // Dirty rows of stage g back to the bank (CPR lanes per row slice, 16-byte stores).
-  auto write_back = [&](int g) {
+  // Dirty rows of stage g back to the bank: early = the rows its last token does not
+  // write (stored while that token runs), late = the rest (stored after the stage).
+  auto write_back = [&](int g, bool early) {
     const unsigned char *rec = plan_of(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
-    const int n_wb = hdr_ok(hdr) ? hdr[3] : 0;
+    const bool ok = hdr_ok(hdr);
+    const int n_all = ok ? hdr[3] : 0, n_late = ok ? hdr[5] : 0;
+    const int lo = early ? 0 : n_all - n_late, n_wb = early ? n_all - n_late : n_all;
     const int32_t *wb_slot = reinterpret_cast<const int32_t *>(rec + lay.off_wb_slot);
     const uint16_t *wb_u = reinterpret_cast<const uint16_t *>(rec + lay.off_wb_u);
     const unsigned char *src = rowbuf(g & 1) + sub * 16;
     unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + sub * 16;
 #pragma unroll 4
-    for (int e = grp; e < n_wb; e += GRP) {
+    for (int e = lo + grp; e < n_wb; e += GRP) {
       const int32_t slot = wb_slot[e];
       const int u = wb_u[e];
       if (u >= L || slot < 0 || slot >= a.N) {
@@ -210,8 +219,9 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
     if (is_loader) cp_async_wait_all();
     named_barrier(2, NTHR);                                      // stage g resident
     const unsigned char *rec = plan_of(g);
-    if (!is_loader) {
-      // rows shared with stage g-1 come from its buffer (the bank may still be stale)
+    {
+      // rows shared with stage g-1 come from its buffer (the bank may still be stale);
+      // every warp of the CTA copies
       const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
       const bool ok = hdr_ok(hdr);
       if (!ok && tid == 0) raise_error(a.err, SDM_DEVERR_PLAN);
@@ -219,7 +229,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
       const uint32_t *carry = reinterpret_cast<const uint32_t *>(rec + lay.off_carry);
       const unsigned char *from = rowbuf((g + 1) & 1);
       unsigned char *to = rowbuf(g & 1);
-      for (int i = tid; i < n_carry * CPR; i += 32 * NCW) {
+      for (int i = tid; i < n_carry * CPR; i += NTHR) {
         const int e = i / CPR, c = i % CPR;
         const int u = carry[e] & 0xffff, src = carry[e] >> 16;
         if (u >= L || src >= L) {
@@ -250,6 +260,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
       if constexpr (JB > 0) {
         unsigned char *brows = rowbuf(g & 1) + (lane & 7) * 16;
         ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + (lane & 7) * VEC;
+        if (nt <= 1) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);
         for (int t = 0; t < nt; ++t) {
           float v[VEC], out[VEC];
           load_vec<ACT, VEC>(vv + t * CW + (lane & 7) * VEC, v);
@@ -257,6 +268,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
                                        tokflag[t] != 0, out);
           if (lane < 8) store_vec<ACT, VEC>(ybase + t * ystep, out);
           __syncwarp();
+          if (t == nt - 2) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);  // rows the last token leaves alone are final
         }
       } else if (fast) {
         auto load_refs = [&](int t, LaneRefs &r) {
@@ -271,6 +283,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
         };
         LaneRefs cur, nxt;
         if (nt > 0) load_refs(0, cur);
+        if (nt <= 1) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);
         for (int t = 0; t < nt; ++t) {
           if (t + 1 < nt) load_refs(t + 1, nxt);
           float v[VEC], out[VEC];
@@ -279,9 +292,11 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
                                       out);
           if (lane < NCG) store_vec<ACT, VEC>(yrow + t * ystep, out);
           __syncwarp();
+          if (t == nt - 2) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);  // rows the last token leaves alone are final
           cur = nxt;
         }
       } else {
+        if (nt <= 1) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);
         for (int t = 0; t < nt; ++t) {
           const uint16_t *rm = refmap + t * WR;
           const float *w = wts + t * WR;
@@ -300,19 +315,22 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
           weighted_read_cols<BANK, NCG>(R, w + W, rrow, out);
           if (lane < NCG) store_vec<ACT, VEC>(yrow + t * ystep, out);
           __syncwarp();
+          if (t == nt - 2) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);  // rows the last token leaves alone are final
         }
       }
     } else {
       // ---- loaders: retire stage g-1, then fetch stage g+1 into its buffer and record g+2
-      if (g >= 1) write_back(g - 1);
+      if (g >= 1) write_back(g - 1, false);
       named_barrier(1, kLoaderThreads);
       if (g + 1 < S) fetch_stage(g + 1);
       if (g + 2 < S) fetch_record(g + 2);
       cp_async_commit();
+      named_barrier(5, kLoaderThreads + 32 * NCW);             // stage g's next-to-last token done
+      write_back(g, true);
     }
     named_barrier(4, NTHR);                                      // stage g computed
   }
-  if (is_loader && S > 0) write_back(S - 1);
+  if (is_loader && S > 0) write_back(S - 1, false);
 }
 
 }  // namespace wr
