@@ -362,4 +362,134 @@ __device__ __forceinline__ void token_blocks(int W, int R, const uint16_t *rm, c
   block_tree<VEC>(b0, b1, y);
 }
 
+// ------------------------------------------------------------------------------------
+// The same token step with the rows split between two warps (same summation order, so
+// the results are bitwise those of token_blocks).  Warp wsel's row group rg owns block
+// k = 4*wsel + rg alone: a lane adds its block, two xor steps inside the warp give
+// (a0+a1)+(a2+a3) in warp 0 and (a4+a5)+(a6+a7) in warp 1, and the warps swap those
+// through shared memory (xch: [2 warps][8 column groups][VEC] floats) on a 64-thread
+// named barrier `bar`.  JB >= B8: register slot s holds row k*B8 + s.
+template <int JB>
+struct BlockSlots1 {
+  int b8, j0, n;
+  __device__ __forceinline__ BlockSlots1(int n_, int k) : b8((n_ + 7) >> 3), j0(k * ((n_ + 7) >> 3)), n(n_) {}
+  __device__ __forceinline__ int ref(int s) const { return j0 + s; }
+  __device__ __forceinline__ bool has(int s) const { return s < b8 && j0 + s < n; }
+};
+
+template <int VEC>
+__device__ __forceinline__ void pair_tree(const float (&a)[VEC], float (&out)[VEC], float *xch, int wsel, int bar) {
+  const int lane = threadIdx.x & 31;
+  float x[VEC];
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) {
+    x[c] = __fadd_rn(a[c], __shfl_xor_sync(0xffffffffu, a[c], 8));
+    x[c] = __fadd_rn(x[c], __shfl_xor_sync(0xffffffffu, x[c], 16));
+  }
+  float *mine = xch + (wsel * 8 + (lane & 7)) * VEC;
+  const float *theirs = xch + ((wsel ^ 1) * 8 + (lane & 7)) * VEC;
+  if (lane < 8) {
+#pragma unroll
+    for (int c = 0; c < VEC; c += 4)
+      *reinterpret_cast<float4 *>(mine + c) = make_float4(x[c], x[c + 1], x[c + 2], x[c + 3]);
+  }
+  named_barrier(bar, 64);
+#pragma unroll
+  for (int c = 0; c < VEC; c += 4) {
+    const float4 o = *reinterpret_cast<const float4 *>(theirs + c);
+    out[c] = __fadd_rn(x[c], o.x);
+    out[c + 1] = __fadd_rn(x[c + 1], o.y);
+    out[c + 2] = __fadd_rn(x[c + 2], o.z);
+    out[c + 3] = __fadd_rn(x[c + 3], o.w);
+  }
+}
+
+template <typename BANK, int JB>
+__device__ __forceinline__ void pair_read(const BlockSlots1<JB> &rs, const uint16_t *rm_r, const float *wt_r,
+                                          const unsigned char *rows, float (&b)[Vec16<BANK>::N]) {
+  constexpr int VEC = Vec16<BANK>::N, RB = 128;
+#pragma unroll
+  for (int s0 = 0; s0 < JB; s0 += 4) {
+    uint4 raw[4];
+    float wr[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int s = s0 + q;
+      if (rs.has(s)) {
+        raw[q] = *reinterpret_cast<const uint4 *>(rows + (int)rm_r[rs.ref(s)] * RB);
+        wr[q] = wt_r[rs.ref(s)];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (rs.has(s0 + q)) {
+        float m[VEC];
+        unpack16<BANK>(raw[q], m);
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) b[c] = __fmaf_rn(wr[q], m[c], b[c]);
+      }
+    }
+  }
+}
+
+// FULL: W == R == 8 * JB.  The read's exchange barrier comes after the row stores, so it
+// also orders this token's writes before the next token's loads in the other warp.
+template <typename BANK, int JB, bool FULL = false>
+__device__ __forceinline__ void token_blocks2(int W, int R, const uint16_t *rm, const float *wt, float alpha,
+                                              float beta, const float (&v)[Vec16<BANK>::N], unsigned char *rows,
+                                              bool overlap, float (&y)[Vec16<BANK>::N], float *xch_p, float *xch_y,
+                                              int wsel, int bar) {
+  constexpr int VEC = Vec16<BANK>::N, RB = 128;
+  if constexpr (FULL) W = R = 8 * JB;
+  const int k = 4 * wsel + ((threadIdx.x & 31) >> 3);
+  const BlockSlots1<JB> ws(W, k), rs(R, k);
+  int ow[JB];
+  float ww[JB];
+  uint4 rw[JB];
+#pragma unroll
+  for (int s = 0; s < JB; ++s) {
+    ow[s] = ws.has(s) ? (int)rm[ws.ref(s)] * RB : 0;
+    ww[s] = ws.has(s) ? wt[ws.ref(s)] : 0.0f;
+  }
+#pragma unroll
+  for (int s = 0; s < JB; ++s)
+    if (ws.has(s)) rw[s] = *reinterpret_cast<const uint4 *>(rows + ow[s]);
+  float b[VEC];
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) b[c] = 0.0f;
+  if (!overlap) pair_read<BANK, JB>(rs, rm + W, wt + W, rows, b);
+
+  float a[VEC];
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) a[c] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < JB; ++s) {
+    if (ws.has(s)) {
+      float m[VEC];
+      unpack16<BANK>(rw[s], m);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) a[c] = __fmaf_rn(ww[s], __fmul_rn(alpha, m[c]), a[c]);
+    }
+  }
+  float p[VEC], d[VEC];
+  pair_tree<VEC>(a, p, xch_p, wsel, bar);
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], p[c]));
+#pragma unroll
+  for (int s = 0; s < JB; ++s) {
+    if (ws.has(s)) {
+      float m[VEC];
+      unpack16<BANK>(rw[s], m);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) m[c] = __fmaf_rn(ww[s], d[c], __fmul_rn(alpha, m[c]));
+      store_vec16<BANK>(reinterpret_cast<BANK *>(rows + ow[s]), m);
+    }
+  }
+  if (overlap) {
+    named_barrier(bar, 64);
+    pair_read<BANK, JB>(rs, rm + W, wt + W, rows, b);
+  }
+  pair_tree<VEC>(b, y, xch_y, wsel, bar);
+}
+
 }  // namespace sdm

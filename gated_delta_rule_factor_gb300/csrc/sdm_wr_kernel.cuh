@@ -56,7 +56,7 @@ struct WrGeometry {
   static constexpr int VEC = Vec16<BANK>::N;          // elements per 16 B
   static constexpr int NCGT = CW / VEC;               // 16-byte column groups of the slice
   static constexpr int NCG = JB > 0 ? 8 : (NCGT < 4 ? NCGT : 4);  // column groups per compute warp
-  static constexpr int NCW = NCGT / NCG;              // compute warps
+  static constexpr int NCW = JB > 0 ? 2 : NCGT / NCG;  // compute warps (block layout: rows split)
   static constexpr int LW = JB > 0 ? 8 : 4;           // loader warps
   static constexpr int NTHR = 32 * (NCW + LW);
   static_assert(JB == 0 || NCGT == 8, "the block-ordered layout takes 128-byte slices");
@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
   constexpr int CPR = RB / 16;                        // 16-byte chunks per row slice
 
   extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ __align__(16) float xch[JB > 0 ? 2 * 2 * 8 * VEC : 4];  // block layout: the two warps' partial sums
   const PlanLayout &lay = a.lay;
   const int L = lay.L, G = lay.G, S = lay.n_stages;
   const int W = a.W, R = a.R, WR = W + R;
@@ -258,15 +259,17 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
       ACT *yrow = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + cg * VEC;
       const int64_t ystep = (int64_t)a.H * a.d_v;
       if constexpr (JB > 0) {
+        // both compute warps work on the same 16-byte column groups, rows split (sdm_delta.cuh
+        // token_blocks2); warp 0 stores y
         unsigned char *brows = rowbuf(g & 1) + (lane & 7) * 16;
         ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + (lane & 7) * VEC;
         if (nt <= 1) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);
         for (int t = 0; t < nt; ++t) {
           float v[VEC], out[VEC];
           load_vec<ACT, VEC>(vv + t * CW + (lane & 7) * VEC, v);
-          token_blocks<BANK, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, brows,
-                                       tokflag[t] != 0, out);
-          if (lane < 8) store_vec<ACT, VEC>(ybase + t * ystep, out);
+          token_blocks2<BANK, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, brows,
+                                        tokflag[t] != 0, out, xch, xch + 2 * 8 * VEC, warp, 6);
+          if (warp == 0 && lane < 8) store_vec<ACT, VEC>(ybase + t * ystep, out);
           __syncwarp();
           if (t == nt - 2) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);  // rows the last token leaves alone are final
         }

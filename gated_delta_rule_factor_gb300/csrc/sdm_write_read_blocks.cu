@@ -1,7 +1,7 @@
 // Instances of the write/read kernel on 128-byte row slices with the block-ordered
-// token step (sdm_delta.cuh token_blocks): one compute warp per slice, JB = the most
-// rows a lane holds (8, 16 or 32: W and R up to 32, 64 or 128), and W = R = 64 with the
-// row counts fixed at compile time.
+// token step (sdm_delta.cuh token_blocks2): two compute warps per slice splitting the
+// rows, JB = the most rows a lane holds (4, 8 or 16: W and R up to 32, 64 or 128), and
+// W = R = 64 with the row counts fixed at compile time.
 #include "sdm_wr_kernel.cuh"
 
 namespace sdm {
@@ -18,14 +18,14 @@ cudaError_t launch_blocks_t(const WriteReadArgs &a, int64_t streams, int64_t sme
     kern<<<grid, threads, smem, st>>>(a);
     return cudaGetLastError();
   };
-  // rows per lane: 2 * ceil(n / 8) for the larger of W and R
+  // rows per lane: one block of ceil(n / 8) rows for the larger of W and R
   const int n = a.W > a.R ? a.W : a.R;
-  const int per_lane = 2 * ((n + 7) / 8);
+  const int per_lane = (n + 7) / 8;
   if (a.W == 64 && a.R == 64)
-    return go(wr::write_read_kernel<BANK, ACT, CW, 16, true>, wr::WrGeometry<BANK, CW, 16>::NTHR);
+    return go(wr::write_read_kernel<BANK, ACT, CW, 8, true>, wr::WrGeometry<BANK, CW, 8>::NTHR);
+  if (per_lane <= 4) return go(wr::write_read_kernel<BANK, ACT, CW, 4>, wr::WrGeometry<BANK, CW, 4>::NTHR);
   if (per_lane <= 8) return go(wr::write_read_kernel<BANK, ACT, CW, 8>, wr::WrGeometry<BANK, CW, 8>::NTHR);
   if (per_lane <= 16) return go(wr::write_read_kernel<BANK, ACT, CW, 16>, wr::WrGeometry<BANK, CW, 16>::NTHR);
-  if (per_lane <= 32) return go(wr::write_read_kernel<BANK, ACT, CW, 32>, wr::WrGeometry<BANK, CW, 32>::NTHR);
   return cudaErrorInvalidValue;
 }
 
