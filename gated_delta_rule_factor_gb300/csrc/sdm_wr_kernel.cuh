@@ -11,14 +11,14 @@
 //   compute warps: 128-byte slices, one warp (block-ordered token step); narrower slices,
 //               1 or 2 warps of up to four 16-byte column groups (row-group step).  They
 //               run the tokens of the current stage on the shared-memory rows;
-//   loader warps (8 for 128-byte slices, 4 otherwise): write back the previous stage's
-//               remaining dirty rows (the ones its last token wrote), fetch the next
-//               stage's rows, its token data and the stage record after it, all with
-//               16-byte cp.async on the LSU path (a bulk/TMA copy per 128-byte row costs
-//               more than it saves at this granularity), then, once the compute warps
-//               signal (barrier 5) that the current stage's next-to-last token is done,
-//               write back the current stage's dirty rows its last token leaves alone.
-//               More loader warps keep more row requests in flight.
+//   loader warps (8 for 128-byte slices, 4 otherwise): fetch the next stage's rows, its
+//               token data and the stage record after it, all with 16-byte cp.async on the
+//               LSU path (a bulk/TMA copy per 128-byte row costs more than it saves at this
+//               granularity); once the compute warps signal (barrier 5) that the current
+//               stage's next-to-last token is done, write back the current stage's dirty
+//               rows its last token leaves alone, and after the stage the rest of them,
+//               while the next stage's rows are still landing.  More loader warps keep
+//               more row requests in flight.
 //   every warp copies the rows carried over from the previous stage.
 // Two row buffers alternate between stages; rows shared by consecutive stages are
 // copied across buffers instead of re-read, because the bank copy may be stale.  Stage
@@ -322,9 +322,9 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
         }
       }
     } else {
-      // ---- loaders: retire stage g-1, then fetch stage g+1 into its buffer and record g+2
-      if (g >= 1) write_back(g - 1, false);
-      named_barrier(1, kLoaderThreads);
+      // ---- loaders: fetch stage g+1 into its buffer (stage g-1's, fully written back at
+      // the end of that stage) and record g+2, then store the rows of stage g its last
+      // token leaves alone once the compute warps are past its next-to-last token
       if (g + 1 < S) fetch_stage(g + 1);
       if (g + 2 < S) fetch_record(g + 2);
       cp_async_commit();
@@ -332,8 +332,10 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
       write_back(g, true);
     }
     named_barrier(4, NTHR);                                      // stage g computed
+    // the rest of stage g's dirty rows go back while the next stage's rows land; the next
+    // stage barrier orders these stores before any later load of the same rows
+    if (is_loader) write_back(g, false);
   }
-  if (is_loader && S > 0) write_back(S - 1, false);
 }
 
 }  // namespace wr
