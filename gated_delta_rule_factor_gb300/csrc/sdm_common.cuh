@@ -71,6 +71,45 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t (&key)[E]) {
   }
 }
 
+// Two independent warp_sort_desc runs interleaved step by step (twice the work in
+// flight per shuffle latency).
+template <int E>
+__device__ __forceinline__ void warp_sort_desc2(uint64_t (&ka)[E], uint64_t (&kb)[E]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32 * E; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= E) {
+        const int lj = j / E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = lane * E + e;
+          const uint64_t oa = __shfl_xor_sync(0xffffffffu, ka[e], lj);
+          const uint64_t ob = __shfl_xor_sync(0xffffffffu, kb[e], lj);
+          const bool keep_max = ((i & k) == 0) == ((i & j) == 0);
+          ka[e] = keep_max ? (ka[e] > oa ? ka[e] : oa) : (ka[e] < oa ? ka[e] : oa);
+          kb[e] = keep_max ? (kb[e] > ob ? kb[e] : ob) : (kb[e] < ob ? kb[e] : ob);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & j) == 0) {
+            const int i = lane * E + e;
+            const bool desc = (i & k) == 0;
+            const uint64_t a = ka[e], b = ka[e | j], c = kb[e], d = kb[e | j];
+            const bool sa = desc ? (a < b) : (a > b), sc = desc ? (c < d) : (c > d);
+            ka[e] = sa ? b : a;
+            ka[e | j] = sa ? a : b;
+            kb[e] = sc ? d : c;
+            kb[e | j] = sc ? c : d;
+          }
+        }
+      }
+    }
+  }
+}
+
 // Keeps the 32*E largest of two descending lists: `key` becomes the descending
 // merge of max(key[i], other[P-1-i]) (a bitonic sequence), P = 32*E.
 template <int E>

@@ -10,7 +10,7 @@ namespace sdm {
 namespace {
 
 template <int EF, int EC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
     select_kernel(const __grid_constant__ SelectArgs a, const __grid_constant__ CandidateList cl) {
   __shared__ uint32_t cand[2 * SDM_MAX_CANDIDATES];
   __shared__ RowScratch rs[kThreads / 32];

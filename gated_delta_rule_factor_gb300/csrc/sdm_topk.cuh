@@ -33,6 +33,40 @@ struct RowScratch {
   int32_t fi[SDM_MAX_FACTORS * SDM_MAX_K];
 };
 
+// The 32*E best keys of a list of n keys, best first: chunks of 32*E keys (made by
+// make(first index, keys)) are sorted two at a time and merged into the running best.
+template <int E, class Make>
+__device__ __forceinline__ void top_of_chunks(int n, Make make, uint64_t (&best)[E]) {
+  constexpr int P = 32 * E;
+  bool have = false;
+  int c0 = 0;
+  for (; c0 + P < n; c0 += 2 * P) {
+    uint64_t ka[E], kb[E];
+    make(c0, ka);
+    make(c0 + P, kb);
+    warp_sort_desc2<E>(ka, kb);
+    if (!have) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) best[e] = ka[e];
+      have = true;
+    } else {
+      warp_merge_top_desc<E>(best, ka);
+    }
+    warp_merge_top_desc<E>(best, kb);
+  }
+  if (c0 < n) {
+    uint64_t ka[E];
+    make(c0, ka);
+    warp_sort_desc<E>(ka);
+    if (!have) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) best[e] = ka[e];
+    } else {
+      warp_merge_top_desc<E>(best, ka);
+    }
+  }
+}
+
 // scores: the row's ntot factor scores (shared memory), factor f at g.off[f].
 // qsel: 0 = write query (k = W), 1 = read query (k = R).
 // cand: the candidate tuples of this query kind (shared memory), ncand entries.
@@ -43,28 +77,19 @@ __device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry 
                                          int32_t *idx_out, float *wt_out) {
   const int lane = threadIdx.x & 31;
   const int k = g.k[qsel];
-  constexpr int P = 32 * EF;
 
   // 1. best-first order of each factor, kept to its first min(k, n_f) positions
   for (int f = 0; f < g.F; ++f) {
     const int nf = g.nf[f];
     const float *s = scores + g.off[f];
     uint64_t best[EF];
-    for (int c0 = 0; c0 < nf; c0 += P) {
-      uint64_t key[EF];
+    top_of_chunks<EF>(nf, [&](int c0, uint64_t(&key)[EF]) {
 #pragma unroll
       for (int e = 0; e < EF; ++e) {
         const int a = c0 + lane * EF + e;
         key[e] = (a < nf) ? ((uint64_t)ordered_bits(s[a]) << 32) | (uint32_t)a : 0ull;
       }
-      warp_sort_desc<EF>(key);
-      if (c0 == 0) {
-#pragma unroll
-        for (int e = 0; e < EF; ++e) best[e] = key[e];
-      } else {
-        warp_merge_top_desc<EF>(best, key);
-      }
-    }
+    }, best);
     const int kf = g.kf[qsel][f];
 #pragma unroll
     for (int e = 0; e < EF; ++e) {
@@ -77,11 +102,9 @@ __device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry 
   }
   __syncwarp();
 
-  // 2. candidate tuples, keyed and kept best first: chunks of 32*EC keys are sorted and
-  // merged into the running 32*EC best (k <= 32*EC)
+  // 2. candidate tuples, keyed and kept best first (k <= 32*EC)
   uint64_t ck[EC];
-  for (int c0 = 0; c0 < ncand; c0 += 32 * EC) {
-    uint64_t kk[EC];
+  top_of_chunks<EC>(ncand, [&](int c0, uint64_t(&kk)[EC]) {
 #pragma unroll
     for (int e = 0; e < EC; ++e) {
       const int c = c0 + lane * EC + e;
@@ -100,14 +123,7 @@ __device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry 
         kk[e] = 0ull;
       }
     }
-    warp_sort_desc<EC>(kk);
-    if (c0 == 0) {
-#pragma unroll
-      for (int e = 0; e < EC; ++e) ck[e] = kk[e];
-    } else {
-      warp_merge_top_desc<EC>(ck, kk);
-    }
-  }
+  }, ck);
 
   // 3. softmax weights of the k best (fixed summation order) and slot ids
   const float S0 = from_ordered_bits((uint32_t)(__shfl_sync(0xffffffffu, ck[0], 0) >> 32));
