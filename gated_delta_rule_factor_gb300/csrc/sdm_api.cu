@@ -187,11 +187,13 @@ int pow2_at_least(int64_t x) {
 }
 
 // Sort width of a factor (EF) and of the candidate list (EC), in keys per lane: both are
-// sorted in chunks of 128 keys merged into a running best 128 (k <= SDM_MAX_K = 128),
-// which keeps the selection kernels' register use low enough for several CTAs per SM.
-void sort_widths(const Derived &, const CandidateList &, int *EF, int *EC) {
-  *EF = 4;
-  *EC = 4;
+// sorted in chunks of 32*E keys merged into a running best 32*E (k <= 32*E), which keeps
+// the selection kernels' register use low enough for several CTAs per SM.  E = 2 when
+// both k are at most 64 (fewer compare-exchange steps per key), else 4 (k <= 128).
+void sort_widths(const Derived &d, const CandidateList &, int *EF, int *EC) {
+  const int kmax = std::max(d.g.k[0], d.g.k[1]);
+  *EF = kmax <= 64 ? 2 : 4;
+  *EC = *EF;
 }
 
 // ---------------------------------------------------------------- plan / kernel config

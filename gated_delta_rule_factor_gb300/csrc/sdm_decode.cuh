@@ -160,6 +160,7 @@ cudaError_t launch_decode_dt(const DecodeArgs &a, const CandidateList &cl, int E
     kern<<<(unsigned)(a.B * a.H), kThreads, smem, st>>>(a, cl);
     return cudaGetLastError();
   };
+  if (EF == 2 && EC == 2) return go(decode_kernel<2, 2, ACT, BANK>);
   if (EF == 4 && EC == 4) return go(decode_kernel<4, 4, ACT, BANK>);
   return cudaErrorInvalidValue;
 }

@@ -50,6 +50,7 @@ cudaError_t launch_select_t(const SelectArgs &a, const CandidateList &cl, int sm
 cudaError_t launch_select(const SelectArgs &a, const CandidateList &cl, int EF, int EC, int sm_count,
                           cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
+  if (EF == 2 && EC == 2) return launch_select_t<2, 2>(a, cl, sm_count, st);
   if (EF == 4 && EC == 4) return launch_select_t<4, 4>(a, cl, sm_count, st);
   return cudaErrorInvalidValue;
 }
