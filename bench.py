@@ -190,6 +190,20 @@ def _time_oracle(workload: str, budget_s: float, t_max: int, per: int) -> dict:
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def chunk_collision_rate(idx_w, idx_r, chunk: int) -> float:
+    """1 - (distinct rows / references), summed over every chunk of every stream."""
+    import numpy as np
+    B, T, H, _ = idx_w.shape
+    refs = distinct = 0
+    for b in range(B):
+        for h in range(H):
+            for t0 in range(0, T, chunk):
+                ids = np.concatenate([idx_w[b, t0:t0 + chunk, h].ravel(), idx_r[b, t0:t0 + chunk, h].ravel()])
+                refs += ids.size
+                distinct += np.unique(ids).size
+    return 1.0 - distinct / max(refs, 1)
+
+
 def cpu_baseline(workload: str, budget_s: float = 15.0) -> dict:
     """Time the CPU oracle (one thread, fresh process) on a bounded sample of the workload."""
     try:
@@ -323,6 +337,14 @@ def main():
     copy_bytes = 2 * B * H * cfg.N * cfg.d_v * sb
     step_alg = alg_bytes + copy_bytes
 
+    # ---- within-chunk collision rate: 1 - distinct rows / references per chunk of a stream
+    idx_w = torch.empty((B, T, H, cfg.W), dtype=torch.int32, device=dev)
+    idx_r = torch.empty((B, T, H, cfg.R), dtype=torch.int32, device=dev)
+    sdm.sdm_write_read(g["q_w"], g["q_r"], g["k_val"], g["gates"], g["subkeys"], bank, cfg.chunk_size,
+                       cfg.W, cfg.R, factor_dims=cfg.factor_dims, bank_init=g["bank_init"], y=y, idx_w=idx_w,
+                       idx_r=idx_r, workspace=ws, stream=stream)
+    collision = chunk_collision_rate(idx_w.cpu().numpy(), idx_r.cpu().numpy(), cfg.chunk_size)
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -371,7 +393,11 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "parallelism": f"streams sharded, {world} independent ranks",
                    "l2": "inputs larger than L2: the 1 GiB bank is rewritten from the learned table every step",
-                   "step": "bank copy + scoring/top-k + chunk plan + fused write/read"},
+                   "step": "bank copy + scoring/top-k + chunk plan + fused write/read",
+                   "chunk_collision_rate": collision},
+        "roofline_2w_r": {"note": "written rows counted as read and written: B*T*H*(2W+R)*d_v*elem",
+                          "achieved": alg_bytes * (2 * cfg.W + cfg.R) / (cfg.W + cfg.R) / wr_avg_s / 1e9,
+                          "frac": alg_bytes * (2 * cfg.W + cfg.R) / (cfg.W + cfg.R) / wr_avg_s / 1e9 / peak},
         "roofline": {"bound": "hbm", "kernel": "write_read", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_kind,
