@@ -38,8 +38,9 @@ METRIC = "SDM write/read tokens/s per layer on 1 GB300; achieved HBM GB/s vs roo
 UNIT = "tokens/s"
 WORKLOADS = {"layer": "layer", "train_fwd": "train_fwd", "three_factor": "three_factor",
              "decode": "decode", "tiny": "tiny"}
-KERNEL_SOURCES = ("sdm_write_read.cu", "sdm_write_read_blocks.cu", "sdm_wr_kernel.cuh", "sdm_delta.cuh",
-                  "sdm_common.cuh", "sdm_internal.h")
+KERNEL_SOURCES = ("sdm_write_read.cu", "sdm_write_read_f32_f32.cu", "sdm_write_read_f32_bf16.cu",
+                  "sdm_write_read_bf16_f32.cu", "sdm_write_read_bf16_bf16.cu", "sdm_wr_kernel.cuh",
+                  "sdm_delta.cuh", "sdm_common.cuh", "sdm_internal.h")
 
 
 def dist_env():

@@ -226,12 +226,14 @@ struct WrChoice {
   int64_t smem = 0;
 };
 
-// Column slices the write/read kernel is compiled for: 16..128 bytes of a row.
+// Column slices the write/read kernel is compiled for: 16..128 bytes of a row and at
+// least 8 columns (one or more per compute lane).
 void cw_candidates(const sdm_shape *sh, std::vector<int> &out) {
   out.clear();
   const int sb = (int)elem_bytes(sh->bank_dtype), ab = (int)elem_bytes(sh->act_dtype);
   for (int bytes = 128; bytes >= 16; bytes >>= 1) {
     const int cw = bytes / sb;
+    if (cw < 8) continue;
     if (cw * ab < 16) continue;            // value slice must be a whole 16-byte chunk
     if (sh->d_v % cw != 0) continue;
     out.push_back(cw);

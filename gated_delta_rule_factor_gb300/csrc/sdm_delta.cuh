@@ -1,6 +1,4 @@
-// Per-token gated delta-rule write and weighted read over a column slice, by one warp
-// (shared by the write/read kernel, which keeps rows in shared memory, and the decode
-// kernel, which works on the bank in global memory, so both do identical arithmetic).
+// Per-token gated delta-rule write and weighted read.
 //
 // For one token with forget gate alpha, input gate beta, value v and the W selected
 // rows M[i_j] with weights w_j (a reading of the gated delta rule of Yang et al., cited
@@ -8,15 +6,17 @@
 //   m_j = alpha * M[i_j]
 //   p   = sum_j w_j m_j
 //   M[i_j] <- m_j + w_j * beta * (v - p)          (rounded to the bank type)
-// and then the read over the R selected rows: y = sum_j r_j M[i^r_j].
-// Every column is independent, so a warp owns NCG 16-byte column groups (lane % NCG)
-// and splits the rows of the token over RG = 32 / NCG row groups (lane / NCG): row j
-// belongs to row group j % RG and is accumulated in increasing j; the RG partial sums
-// are combined by an xor butterfly.  All of it is float32 with fixed operation order,
-// so results are bitwise repeatable and independent of how tokens are staged.
+// and then the read over the R selected rows: y = sum_j r_j M[i^r_j].  Every column is
+// independent.  All of it is float32 with a fixed operation order, so results are
+// bitwise repeatable and independent of how tokens are staged.
 //
-// Rows are fetched kJB at a time per lane (independent loads in flight) because the
-// token chain is latency-bound: one warp walks the tokens of a stream in order.
+// Two layouts:
+//   * delta_write_cols / weighted_read_cols (the decode kernel, rows in global memory): a
+//     warp owns NCG 16-byte column groups (lane % NCG) and splits the rows over
+//     RG = 32 / NCG row groups (lane / NCG): row j belongs to row group j % RG and is
+//     accumulated in increasing j; the RG partial sums are combined by an xor butterfly.
+//     Rows are fetched kJB at a time per lane (independent loads in flight).
+//   * token_blocks2 (the write/read kernel, rows in shared memory), below.
 #pragma once
 
 #include "sdm_common.cuh"
@@ -122,114 +122,8 @@ __device__ __forceinline__ void weighted_read_cols(int R, const float *r, SrcRow
     for (int c = 0; c < VEC; ++c) y[c] = __fadd_rn(y[c], __shfl_xor_sync(0xffffffffu, y[c], o));
 }
 
-// The row references of one token that one lane handles: row group rg takes the refs
-// j = rg + b*RG, b < kJB (valid while j < W, resp. j < R).
-struct LaneRefs {
-  int uw[kJB], ur[kJB];      // row byte offsets in the stage buffer
-};
-
-// One token, when each lane holds at most kJB write rows and kJB read rows (W, R <=
-// RG*kJB).  Same arithmetic, in the same order, as delta_write_cols followed by
-// weighted_read_cols.  When the token reads no row it writes (overlap == false) its
-// read rows are fetched together with the write rows and both reductions run side by
-// side: the rows it reads hold the same values before and after its write.
-template <typename BANK, int NCG>
-__device__ __forceinline__ void token_write_read(int W, int R, const LaneRefs &ref, const float *w,
-                                                 float alpha, float beta, const float (&v)[Vec16<BANK>::N],
-                                                 unsigned char *rows, bool overlap, float (&y)[Vec16<BANK>::N]) {
-  constexpr int VEC = Vec16<BANK>::N, RG = 32 / NCG;
-  const int rg = (threadIdx.x & 31) / NCG;
-  uint4 rw[kJB], rr[kJB];
-  struct {
-    float ww[kJB], wr[kJB];
-  } wt;
-#pragma unroll
-  for (int b = 0; b < kJB; ++b) {
-    const int j = rg + b * RG;
-    wt.ww[b] = j < W ? w[j] : 0.0f;
-    wt.wr[b] = j < R ? w[W + j] : 0.0f;
-  }
-#pragma unroll
-  for (int b = 0; b < kJB; ++b)
-    if (rg + b * RG < W) rw[b] = *reinterpret_cast<const uint4 *>(rows + ref.uw[b]);
-  if (!overlap) {
-#pragma unroll
-    for (int b = 0; b < kJB; ++b)
-      if (rg + b * RG < R) rr[b] = *reinterpret_cast<const uint4 *>(rows + ref.ur[b]);
-  }
-  float acc[VEC], ya[VEC];
-#pragma unroll
-  for (int c = 0; c < VEC; ++c) acc[c] = ya[c] = 0.0f;
-#pragma unroll
-  for (int b = 0; b < kJB; ++b) {
-    if (rg + b * RG < W) {
-      float r[VEC];
-      unpack16<BANK>(rw[b], r);
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) acc[c] = __fmaf_rn(wt.ww[b], __fmul_rn(alpha, r[c]), acc[c]);
-    }
-  }
-  if (!overlap) {
-#pragma unroll
-    for (int b = 0; b < kJB; ++b) {
-      if (rg + b * RG < R) {
-        float m[VEC];
-        unpack16<BANK>(rr[b], m);
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) ya[c] = __fmaf_rn(wt.wr[b], m[c], ya[c]);
-      }
-    }
-#pragma unroll
-    for (int o = NCG; o < 32; o <<= 1)
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) {
-        acc[c] = __fadd_rn(acc[c], __shfl_xor_sync(0xffffffffu, acc[c], o));
-        ya[c] = __fadd_rn(ya[c], __shfl_xor_sync(0xffffffffu, ya[c], o));
-      }
-  } else {
-#pragma unroll
-    for (int o = NCG; o < 32; o <<= 1)
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) acc[c] = __fadd_rn(acc[c], __shfl_xor_sync(0xffffffffu, acc[c], o));
-  }
-  float d[VEC];
-#pragma unroll
-  for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], acc[c]));
-#pragma unroll
-  for (int b = 0; b < kJB; ++b) {
-    if (rg + b * RG < W) {
-      float r[VEC];
-      unpack16<BANK>(rw[b], r);
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) r[c] = __fmaf_rn(wt.ww[b], d[c], __fmul_rn(alpha, r[c]));
-      store_vec16<BANK>(reinterpret_cast<BANK *>(rows + ref.uw[b]), r);
-    }
-  }
-  if (overlap) {
-    __syncwarp();
-#pragma unroll
-    for (int b = 0; b < kJB; ++b)
-      if (rg + b * RG < R) rr[b] = *reinterpret_cast<const uint4 *>(rows + ref.ur[b]);
-#pragma unroll
-    for (int b = 0; b < kJB; ++b) {
-      if (rg + b * RG < R) {
-        float m[VEC];
-        unpack16<BANK>(rr[b], m);
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) ya[c] = __fmaf_rn(wt.wr[b], m[c], ya[c]);
-      }
-    }
-#pragma unroll
-    for (int o = NCG; o < 32; o <<= 1)
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) ya[c] = __fadd_rn(ya[c], __shfl_xor_sync(0xffffffffu, ya[c], o));
-  }
-#pragma unroll
-  for (int c = 0; c < VEC; ++c) y[c] = ya[c];
-}
-
 // ------------------------------------------------------------------------------------
-// Block-ordered token step of the write/read kernel on a 128-byte row slice (one warp).
+// Block-ordered token step of the write/read kernel, two warps per row slice.
 //
 // Summation order.  The n rows of a sum (n = W for the prediction p, n = R for the
 // read y) are cut into 8 consecutive blocks of B8 = ceil(n / 8) rows; block k is summed
@@ -237,138 +131,43 @@ __device__ __forceinline__ void token_write_read(int W, int R, const LaneRefs &r
 //   ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)).
 // The order depends on n alone: not on the stage length, nor on the column slicing.
 //
-// Lane layout.  Lane % 8 is a 16-byte column group of the slice (8 x 16 = 128 bytes)
-// and lane / 8 = rg a row group that owns blocks 2rg and 2rg+1, so a lane adds its own
-// pair and two xor steps (8 and 16 lanes apart) finish the tree; IEEE addition is
-// commutative, so both partners of a step hold the same bits afterwards.
-//
-// JB = the most rows one lane holds, >= 2 * B8 for both sums.  Register slot s < JB/2
-// holds row 2rg*B8 + s (block 2rg), slot JB/2 + s holds row 2rg*B8 + B8 + s (block
-// 2rg+1); slots past the block or past n hold nothing.
-template <int JB>
-struct BlockSlots {
-  static constexpr int H = JB / 2;
-  int b8, j0, n;
-  __device__ __forceinline__ BlockSlots(int n_, int rg) : b8((n_ + 7) >> 3), j0(2 * rg * ((n_ + 7) >> 3)), n(n_) {}
-  __device__ __forceinline__ int ref(int s) const { return j0 + (s < H ? s : b8 + s - H); }
-  __device__ __forceinline__ bool has(int s) const { return (s < H ? s : s - H) < b8 && ref(s) < n; }
+// Layout.  Lane % 8 owns VEC consecutive elements of the slice (the slice is 8*VEC
+// elements wide) and warp wsel's row group rg = lane / 8 owns block k = 4*wsel + rg: a
+// lane adds its block, two xor steps inside the warp give (a0+a1)+(a2+a3) in warp 0 and
+// (a4+a5)+(a6+a7) in warp 1, and the warps swap those through shared memory (xch:
+// [2 warps][8 column groups][VEC] floats) on a 64-thread named barrier `bar`.  IEEE
+// addition is commutative, so both partners of every step hold the same bits.
+// JB >= B8: register slot s holds row k*B8 + s.
+template <int BYTES>
+struct RawVec;
+template <>
+struct RawVec<16> { using T = uint4; };
+template <>
+struct RawVec<8> { using T = uint2; };
+template <>
+struct RawVec<4> { using T = uint32_t; };
+template <>
+struct RawVec<2> { using T = uint16_t; };
+
+// VEC elements of BANK <-> float32.
+template <typename BANK, int VEC>
+struct LaneRow {
+  using Raw = typename RawVec<VEC * (int)sizeof(BANK)>::T;
+  __device__ __forceinline__ static Raw load(const unsigned char *p) { return *reinterpret_cast<const Raw *>(p); }
+  __device__ __forceinline__ static void unpack(const Raw &r, float (&out)[VEC]) {
+    const BANK *e = reinterpret_cast<const BANK *>(&r);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) out[i] = to_f32(e[i]);
+  }
+  __device__ __forceinline__ static void store(unsigned char *p, const float (&in)[VEC]) {
+    Raw r;
+    BANK *e = reinterpret_cast<BANK *>(&r);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) e[i] = from_f32<BANK>(in[i]);
+    *reinterpret_cast<Raw *>(p) = r;
+  }
 };
 
-template <int VEC>
-__device__ __forceinline__ void block_tree(const float (&a0)[VEC], const float (&a1)[VEC], float (&out)[VEC]) {
-#pragma unroll
-  for (int c = 0; c < VEC; ++c) {
-    float x = __fadd_rn(a0[c], a1[c]);
-    x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, 8));
-    out[c] = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, 16));
-  }
-}
-
-// Accumulates the read rows of the token (slots of `rs`) into b0 / b1.
-template <typename BANK, int JB>
-__device__ __forceinline__ void block_read(const BlockSlots<JB> &rs, const uint16_t *rm_r, const float *wt_r,
-                                           const unsigned char *rows, float (&b0)[Vec16<BANK>::N],
-                                           float (&b1)[Vec16<BANK>::N]) {
-  constexpr int VEC = Vec16<BANK>::N, H = JB / 2, RB = 128;
-#pragma unroll
-  for (int s0 = 0; s0 < JB; s0 += 4) {
-    uint4 raw[4];
-    float wr[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int s = s0 + q;
-      if (rs.has(s)) {
-        raw[q] = *reinterpret_cast<const uint4 *>(rows + (int)rm_r[rs.ref(s)] * RB);
-        wr[q] = wt_r[rs.ref(s)];
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int s = s0 + q;
-      if (rs.has(s)) {
-        float m[VEC];
-        unpack16<BANK>(raw[q], m);
-        float(&b)[VEC] = s < H ? b0 : b1;
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) b[c] = __fmaf_rn(wr[q], m[c], b[c]);
-      }
-    }
-  }
-}
-
-// One token: the gated delta-rule write of its W rows, then the read of its R rows,
-// with the arithmetic of delta_write_cols / weighted_read_cols per element and the
-// block order above for both sums.  rm / wt: the token's row references (stage-buffer
-// row indices) and weights, W write entries then R read entries; rows: the stage
-// buffer offset by this lane's 16-byte column group.  When the token reads none of the
-// rows it writes (overlap == false) the read runs before the write: those rows hold
-// the same values before and after it.
-// FULL: W == R == 4 * JB, every slot of every lane holds a row (no predicates).
-template <typename BANK, int JB, bool FULL = false>
-__device__ __forceinline__ void token_blocks(int W, int R, const uint16_t *rm, const float *wt, float alpha,
-                                             float beta, const float (&v)[Vec16<BANK>::N], unsigned char *rows,
-                                             bool overlap, float (&y)[Vec16<BANK>::N]) {
-  constexpr int VEC = Vec16<BANK>::N, H = JB / 2, RB = 128;
-  if constexpr (FULL) W = R = 4 * JB;
-  const int rg = (threadIdx.x & 31) >> 3;
-  const BlockSlots<JB> ws(W, rg), rs(R, rg);
-  int ow[JB];
-  float ww[JB];
-  uint4 rw[JB];
-#pragma unroll
-  for (int s = 0; s < JB; ++s) {
-    ow[s] = ws.has(s) ? (int)rm[ws.ref(s)] * RB : 0;
-    ww[s] = ws.has(s) ? wt[ws.ref(s)] : 0.0f;
-  }
-#pragma unroll
-  for (int s = 0; s < JB; ++s)
-    if (ws.has(s)) rw[s] = *reinterpret_cast<const uint4 *>(rows + ow[s]);
-  float b0[VEC], b1[VEC];
-#pragma unroll
-  for (int c = 0; c < VEC; ++c) b0[c] = b1[c] = 0.0f;
-  if (!overlap) block_read<BANK, JB>(rs, rm + W, wt + W, rows, b0, b1);
-
-  float a0[VEC], a1[VEC];
-#pragma unroll
-  for (int c = 0; c < VEC; ++c) a0[c] = a1[c] = 0.0f;
-#pragma unroll
-  for (int s = 0; s < JB; ++s) {
-    if (ws.has(s)) {
-      float m[VEC];
-      unpack16<BANK>(rw[s], m);
-      float(&a)[VEC] = s < H ? a0 : a1;
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) a[c] = __fmaf_rn(ww[s], __fmul_rn(alpha, m[c]), a[c]);
-    }
-  }
-  float p[VEC], d[VEC];
-  block_tree<VEC>(a0, a1, p);
-#pragma unroll
-  for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], p[c]));
-#pragma unroll
-  for (int s = 0; s < JB; ++s) {
-    if (ws.has(s)) {
-      float m[VEC];
-      unpack16<BANK>(rw[s], m);
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) m[c] = __fmaf_rn(ww[s], d[c], __fmul_rn(alpha, m[c]));
-      store_vec16<BANK>(reinterpret_cast<BANK *>(rows + ow[s]), m);
-    }
-  }
-  if (overlap) {
-    __syncwarp();
-    block_read<BANK, JB>(rs, rm + W, wt + W, rows, b0, b1);
-  }
-  block_tree<VEC>(b0, b1, y);
-}
-
-// ------------------------------------------------------------------------------------
-// The same token step with the rows split between two warps (same summation order, so
-// the results are bitwise those of token_blocks).  Warp wsel's row group rg owns block
-// k = 4*wsel + rg alone: a lane adds its block, two xor steps inside the warp give
-// (a0+a1)+(a2+a3) in warp 0 and (a4+a5)+(a6+a7) in warp 1, and the warps swap those
-// through shared memory (xch: [2 warps][8 column groups][VEC] floats) on a 64-thread
-// named barrier `bar`.  JB >= B8: register slot s holds row k*B8 + s.
 template <int JB>
 struct BlockSlots1 {
   int b8, j0, n;
@@ -390,33 +189,26 @@ __device__ __forceinline__ void pair_tree(const float (&a)[VEC], float (&out)[VE
   const float *theirs = xch + ((wsel ^ 1) * 8 + (lane & 7)) * VEC;
   if (lane < 8) {
 #pragma unroll
-    for (int c = 0; c < VEC; c += 4)
-      *reinterpret_cast<float4 *>(mine + c) = make_float4(x[c], x[c + 1], x[c + 2], x[c + 3]);
+    for (int c = 0; c < VEC; ++c) mine[c] = x[c];
   }
   named_barrier(bar, 64);
 #pragma unroll
-  for (int c = 0; c < VEC; c += 4) {
-    const float4 o = *reinterpret_cast<const float4 *>(theirs + c);
-    out[c] = __fadd_rn(x[c], o.x);
-    out[c + 1] = __fadd_rn(x[c + 1], o.y);
-    out[c + 2] = __fadd_rn(x[c + 2], o.z);
-    out[c + 3] = __fadd_rn(x[c + 3], o.w);
-  }
+  for (int c = 0; c < VEC; ++c) out[c] = __fadd_rn(x[c], theirs[c]);
 }
 
-template <typename BANK, int JB>
+template <typename BANK, int VEC, int JB>
 __device__ __forceinline__ void pair_read(const BlockSlots1<JB> &rs, const uint16_t *rm_r, const float *wt_r,
-                                          const unsigned char *rows, float (&b)[Vec16<BANK>::N]) {
-  constexpr int VEC = Vec16<BANK>::N, RB = 128;
+                                          const unsigned char *rows, int RB, float (&b)[VEC]) {
+  using LR = LaneRow<BANK, VEC>;
 #pragma unroll
   for (int s0 = 0; s0 < JB; s0 += 4) {
-    uint4 raw[4];
+    typename LR::Raw raw[4];
     float wr[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int s = s0 + q;
       if (rs.has(s)) {
-        raw[q] = *reinterpret_cast<const uint4 *>(rows + (int)rm_r[rs.ref(s)] * RB);
+        raw[q] = LR::load(rows + (int)rm_r[rs.ref(s)] * RB);
         wr[q] = wt_r[rs.ref(s)];
       }
     }
@@ -424,7 +216,7 @@ __device__ __forceinline__ void pair_read(const BlockSlots1<JB> &rs, const uint1
     for (int q = 0; q < 4; ++q) {
       if (rs.has(s0 + q)) {
         float m[VEC];
-        unpack16<BANK>(raw[q], m);
+        LR::unpack(raw[q], m);
 #pragma unroll
         for (int c = 0; c < VEC; ++c) b[c] = __fmaf_rn(wr[q], m[c], b[c]);
       }
@@ -432,20 +224,27 @@ __device__ __forceinline__ void pair_read(const BlockSlots1<JB> &rs, const uint1
   }
 }
 
-// FULL: W == R == 8 * JB.  The read's exchange barrier comes after the row stores, so it
-// also orders this token's writes before the next token's loads in the other warp.
-template <typename BANK, int JB, bool FULL = false>
+// One token: the gated delta-rule write of its W rows, then the read of its R rows, with
+// the arithmetic of delta_write_cols / weighted_read_cols per element and the block order
+// above for both sums.  rm / wt: the token's row references (stage-buffer row indices)
+// and weights, W write entries then R read entries; rows: the stage buffer offset by this
+// lane's column group; RB: the row slice in bytes.  When the token reads none of the rows
+// it writes (overlap == false) the read runs before the write: those rows hold the same
+// values before and after it.  FULL: W == R == 8 * JB.  The read's exchange barrier comes
+// after the row stores, so it also orders this token's writes before the next token's
+// loads in the other warp.
+template <typename BANK, int VEC, int JB, bool FULL = false>
 __device__ __forceinline__ void token_blocks2(int W, int R, const uint16_t *rm, const float *wt, float alpha,
-                                              float beta, const float (&v)[Vec16<BANK>::N], unsigned char *rows,
-                                              bool overlap, float (&y)[Vec16<BANK>::N], float *xch_p, float *xch_y,
-                                              int wsel, int bar) {
-  constexpr int VEC = Vec16<BANK>::N, RB = 128;
+                                              float beta, const float (&v)[VEC], unsigned char *rows, int RB,
+                                              bool overlap, float (&y)[VEC], float *xch_p, float *xch_y, int wsel,
+                                              int bar) {
+  using LR = LaneRow<BANK, VEC>;
   if constexpr (FULL) W = R = 8 * JB;
   const int k = 4 * wsel + ((threadIdx.x & 31) >> 3);
   const BlockSlots1<JB> ws(W, k), rs(R, k);
   int ow[JB];
   float ww[JB];
-  uint4 rw[JB];
+  typename LR::Raw rw[JB];
 #pragma unroll
   for (int s = 0; s < JB; ++s) {
     ow[s] = ws.has(s) ? (int)rm[ws.ref(s)] * RB : 0;
@@ -453,11 +252,11 @@ __device__ __forceinline__ void token_blocks2(int W, int R, const uint16_t *rm, 
   }
 #pragma unroll
   for (int s = 0; s < JB; ++s)
-    if (ws.has(s)) rw[s] = *reinterpret_cast<const uint4 *>(rows + ow[s]);
+    if (ws.has(s)) rw[s] = LR::load(rows + ow[s]);
   float b[VEC];
 #pragma unroll
   for (int c = 0; c < VEC; ++c) b[c] = 0.0f;
-  if (!overlap) pair_read<BANK, JB>(rs, rm + W, wt + W, rows, b);
+  if (!overlap) pair_read<BANK, VEC, JB>(rs, rm + W, wt + W, rows, RB, b);
 
   float a[VEC];
 #pragma unroll
@@ -466,7 +265,7 @@ __device__ __forceinline__ void token_blocks2(int W, int R, const uint16_t *rm, 
   for (int s = 0; s < JB; ++s) {
     if (ws.has(s)) {
       float m[VEC];
-      unpack16<BANK>(rw[s], m);
+      LR::unpack(rw[s], m);
 #pragma unroll
       for (int c = 0; c < VEC; ++c) a[c] = __fmaf_rn(ww[s], __fmul_rn(alpha, m[c]), a[c]);
     }
@@ -479,15 +278,15 @@ __device__ __forceinline__ void token_blocks2(int W, int R, const uint16_t *rm, 
   for (int s = 0; s < JB; ++s) {
     if (ws.has(s)) {
       float m[VEC];
-      unpack16<BANK>(rw[s], m);
+      LR::unpack(rw[s], m);
 #pragma unroll
       for (int c = 0; c < VEC; ++c) m[c] = __fmaf_rn(ww[s], d[c], __fmul_rn(alpha, m[c]));
-      store_vec16<BANK>(reinterpret_cast<BANK *>(rows + ow[s]), m);
+      LR::store(rows + ow[s], m);
     }
   }
   if (overlap) {
     named_barrier(bar, 64);
-    pair_read<BANK, JB>(rs, rm + W, wt + W, rows, b);
+    pair_read<BANK, VEC, JB>(rs, rm + W, wt + W, rows, RB, b);
   }
   pair_tree<VEC>(b, y, xch_y, wsel, bar);
 }

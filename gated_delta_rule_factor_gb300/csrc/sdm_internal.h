@@ -141,9 +141,12 @@ cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int sort_pow2,
 cudaError_t launch_plan_link(const PlanArgs &a, int64_t streams, cudaStream_t st);
 cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_dtype,
                               int act_dtype, int CW, int64_t smem_bytes, cudaStream_t st);
-// The 128-byte-slice (block-ordered) instances, from sdm_write_read_blocks.cu.
-cudaError_t launch_write_read_blocks(const WriteReadArgs &a, int64_t streams, int bank_dtype,
-                                     int act_dtype, int64_t smem_bytes, cudaStream_t st);
+// The instances of one (bank, activation) type pair, from sdm_write_read_<bank>_<act>.cu.
+cudaError_t launch_write_read_f32_f32(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem, cudaStream_t st);
+cudaError_t launch_write_read_f32_bf16(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem, cudaStream_t st);
+cudaError_t launch_write_read_bf16_f32(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem, cudaStream_t st);
+cudaError_t launch_write_read_bf16_bf16(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem,
+                                        cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, const CandidateList &cl, int act_dtype,
                           int bank_dtype, int EF, int EC, int64_t smem_bytes,
                           cudaStream_t st);

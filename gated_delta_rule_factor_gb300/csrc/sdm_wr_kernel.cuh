@@ -3,22 +3,20 @@
 //
 // Parallel axes: streams (b, h) are independent, and so is every bank column (the
 // update of a column reads only that column, see sdm_delta.cuh).  One CTA owns one
-// stream and a slice of CW columns (CW * elem = 32..128 bytes of every row) and runs
+// stream and a slice of CW columns (CW * elem = 16..128 bytes of every row) and runs
 // the stream's tokens in order.  Tokens are staged G at a time; the chunk plan
 // (sdm_plan.cu) lists the distinct rows of each stage.
 //
 // Warp roles (one CTA):
-//   compute warps: 128-byte slices, one warp (block-ordered token step); narrower slices,
-//               1 or 2 warps of up to four 16-byte column groups (row-group step).  They
-//               run the tokens of the current stage on the shared-memory rows;
-//   loader warps (8 for 128-byte slices, 4 otherwise): fetch the next stage's rows, its
-//               token data and the stage record after it, all with 16-byte cp.async on the
-//               LSU path (a bulk/TMA copy per 128-byte row costs more than it saves at this
-//               granularity); once the compute warps signal (barrier 5) that the current
-//               stage's next-to-last token is done, write back the current stage's dirty
-//               rows its last token leaves alone, and after the stage the rest of them,
-//               while the next stage's rows are still landing.  More loader warps keep
-//               more row requests in flight.
+//   2 compute warps: the tokens of the current stage on the shared-memory rows, with the
+//               block-ordered token step (sdm_delta.cuh token_blocks2);
+//   8 loader warps: fetch the next stage's rows, its token data and the stage record
+//               after it, all with 16-byte cp.async on the LSU path (a bulk/TMA copy per
+//               row slice costs more than it saves at this granularity); once the compute
+//               warps signal (barrier 5) that the current stage's next-to-last token is
+//               done, write back the current stage's dirty rows its last token leaves
+//               alone, and after the stage the rest of them, while the next stage's rows
+//               are still landing.  More loader warps keep more row requests in flight.
 //   every warp copies the rows carried over from the previous stage.
 // Two row buffers alternate between stages; rows shared by consecutive stages are
 // copied across buffers instead of re-read, because the bank copy may be stale.  Stage
@@ -48,33 +46,30 @@ __host__ __device__ inline TokLayout tok_layout(int G, int W, int R, int CW, int
   return t;
 }
 
-// JB == 0: row-group layout (sdm_delta.cuh token_write_read / delta_write_cols), up to
-// four column groups per compute warp.  JB > 0: the block-ordered layout
-// (token_blocks) on a 128-byte slice, one compute warp, at most JB rows per lane.
-template <typename BANK, int CW, int JB>
+// A CTA owns a slice of CW columns (CW * elem = 16..128 bytes of every row): two compute
+// warps, 8 loader warps.  Lane % 8 of a compute warp owns VB = CW / 8 consecutive columns.
+template <typename BANK, int CW>
 struct WrGeometry {
-  static constexpr int VEC = Vec16<BANK>::N;          // elements per 16 B
-  static constexpr int NCGT = CW / VEC;               // 16-byte column groups of the slice
-  static constexpr int NCG = JB > 0 ? 8 : (NCGT < 4 ? NCGT : 4);  // column groups per compute warp
-  static constexpr int NCW = JB > 0 ? 2 : NCGT / NCG;  // compute warps (block layout: rows split)
-  static constexpr int LW = JB > 0 ? 8 : 4;           // loader warps
+  static constexpr int VB = CW / 8;                   // columns per compute lane
+  static constexpr int RB = CW * (int)sizeof(BANK);   // row slice bytes
+  static constexpr int NCW = 2;                       // compute warps (rows split)
+  static constexpr int LW = 8;                        // loader warps
   static constexpr int NTHR = 32 * (NCW + LW);
-  static_assert(JB == 0 || NCGT == 8, "the block-ordered layout takes 128-byte slices");
+  static_assert(CW % 8 == 0 && RB >= 16 && RB <= 128 && (RB & (RB - 1)) == 0, "column slice");
 };
 
-// FULL (block layout only): W == R == 4 * JB, fixed at compile time.
+// JB = the most rows a compute lane holds (one of the 8 row blocks of a token);
+// FULL: W == R == 8 * JB, fixed at compile time.
 template <typename BANK, typename ACT, int CW, int JB, bool FULL = false>
-__global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
+__global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
     write_read_kernel(const __grid_constant__ WriteReadArgs a) {
-  using Geo = WrGeometry<BANK, CW, JB>;
+  using Geo = WrGeometry<BANK, CW>;
   constexpr int kLoaderThreads = 32 * Geo::LW;
-  constexpr int VEC = Geo::VEC, NCG = Geo::NCG, NCW = Geo::NCW, NTHR = Geo::NTHR;
-  static_assert(Geo::NCGT >= 1 && Geo::NCGT <= 8 && (Geo::NCGT & (Geo::NCGT - 1)) == 0, "column slice");
-  constexpr int RB = CW * (int)sizeof(BANK);          // row slice bytes in smem
+  constexpr int VB = Geo::VB, NCW = Geo::NCW, NTHR = Geo::NTHR, RB = Geo::RB;
   constexpr int CPR = RB / 16;                        // 16-byte chunks per row slice
 
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ __align__(16) float xch[JB > 0 ? 2 * 2 * 8 * VEC : 4];  // block layout: the two warps' partial sums
+  __shared__ __align__(16) float xch[2 * 2 * 8 * VB];  // the two compute warps' partial sums
   const PlanLayout &lay = a.lay;
   const int L = lay.L, G = lay.G, S = lay.n_stages;
   const int W = a.W, R = a.R, WR = W + R;
@@ -103,8 +98,7 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
            hdr[3] >= 0 && hdr[3] <= L && hdr[4] >= 0 && hdr[4] <= hdr[1] && hdr[5] >= 0 && hdr[5] <= hdr[3];
   };
 
-  constexpr int VB = CW * (int)sizeof(ACT);          // value bytes per token (>= 16)
-  constexpr int RG = 32 / NCG;
+  constexpr int VBYTES = CW * (int)sizeof(ACT);      // value bytes per token (>= 16)
 
   // ---- loader helpers (threads of the loader warps).  Every copy is a 16-byte cp.async
   // (or 8/4-byte for the gates and unaligned weights) on the LSU path: CPR lanes take
@@ -168,10 +162,10 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
       cp_async8(gt + 2 * i, a.gates + row * 2);
     }
     unsigned char *vb = tb + tl.v;
-    for (int i = ltid; i < nt * (VB / 16); i += kLoaderThreads) {
-      const int t = i / (VB / 16), c = i % (VB / 16);
+    for (int i = ltid; i < nt * (VBYTES / 16); i += kLoaderThreads) {
+      const int t = i / (VBYTES / 16), c = i % (VBYTES / 16);
       const int64_t row = (b * a.T + t0 + t) * a.H + h;
-      cp_async16(vb + (int64_t)t * VB + c * 16,
+      cp_async16(vb + (int64_t)t * VBYTES + c * 16,
                  reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
     }
   };
@@ -215,7 +209,6 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
     cp_async_commit();
   }
 
-  const bool fast = W <= RG * kJB && R <= RG * kJB;
   for (int g = 0; g < S; ++g) {
     if (is_loader) cp_async_wait_all();
     named_barrier(2, NTHR);                                      // stage g resident
@@ -244,82 +237,30 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
     named_barrier(3, NTHR);                                      // carries in place
 
     if (!is_loader) {
-      // ---- compute: tokens of stage g in order; warp w owns column groups [w*NCG, w*NCG+NCG)
+      // ---- compute: tokens of stage g in order; both compute warps work on the same
+      // column groups, the token's row blocks split between them (token_blocks2); warp 0
+      // stores y
       const uint16_t *refmap = reinterpret_cast<const uint16_t *>(rec + lay.off_refmap);
       const uint8_t *tokflag = rec + lay.off_tokflag;
-      const unsigned char *tb = tokbuf(g & 1);
+      const unsigned char *tb = tokbuf(g);
       const float *wts = reinterpret_cast<const float *>(tb + tl.wts);
       const float *gt = reinterpret_cast<const float *>(tb + tl.gates);
       const ACT *vv = reinterpret_cast<const ACT *>(tb + tl.v);
-      const int cg = warp * NCG + lane % NCG;                 // column group in the slice
-      const int rg = lane / NCG;
-      unsigned char *rows = rowbuf(g & 1) + cg * 16;
+      const int cl = lane & 7;                                 // column group in the slice
+      unsigned char *rows = rowbuf(g) + cl * VB * (int)sizeof(BANK);
       const int64_t t0 = (int64_t)g * G;
       const int nt = (int)min((int64_t)G, a.T - t0);
-      ACT *yrow = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + cg * VEC;
+      ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + cl * VB;
       const int64_t ystep = (int64_t)a.H * a.d_v;
-      if constexpr (JB > 0) {
-        // both compute warps work on the same 16-byte column groups, rows split (sdm_delta.cuh
-        // token_blocks2); warp 0 stores y
-        unsigned char *brows = rowbuf(g & 1) + (lane & 7) * 16;
-        ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + (lane & 7) * VEC;
-        if (nt <= 1) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);
-        for (int t = 0; t < nt; ++t) {
-          float v[VEC], out[VEC];
-          load_vec<ACT, VEC>(vv + t * CW + (lane & 7) * VEC, v);
-          token_blocks2<BANK, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, brows,
-                                        tokflag[t] != 0, out, xch, xch + 2 * 8 * VEC, warp, 6);
-          if (warp == 0 && lane < 8) store_vec<ACT, VEC>(ybase + t * ystep, out);
-          __syncwarp();
-          if (t == nt - 2) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);  // rows the last token leaves alone are final
-        }
-      } else if (fast) {
-        auto load_refs = [&](int t, LaneRefs &r) {
-          const uint16_t *rm = refmap + t * WR;
-#pragma unroll
-          for (int bb = 0; bb < kJB; ++bb) {
-            const int j = rg + bb * RG;
-            const int uw = j < W ? rm[j] : 0, ur = j < R ? rm[W + j] : 0;
-            r.uw[bb] = (uw < L ? uw : 0) * RB;
-            r.ur[bb] = (ur < L ? ur : 0) * RB;
-          }
-        };
-        LaneRefs cur, nxt;
-        if (nt > 0) load_refs(0, cur);
-        if (nt <= 1) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);
-        for (int t = 0; t < nt; ++t) {
-          if (t + 1 < nt) load_refs(t + 1, nxt);
-          float v[VEC], out[VEC];
-          load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
-          token_write_read<BANK, NCG>(W, R, cur, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, rows, tokflag[t] != 0,
-                                      out);
-          if (lane < NCG) store_vec<ACT, VEC>(yrow + t * ystep, out);
-          __syncwarp();
-          if (t == nt - 2) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);  // rows the last token leaves alone are final
-          cur = nxt;
-        }
-      } else {
-        if (nt <= 1) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);
-        for (int t = 0; t < nt; ++t) {
-          const uint16_t *rm = refmap + t * WR;
-          const float *w = wts + t * WR;
-          auto row_ptr = [&](int j) -> BANK * {
-            int u = rm[j];
-            if (u >= L) u = 0;                         // plan_sort never emits these
-            return reinterpret_cast<BANK *>(rows + (int64_t)u * RB);
-          };
-          auto wrow = [&](int j) { return row_ptr(j); };
-          auto rrow = [&](int j) { return row_ptr(W + j); };
-          float v[VEC];
-          load_vec<ACT, VEC>(vv + t * CW + cg * VEC, v);
-          delta_write_cols<BANK, NCG>(W, w, gt[2 * t], gt[2 * t + 1], v, wrow, wrow);
-          __syncwarp();
-          float out[VEC];
-          weighted_read_cols<BANK, NCG>(R, w + W, rrow, out);
-          if (lane < NCG) store_vec<ACT, VEC>(yrow + t * ystep, out);
-          __syncwarp();
-          if (t == nt - 2) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);  // rows the last token leaves alone are final
-        }
+      if (nt <= 1) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);
+      for (int t = 0; t < nt; ++t) {
+        float v[VB], out[VB];
+        load_vec<ACT, VB>(vv + t * CW + cl * VB, v);
+        token_blocks2<BANK, VB, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, rows,
+                                          RB, tokflag[t] != 0, out, xch, xch + 2 * 8 * VB, warp, 6);
+        if (warp == 0 && lane < 8) store_vec<ACT, VB>(ybase + t * ystep, out);
+        __syncwarp();
+        if (t == nt - 2) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);  // rows the last token leaves alone are final
       }
     } else {
       // ---- loaders: fetch stage g+1 into its buffer (stage g-1's, fully written back at
@@ -336,6 +277,26 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW, JB>::NTHR)
     // stage barrier orders these stores before any later load of the same rows
     if (is_loader) write_back(g, false);
   }
+}
+
+// Launches the instance for the shape: W = R = 64 fixed at compile time, else the
+// smallest JB >= ceil(max(W, R) / 8).
+template <typename BANK, typename ACT, int CW>
+cudaError_t launch_cw(const WriteReadArgs &a, int64_t streams, int64_t smem, cudaStream_t st) {
+  const dim3 grid((unsigned)a.slices, (unsigned)streams);
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, WrGeometry<BANK, CW>::NTHR, smem, st>>>(a);
+    return cudaGetLastError();
+  };
+  const int n = a.W > a.R ? a.W : a.R;
+  const int per_lane = (n + 7) / 8;
+  if (a.W == 64 && a.R == 64) return go(write_read_kernel<BANK, ACT, CW, 8, true>);
+  if (per_lane <= 4) return go(write_read_kernel<BANK, ACT, CW, 4>);
+  if (per_lane <= 8) return go(write_read_kernel<BANK, ACT, CW, 8>);
+  if (per_lane <= 16) return go(write_read_kernel<BANK, ACT, CW, 16>);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace wr

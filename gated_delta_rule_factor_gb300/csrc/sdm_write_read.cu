@@ -1,37 +1,15 @@
-// The fused gather / gated delta-rule update / read kernel of sdm_write_read (the
-// row-group layout for slices narrower than 128 bytes; sdm_write_read_blocks.cu holds the
-// 128-byte block-ordered instances), its launch, and the per-call bank copy (learned
-// table -> per-stream banks).  The kernel itself is in sdm_wr_kernel.cuh.
+// Launch dispatch of the fused gather / gated delta-rule update / read kernel of
+// sdm_write_read (kernel in sdm_wr_kernel.cuh, instances per type pair in
+// sdm_write_read_<bank>_<act>.cu), its shared-memory size, and the per-call bank copy
+// (learned table -> per-stream banks).
 #include "sdm_wr_kernel.cuh"
 
 namespace sdm {
 
 namespace {
 
-using wr::write_read_kernel;
-using wr::WrGeometry;
 using wr::tok_layout;
 using wr::TokLayout;
-
-template <typename BANK, typename ACT>
-cudaError_t launch_wr_t(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem, cudaStream_t st) {
-  dim3 grid((unsigned)a.slices, (unsigned)streams);
-  auto go = [&](auto kern, int threads) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, threads, smem, st>>>(a);
-    return cudaGetLastError();
-  };
-  constexpr int V = Vec16<BANK>::N;
-  switch (CW / V) {
-    case 1: return go(write_read_kernel<BANK, ACT, V * 1, 0>, WrGeometry<BANK, V * 1, 0>::NTHR);
-    case 2: return go(write_read_kernel<BANK, ACT, V * 2, 0>, WrGeometry<BANK, V * 2, 0>::NTHR);
-    case 4: return go(write_read_kernel<BANK, ACT, V * 4, 0>, WrGeometry<BANK, V * 4, 0>::NTHR);
-    case 8: return launch_write_read_blocks(a, streams, sizeof(BANK) == 4 ? SDM_F32 : SDM_BF16,
-                                            sizeof(ACT) == 4 ? SDM_F32 : SDM_BF16, smem, st);
-    default: return cudaErrorInvalidValue;
-  }
-}
 
 // Learned table [H, N, d_v] -> every stream's bank [B, H, N, d_v]: each 16-byte chunk
 // of the source is read once and written B times.
@@ -61,11 +39,11 @@ cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_
                               int act_dtype, int CW, int64_t smem, cudaStream_t st) {
   if (streams == 0 || a.slices == 0) return cudaSuccess;
   if (bank_dtype == SDM_F32) {
-    if (act_dtype == SDM_F32) return launch_wr_t<float, float>(a, streams, CW, smem, st);
-    return launch_wr_t<float, __nv_bfloat16>(a, streams, CW, smem, st);
+    if (act_dtype == SDM_F32) return launch_write_read_f32_f32(a, streams, CW, smem, st);
+    return launch_write_read_f32_bf16(a, streams, CW, smem, st);
   }
-  if (act_dtype == SDM_F32) return launch_wr_t<__nv_bfloat16, float>(a, streams, CW, smem, st);
-  return launch_wr_t<__nv_bfloat16, __nv_bfloat16>(a, streams, CW, smem, st);
+  if (act_dtype == SDM_F32) return launch_write_read_bf16_f32(a, streams, CW, smem, st);
+  return launch_write_read_bf16_bf16(a, streams, CW, smem, st);
 }
 
 cudaError_t launch_bank_copy(const BankCopyArgs &a, int sm_count, cudaStream_t st) {
