@@ -224,6 +224,7 @@ struct WrChoice {
   int CW = 0;
   PlanLayout lay{};
   int64_t smem = 0;
+  bool two_per_sm = false;
 };
 
 // Column slices the write/read kernel is compiled for: 16..128 bytes of a row and at
@@ -287,6 +288,7 @@ WrChoice choose_write_read(const sdm_shape *sh, int sm_count) {
   const int64_t ctas = streams * (sh->d_v / std::max(cw, 1));
   const int64_t budget = ctas > sm_count ? kSmemTwoCta : kSmemOneCta;
   WrChoice c = stage_for(sh, cw, budget);
+  c.two_per_sm = budget == kSmemTwoCta;
   const int forced_g = env_int("SDM_WR_G", 0);
   if (forced_g > 0 && forced_g < c.lay.G) {
     c.lay = plan_layout(forced_g, sh->W, sh->R, sh->T);
@@ -591,6 +593,7 @@ sdm_status write_read_impl(const sdm_shape *sh, const void *q_w, const void *q_r
   wa.R = sh->R;
   wa.slices = (int32_t)(sh->d_v / wc.CW);
   wa.tok_bulk = (sh->W % 4 == 0 && sh->R % 4 == 0 && aligned(ww, 16) && aligned(wr, 16)) ? 1 : 0;
+  wa.two_per_sm = wc.two_per_sm ? 1 : 0;
   wa.lay = wc.lay;
   if (side) {                                          // the bank copy must land first
     ce = cudaStreamWaitEvent(cs, side->join, 0);

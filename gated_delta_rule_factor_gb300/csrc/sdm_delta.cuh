@@ -188,12 +188,36 @@ __device__ __forceinline__ void pair_tree(const float (&a)[VEC], float (&out)[VE
   float *mine = xch + (wsel * 8 + (lane & 7)) * VEC;
   const float *theirs = xch + ((wsel ^ 1) * 8 + (lane & 7)) * VEC;
   if (lane < 8) {
+    if constexpr (VEC % 4 == 0) {
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) mine[c] = x[c];
+      for (int c = 0; c < VEC; c += 4)
+        *reinterpret_cast<float4 *>(mine + c) = make_float4(x[c], x[c + 1], x[c + 2], x[c + 3]);
+    } else if constexpr (VEC == 2) {
+      *reinterpret_cast<float2 *>(mine) = make_float2(x[0], x[1]);
+    } else {
+      mine[0] = x[0];
+    }
   }
   named_barrier(bar, 64);
+  float o[VEC];
+  if constexpr (VEC % 4 == 0) {
 #pragma unroll
-  for (int c = 0; c < VEC; ++c) out[c] = __fadd_rn(x[c], theirs[c]);
+    for (int c = 0; c < VEC; c += 4) {
+      const float4 q = *reinterpret_cast<const float4 *>(theirs + c);
+      o[c] = q.x;
+      o[c + 1] = q.y;
+      o[c + 2] = q.z;
+      o[c + 3] = q.w;
+    }
+  } else if constexpr (VEC == 2) {
+    const float2 q = *reinterpret_cast<const float2 *>(theirs);
+    o[0] = q.x;
+    o[1] = q.y;
+  } else {
+    o[0] = theirs[0];
+  }
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) out[c] = __fadd_rn(x[c], o[c]);
 }
 
 template <typename BANK, int VEC, int JB>

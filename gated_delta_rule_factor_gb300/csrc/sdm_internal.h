@@ -101,6 +101,7 @@ struct WriteReadArgs {
   int32_t H, W, R;
   int32_t slices;         // d_v / CW
   int32_t tok_bulk;       // weights and values of a token fetched by bulk copies (16-byte aligned)
+  int32_t two_per_sm;     // the launch plans for two CTAs per SM (fewer loader warps)
   PlanLayout lay;
 };
 

@@ -10,7 +10,7 @@
 // Warp roles (one CTA):
 //   2 compute warps: the tokens of the current stage on the shared-memory rows, with the
 //               block-ordered token step (sdm_delta.cuh token_blocks2);
-//   8 loader warps: fetch the next stage's rows, its token data and the stage record
+//   8 loader warps (4 when two CTAs share an SM): fetch the next stage's rows, its token data and the stage record
 //               after it, all with 16-byte cp.async on the LSU path (a bulk/TMA copy per
 //               row slice costs more than it saves at this granularity); once the compute
 //               warps signal (barrier 5) that the current stage's next-to-last token is
@@ -47,23 +47,24 @@ __host__ __device__ inline TokLayout tok_layout(int G, int W, int R, int CW, int
 }
 
 // A CTA owns a slice of CW columns (CW * elem = 16..128 bytes of every row): two compute
-// warps, 8 loader warps.  Lane % 8 of a compute warp owns VB = CW / 8 consecutive columns.
-template <typename BANK, int CW>
+// warps and LW loader warps (8 when one CTA runs per SM, 4 when two share an SM, so that
+// their registers fit).  Lane % 8 of a compute warp owns VB = CW / 8 consecutive columns.
+template <typename BANK, int CW, int LW_ = 8>
 struct WrGeometry {
   static constexpr int VB = CW / 8;                   // columns per compute lane
   static constexpr int RB = CW * (int)sizeof(BANK);   // row slice bytes
   static constexpr int NCW = 2;                       // compute warps (rows split)
-  static constexpr int LW = 8;                        // loader warps
+  static constexpr int LW = LW_;                      // loader warps
   static constexpr int NTHR = 32 * (NCW + LW);
   static_assert(CW % 8 == 0 && RB >= 16 && RB <= 128 && (RB & (RB - 1)) == 0, "column slice");
 };
 
 // JB = the most rows a compute lane holds (one of the 8 row blocks of a token);
 // FULL: W == R == 8 * JB, fixed at compile time.
-template <typename BANK, typename ACT, int CW, int JB, bool FULL = false>
-__global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
+template <typename BANK, typename ACT, int CW, int JB, bool FULL = false, int LW = 8>
+__global__ void __launch_bounds__(WrGeometry<BANK, CW, LW>::NTHR)
     write_read_kernel(const __grid_constant__ WriteReadArgs a) {
-  using Geo = WrGeometry<BANK, CW>;
+  using Geo = WrGeometry<BANK, CW, LW>;
   constexpr int kLoaderThreads = 32 * Geo::LW;
   constexpr int VB = Geo::VB, NCW = Geo::NCW, NTHR = Geo::NTHR, RB = Geo::RB;
   constexpr int CPR = RB / 16;                        // 16-byte chunks per row slice
@@ -280,23 +281,29 @@ __global__ void __launch_bounds__(WrGeometry<BANK, CW>::NTHR)
 }
 
 // Launches the instance for the shape: W = R = 64 fixed at compile time, else the
-// smallest JB >= ceil(max(W, R) / 8).
-template <typename BANK, typename ACT, int CW>
-cudaError_t launch_cw(const WriteReadArgs &a, int64_t streams, int64_t smem, cudaStream_t st) {
+// smallest JB >= ceil(max(W, R) / 8); 4 loader warps when two CTAs share an SM.
+template <typename BANK, typename ACT, int CW, int LW>
+cudaError_t launch_cw_lw(const WriteReadArgs &a, int64_t streams, int64_t smem, cudaStream_t st) {
   const dim3 grid((unsigned)a.slices, (unsigned)streams);
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, WrGeometry<BANK, CW>::NTHR, smem, st>>>(a);
+    kern<<<grid, WrGeometry<BANK, CW, LW>::NTHR, smem, st>>>(a);
     return cudaGetLastError();
   };
   const int n = a.W > a.R ? a.W : a.R;
   const int per_lane = (n + 7) / 8;
-  if (a.W == 64 && a.R == 64) return go(write_read_kernel<BANK, ACT, CW, 8, true>);
-  if (per_lane <= 4) return go(write_read_kernel<BANK, ACT, CW, 4>);
-  if (per_lane <= 8) return go(write_read_kernel<BANK, ACT, CW, 8>);
-  if (per_lane <= 16) return go(write_read_kernel<BANK, ACT, CW, 16>);
+  if (a.W == 64 && a.R == 64) return go(write_read_kernel<BANK, ACT, CW, 8, true, LW>);
+  if (per_lane <= 4) return go(write_read_kernel<BANK, ACT, CW, 4, false, LW>);
+  if (per_lane <= 8) return go(write_read_kernel<BANK, ACT, CW, 8, false, LW>);
+  if (per_lane <= 16) return go(write_read_kernel<BANK, ACT, CW, 16, false, LW>);
   return cudaErrorInvalidValue;
+}
+
+template <typename BANK, typename ACT, int CW>
+cudaError_t launch_cw(const WriteReadArgs &a, int64_t streams, int64_t smem, cudaStream_t st) {
+  if (a.two_per_sm) return launch_cw_lw<BANK, ACT, CW, 4>(a, streams, smem, st);
+  return launch_cw_lw<BANK, ACT, CW, 8>(a, streams, smem, st);
 }
 
 }  // namespace wr
