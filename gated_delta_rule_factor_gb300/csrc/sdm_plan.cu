@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
   for (int k = 2; k <= P; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
       for (int i = tid; i < P / 2; i += kThreads) {
-        const int lo = (i / j) * 2 * j + (i % j), hi = lo + j;
+        const int lo = ((i & ~(j - 1)) << 1) | (i & (j - 1)), hi = lo + j;   // j is a power of two
         const bool asc = (lo & k) == 0;
         const uint64_t x = keys[lo], y = keys[hi];
         if ((x > y) == asc) { keys[lo] = y; keys[hi] = x; }
