@@ -692,8 +692,10 @@ sdm_status sdm_decode_step(const sdm_shape *sh, const void *q_w, const void *q_r
     if (overlap(o, r_bi)) return fail(SDM_ERR_ALIAS, "%s overlaps bank_in", o.name);
   if (!donate && overlap(r_bi, r_bo)) return fail(SDM_ERR_ALIAS, "bank_out overlaps bank_in (use donate)");
 
-  const int64_t smem = (int64_t)2 * sh->F * sh->d_sub * 4 + (int64_t)2 * d.ntot * 4 + (int64_t)(cl.n[0] + cl.n[1]) * 4;
-  if (smem > 160 * 1024) return fail(SDM_ERR_UNSUPPORTED, "decode needs %lld bytes of shared memory", (long long)smem);
+  const int64_t region = decode_region_bytes(sh->W, sh->R, !donate);
+  const int64_t smem = region + (int64_t)2 * sh->F * sh->d_sub * 4 + (int64_t)2 * d.ntot * 4 +
+                       (int64_t)(cl.n[0] + cl.n[1]) * 4;
+  if (smem > 200 * 1024) return fail(SDM_ERR_UNSUPPORTED, "decode needs %lld bytes of shared memory", (long long)smem);
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   int32_t *err = static_cast<int32_t *>(workspace);
@@ -723,6 +725,7 @@ sdm_status sdm_decode_step(const sdm_shape *sh, const void *q_w, const void *q_r
   da.H = (int32_t)sh->H;
   da.bank_in_shared = bank_in_shared ? 1 : 0;
   da.copy_rest = donate ? 0 : 1;
+  da.region_bytes = region;
   da.g = d.g;
   if ((st = run_kernel(SDM_KERNEL_DECODE, cs, "decode",
                        [&] { return launch_decode(da, cl, sh->act_dtype, sh->bank_dtype, EF, EC, smem, cs); })) != SDM_OK)

@@ -339,6 +339,12 @@ __device__ __forceinline__ void bulk_store(void *dst_gmem, const void *src_smem,
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // Waits until this thread's bulk stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// Waits until at most N of this thread's newest bulk store groups are still reading
+// shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_pending() {
+  asm volatile("cp.async.bulk.wait_group.read %0;\n" ::"n"(N) : "memory");
+}
 // Waits until this thread's bulk stores are complete (their writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 

@@ -11,19 +11,18 @@
 // bitwise repeatable and independent of how tokens are staged.
 //
 // Two layouts:
-//   * delta_write_cols / weighted_read_cols (the decode kernel, rows in global memory): a
-//     warp owns NCG 16-byte column groups (lane % NCG) and splits the rows over
-//     RG = 32 / NCG row groups (lane / NCG): row j belongs to row group j % RG and is
-//     accumulated in increasing j; the RG partial sums are combined by an xor butterfly.
-//     Rows are fetched kJB at a time per lane (independent loads in flight).
+//   * delta_write_staged / weighted_read_staged (the decode kernel): a warp owns NCG
+//     16-byte column groups (lane % NCG) and splits the rows over RG = 32 / NCG row
+//     groups (lane / NCG): row j belongs to row group j % RG and is accumulated in
+//     increasing j; the RG partial sums are combined by an xor butterfly.  Each lane
+//     fetches all of its rows into shared memory with cp.async at once (one memory round
+//     trip per sum) and reads back only what it fetched.
 //   * token_blocks2 (the write/read kernel, rows in shared memory), below.
 #pragma once
 
 #include "sdm_common.cuh"
 
 namespace sdm {
-
-constexpr int kJB = 8;  // rows in flight per lane
 
 // 16-byte raw row chunk <-> float32 lanes.
 template <typename BANK>
@@ -33,93 +32,86 @@ __device__ __forceinline__ void unpack16(const uint4 &u, float (&out)[Vec16<BANK
   for (int i = 0; i < Vec16<BANK>::N; ++i) out[i] = to_f32(e[i]);
 }
 
+// stage: this warp's rows, NCG * 16 bytes each (at least n rows); src(j): row j's 16
+// bytes of this lane's column group in global memory.  valid == false (a column group
+// past d_v) fetches and stores nothing; its lanes' sums are not used.
+template <int NCG, class SrcRow>
+__device__ __forceinline__ void stage_rows(int n, bool valid, unsigned char *stage, SrcRow src) {
+  constexpr int RG = 32 / NCG, RB = NCG * 16;
+  const int lane = threadIdx.x & 31, rg = lane / NCG;
+  unsigned char *mine = stage + (lane % NCG) * 16;
+  if (valid)
+#pragma unroll 4
+    for (int j = rg; j < n; j += RG) cp_async16(mine + j * RB, src(j));
+  cp_async_commit();
+  cp_async_wait_all();
+}
+
+template <typename BANK, int NCG>
+__device__ __forceinline__ void staged_row(const unsigned char *stage, int j, float (&out)[Vec16<BANK>::N]) {
+  const int lane = threadIdx.x & 31;
+  unpack16<BANK>(*reinterpret_cast<const uint4 *>(stage + j * (NCG * 16) + (lane % NCG) * 16), out);
+}
+
+template <int NCG, int VEC>
+__device__ __forceinline__ void row_group_butterfly(float (&x)[VEC]) {
+#pragma unroll
+  for (int o = NCG; o < 32; o <<= 1)
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) x[c] = __fadd_rn(x[c], __shfl_xor_sync(0xffffffffu, x[c], o));
+}
+
+// The gated delta-rule write of W rows: p = sum_j w_j alpha m_j, then
+// m_j <- alpha m_j + w_j beta (v - p), stored through dst(j).
 template <typename BANK, int NCG, class SrcRow, class DstRow>
-__device__ __forceinline__ void delta_write_cols(int W, const float *w, float alpha, float beta,
-                                                 const float (&v)[Vec16<BANK>::N], SrcRow src,
-                                                 DstRow dst) {
+__device__ __forceinline__ void delta_write_staged(int W, const float *w, float alpha, float beta,
+                                                   const float (&v)[Vec16<BANK>::N], bool valid,
+                                                   unsigned char *stage, SrcRow src, DstRow dst) {
   constexpr int VEC = Vec16<BANK>::N, RG = 32 / NCG;
   const int rg = (threadIdx.x & 31) / NCG;
+  stage_rows<NCG>(W, valid, stage, src);
   float acc[VEC];
 #pragma unroll
   for (int c = 0; c < VEC; ++c) acc[c] = 0.0f;
-  for (int j0 = rg; j0 < W; j0 += RG * kJB) {
-    uint4 raw[kJB];
+  for (int j = rg; j < W; j += RG) {
+    const float wj = w[j];
+    float r[VEC];
+    staged_row<BANK, NCG>(stage, j, r);
 #pragma unroll
-    for (int b = 0; b < kJB; ++b) {
-      const int j = j0 + b * RG;
-      if (j < W) raw[b] = *reinterpret_cast<const uint4 *>(src(j));
-    }
-#pragma unroll
-    for (int b = 0; b < kJB; ++b) {
-      const int j = j0 + b * RG;
-      if (j < W) {
-        const float wj = w[j];
-        float r[VEC];
-        unpack16<BANK>(raw[b], r);
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) acc[c] = __fmaf_rn(wj, __fmul_rn(alpha, r[c]), acc[c]);
-      }
-    }
+    for (int c = 0; c < VEC; ++c) acc[c] = __fmaf_rn(wj, __fmul_rn(alpha, r[c]), acc[c]);
   }
-#pragma unroll
-  for (int o = NCG; o < 32; o <<= 1)
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) acc[c] = __fadd_rn(acc[c], __shfl_xor_sync(0xffffffffu, acc[c], o));
+  row_group_butterfly<NCG>(acc);
   float d[VEC];
 #pragma unroll
   for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], acc[c]));
-  for (int j0 = rg; j0 < W; j0 += RG * kJB) {
-    uint4 raw[kJB];
+  if (!valid) return;
+  for (int j = rg; j < W; j += RG) {
+    const float wj = w[j];
+    float r[VEC];
+    staged_row<BANK, NCG>(stage, j, r);
 #pragma unroll
-    for (int b = 0; b < kJB; ++b) {
-      const int j = j0 + b * RG;
-      if (j < W) raw[b] = *reinterpret_cast<const uint4 *>(src(j));
-    }
-#pragma unroll
-    for (int b = 0; b < kJB; ++b) {
-      const int j = j0 + b * RG;
-      if (j < W) {
-        const float wj = w[j];
-        float r[VEC];
-        unpack16<BANK>(raw[b], r);
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) r[c] = __fmaf_rn(wj, d[c], __fmul_rn(alpha, r[c]));
-        store_vec16<BANK>(dst(j), r);
-      }
-    }
+    for (int c = 0; c < VEC; ++c) r[c] = __fmaf_rn(wj, d[c], __fmul_rn(alpha, r[c]));
+    store_vec16<BANK>(dst(j), r);
   }
 }
 
+// The weighted read y = sum_j r_j m_j of R rows fetched through src(j).
 template <typename BANK, int NCG, class SrcRow>
-__device__ __forceinline__ void weighted_read_cols(int R, const float *r, SrcRow src,
-                                                   float (&y)[Vec16<BANK>::N]) {
+__device__ __forceinline__ void weighted_read_staged(int R, const float *r, bool valid, unsigned char *stage,
+                                                     SrcRow src, float (&y)[Vec16<BANK>::N]) {
   constexpr int VEC = Vec16<BANK>::N, RG = 32 / NCG;
   const int rg = (threadIdx.x & 31) / NCG;
+  stage_rows<NCG>(R, valid, stage, src);
 #pragma unroll
   for (int c = 0; c < VEC; ++c) y[c] = 0.0f;
-  for (int j0 = rg; j0 < R; j0 += RG * kJB) {
-    uint4 raw[kJB];
+  for (int j = rg; j < R; j += RG) {
+    const float rj = r[j];
+    float m[VEC];
+    staged_row<BANK, NCG>(stage, j, m);
 #pragma unroll
-    for (int b = 0; b < kJB; ++b) {
-      const int j = j0 + b * RG;
-      if (j < R) raw[b] = *reinterpret_cast<const uint4 *>(src(j));
-    }
-#pragma unroll
-    for (int b = 0; b < kJB; ++b) {
-      const int j = j0 + b * RG;
-      if (j < R) {
-        const float rj = r[j];
-        float m[VEC];
-        unpack16<BANK>(raw[b], m);
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) y[c] = __fmaf_rn(rj, m[c], y[c]);
-      }
-    }
+    for (int c = 0; c < VEC; ++c) y[c] = __fmaf_rn(rj, m[c], y[c]);
   }
-#pragma unroll
-  for (int o = NCG; o < 32; o <<= 1)
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) y[c] = __fadd_rn(y[c], __shfl_xor_sync(0xffffffffu, y[c], o));
+  row_group_butterfly<NCG>(y);
 }
 
 // ------------------------------------------------------------------------------------
@@ -249,7 +241,7 @@ __device__ __forceinline__ void pair_read(const BlockSlots1<JB> &rs, const uint1
 }
 
 // One token: the gated delta-rule write of its W rows, then the read of its R rows, with
-// the arithmetic of delta_write_cols / weighted_read_cols per element and the block order
+// the arithmetic of delta_write_staged / weighted_read_staged per element and the block order
 // above for both sums.  rm / wt: the token's row references (stage-buffer row indices)
 // and weights, W write entries then R read entries; rows: the stage buffer offset by this
 // lane's column group; RB: the row slice in bytes.  When the token reads none of the rows

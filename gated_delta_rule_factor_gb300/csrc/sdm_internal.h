@@ -10,6 +10,23 @@ namespace sdm {
 
 constexpr int kThreads = 256;
 
+// Decode kernel geometry.  Its dynamic shared memory starts with one region that serves,
+// in turn, as the sub-key tile of the scoring, the ring through which the copying form
+// streams the table, and the rows of the write and the read; the queries, factor scores
+// and candidate tuples follow it.
+constexpr int kDecodeNCG = 8;                               // 16-byte column groups per warp
+constexpr int64_t kDecodeRowSlice = kDecodeNCG * 16;        // bytes of a row a warp stages
+constexpr int kDecodeScoreRows = kThreads / 2;              // sub-key rows per scoring tile
+constexpr int kDecodeScoreCols = 32;                        // sub-key columns per scoring tile
+constexpr int64_t kDecodeCopyRingBytes = 3 * 16384;
+inline int64_t decode_region_bytes(int64_t W, int64_t R, bool copy) {
+  int64_t b = (int64_t)(kThreads / 32) * (W > R ? W : R) * kDecodeRowSlice;
+  const int64_t tile = (int64_t)kDecodeScoreRows * (kDecodeScoreCols + 1) * 4;
+  if (tile > b) b = tile;
+  if (copy && kDecodeCopyRingBytes > b) b = kDecodeCopyRingBytes;
+  return (b + 127) / 128 * 128;
+}
+
 // Position tuples (p_1..p_F), p_f < min(k, n_f), with prod(p_f + 1) <= k, in
 // lexicographic order; byte f of an entry holds p_f.  Index 0 = write query (k = W),
 // 1 = read query (k = R).  Passed to kernels by value.
@@ -119,7 +136,8 @@ struct DecodeArgs {
   int64_t B, N, d_v;
   int32_t H;
   int32_t bank_in_shared; // bank_in is one [H,N,d_v] table for all streams
-  int32_t copy_rest;      // copy the unwritten rows bank_in -> bank_out
+  int32_t copy_rest;      // copy the table bank_in -> bank_out (then write its written rows)
+  int64_t region_bytes;   // decode_region_bytes(W, R, copy_rest)
   KeyGeometry g;
 };
 

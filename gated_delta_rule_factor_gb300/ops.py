@@ -8,6 +8,7 @@ There is no CPU path: without the library, importing the package fails.
 from __future__ import annotations
 
 import ctypes
+import math
 from typing import Optional, Sequence
 
 import torch
@@ -202,7 +203,7 @@ def sdm_decode_step(q_w: torch.Tensor, q_r: torch.Tensor, k_val: torch.Tensor, g
                     ("workspace", workspace)):
         _require_cuda_contig(name, t, dev)
     shape = _shape_of(q_w, k_val, bank_in, factor_dims, W, R, 1, T=1)
-    N = int(torch.tensor(list(factor_dims)).prod().item())
+    N = math.prod(int(n) for n in factor_dims)
     if donate:
         bank_out = bank
     elif bank_out is None:
