@@ -453,8 +453,36 @@ def bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg):
     kt = sdm.profile_end()
     ms = ev0.elapsed_time(ev1)
     value = cfg.B * args.steps * world / (ms / 1e3)
+    launches = sdm.launch_count() - launches0
     sb = 4 if cfg.bank_dtype == "f32" else 2
     alg = cfg.B * cfg.H * (cfg.W + cfg.R) * cfg.d_v * sb + (0 if donate else 2 * cfg.B * cfg.H * cfg.N * cfg.d_v * sb)
+
+    # the same donated steps replayed from one CUDA graph of nT steps (no per-call host
+    # work or launch gaps); the copying form is left out: every captured step would keep
+    # its own successor table alive in the graph's memory pool
+    graph = None
+    if donate:
+        def gstep(i):
+            nonlocal state
+            _, state = sdm.sdm_decode_step(*per_step[i % nT], g["subkeys"], state, cfg.W, cfg.R,
+                                           factor_dims=cfg.factor_dims, donate=True, y=y, workspace=ws)
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            for i in range(nT):
+                gstep(i)
+        cg.replay()
+        reps = max(1, args.steps // nT)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        g0.record(stream)
+        for _ in range(reps):
+            cg.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        gms = g0.elapsed_time(g1) / (reps * nT)
+        graph = {"ms_per_step": gms, "value": cfg.B * world / (gms / 1e3), "unit": UNIT,
+                 "steps": reps * nT, "steps_per_graph": nT}
     n, kms = kt["decode"]
     achieved = alg / (kms / max(n, 1) / 1e3) / 1e9
     peak, peak_kind = peaks()
@@ -466,7 +494,7 @@ def bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg):
             "config": {"workload": workload_desc(cfg), "donate": donate},
             "roofline": {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None, "peak_source": peak_kind},
-            "gpu_launches": sdm.launch_count() - launches0, "clocks": clk.summary()}), flush=True)
+            "gpu_launches": launches, "clocks": clk.summary(), "graph": graph}), flush=True)
     return 0
 
 

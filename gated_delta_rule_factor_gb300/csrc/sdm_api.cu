@@ -16,6 +16,30 @@
 
 using namespace sdm;
 
+cudaError_t sdm::raise_smem_limit(const void *kernel, int64_t smem) {
+  struct Raised {
+    const void *kernel;
+    int dev;
+    int64_t smem;
+  };
+  static std::mutex mu;
+  static std::vector<Raised> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (Raised &r : done) {
+    if (r.kernel != kernel || r.dev != dev) continue;
+    if (r.smem >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) r.smem = smem;
+    return e;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) done.push_back({kernel, dev, smem});
+  return e;
+}
+
 namespace {
 
 // ---------------------------------------------------------------- error reporting

@@ -10,8 +10,6 @@
 // write with bank_out as the destination (the written rows are copied, then replaced).
 #pragma once
 
-#include <atomic>
-
 #include "sdm_common.cuh"
 #include "sdm_delta.cuh"
 #include "sdm_internal.h"
@@ -235,20 +233,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-// Launches one decode_kernel instance.  Its dynamic shared-memory limit is raised once
-// per device and size: a decode step is short enough for the attribute call to show.
+// Launches one decode_kernel instance.
 template <int EF, int EC, typename ACT, typename BANK>
 cudaError_t launch_decode_k(const DecodeArgs &a, const CandidateList &cl, int64_t smem, cudaStream_t st) {
-  static std::atomic<int64_t> raised[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(decode_kernel<EF, EC, ACT, BANK>), smem);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || smem > raised[dev].load(std::memory_order_relaxed)) {
-    e = cudaFuncSetAttribute(decode_kernel<EF, EC, ACT, BANK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) raised[dev].store(smem, std::memory_order_relaxed);
-  }
   decode_kernel<EF, EC, ACT, BANK><<<(unsigned)(a.B * a.H), kThreads, smem, st>>>(a, cl);
   return cudaGetLastError();
 }

@@ -148,6 +148,11 @@ struct WriteReadConfig {
   int64_t smem_bytes;
 };
 
+// Raises a kernel's dynamic shared-memory limit to at least `smem` bytes on the current
+// device, once per (kernel, device, larger size): the attribute call is not repeated per
+// launch, so steady-state calls make only stream-ordered CUDA calls (graph capture).
+cudaError_t raise_smem_limit(const void *kernel, int64_t smem);
+
 // Launchers, defined next to their kernels.  Each returns the launch error.
 cudaError_t launch_score_simt(const ScoreArgs &a, int act_dtype, cudaStream_t st);
 cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t st);   // bf16, tensor cores

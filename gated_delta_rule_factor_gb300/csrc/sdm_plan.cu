@@ -242,8 +242,7 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
 cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int P, cudaStream_t st) {
   if (streams == 0 || a.lay.n_stages == 0) return cudaSuccess;
   const int64_t smem = (int64_t)P * 8 + ((P + 3) & ~3) + a.lay.G;
-  cudaError_t e = cudaFuncSetAttribute(plan_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(plan_sort_kernel), smem);
   if (e != cudaSuccess) return e;
   plan_sort_kernel<<<dim3((unsigned)a.lay.n_stages, (unsigned)streams), kThreads, smem, st>>>(a, P);
   return cudaGetLastError();
@@ -252,8 +251,7 @@ cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int P, cudaStre
 cudaError_t launch_plan_link(const PlanArgs &a, int64_t streams, cudaStream_t st) {
   if (streams == 0 || a.lay.n_stages == 0) return cudaSuccess;
   const int64_t smem = (int64_t)a.lay.L * 12;
-  cudaError_t e = cudaFuncSetAttribute(plan_link_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(plan_link_kernel), smem);
   if (e != cudaSuccess) return e;
   plan_link_kernel<<<dim3((unsigned)a.lay.n_stages, (unsigned)streams), kThreads, smem, st>>>(a);
   return cudaGetLastError();

@@ -275,7 +275,7 @@ cudaError_t launch_score_tc(const ScoreArgs &s, cudaStream_t st) {
     a.off[f] = g.off[f];
   }
   const int64_t smem = 1024 + (int64_t)kTcStages * (kTcM + a.n_tile) * 128 + 256;
-  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(score_tc_kernel), smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((s.BT + kTcM - 1) / kTcM), (unsigned)(2 * s.H * g.F * a.n_tiles));
   score_tc_kernel<<<grid, kTcThreads, smem, st>>>(a);

@@ -286,7 +286,7 @@ template <typename BANK, typename ACT, int CW, int LW>
 cudaError_t launch_cw_lw(const WriteReadArgs &a, int64_t streams, int64_t smem, cudaStream_t st) {
   const dim3 grid((unsigned)a.slices, (unsigned)streams);
   auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, WrGeometry<BANK, CW, LW>::NTHR, smem, st>>>(a);
     return cudaGetLastError();
