@@ -226,3 +226,34 @@ def test_decode_bf16(sdm):
                                            donate=True, act_dtype="bf16", bank_dtype="bf16")
         assert_close(y_c[:, t], y_o, RTOL["bf16"], "bf16 decode y")
     assert_close(b_c, bank, RTOL["bf16"], "bf16 decode bank")
+
+
+# Decode shapes beyond the benchmark's: bfloat16 rows (8 per 16-byte group), a d_v whose
+# last column block is partly past the row end, W != R with three factors, and the
+# largest k.  Each runs donated and copying steps (bit-equal) against the oracle.
+_DECODE_SHAPES = {
+    "bf16_bank_and_acts": dict(act_dtype="bf16", bank_dtype="bf16", B=4),
+    "ragged_d_v": dict(d_v=104, B=3),
+    "bf16_bank_ragged_d_v": dict(bank_dtype="bf16", d_v=72, B=3),
+    "w_ne_r_three_factors": dict(factor_dims=(8, 8, 16), d_sub=32, W=8, R=24, B=3),
+    "max_k": dict(W=128, R=128, B=2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(_DECODE_SHAPES))
+def test_decode_shapes_against_oracle(sdm, name):
+    cfg = CONFIGS["decode"].replace(**_DECODE_SHAPES[name])
+    steps = 3
+    d = sdm_inputs.make_decode_inputs(cfg, steps=steps)
+    y_d, b_d = _decode_steps(sdm, cfg, d, steps, donate=True)
+    y_c, b_c = _decode_steps(sdm, cfg, d, steps, donate=False)
+    assert torch.equal(y_d, y_c) and torch.equal(b_d, b_c)
+    bank = d["bank"].double().numpy().copy()
+    tol = RTOL[cfg.bank_dtype if cfg.bank_dtype == "bf16" else cfg.act_dtype]
+    for t in range(steps):
+        y_o, bank = oracle.sdm_decode_step(d["q_w"][:, t], d["q_r"][:, t], d["k_val"][:, t],
+                                           d["gates"][:, t], d["subkeys"], bank, factor_dims=cfg.factor_dims,
+                                           W=cfg.W, R=cfg.R, donate=True, act_dtype=cfg.act_dtype,
+                                           bank_dtype=cfg.bank_dtype)
+        assert_close(y_d[:, t], y_o, tol, f"{name} y step {t}")
+    assert_close(b_d, bank, tol, f"{name} bank")
