@@ -19,7 +19,8 @@ namespace sdm {
 namespace dec {
 
 constexpr int kDecodeWarps = kThreads / 32;
-constexpr int kSelectWarp = 4;                 // warps 4 and 5 select (write, read query)
+constexpr int kSelectWarp = 4;                 // warps 4..7 select (two per query)
+constexpr int kBarSelect = 1;                  // named barrier of the selecting warps
 constexpr int kCopyWarp = 2;                   // streams the copy meanwhile
 constexpr int kScoreRows = kDecodeScoreRows;   // sub-key rows per scoring tile (two queries each)
 constexpr int kScoreCols = kDecodeScoreCols;   // sub-key columns per scoring tile
@@ -68,7 +69,7 @@ __device__ __forceinline__ bool copy_table(unsigned char *ring, uint64_t *bar, c
   return ok;
 }
 
-// One CTA per stream: all warps score, warps kSelectWarp and kSelectWarp + 1 select
+// One CTA per stream: all warps score, warps kSelectWarp .. kSelectWarp + 3 select
 // (in the copying form warp kCopyWarp copies the whole table bank_in -> bank_out
 // meanwhile), all warps write and read.  The selection stays off warp 0: measured on
 // GB300, the same selection code ran about six times slower on warp 0 than on any
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int32_t wsorted[SDM_MAX_K];
   __shared__ uint8_t read_written[SDM_MAX_K];
   __shared__ __align__(8) uint64_t copy_bar[kCopyStages];
+  __shared__ uint64_t part_keys[2][32 * EC];  // part 1's best candidate keys per query
 
   const KeyGeometry &g = a.g;
   const int64_t s = blockIdx.x;
@@ -155,22 +157,41 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
 
-  // exact top-k: warp kSelectWarp the write query, warp kSelectWarp + 1 the read query
-  if (warp == kSelectWarp || warp == kSelectWarp + 1) {
-    // one body for both queries: q is opaque to the compiler, so that it does not
-    // specialise the selection per warp
-    int q = warp - kSelectWarp;
-    asm volatile("" : "+r"(q));
-    row_topk<EF, EC>(scores + q * g.ntot, g, q, cand + (q ? cl.n[0] : 0), cl.n[q], rs[q], sel_idx[q],
-                     sel_wt[q]);
-    const int k = g.k[q];
-    for (int j = lane; j < k; j += 32) {
-      if (sel_idx[q][j] < 0 || sel_idx[q][j] >= a.N) {
-        raise_error(a.err, SDM_DEVERR_SLOT_RANGE);
-        sel_idx[q][j] = 0;
+  // exact top-k on warps kSelectWarp .. kSelectWarp + 3: warp (q, part) = (w / 2, w % 2)
+  // with w = warp - kSelectWarp sorts the factors part, part + 2, ... of query q, then
+  // keeps the best of its part of q's candidate tuples; part 0 merges part 1's list
+  // into its own (exact: the keys are unique) and computes the weights.  The result is
+  // the one row_topk gives on one warp.
+  if (warp >= kSelectWarp && warp < kSelectWarp + 4) {
+    int w = warp - kSelectWarp;
+    asm volatile("" : "+r"(w));  // one body for every selecting warp, not one per warp
+    const int q = w >> 1, part = w & 1;
+    for (int f = part; f < g.F; f += 2) factor_topk<EF>(scores + q * g.ntot, g, q, f, rs[q]);
+    named_barrier(kBarSelect, 4 * 32);
+    const int n = cl.n[q];
+    const int mid = min(n, (n / 2 + 32 * EC - 1) / (32 * EC) * (32 * EC));  // whole chunks first
+    uint64_t ck[EC];
+    candidate_topk<EC>(cand + (q ? cl.n[0] : 0), part ? mid : 0, part ? n : mid, g, rs[q], ck);
+    if (part == 1) {
+#pragma unroll
+      for (int e = 0; e < EC; ++e) part_keys[q][lane * EC + e] = ck[e];
+    }
+    named_barrier(kBarSelect, 4 * 32);
+    if (part == 0) {
+      uint64_t other[EC];
+#pragma unroll
+      for (int e = 0; e < EC; ++e) other[e] = part_keys[q][lane * EC + e];
+      warp_merge_top_desc<EC>(ck, other);
+      finish_topk<EC>(ck, g, q, rs[q], sel_idx[q], sel_wt[q]);
+      const int k = g.k[q];
+      for (int j = lane; j < k; j += 32) {
+        if (sel_idx[q][j] < 0 || sel_idx[q][j] >= a.N) {
+          raise_error(a.err, SDM_DEVERR_SLOT_RANGE);
+          sel_idx[q][j] = 0;
+        }
+        if (a.idx[q]) a.idx[q][s * k + j] = sel_idx[q][j];
+        if (a.wt[q]) a.wt[q][s * k + j] = sel_wt[q][j];
       }
-      if (a.idx[q]) a.idx[q][s * k + j] = sel_idx[q][j];
-      if (a.wt[q]) a.wt[q][s * k + j] = sel_wt[q][j];
     }
   } else if (warp == kCopyWarp && a.copy_rest) {
     // bank_out <- bank_in, all rows: the write below then replaces the written ones

@@ -67,48 +67,52 @@ __device__ __forceinline__ void top_of_chunks(int n, Make make, uint64_t (&best)
   }
 }
 
-// scores: the row's ntot factor scores (shared memory), factor f at g.off[f].
-// qsel: 0 = write query (k = W), 1 = read query (k = R).
-// cand: the candidate tuples of this query kind (shared memory), ncand entries.
-// Writes k slot ids (best first) to idx_out and their softmax weights to wt_out.
-template <int EF, int EC>
-__device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry &g, int qsel,
-                                         const uint32_t *cand, int ncand, RowScratch &sc,
-                                         int32_t *idx_out, float *wt_out) {
-  const int lane = threadIdx.x & 31;
-  const int k = g.k[qsel];
+// The phases of one row's selection, each run by one warp: factor_topk for every
+// factor, then candidate_topk over the candidate tuples (or a part of them, whose best
+// lists warp_merge_top_desc can merge, since the keys are unique), then finish_topk.
 
-  // 1. best-first order of each factor, kept to its first min(k, n_f) positions
-  for (int f = 0; f < g.F; ++f) {
-    const int nf = g.nf[f];
-    const float *s = scores + g.off[f];
-    uint64_t best[EF];
-    top_of_chunks<EF>(nf, [&](int c0, uint64_t(&key)[EF]) {
-#pragma unroll
-      for (int e = 0; e < EF; ++e) {
-        const int a = c0 + lane * EF + e;
-        key[e] = (a < nf) ? ((uint64_t)ordered_bits(s[a]) << 32) | (uint32_t)a : 0ull;
-      }
-    }, best);
-    const int kf = g.kf[qsel][f];
+// Best-first order of factor f, kept to its first min(k, n_f) positions (sc.fs, sc.fi).
+template <int EF>
+__device__ __forceinline__ void factor_topk(const float *scores, const KeyGeometry &g, int qsel, int f,
+                                            RowScratch &sc) {
+  const int lane = threadIdx.x & 31;
+  const int nf = g.nf[f];
+  const float *s = scores + g.off[f];
+  uint64_t best[EF];
+  top_of_chunks<EF>(nf, [&](int c0, uint64_t(&key)[EF]) {
 #pragma unroll
     for (int e = 0; e < EF; ++e) {
-      const int pos = lane * EF + e;
-      if (pos < kf) {
-        sc.fs[f * SDM_MAX_K + pos] = from_ordered_bits((uint32_t)(best[e] >> 32));
-        sc.fi[f * SDM_MAX_K + pos] = (int32_t)(uint32_t)(best[e] & 0xffffffffu);
-      }
+      const int a = c0 + lane * EF + e;
+      key[e] = (a < nf) ? ((uint64_t)ordered_bits(s[a]) << 32) | (uint32_t)a : 0ull;
+    }
+  }, best);
+  const int kf = g.kf[qsel][f];
+#pragma unroll
+  for (int e = 0; e < EF; ++e) {
+    const int pos = lane * EF + e;
+    if (pos < kf) {
+      sc.fs[f * SDM_MAX_K + pos] = from_ordered_bits((uint32_t)(best[e] >> 32));
+      sc.fi[f * SDM_MAX_K + pos] = (int32_t)(uint32_t)(best[e] & 0xffffffffu);
     }
   }
-  __syncwarp();
+}
 
-  // 2. candidate tuples, keyed and kept best first (k <= 32*EC)
-  uint64_t ck[EC];
-  top_of_chunks<EC>(ncand, [&](int c0, uint64_t(&kk)[EC]) {
+// Candidate tuples cand[c0, c1), keyed and kept best first (k <= 32 * EC); an empty
+// range gives all-zero keys, which order after every real key.
+template <int EC>
+__device__ __forceinline__ void candidate_topk(const uint32_t *cand, int c0, int c1, const KeyGeometry &g,
+                                               const RowScratch &sc, uint64_t (&ck)[EC]) {
+  const int lane = threadIdx.x & 31;
+  if (c1 <= c0) {
+#pragma unroll
+    for (int e = 0; e < EC; ++e) ck[e] = 0ull;
+    return;
+  }
+  top_of_chunks<EC>(c1 - c0, [&](int b0, uint64_t(&kk)[EC]) {
 #pragma unroll
     for (int e = 0; e < EC; ++e) {
-      const int c = c0 + lane * EC + e;
-      if (c < ncand) {
+      const int c = c0 + b0 + lane * EC + e;
+      if (c < c1) {
         const uint32_t t = cand[c];
         const int p0 = t & 255, p1 = (t >> 8) & 255, p2 = (t >> 16) & 255, p3 = t >> 24;
         float S = sc.fs[p0];
@@ -124,8 +128,14 @@ __device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry 
       }
     }
   }, ck);
+}
 
-  // 3. softmax weights of the k best (fixed summation order) and slot ids
+// Softmax weights of the k best keys (fixed summation order) and their slot ids.
+template <int EC>
+__device__ __forceinline__ void finish_topk(const uint64_t (&ck)[EC], const KeyGeometry &g, int qsel,
+                                            const RowScratch &sc, int32_t *idx_out, float *wt_out) {
+  const int lane = threadIdx.x & 31;
+  const int k = g.k[qsel];
   const float S0 = from_ordered_bits((uint32_t)(__shfl_sync(0xffffffffu, ck[0], 0) >> 32));
   float ex[EC];
   float part = 0.0f;
@@ -160,6 +170,21 @@ __device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry 
     }
   }
   __syncwarp();
+}
+
+// One row by one warp.  scores: the row's ntot factor scores (shared memory), factor f
+// at g.off[f]; qsel: 0 = write query (k = W), 1 = read query (k = R); cand: the
+// candidate tuples of this query kind (shared memory), ncand entries.  Writes k slot
+// ids (best first) to idx_out and their softmax weights to wt_out.
+template <int EF, int EC>
+__device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry &g, int qsel,
+                                         const uint32_t *cand, int ncand, RowScratch &sc,
+                                         int32_t *idx_out, float *wt_out) {
+  for (int f = 0; f < g.F; ++f) factor_topk<EF>(scores, g, qsel, f, sc);
+  __syncwarp();
+  uint64_t ck[EC];
+  candidate_topk<EC>(cand, 0, ncand, g, sc, ck);
+  finish_topk<EC>(ck, g, qsel, sc, idx_out, wt_out);
 }
 
 // Terms [0, n) of one factor score folded into acc, n <= kBf16Block: one block of the
