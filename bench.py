@@ -50,6 +50,25 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(cfg, rank: int) -> int:
+    """Seed of a rank's inputs: every rank runs its own streams (independent problems)."""
+    return cfg.seed + 7919 * rank
+
+
+def max_over_ranks(x: float, pg, device) -> float:
+    """The largest of the ranks' values (a time): the whole job is as slow as its slowest rank."""
+    if pg is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units per second of all ranks together, timed by the slowest rank's ``ms``."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def workload_desc(cfg) -> str:
     dims = "x".join(str(n) for n in cfg.factor_dims)
     return (f"{cfg.name}: B={cfg.B} T={cfg.T} H={cfg.H} d_v={cfg.d_v} factors={dims} "
@@ -284,7 +303,7 @@ def main():
     if cfg.T == 1:
         return bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg)
 
-    d = sdm_inputs.make_inputs(cfg, seed=cfg.seed + 7919 * rank)
+    d = sdm_inputs.make_inputs(cfg, seed=rank_seed(cfg, rank))
     g = {k: v.to(dev) for k, v in d.items()}
     B, T, H = cfg.B, cfg.T, cfg.H
     bank = torch.empty((B, H, cfg.N, cfg.d_v), dtype=g["bank_init"].dtype, device=dev)
@@ -319,13 +338,8 @@ def main():
         barrier()
     kt = sdm.profile_end()
     launches = sdm.launch_count() - launches0
-    ms = ev0.elapsed_time(ev1)
-    if pg is not None:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens_per_rank = B * T * args.steps
-    value = tokens_per_rank * world / (ms / 1e3)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
+    value = whole_job_rate(B * T * args.steps, world, ms)
 
     # ---- roofline of the dominant kernel (fused gather / update / read)
     sb = 4 if cfg.bank_dtype == "f32" else 2
@@ -399,12 +413,8 @@ def main():
             stream.wait_event(ev_back[k])
         e1.record(stream)
         barrier()
-        ems = e0.elapsed_time(e1)
-        if pg is not None:
-            t = torch.tensor([ems], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": B * T * e_steps * world / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        ems = max_over_ranks(e0.elapsed_time(e1), pg, dev)
+        e2e = {"value": whole_job_rate(B * T * e_steps, world, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
                "pipelining": "two device buffer sets; inputs of step i+1 upload and y of step i-1 downloads "
                              "on copy streams while step i computes"}
@@ -449,7 +459,7 @@ def main():
 def bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg):
     """Decode workload: B streams, one token per step, donated (in place) state."""
     steps_total = args.warmup + args.steps
-    d = sdm_inputs.make_decode_inputs(cfg, steps=min(steps_total, 64), seed=cfg.seed + 7919 * rank)
+    d = sdm_inputs.make_decode_inputs(cfg, steps=min(steps_total, 64), seed=rank_seed(cfg, rank))
     g = {k: v.to(dev) for k, v in d.items()}
     state = g["bank"].clone()
     donate = os.environ.get("SDM_DECODE_COPY", "0") != "1"
@@ -479,8 +489,8 @@ def bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg):
         ev1.record(stream)
         barrier()
     kt = sdm.profile_end()
-    ms = ev0.elapsed_time(ev1)
-    value = cfg.B * args.steps * world / (ms / 1e3)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
+    value = whole_job_rate(cfg.B * args.steps, world, ms)
     launches = sdm.launch_count() - launches0
     sb = 4 if cfg.bank_dtype == "f32" else 2
     alg = cfg.B * cfg.H * (cfg.W + cfg.R) * cfg.d_v * sb + (0 if donate else 2 * cfg.B * cfg.H * cfg.N * cfg.d_v * sb)
@@ -508,8 +518,8 @@ def bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg):
             cg.replay()
         g1.record(stream)
         torch.cuda.synchronize(dev)
-        gms = g0.elapsed_time(g1) / (reps * nT)
-        graph = {"ms_per_step": gms, "value": cfg.B * world / (gms / 1e3), "unit": UNIT,
+        gms = max_over_ranks(g0.elapsed_time(g1), pg, dev) / (reps * nT)
+        graph = {"ms_per_step": gms, "value": whole_job_rate(cfg.B, world, gms), "unit": UNIT,
                  "steps": reps * nT, "steps_per_graph": nT}
     n, kms = kt["decode"]
     achieved = alg / (kms / max(n, 1) / 1e3) / 1e9
