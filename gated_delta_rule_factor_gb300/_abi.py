@@ -23,7 +23,7 @@ EXPORTS = (
     "sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
     "sdm_decode_step", "sdm_last_device_error", "sdm_status_string", "sdm_last_error_message",
     "sdm_abi_version", "sdm_launch_count", "sdm_profile_begin", "sdm_profile_end",
-    "sdm_kernel_name", "sdm_write_read_static",
+    "sdm_kernel_name", "sdm_write_read_static", "sdm_test_stall_decode_copy",
 )
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -97,6 +97,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.sdm_profile_end.argtypes = [ctypes.POINTER(KernelTimes)]
     lib.sdm_kernel_name.argtypes = [ctypes.c_int32]
     lib.sdm_kernel_name.restype = ctypes.c_char_p
+    lib.sdm_test_stall_decode_copy.argtypes = [ctypes.c_int]
     for name in ("sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
                  "sdm_write_read_static", "sdm_decode_step", "sdm_last_device_error", "sdm_profile_begin", "sdm_profile_end"):
         getattr(lib, name).restype = ctypes.c_int

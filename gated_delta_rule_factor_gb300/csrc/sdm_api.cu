@@ -60,6 +60,7 @@ sdm_status ok() {
 }
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_test_stall_decode_copy{0};  // sdm_test_stall_decode_copy
 
 // ---------------------------------------------------------------- profiling
 
@@ -750,6 +751,7 @@ sdm_status sdm_decode_step(const sdm_shape *sh, const void *q_w, const void *q_r
   da.bank_in_shared = bank_in_shared ? 1 : 0;
   da.copy_rest = donate ? 0 : 1;
   da.region_bytes = region;
+  da.test_stall_copy = g_test_stall_decode_copy.load();
   da.g = d.g;
   if ((st = run_kernel(SDM_KERNEL_DECODE, cs, "decode",
                        [&] { return launch_decode(da, cl, sh->act_dtype, sh->bank_dtype, EF, EC, smem, cs); })) != SDM_OK)
@@ -789,6 +791,11 @@ const char *sdm_last_error_message(void) { return g_msg; }
 int32_t sdm_abi_version(void) { return SDM_ABI_VERSION; }
 
 uint64_t sdm_launch_count(void) { return g_launches.load(); }
+
+sdm_status sdm_test_stall_decode_copy(int on) {
+  g_test_stall_decode_copy.store(on ? 1 : 0);
+  return SDM_OK;
+}
 
 sdm_status sdm_profile_begin(void) {
   std::lock_guard<std::mutex> lk(g_prof.mu);

@@ -194,10 +194,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   } else if (warp == kCopyWarp && a.copy_rest) {
-    // bank_out <- bank_in, all rows: the write below then replaces the written ones
-    if (lane == 0 && !copy_table(ring, copy_bar, reinterpret_cast<const unsigned char *>(table_in()),
-                                 reinterpret_cast<unsigned char *>(table_out()), a.N * a.d_v * (int64_t)sizeof(BANK)))
-      raise_error(a.err, SDM_DEVERR_TIMEOUT);
+    // bank_out <- bank_in, all rows: the write below then replaces the written ones.
+    // test_stall_copy: wait instead on stage 0's barrier, which nothing arrives at, so
+    // that the bounded wait gives up (no copy issued, nothing left in flight).
+    if (lane == 0) {
+      const bool ok = a.test_stall_copy
+                          ? mbar_wait(&copy_bar[0], 0)
+                          : copy_table(ring, copy_bar, reinterpret_cast<const unsigned char *>(table_in()),
+                                       reinterpret_cast<unsigned char *>(table_out()),
+                                       a.N * a.d_v * (int64_t)sizeof(BANK));
+      if (!ok) raise_error(a.err, SDM_DEVERR_TIMEOUT);
+    }
     __syncwarp();
   }
   __syncthreads();

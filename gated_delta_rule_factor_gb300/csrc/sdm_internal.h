@@ -138,6 +138,7 @@ struct DecodeArgs {
   int32_t bank_in_shared; // bank_in is one [H,N,d_v] table for all streams
   int32_t copy_rest;      // copy the table bank_in -> bank_out (then write its written rows)
   int64_t region_bytes;   // decode_region_bytes(W, R, copy_rest)
+  int32_t test_stall_copy;  // test hook: the copy waits on a barrier nothing arrives at
   KeyGeometry g;
 };
 

@@ -235,6 +235,11 @@ def launch_count() -> int:
     return int(_abi.load().sdm_launch_count())
 
 
+def test_stall_decode_copy(on: bool) -> None:
+    """Test hook of the device failure path (see sdm_test_stall_decode_copy in sdm.h)."""
+    _abi.check(_abi.load().sdm_test_stall_decode_copy(1 if on else 0), "sdm_test_stall_decode_copy")
+
+
 def profile_begin() -> None:
     _abi.check(_abi.load().sdm_profile_begin(), "sdm_profile_begin")
 

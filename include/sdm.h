@@ -234,6 +234,14 @@ sdm_status sdm_profile_end(sdm_kernel_times *out);
 /* Name of a kernel kind ("write_read", ...). */
 const char *sdm_kernel_name(int32_t kind);
 
+/* Test hook of the device-side failure path; not for production use.  While `on` is
+ * nonzero, the copying form of sdm_decode_step (donate == 0) makes its copy thread wait
+ * on an mbarrier that nothing arrives at, instead of streaming the table: the bounded
+ * wait gives up after its limit (2 s), issues no copy, records SDM_DEVERR_TIMEOUT in
+ * the workspace flag and the step completes with an unspecified bank_out.  The GPU
+ * context stays usable.  Process-wide; returns SDM_OK. */
+sdm_status sdm_test_stall_decode_copy(int on);
+
 #ifdef __cplusplus
 }
 #endif

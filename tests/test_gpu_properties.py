@@ -257,3 +257,31 @@ def test_decode_shapes_against_oracle(sdm, name):
                                            bank_dtype=cfg.bank_dtype)
         assert_close(y_d[:, t], y_o, tol, f"{name} y step {t}")
     assert_close(b_d, bank, tol, f"{name} bank")
+
+
+def test_decode_copy_wait_that_runs_out_reports_timeout_and_the_context_survives(sdm):
+    # The copy thread's bounded mbarrier wait is made to run out (a barrier nothing
+    # arrives at): the step completes, the workspace flag reads SDM_DEVERR_TIMEOUT, and
+    # the next step on the same context is correct again.
+    SDM_DEVERR_TIMEOUT = 3
+    cfg = CONFIGS["decode"].replace(B=2)
+    d = to_device(sdm_inputs.make_decode_inputs(cfg, steps=1))
+    inp = tuple(d[k][:, 0].contiguous() for k in ("q_w", "q_r", "k_val", "gates"))
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    y_ref, out_ref = sdm.sdm_decode_step(*inp, d["subkeys"], d["bank"], cfg.W, cfg.R,
+                                         factor_dims=cfg.factor_dims, donate=False, workspace=ws)
+    torch.cuda.synchronize()
+    assert sdm.last_device_error(ws) == 0
+    sdm.test_stall_decode_copy(True)
+    try:
+        sdm.sdm_decode_step(*inp, d["subkeys"], d["bank"], cfg.W, cfg.R, factor_dims=cfg.factor_dims,
+                            donate=False, workspace=ws)
+        torch.cuda.synchronize()
+        assert sdm.last_device_error(ws) == SDM_DEVERR_TIMEOUT
+    finally:
+        sdm.test_stall_decode_copy(False)
+    y, out = sdm.sdm_decode_step(*inp, d["subkeys"], d["bank"], cfg.W, cfg.R, factor_dims=cfg.factor_dims,
+                                 donate=False, workspace=ws)
+    torch.cuda.synchronize()
+    assert sdm.last_device_error(ws) == 0
+    assert torch.equal(y, y_ref) and torch.equal(out, out_ref)
