@@ -718,7 +718,7 @@ sdm_status sdm_decode_step(const sdm_shape *sh, const void *q_w, const void *q_r
   if (!donate && overlap(r_bi, r_bo)) return fail(SDM_ERR_ALIAS, "bank_out overlaps bank_in (use donate)");
 
   const int64_t region = decode_region_bytes(sh->W, sh->R, !donate);
-  const int64_t smem = region + (int64_t)2 * sh->F * sh->d_sub * 4 + (int64_t)2 * d.ntot * 4 +
+  const int64_t smem = region + (int64_t)2 * (sh->F * sh->d_sub + 1) * 4 + (int64_t)2 * d.ntot * 4 +
                        (int64_t)(cl.n[0] + cl.n[1]) * 4;
   if (smem > 200 * 1024) return fail(SDM_ERR_UNSUPPORTED, "decode needs %lld bytes of shared memory", (long long)smem);
 

@@ -101,15 +101,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   // region: the scoring tile, then the copy ring (copying form), then the row stage
   float(*ktile)[kScoreCols + 1] = reinterpret_cast<float(*)[kScoreCols + 1]>(smem);
   unsigned char *ring = smem;
-  float *qf = reinterpret_cast<float *>(smem + a.region_bytes);  // [2][qdim]
-  float *scores = qf + 2 * qdim;                                // [2][ntot]
+  // the read query starts one float after the write query's end: the two rows are read
+  // together by neighbouring lanes, and this puts their words in different banks
+  const int qpitch = qdim + 1;
+  float *qf = reinterpret_cast<float *>(smem + a.region_bytes);  // [2][qpitch]
+  float *scores = qf + 2 * qpitch;                              // [2][ntot]
   uint32_t *cand = reinterpret_cast<uint32_t *>(scores + 2 * g.ntot);
 
   const ACT *q0 = static_cast<const ACT *>(a.q[0]) + s * qdim;
   const ACT *q1 = static_cast<const ACT *>(a.q[1]) + s * qdim;
   for (int i = tid; i < qdim; i += kThreads) {
     qf[i] = to_f32(q0[i]);
-    qf[qdim + i] = to_f32(q1[i]);
+    qf[qpitch + i] = to_f32(q1[i]);
   }
   for (int i = tid; i < cl.n[0]; i += kThreads) cand[i] = cl.tup[0][i];
   for (int i = tid; i < cl.n[1]; i += kThreads) cand[cl.n[0] + i] = cl.tup[1][i];
@@ -127,10 +130,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int kPer = kScoreRows * kScoreCols / kThreads;  // tile elements per thread
   for (int r0 = 0; r0 < g.ntot; r0 += kScoreRows) {
     const int nr = min(kScoreRows, g.ntot - r0);
-    const int row = tid % kScoreRows, qsel = tid / kScoreRows, arow = r0 + row;
+    // thread t: row t / 2 of query t % 2, so that the rows in use (at most rows_t per
+    // query) fill the low warps, one per SM sub-partition, instead of two per query
+    const int row = tid >> 1, qsel = tid & 1, arow = r0 + row;
     int f = 0;
     while (f + 1 < g.F && arow >= g.off[f + 1]) ++f;
-    const float *qrow = qf + qsel * qdim + f * g.d_sub;
+    const float *qrow = qf + qsel * qpitch + f * g.d_sub;
     float pre[kPer];
     auto fetch = [&](int d0) {
       const int nc = min(kScoreCols, g.d_sub - d0);
