@@ -28,7 +28,6 @@ static_assert(kScoreCols == kBf16Block, "a scoring tile is one block of the bflo
 static_assert(2 * kScoreRows == kThreads, "one thread per (query, tile row)");
 constexpr int kCopyStages = 3;
 constexpr uint32_t kCopyChunk = (uint32_t)(kDecodeCopyRingBytes / kCopyStages);  // bytes per copy stage
-constexpr int64_t kCopyRingBytes = kDecodeCopyRingBytes;
 
 // Streams `bytes` (a multiple of 16, both ends 16-byte aligned) from src to dst through
 // kCopyStages shared-memory stages with bulk copies; one thread.  Every copy has landed
@@ -124,8 +123,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // factor scores of both queries: the sub-keys pass through shared memory in tiles of
   // kScoreRows rows x kScoreCols columns (coalesced loads, the next tile in flight while
-  // this one is used); thread (query, row) folds each tile into its sum in score_dot's
-  // order.
+  // this one is used); each thread folds each tile into its sum in block order.
   const ACT *K = static_cast<const ACT *>(a.subkeys) + h * (int64_t)g.ntot * g.d_sub;
   constexpr int kPer = kScoreRows * kScoreCols / kThreads;  // tile elements per thread
   for (int r0 = 0; r0 < g.ntot; r0 += kScoreRows) {

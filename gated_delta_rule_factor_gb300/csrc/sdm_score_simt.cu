@@ -5,9 +5,9 @@
 // takes 16 consecutive tokens of one head = 32 query rows (row 2t = write query, 2t+1 =
 // read query) and computes every factor score of those rows as a tiled product with
 // the sub-key table: 32-wide slices of d_sub and 256 sub-keys at a time are staged in
-// shared memory, 4x8 outputs per thread.  Accumulation follows score_dot (sdm_topk.cuh):
-// compensated for float32 inputs, FMA blocks of 32 folded into a TwoSum pair for
-// bfloat16, so that the decode kernel's scores are the same bits.
+// shared memory, 4x8 outputs per thread.  Accumulation follows the block order of
+// score_block (sdm_topk.cuh): compensated for float32 inputs, FMA blocks of 32 folded
+// into a TwoSum pair for bfloat16, so that the decode kernel's scores are the same bits.
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 #include "sdm_topk.cuh"

@@ -188,9 +188,10 @@ __device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry 
 }
 
 // Terms [0, n) of one factor score folded into acc, n <= kBf16Block: one block of the
-// bfloat16 dot product (BF16) or n compensated float32 steps; k holds sub-key values of
-// the activation type, read as float32.  A factor score is the blocks of d_sub terms
-// starting at 0, kBf16Block, 2 * kBf16Block, ... folded in order (score_dot).
+// bfloat16 dot product (BF16) or n compensated float32 steps (accurate accumulation as
+// described in sdm_common.cuh); k holds sub-key values of the activation type, read as
+// float32.  A factor score <q, k> over d_sub terms is the blocks starting at 0,
+// kBf16Block, 2 * kBf16Block, ... folded in order into Acc2{0, 0}, then acc2_value.
 template <bool BF16, typename KT>
 __device__ __forceinline__ void score_block(Acc2 &acc, const float *q, const KT *k, int n) {
   if constexpr (BF16) {
@@ -202,16 +203,6 @@ __device__ __forceinline__ void score_block(Acc2 &acc, const float *q, const KT 
 #pragma unroll 8
     for (int d = 0; d < n; ++d) dot2_step(acc, q[d], to_f32(k[d]));
   }
-}
-
-// One factor score: <q, k> over d_sub terms with the accurate accumulation described
-// in sdm_common.cuh.  q is float32 (shared memory), k of the activation type.
-template <typename ACT>
-__device__ __forceinline__ float score_dot(const float *q, const ACT *k, int d_sub) {
-  Acc2 acc{0.0f, 0.0f};
-  for (int d0 = 0; d0 < d_sub; d0 += kBf16Block)
-    score_block<sizeof(ACT) == 2>(acc, q + d0, k + d0, min(kBf16Block, d_sub - d0));
-  return acc2_value(acc);
 }
 
 }  // namespace sdm
