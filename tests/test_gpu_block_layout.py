@@ -3,8 +3,8 @@
 The launch picks 128-byte slices on its own only when a shape has enough columns to
 fill the GPU (the full-size layer and training shapes); SDM_WR_CW forces the slice so
 that these shapes, which the oracle checks on every stream and token, run the same
-kernel: parity with the oracle, chunk-size independence, bitwise repeatability and
-agreement with the narrower-slice layout.
+kernel: parity with the oracle, chunk-size independence, bitwise repeatability and the
+same bits as narrower slices.
 """
 
 import pytest
@@ -12,7 +12,7 @@ import torch
 
 import sdm_inputs
 from sdm_inputs import CONFIGS
-from sdm_testlib import RTOL, assert_close, compare_stream, gpu_write_read, run_oracle
+from sdm_testlib import compare_stream, gpu_write_read, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -83,14 +83,14 @@ def test_block_layout_bitwise_repeatable(blocks):
             assert torch.equal(first[k], out[k]), k
 
 
-def test_block_layout_agrees_with_narrow_slices(monkeypatch):
-    # two summation orders of the same sums: equal selections, values within rounding
+def test_results_do_not_depend_on_the_slice_width(monkeypatch):
+    # every slice width runs the same block-ordered step: an element's sums depend on
+    # W and R only, so 128-byte and 32-byte slices give the same bits
     cfg = CONFIGS["tiny"].replace(W=64, R=64, B=2, H=2, T=60, d_v=128)
     d = sdm_inputs.make_inputs(cfg)
     monkeypatch.setenv("SDM_WR_CW", str(_slice_cols(cfg)))
     wide = gpu_write_read(cfg, d)
     monkeypatch.setenv("SDM_WR_CW", "8")
     narrow = gpu_write_read(cfg, d)
-    assert torch.equal(wide["idx_w"], narrow["idx_w"]) and torch.equal(wide["idx_r"], narrow["idx_r"])
-    assert_close(wide["y"], narrow["y"], 2 * RTOL["f32"], "y")
-    assert_close(wide["bank"], narrow["bank"], 2 * RTOL["f32"], "bank")
+    for k in wide:
+        assert torch.equal(wide[k], narrow[k]), k
