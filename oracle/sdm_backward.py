@@ -20,7 +20,14 @@ Readings (also listed in the design doc):
   * the float32 rounding of factor and slot scores and the rounding of stored bank rows
     and outputs are passed straight through (their derivative is taken as 1);
   * gates are the post-sigmoid values (alpha, beta) the op takes, so their gradient is
-    with respect to those values.
+    with respect to those values;
+  * snapshot precision (CHANGELOG > 2.0.0 > Package, bf16 snapshots): the snapshot of the
+    rows a token overwrites holds them exactly by default (a float32 snapshot of a float32
+    or bfloat16 bank), or rounded to ``snapshot_dtype`` ("bf16");
+    the backward reads the snapshot wherever it needs the rows before the write (the
+    alpha, beta and weight gradients, so those of the gates and queries) and restores
+    the bank from it.  On a bfloat16 bank the rows are already bfloat16, so a bfloat16
+    snapshot changes nothing (the pages state this, bit for bit).
 
 Per token t of one stream, with X_j the W rows before the write (the snapshot),
 m_j = alpha X_j, p = sum_j w_j m_j, u = v - p, M'[i_j] = m_j + beta w_j u, and
@@ -78,12 +85,15 @@ def select_record(q: np.ndarray, subkeys: np.ndarray, factor_dims, d_sub: int, k
 
 
 def stream_forward(M: np.ndarray, q_w, q_r, k_val, gates, subkeys, *, factor_dims, d_sub: int, W: int,
-                   R: int, act_dtype: str = "f32", bank_dtype: str = "f32", exact: bool = False) -> dict:
+                   R: int, act_dtype: str = "f32", bank_dtype: str = "f32", exact: bool = False,
+                   snapshot_dtype: Optional[str] = None) -> dict:
     """The forward of one stream (M advances in place), keeping the backward's record.
 
     Same arithmetic as sdm_oracle.run_stream; additionally stores per token the write
-    and read selections and the snapshot of the W rows before the write.  ``exact``:
-    float64 scores (bank_dtype / act_dtype "f64" then make the whole forward float64).
+    and read selections and the snapshot of the W rows before the write: exact, or
+    rounded to ``snapshot_dtype`` (the forward itself uses the rows as they are).
+    ``exact``: float64 scores (bank_dtype / act_dtype "f64" then make the whole forward
+    float64).
     """
     T, d_v = q_w.shape[0], M.shape[1]
     y = np.zeros((T, d_v))
@@ -92,13 +102,13 @@ def stream_forward(M: np.ndarray, q_w, q_r, k_val, gates, subkeys, *, factor_dim
         sw = select_record(q_w[t], subkeys, factor_dims, d_sub, W, exact)
         sr = select_record(q_r[t], subkeys, factor_dims, d_sub, R, exact)
         alpha, beta = float(gates[t, 0]), float(gates[t, 1])
-        X = M[sw["idx"]].copy()                                     # snapshot
+        X = M[sw["idx"]].copy()
         m = alpha * X
         p = sw["w"] @ m
         M[sw["idx"]] = round_to(m + beta * sw["w"][:, None] * (np.asarray(k_val[t], np.float64) - p)[None, :],
                                 bank_dtype)
         y[t] = round_to(sr["w"] @ M[sr["idx"]], act_dtype)
-        rec.append({"w": sw, "r": sr, "X": X})
+        rec.append({"w": sw, "r": sr, "X": X if snapshot_dtype is None else round_to(X, snapshot_dtype)})
     return {"y": y, "rec": rec}
 
 
@@ -162,7 +172,7 @@ def stream_backward(M: np.ndarray, fwd: dict, dy: np.ndarray, dM: np.ndarray, q_
 
 
 def sdm_write_read_backward(q_w, q_r, k_val, gates, subkeys, bank, dy, dbank, *, factor_dims, W: int, R: int,
-                            act_dtype: str = "f32", bank_dtype: str = "f32",
+                            act_dtype: str = "f32", bank_dtype: str = "f32", snapshot_dtype: Optional[str] = None,
                             streams: Optional[Iterable] = None) -> dict:
     """Gradients of the write/read op over all (or the listed) streams.
 
@@ -184,7 +194,7 @@ def sdm_write_read_backward(q_w, q_r, k_val, gates, subkeys, bank, dy, dbank, *,
         M = bank[b, h].copy()
         fwd = stream_forward(M, q_w[b, :, h], q_r[b, :, h], k_val[b, :, h], gates[b, :, h], subkeys[h],
                              factor_dims=factor_dims, d_sub=d_sub, W=W, R=R, act_dtype=act_dtype,
-                             bank_dtype=bank_dtype)
+                             bank_dtype=bank_dtype, snapshot_dtype=snapshot_dtype)
         g = stream_backward(M, fwd, dy[b, :, h], dbank[b, h], q_w[b, :, h], q_r[b, :, h], k_val[b, :, h],
                             gates[b, :, h], subkeys[h], factor_dims=factor_dims, d_sub=d_sub)
         out["bank"][b, h] = g["bank"]

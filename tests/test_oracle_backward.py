@@ -189,3 +189,39 @@ def test_batched_entry_sums_subkey_gradients_over_batch():
             assert np.array_equal(out["q_w"][b, :, h], g["q_w"])
             dK[h] += g["subkeys"]
     assert np.array_equal(out["subkeys"], dK)
+
+
+def _batched(seed, bank_dtype, snapshot_dtype=None):
+    rng = np.random.default_rng(seed)
+    B, T, H, fd, d_sub, d_v, W, R = 1, 4, 2, (6, 5), 4, 8, 3, 3
+    N = 30
+    q_w = rng.normal(0, 2, (B, T, H, 2 * d_sub))
+    q_r = rng.normal(0, 2, (B, T, H, 2 * d_sub))
+    k_val = rng.normal(0, 1, (B, T, H, d_v))
+    gates = rng.uniform(0.2, 0.9, (B, T, H, 2))
+    subkeys = rng.normal(0, 0.5, (H, sum(fd), d_sub))
+    bank = fwd_oracle.round_to(rng.normal(0, 0.5, (B, H, N, d_v)), bank_dtype)
+    dy = rng.normal(0, 1, (B, T, H, d_v))
+    dbank = rng.normal(0, 1, (B, H, N, d_v))
+    return bwd.sdm_write_read_backward(q_w, q_r, k_val, gates, subkeys, bank, dy, dbank, factor_dims=fd,
+                                       W=W, R=R, bank_dtype=bank_dtype, snapshot_dtype=snapshot_dtype)
+
+
+def test_bf16_snapshot_on_a_bf16_bank_changes_nothing():
+    # CHANGELOG 2.0.0 > Package: on a bfloat16 bank the bf16 snapshot is bit-identical to
+    # the default one (the rows it keeps are bfloat16 already)
+    a = _batched(9, "bf16")
+    b = _batched(9, "bf16", "bf16")
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_bf16_snapshot_on_a_float32_bank_moves_only_the_gradients_that_read_it():
+    # the value gradient never reads the rows before the write; the gate and query
+    # gradients do, and move by about bfloat16's rounding of those rows
+    a = _batched(10, "f32")
+    b = _batched(10, "f32", "bf16")
+    assert np.array_equal(a["k_val"], b["k_val"])
+    for k in ("gates", "q_w"):
+        diff = np.abs(a[k] - b[k]).max()
+        assert 0 < diff <= 2.0 ** -6 * np.abs(a[k]).max(), (k, diff)
