@@ -14,7 +14,7 @@ What the pages fix (page title > section):
 The gradient itself is the plain chain rule through the oracle's forward
 (sdm_oracle.run_stream), taken in float64; the pages print no formulas for it, so it
 is pinned against central finite differences of that forward (tests/test_oracle_backward.py).
-Readings (also listed in the design doc):
+Readings where the pages are silent:
   * the selected slot ids are piecewise constant in the queries and sub-keys: the
     gradient flows through the softmax weights of the selected slots only;
   * the float32 rounding of factor and slot scores and the rounding of stored bank rows

@@ -25,7 +25,7 @@ Sources (page title > section):
   * lumen PR #29 > Donating is a permission: the in-place (donated) and copying
     step run one body and agree bit for bit.
 
-Readings where the pages are silent (each one is also listed in the design doc):
+Readings where the pages are silent:
   * update: the coupled gated delta rule restricted to the W selected rows,
         m_j = alpha * M[i_j];  p = sum_j w_j m_j;  M[i_j] <- m_j + beta w_j (v - p)
     (the forget gate decays only the selected rows);
