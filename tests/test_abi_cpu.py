@@ -25,6 +25,19 @@ except RuntimeError as e:      # no toolkit: only a prebuilt library can be test
 from gated_delta_rule_factor_gb300 import _abi  # noqa: E402
 
 
+def _device_present() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+# A call that passes every host check goes on to launch kernels; with the fake addresses
+# of these tests that must never happen on a machine that has a GPU.
+without_a_device = pytest.mark.skipif(_device_present(), reason="would launch kernels on fake addresses")
+
+
 @pytest.fixture(scope="module")
 def lib():
     return _abi.load()
@@ -191,9 +204,37 @@ def test_decode_donate_rules(lib):
     assert lib.sdm_launch_count() == before
 
 
+@without_a_device
 def test_valid_call_without_a_gpu_reports_a_cuda_error(lib):
     # all checks pass; the first CUDA call finds no device and the status says so
     st = call_write_read(lib, shape())
     assert st in (_abi.SDM_ERR_CUDA, _abi.SDM_OK)
     if st == _abi.SDM_ERR_CUDA:
         assert b"cuda" in lib.sdm_last_error_message().lower() or lib.sdm_last_error_message()
+
+
+def test_decode_shape_beyond_the_shared_memory_budget_is_refused_before_work(lib):
+    # W = R = 128 stages 128 KB of rows per CTA; two 4096-wide query rows and 2048 factor
+    # scores bring the decode kernel past its 200 KB of shared memory: UNSUPPORTED, with
+    # nothing enqueued (the pointers below are never dereferenced)
+    sh = shape(B=1, T=1, H=1, factor_dims=(1024, 1024), d_sub=4096, d_v=8, W=128, R=128)
+    n = ctypes.c_size_t(0)
+    assert lib.sdm_decode_workspace_size(ctypes.byref(sh), ctypes.byref(n)) == _abi.SDM_OK
+    before = lib.sdm_launch_count()
+    st = lib.sdm_decode_step(ctypes.byref(sh), fake(1), fake(2), fake(3), fake(4), fake(5), fake(6), 0,
+                             fake(9), 0, fake(7), None, None, None, None, fake(8), n.value, None)
+    assert st == _abi.SDM_ERR_UNSUPPORTED, lib.sdm_last_error_message()
+    assert b"shared memory" in lib.sdm_last_error_message()
+    assert lib.sdm_launch_count() == before
+
+
+@without_a_device
+def test_decode_shape_within_the_shared_memory_budget_passes_the_checks(lib):
+    # the same step with a narrower query fits: every check passes and the first CUDA
+    # call finds no device
+    sh = shape(B=1, T=1, H=1, factor_dims=(1024, 1024), d_sub=128, d_v=8, W=128, R=128)
+    n = ctypes.c_size_t(0)
+    assert lib.sdm_decode_workspace_size(ctypes.byref(sh), ctypes.byref(n)) == _abi.SDM_OK
+    st = lib.sdm_decode_step(ctypes.byref(sh), fake(1), fake(2), fake(3), fake(4), fake(5), fake(6), 0,
+                             fake(9), 0, fake(7), None, None, None, None, fake(8), n.value, None)
+    assert st in (_abi.SDM_ERR_CUDA, _abi.SDM_OK), lib.sdm_last_error_message()
