@@ -49,13 +49,13 @@ not pinned by the pages: "parity unpinned" for that reading.
 from __future__ import annotations
 
 import math
-from typing import Iterable, Optional
+from typing import Callable, Iterable, Optional
 
 import numpy as np
 
 __all__ = [
     "round_to_bf16", "round_to", "factor_scores", "factor_ranks", "slot_scores",
-    "slot_tie_keys", "topk_slots", "softmax_weights", "select", "gated_delta_write",
+    "slot_tie_keys", "topk_slots", "softmax_weights", "select", "weights_of", "gated_delta_write",
     "weighted_read", "run_stream", "sdm_write_read", "sdm_decode_step",
 ]
 
@@ -180,6 +180,17 @@ def select(q: np.ndarray, subkeys: np.ndarray, factor_dims, d_sub: int, k: int,
     return idx, w, S[idx]
 
 
+def weights_of(q: np.ndarray, subkeys: np.ndarray, factor_dims, d_sub: int, idx) -> np.ndarray:
+    """Softmax weights of the given slots, in the given order, from this query's slot scores.
+
+    Used when a caller supplies the selected slots itself: at a near tie several
+    slot sets are valid top-k answers, and the rest of the arithmetic (weights,
+    update, read) is the same for any of them.
+    """
+    S = slot_scores(factor_scores(q, subkeys, factor_dims, d_sub))
+    return softmax_weights(S[np.asarray(idx, dtype=np.int64)])
+
+
 # --------------------------------------------------------------------------- update / read
 
 def gated_delta_write(M: np.ndarray, idx: np.ndarray, w: np.ndarray, alpha: float,
@@ -204,13 +215,20 @@ def weighted_read(M: np.ndarray, idx: np.ndarray, r: np.ndarray) -> np.ndarray:
 
 def run_stream(M: np.ndarray, q_w: np.ndarray, q_r: np.ndarray, k_val: np.ndarray,
                gates: np.ndarray, subkeys: np.ndarray, *, factor_dims, d_sub: int, W: int,
-               R: int, act_dtype: str, bank_dtype: str, prefilter: bool = True) -> dict:
+               R: int, act_dtype: str, bank_dtype: str, prefilter: bool = True,
+               pick: Optional[Callable] = None) -> dict:
     """Run T tokens of one stream through the op, in token order; M advances in place.
 
     q_w, q_r: [T, F*d_sub]; k_val: [T, d_v]; gates: [T, 2] = (alpha, beta);
     subkeys: [sum(n_f), d_sub] of this head; M: [N, d_v] float64 holding values of
     the bank type.  Returns y [T, d_v] (rounded to the activation type), the write
     and read slot ids and weights.
+
+    ``pick(t, which, idx, w)`` (which = 0 for the write query, 1 for the read query),
+    if given, sees each exact top-k and may return other slot ids to use instead (a
+    different valid answer at a near tie); their weights are then the softmax of
+    their own slot scores (``weights_of``), and the update and read run on them.
+    Returning None keeps the exact top-k.
     """
     T = q_w.shape[0]
     d_v = M.shape[1]
@@ -222,6 +240,15 @@ def run_stream(M: np.ndarray, q_w: np.ndarray, q_r: np.ndarray, k_val: np.ndarra
     for t in range(T):
         iw, ww, _ = select(q_w[t], subkeys, factor_dims, d_sub, W, prefilter)
         ir, rr, _ = select(q_r[t], subkeys, factor_dims, d_sub, R, prefilter)
+        if pick is not None:
+            alt = pick(t, 0, iw, ww)
+            if alt is not None:
+                iw = np.asarray(alt, dtype=np.int64)
+                ww = weights_of(q_w[t], subkeys, factor_dims, d_sub, iw)
+            alt = pick(t, 1, ir, rr)
+            if alt is not None:
+                ir = np.asarray(alt, dtype=np.int64)
+                rr = weights_of(q_r[t], subkeys, factor_dims, d_sub, ir)
         alpha, beta = float(gates[t, 0]), float(gates[t, 1])
         gated_delta_write(M, iw, ww, alpha, beta, k_val[t], bank_dtype)
         y[t] = round_to(weighted_read(M, ir, rr), act_dtype)

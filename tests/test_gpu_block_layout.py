@@ -12,7 +12,7 @@ import torch
 
 import sdm_inputs
 from sdm_inputs import CONFIGS
-from sdm_testlib import compare_stream, gpu_write_read, run_oracle
+from sdm_testlib import compare_stream, gpu_write_read
 
 pytestmark = pytest.mark.gpu
 
@@ -56,8 +56,7 @@ def test_block_layout_matches_oracle(blocks, name):
     d = sdm_inputs.make_inputs(cfg)
     gpu = gpu_write_read(cfg, d, chunk_size=chunk)
     streams = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
-    ora = run_oracle(cfg, d, streams)
-    res = [compare_stream(cfg, d, gpu, ora, b, h) for (b, h) in streams]
+    res = [compare_stream(cfg, d, gpu, b, h) for (b, h) in streams]
     assert sum(r["near_ties"] for r in res) <= 1
 
 

@@ -3,16 +3,24 @@
 Small shapes are compared on every stream and token; the full-size workloads (the
 README layer call, the training-shape forward, the three-factor shape) run on the GPU
 exactly as bench.py launches them and are compared on sampled whole streams, which
-the oracle can compute one at a time.
+the oracle can compute one at a time.  Every compared stream is compared through its
+last token: at a valid near tie the oracle follows the GPU's pick (sdm_testlib).
+
+Grid-valued inputs (sdm_inputs, grid=True) make every factor score and slot score
+exact in float32, whatever the summation order, so there the selections must agree
+with the oracle bit for bit, ties decided by the tie rule included; they run at the
+layer's factor shape (tensor-core scorer, multi-chunk sorts at n_f = 256 and the
+280-candidate merge at k = 64) and at the three-factor shape (796 candidates).
 """
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import sdm_inputs
 from sdm_inputs import CONFIGS
-from sdm_testlib import compare_stream, gpu_write_read, run_oracle
+from sdm_testlib import _f64, compare_stream, gpu_write_read
 
 pytestmark = pytest.mark.gpu
 
@@ -25,25 +33,72 @@ def _parity(cfg, *, grid=False, streams=None, seed=None, chunk_size=None, bank_i
     d = sdm_inputs.make_inputs(cfg, grid=grid, seed=seed, T=T)
     gpu = gpu_write_read(cfg, d, chunk_size=chunk_size, bank_init=bank_init)
     streams = streams or _all_streams(cfg)
-    ora = run_oracle(cfg, d, streams)
-    results = [compare_stream(cfg, d, gpu, ora, b, h) for (b, h) in streams]
-    return d, gpu, ora, results
+    results = [compare_stream(cfg, d, gpu, b, h) for (b, h) in streams]
+    return d, gpu, results
+
+
+def _oracle_selections(cfg, d, b, h):
+    """The oracle's own write and read selections of stream (b, h), every token."""
+    K = _f64(d["subkeys"][h])
+    sel = {"idx_w": [], "idx_r": []}
+    for t in range(d["q_w"].shape[1]):
+        for name, q, k in (("idx_w", d["q_w"], cfg.W), ("idx_r", d["q_r"], cfg.R)):
+            idx, _, _ = oracle.select(_f64(q[b, t, h]), K, cfg.factor_dims, cfg.d_sub, k)
+            sel[name].append(idx)
+    return {k: np.stack(v) for k, v in sel.items()}
+
+
+def _assert_identical_selections(cfg, d, gpu, streams):
+    for (b, h) in streams:
+        o = _oracle_selections(cfg, d, b, h)
+        np.testing.assert_array_equal(gpu["idx_w"][b, :, h].numpy(), o["idx_w"], err_msg=f"idx_w ({b},{h})")
+        np.testing.assert_array_equal(gpu["idx_r"][b, :, h].numpy(), o["idx_r"], err_msg=f"idx_r ({b},{h})")
 
 
 def test_tiny_matches_oracle():
     cfg = CONFIGS["tiny"]
-    _, _, _, res = _parity(cfg)
-    assert all(r["diverged_at"] is None for r in res)
+    _, _, res = _parity(cfg)
+    assert all(r["near_ties"] == 0 for r in res), res
 
 
 def test_tiny_grid_inputs_select_identically():
     # grid-valued queries and sub-keys make every score exact: the selections must agree
     # bit for bit everywhere, ties (decided by ranks) included
     cfg = CONFIGS["tiny"]
-    d, gpu, ora, res = _parity(cfg, grid=True)
-    o = ora[(0, 0)]
-    np.testing.assert_array_equal(gpu["idx_w"][0, :, 0].numpy(), o["idx_w"])
-    np.testing.assert_array_equal(gpu["idx_r"][0, :, 0].numpy(), o["idx_r"])
+    d, gpu, res = _parity(cfg, grid=True)
+    assert all(r["near_ties"] == 0 for r in res), res
+    _assert_identical_selections(cfg, d, gpu, _all_streams(cfg))
+
+
+def _grid_has_ties(cfg, d, b, h):
+    """Number of tokens with equal slot scores among their k+1 best (real ties that the
+    tie rule decides, inside the top k or at its edge)."""
+    K = _f64(d["subkeys"][h])
+    n = 0
+    for t in range(d["q_w"].shape[1]):
+        q = _f64(d["q_w"][b, t, h])
+        S = oracle.slot_scores(oracle.factor_scores(q, K, cfg.factor_dims, cfg.d_sub))
+        top = np.sort(S)[::-1][:cfg.W + 1]
+        n += int(len(np.unique(top)) < len(top))
+    return n
+
+
+def test_layer_factors_grid_inputs_select_identically():
+    # the layer's product keys (256 x 256, d_sub 512, bf16 queries: tensor-core scorer),
+    # W = R = 64, on grid inputs: real ties at the k-th slot, decided by the tie rule
+    cfg = CONFIGS["layer"].replace(B=1, T=64, d_v=128)
+    d, gpu, res = _parity(cfg, grid=True)
+    assert all(r["near_ties"] == 0 for r in res), res
+    assert _grid_has_ties(cfg, d, 0, 0) >= 8, "grid inputs produced too few ties"
+    _assert_identical_selections(cfg, d, gpu, _all_streams(cfg))
+
+
+def test_three_factor_grid_inputs_select_identically():
+    cfg = CONFIGS["three_factor"].replace(T=48, H=2, d_v=64, low_rank_queries=False)
+    d, gpu, res = _parity(cfg, grid=True)
+    assert all(r["near_ties"] == 0 for r in res), res
+    assert _grid_has_ties(cfg, d, 0, 1) >= 8, "grid inputs produced too few ties"
+    _assert_identical_selections(cfg, d, gpu, _all_streams(cfg))
 
 
 SMALL_VARIANTS = {
@@ -61,11 +116,14 @@ SMALL_VARIANTS = {
     "every_slot": dict(factor_dims=(4, 4), W=16, R=16, T=24),
     "wide_factor": dict(factor_dims=(600, 3), d_sub=8, W=32, R=32, T=48),
     "d_v_8": dict(d_v=8),
+    "d_v_8_bf16_bank": dict(d_v=8, bank_dtype="bf16"),
     "d_v_24": dict(d_v=24),
     "d_v_48_bf16": dict(d_v=48, bank_dtype="bf16", act_dtype="bf16"),
     "many_streams": dict(B=3, H=2, T=50),
     "big_k": dict(factor_dims=(64, 64), W=128, R=96, T=40, d_v=32),
     "long_head": dict(d_v=2048, T=24),
+    "w64_r64": dict(W=64, R=64, T=40),
+    "w48_r64_ragged": dict(W=48, R=64, T=37, chunk_size=5),
 }
 
 
@@ -74,15 +132,16 @@ def test_small_variants_match_oracle(name):
     kw = dict(SMALL_VARIANTS[name])
     chunk = kw.pop("chunk_size", None)
     cfg = CONFIGS["tiny"].replace(**kw)
-    _, _, _, res = _parity(cfg, chunk_size=chunk)
-    # near ties are allowed but must be rare on continuous inputs
-    assert sum(r["near_ties"] for r in res) <= 1
+    _, _, res = _parity(cfg, chunk_size=chunk)
+    # near ties are allowed (the oracle then follows the GPU's valid pick) but must be
+    # rare on continuous inputs
+    assert sum(r["near_ties"] for r in res) <= 1, res
 
 
 def test_bank_given_per_stream_without_learned_table():
     cfg = CONFIGS["tiny"].replace(B=2, H=2, T=40)
-    _, _, _, res = _parity(cfg, bank_init=False)
-    assert all(r["diverged_at"] is None for r in res)
+    _, _, res = _parity(cfg, bank_init=False)
+    assert all(r["near_ties"] == 0 for r in res), res
 
 
 def test_empty_sequence_only_copies_the_table():
@@ -94,17 +153,18 @@ def test_empty_sequence_only_copies_the_table():
     assert torch.equal(gpu["bank"], want)
 
 
-def _full_size(name, streams, min_exact_fraction=0.99):
+def _full_size(name, streams):
     cfg = CONFIGS[name]
     d = sdm_inputs.make_inputs(cfg)
     gpu = gpu_write_read(cfg, d)
-    ora = run_oracle(cfg, d, streams)
-    res = [compare_stream(cfg, d, gpu, ora, b, h) for (b, h) in streams]
-    # at most one stream may end early at a legitimate near tie
-    diverged = [r for r in res if r["diverged_at"] is not None]
-    assert len(diverged) <= 1, res
-    rows = sum(r["rows"] for r in res)
-    assert rows >= min_exact_fraction * cfg.T * len(streams) or len(diverged) == 1
+    res = [compare_stream(cfg, d, gpu, b, h) for (b, h) in streams]
+    for (b, h), r in zip(streams, res):
+        # every token of every sampled stream is compared (y and the final bank)
+        assert r["rows"] == cfg.T, r
+        print(f"{name} stream ({b},{h}): {r['rows']} tokens compared, {r['near_ties']} near-tie picks "
+              f"followed at tokens {r['near_tie_tokens'][:10]}")
+        # near ties are rare on continuous inputs
+        assert r["near_ties"] <= max(2, cfg.T // 256), r
     return res
 
 

@@ -10,7 +10,7 @@ import torch
 import oracle
 import sdm_inputs
 from sdm_inputs import CONFIGS
-from sdm_testlib import RTOL, assert_close, gpu_write_read, to_device
+from sdm_testlib import RTOL, assert_close, check_selection, gpu_write_read, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -133,18 +133,47 @@ def _step_inputs(g, t):
     return tuple(g[k][:, t].contiguous() for k in ("q_w", "q_r", "k_val", "gates"))
 
 
-def _decode_steps(sdm, cfg, d, steps, donate):
+def _decode_steps(sdm, cfg, d, steps, donate, sel=None):
+    """Run `steps` decode steps; every step writes its selections into fresh buffers and
+    its workspace flag is read back (a kernel-side error fails the test).  With a dict
+    `sel`, the per-step idx_w, wt_w, idx_r, wt_r [B, steps, H, k] are stored in it."""
     g = to_device(d)
     state = g["bank"].clone()
-    ys = []
+    B, H = cfg.B, cfg.H
+    ys, got = [], {k: [] for k in ("idx_w", "wt_w", "idx_r", "wt_r")}
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
     for t in range(steps):
+        out = {"idx_w": torch.empty((B, H, cfg.W), dtype=torch.int32, device="cuda"),
+               "wt_w": torch.empty((B, H, cfg.W), dtype=torch.float32, device="cuda"),
+               "idx_r": torch.empty((B, H, cfg.R), dtype=torch.int32, device="cuda"),
+               "wt_r": torch.empty((B, H, cfg.R), dtype=torch.float32, device="cuda")}
         y, new = sdm.sdm_decode_step(*_step_inputs(g, t), g["subkeys"], state, cfg.W, cfg.R,
-                                     factor_dims=cfg.factor_dims, donate=donate)
+                                     factor_dims=cfg.factor_dims, donate=donate, workspace=ws, **out)
         assert (new.data_ptr() == state.data_ptr()) == donate   # in place exactly when donating
+        assert sdm.last_device_error(ws) == 0, f"step {t}: kernel-side error"
         ys.append(y.clone())
+        for k in got:
+            got[k].append(out[k].cpu())
         state = new
     torch.cuda.synchronize()
+    if sel is not None:
+        sel.update({k: torch.stack(v, 1) for k, v in got.items()})
     return torch.stack(ys, 1).cpu(), state.cpu()
+
+
+def _check_decode_selections(cfg, d, sel, t):
+    """Step t's selections of every stream against the oracle's (exact under the margin
+    rule; a valid near-tie alternative is counted and returned)."""
+    near = 0
+    for b in range(cfg.B):
+        for h in range(cfg.H):
+            K = d["subkeys"][h].float().double().numpy()
+            for name, wname, qk, k in (("idx_w", "wt_w", "q_w", cfg.W), ("idx_r", "wt_r", "q_r", cfg.R)):
+                q = d[qk][b, t, h].float().double().numpy()
+                oi, ow, _ = oracle.select(q, K, cfg.factor_dims, cfg.d_sub, k)
+                near += 0 if check_selection(cfg, q, K, k, sel[name][b, t, h].numpy(),
+                                             sel[wname][b, t, h].numpy(), oi, ow) else 1
+    return near
 
 
 def test_decode_copy_equals_donate_bitwise(sdm):
@@ -187,18 +216,62 @@ def test_decode_from_a_learned_table_never_writes_it(sdm):
     assert torch.equal(state.cpu(), b_ref)
 
 
+def _decode_against_oracle(sdm, cfg, d, steps, tol):
+    """Donated steps against the oracle: selections (exact under the margin rule), y and
+    the final bank.  The oracle's bank follows the GPU's selection when a step took a
+    valid near-tie alternative, so the comparison never stops early."""
+    sel = {}
+    y_gpu, b_gpu = _decode_steps(sdm, cfg, d, steps, donate=True, sel=sel)
+    bank = d["bank"].float().double().numpy().copy()
+    near = 0
+    for t in range(steps):
+        near += _check_decode_selections(cfg, d, sel, t)
+        y_o = np.zeros((cfg.B, cfg.H, cfg.d_v))
+        for b in range(cfg.B):
+            for h in range(cfg.H):
+                gi = {0: sel["idx_w"][b, t, h].numpy(), 1: sel["idx_r"][b, t, h].numpy()}
+
+                def follow(tt, which, idx, w, gi=gi):
+                    return None if np.array_equal(gi[which], idx) else gi[which]
+
+                K = d["subkeys"][h].float().double().numpy()
+                res = oracle.run_stream(bank[b, h], d["q_w"][b, t:t + 1, h].float().double().numpy(),
+                                        d["q_r"][b, t:t + 1, h].float().double().numpy(),
+                                        d["k_val"][b, t:t + 1, h].float().double().numpy(),
+                                        d["gates"][b, t:t + 1, h].double().numpy(), K,
+                                        factor_dims=cfg.factor_dims, d_sub=cfg.d_sub, W=cfg.W, R=cfg.R,
+                                        act_dtype=cfg.act_dtype, bank_dtype=cfg.bank_dtype, pick=follow)
+                y_o[b, h] = res["y"][0]
+        assert_close(y_gpu[:, t], y_o, tol, f"decode y step {t}")
+    assert_close(b_gpu, bank, tol, "decode bank")
+    return near
+
+
 def test_decode_matches_oracle(sdm):
     cfg = CONFIGS["decode"].replace(B=16)
-    steps = 3
-    d = sdm_inputs.make_decode_inputs(cfg, steps=steps)
-    y_gpu, b_gpu = _decode_steps(sdm, cfg, d, steps, donate=True)
-    bank = d["bank"].double().numpy().copy()
-    for t in range(steps):
-        y_o, bank = oracle.sdm_decode_step(d["q_w"][:, t], d["q_r"][:, t], d["k_val"][:, t],
-                                           d["gates"][:, t], d["subkeys"], bank, factor_dims=cfg.factor_dims,
-                                           W=cfg.W, R=cfg.R, donate=True)
-        assert_close(y_gpu[:, t], y_o, RTOL["f32"], f"decode y step {t}")
-    assert_close(b_gpu, bank, RTOL["f32"], "decode bank")
+    d = sdm_inputs.make_decode_inputs(cfg, steps=3)
+    assert _decode_against_oracle(sdm, cfg, d, 3, RTOL["f32"]) <= 1
+
+
+def test_decode_grid_inputs_select_identically(sdm):
+    # exact scores (grid inputs): the decode step's selections equal the oracle's bit for
+    # bit, order and ties included
+    cfg = CONFIGS["decode"].replace(B=8)
+    d = sdm_inputs.make_decode_inputs(cfg, steps=2, grid=True)
+    sel = {}
+    _decode_steps(sdm, cfg, d, 2, donate=True, sel=sel)
+    ties = 0
+    for t in range(2):
+        for b in range(cfg.B):
+            for h in range(cfg.H):
+                K = d["subkeys"][h].float().double().numpy()
+                for name, qk, k in (("idx_w", "q_w", cfg.W), ("idx_r", "q_r", cfg.R)):
+                    q = d[qk][b, t, h].float().double().numpy()
+                    oi, _, S_sel = oracle.select(q, K, cfg.factor_dims, cfg.d_sub, k)
+                    np.testing.assert_array_equal(sel[name][b, t, h].numpy(), oi, err_msg=f"{name} {b},{t},{h}")
+                    ties += int(len(np.unique(S_sel)) < len(S_sel))
+    assert ties > 0, "grid inputs produced no tie inside the top k"
+    assert _decode_against_oracle(sdm, cfg, d, 2, RTOL["f32"]) == 0
 
 
 def test_decode_steps_equal_the_write_read_op(sdm):
@@ -219,13 +292,7 @@ def test_decode_bf16(sdm):
     y_c, b_c = _decode_steps(sdm, cfg, d, 2, donate=False)
     y_d, b_d = _decode_steps(sdm, cfg, d, 2, donate=True)
     assert torch.equal(y_c, y_d) and torch.equal(b_c, b_d)
-    bank = d["bank"].float().double().numpy().copy()
-    for t in range(2):
-        y_o, bank = oracle.sdm_decode_step(d["q_w"][:, t], d["q_r"][:, t], d["k_val"][:, t], d["gates"][:, t],
-                                           d["subkeys"], bank, factor_dims=cfg.factor_dims, W=cfg.W, R=cfg.R,
-                                           donate=True, act_dtype="bf16", bank_dtype="bf16")
-        assert_close(y_c[:, t], y_o, RTOL["bf16"], "bf16 decode y")
-    assert_close(b_c, bank, RTOL["bf16"], "bf16 decode bank")
+    assert _decode_against_oracle(sdm, cfg, d, 2, RTOL["bf16"]) <= 1
 
 
 # Decode shapes beyond the benchmark's: bfloat16 rows (8 per 16-byte group), a d_v whose
@@ -248,15 +315,8 @@ def test_decode_shapes_against_oracle(sdm, name):
     y_d, b_d = _decode_steps(sdm, cfg, d, steps, donate=True)
     y_c, b_c = _decode_steps(sdm, cfg, d, steps, donate=False)
     assert torch.equal(y_d, y_c) and torch.equal(b_d, b_c)
-    bank = d["bank"].double().numpy().copy()
     tol = RTOL[cfg.bank_dtype if cfg.bank_dtype == "bf16" else cfg.act_dtype]
-    for t in range(steps):
-        y_o, bank = oracle.sdm_decode_step(d["q_w"][:, t], d["q_r"][:, t], d["k_val"][:, t],
-                                           d["gates"][:, t], d["subkeys"], bank, factor_dims=cfg.factor_dims,
-                                           W=cfg.W, R=cfg.R, donate=True, act_dtype=cfg.act_dtype,
-                                           bank_dtype=cfg.bank_dtype)
-        assert_close(y_d[:, t], y_o, tol, f"{name} y step {t}")
-    assert_close(b_d, bank, tol, f"{name} bank")
+    assert _decode_against_oracle(sdm, cfg, d, steps, tol) <= 1
 
 
 def test_decode_copy_wait_that_runs_out_reports_timeout_and_the_context_survives(sdm):

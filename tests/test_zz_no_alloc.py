@@ -2,9 +2,8 @@
 
 The entry allocates nothing; it runs the same kernels as sdm_write_read with its
 scratch in a device array of the library.  The GPU test compares it with
-sdm_write_read (caller workspace) on two calls in a row, with the parity tolerances of
-the write/read tests; the CPU test checks the size refusal, which is decided before any
-CUDA call.  This file is collected last so that it also runs after every other test.
+sdm_write_read (caller workspace) on two calls in a row and wants every output bit for
+bit; the CPU test checks the size refusal, which is decided before any CUDA call.  This file is collected last so that it also runs after every other test.
 """
 
 from __future__ import annotations
@@ -17,7 +16,7 @@ import torch
 
 import sdm_inputs
 
-from sdm_testlib import RTOL, assert_close, to_device
+from sdm_testlib import to_device
 
 _TORCH = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -107,17 +106,10 @@ def test_static_scratch_matches_workspace_entry_on_two_calls_in_a_row():
         torch.cuda.synchronize()
         assert sdm.last_device_error(ws) == 0
 
-    rtol_y, rtol_b = RTOL[cfg.act_dtype], RTOL[cfg.bank_dtype]
+    # the static entry runs the same kernels on the same inputs as sdm_write_read: every
+    # output, the whole bank included, must be bitwise identical (this is also the only
+    # check of the static path, whose kernel-side error flag no call can read)
     for i, (s, r) in enumerate(zip(stat, ref)):
-        for k in ("idx_w", "idx_r"):
-            assert torch.equal(s[k], r[k]), f"call {i}: {k} differs"
-        for k in ("wt_w", "wt_r"):
-            assert_close(s[k].cpu().double().numpy(), r[k].cpu().double().numpy(), 1e-6, f"call {i}: {k}")
-        assert_close(s["y"].float().cpu().double().numpy(), r["y"].float().cpu().double().numpy(), rtol_y,
-                     f"call {i}: y")
-        # the bank: every row the call wrote, plus a sample of the others
-        rows = torch.unique(r["idx_w"].reshape(-1).long())
-        rows = torch.cat([rows, torch.arange(0, cfg.N, 997, device=dev)])
-        assert_close(s["bank"][:, :, rows].float().cpu().double().numpy(),
-                     r["bank"][:, :, rows].float().cpu().double().numpy(), rtol_b, f"call {i}: bank")
+        for k in ("y", "idx_w", "wt_w", "idx_r", "wt_r", "bank"):
+            assert torch.equal(s[k], r[k]), f"call {i}: {k} differs from sdm_write_read"
     assert not np.array_equal(stat[0]["y"].float().cpu().numpy(), stat[1]["y"].float().cpu().numpy())
