@@ -275,6 +275,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's T (smaller cases for profiler captures)")
+    ap.add_argument("--wr-slice", type=int, default=0, choices=[0, 32, 128, 256],
+                    help="tuning: force the write/read kernel's row slice per CTA in bytes (0 = automatic)")
+    ap.add_argument("--wr-stage", type=int, default=0,
+                    help="tuning: cap the write/read kernel's stage length in tokens (0 = automatic)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_env()
@@ -289,6 +293,8 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.wr_slice or args.wr_stage:
+        sdm.test_force_write_read_layout(args.wr_slice, args.wr_stage)
     pg = None
     if world > 1:
         import torch.distributed as dist

@@ -11,12 +11,14 @@ from . import _abi
 from ._abi import SdmError, SdmShape
 from .ops import (decode_workspace_size, last_device_error, launch_count, make_shape,
                   profile_begin, profile_end, sdm_decode_step, sdm_write_read,
-                  sdm_write_read_static, test_stall_decode_copy, write_read_workspace_size)
+                  sdm_write_read_static, test_force_simt_scorer, test_force_write_read_layout,
+                  test_stall_decode_copy, write_read_workspace_size)
 
 lib = _abi.load()
 
 __all__ = [
     "SdmError", "SdmShape", "decode_workspace_size", "last_device_error", "launch_count",
     "make_shape", "profile_begin", "profile_end", "sdm_decode_step", "sdm_write_read",
-    "sdm_write_read_static", "test_stall_decode_copy", "write_read_workspace_size", "lib",
+    "sdm_write_read_static", "test_force_simt_scorer", "test_force_write_read_layout",
+    "test_stall_decode_copy", "write_read_workspace_size", "lib",
 ]

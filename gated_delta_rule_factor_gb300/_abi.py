@@ -24,6 +24,7 @@ EXPORTS = (
     "sdm_decode_step", "sdm_last_device_error", "sdm_status_string", "sdm_last_error_message",
     "sdm_abi_version", "sdm_launch_count", "sdm_profile_begin", "sdm_profile_end",
     "sdm_kernel_name", "sdm_write_read_static", "sdm_test_stall_decode_copy",
+    "sdm_test_force_write_read_layout", "sdm_test_force_simt_scorer",
 )
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -98,6 +99,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.sdm_kernel_name.argtypes = [ctypes.c_int32]
     lib.sdm_kernel_name.restype = ctypes.c_char_p
     lib.sdm_test_stall_decode_copy.argtypes = [ctypes.c_int]
+    lib.sdm_test_force_write_read_layout.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.sdm_test_force_simt_scorer.argtypes = [ctypes.c_int]
     for name in ("sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
                  "sdm_write_read_static", "sdm_decode_step", "sdm_last_device_error", "sdm_profile_begin", "sdm_profile_end"):
         getattr(lib, name).restype = ctypes.c_int

@@ -61,6 +61,9 @@ sdm_status ok() {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_test_stall_decode_copy{0};  // sdm_test_stall_decode_copy
+std::atomic<int> g_test_slice_bytes{0};        // sdm_test_force_write_read_layout
+std::atomic<int> g_test_stage_tokens{0};
+std::atomic<int> g_test_simt_scorer{0};        // sdm_test_force_simt_scorer
 
 // ---------------------------------------------------------------- profiling
 
@@ -160,6 +163,9 @@ sdm_status check_shape(const sdm_shape *sh, bool decode, Derived *d) {
     ntot += n;
   }
   if (N > 0x7fffffffLL) return fail(SDM_ERR_UNSUPPORTED, "N = %lld slots exceeds 2^31 - 1", (long long)N);
+  // the write/read kernel addresses a stream's table in 16-byte units with 32 bits
+  if (sh->d_v > 0 && N * sh->d_v * elem_bytes(sh->bank_dtype) / 16 > 0xffffffffLL)
+    return fail(SDM_ERR_UNSUPPORTED, "one stream's table (N * d_v) exceeds 64 GiB");
   if (sh->d_sub < 1) return fail(SDM_ERR_INVALID_ARG, "d_sub must be >= 1");
   if (sh->d_sub > SDM_MAX_SUBKEY_DIM) return fail(SDM_ERR_UNSUPPORTED, "d_sub = %lld > %d", (long long)sh->d_sub, SDM_MAX_SUBKEY_DIM);
   if (sh->d_v < 1) return fail(SDM_ERR_INVALID_ARG, "d_v must be >= 1");
@@ -227,100 +233,101 @@ constexpr int kMaxStageRefs = 4096;
 
 int64_t a16(int64_t x) { return (x + 15) & ~int64_t(15); }
 
-PlanLayout plan_layout(int G, int W, int R, int64_t T) {
+PlanLayout plan_layout(int G, int W, int R, int64_t T, int RB) {
   PlanLayout p{};
   p.G = G;
   p.L = G * (W + R);
   p.n_stages = (int32_t)((T + G - 1) / G);
+  p.RB = RB;
+  p.cmask = RB >= 128 ? 3 : 0;
   const int64_t L = p.L;
-  int64_t o = 32;                                    // header: n_u, n_load, n_carry, n_wb, n_late
-  p.off_load_slot = o; o = a16(o + 4 * L);
-  p.off_load_u = o;    o = a16(o + 2 * L);
-  p.off_carry = o;     o = a16(o + 4 * L);
-  p.off_wb_slot = o;   o = a16(o + 4 * L);
-  p.off_wb_u = o;      o = a16(o + 2 * L);
+  int64_t o = 32;                                    // n_u, n_load, n_c1, n_c2, n_wb
+  p.off_ent = o;       o = a16(o + 8 * L);
+  p.off_wb = o;        o = a16(o + 8 * L);
+  p.lrec_bytes = o;
+  o = 0;
   p.off_refmap = o;    o = a16(o + 2 * L);
   p.off_tokflag = o;   o = a16(o + G);
-  p.rec_bytes = o;
+  p.off_wts = o;       o = a16(o + 4 * L);
+  p.off_gates = o;     o = a16(o + 8 * (int64_t)G);
+  p.crec_bytes = o;
   return p;
 }
 
 struct WrChoice {
-  int CW = 0;
+  int NCW = 1, LW = 8;
+  int slices = 0;
   PlanLayout lay{};
   int64_t smem = 0;
-  bool two_per_sm = false;
 };
-
-// Column slices the write/read kernel is compiled for: 16..128 bytes of a row and at
-// least 8 columns (one or more per compute lane).
-void cw_candidates(const sdm_shape *sh, std::vector<int> &out) {
-  out.clear();
-  const int sb = (int)elem_bytes(sh->bank_dtype), ab = (int)elem_bytes(sh->act_dtype);
-  for (int bytes = 128; bytes >= 16; bytes >>= 1) {
-    const int cw = bytes / sb;
-    if (cw < 8) continue;
-    if (cw * ab < 16) continue;            // value slice must be a whole 16-byte chunk
-    if (sh->d_v % cw != 0) continue;
-    out.push_back(cw);
-  }
-}
-
-// Largest stage length (tokens) whose buffers fit `budget` bytes of shared memory.
-WrChoice stage_for(const sdm_shape *sh, int cw, int64_t budget) {
-  WrChoice c;
-  c.CW = cw;
-  const int WR = sh->W + sh->R;
-  int gmax = std::min<int64_t>(sh->chunk_size, std::max<int64_t>(sh->T, 1));
-  gmax = std::min(gmax, kMaxStageRefs / WR);
-  gmax = std::max(gmax, 1);
-  int G = gmax;
-  for (; G > 1; --G) {
-    const PlanLayout lay = plan_layout(G, sh->W, sh->R, sh->T);
-    if (write_read_smem_bytes(cw, (int)elem_bytes(sh->bank_dtype), (int)elem_bytes(sh->act_dtype), G,
-                              sh->W, sh->R, lay.rec_bytes) <= budget)
-      break;
-  }
-  c.lay = plan_layout(G, sh->W, sh->R, sh->T);
-  c.smem = write_read_smem_bytes(cw, (int)elem_bytes(sh->bank_dtype), (int)elem_bytes(sh->act_dtype), G,
-                                 sh->W, sh->R, c.lay.rec_bytes);
-  return c;
-}
 
 constexpr int64_t kSmemOneCta = 220 * 1024;
 constexpr int64_t kSmemTwoCta = 110 * 1024;
 
-int env_int(const char *name, int dflt) {
-  const char *v = getenv(name);
-  return (v && *v) ? atoi(v) : dflt;
+// Compute warps per CTA the kernel is compiled for (each owns 32 bytes of every row).
+constexpr int kNcwChoices[] = {8, 4, 1};
+
+int64_t row_bytes_of(const sdm_shape *sh) { return sh->d_v * elem_bytes(sh->bank_dtype); }
+
+// Longest stage (tokens) whose buffers fit `budget` bytes of shared memory; 0 if not even
+// one token fits.  Row offsets are 16-bit: L * RB <= 65536.
+int stage_tokens(const sdm_shape *sh, int RB, int64_t budget) {
+  const int WR = sh->W + sh->R;
+  int gmax = (int)std::min<int64_t>(sh->chunk_size, std::max<int64_t>(sh->T, 1));
+  gmax = std::min(gmax, kMaxStageRefs / WR);
+  gmax = std::min(gmax, 65536 / (WR * RB));
+  for (int G = gmax; G >= 1; --G) {
+    const PlanLayout lay = plan_layout(G, sh->W, sh->R, sh->T, RB);
+    if (write_read_smem_bytes(lay, (int)elem_bytes(sh->bank_dtype), (int)elem_bytes(sh->act_dtype)) <=
+        budget)
+      return G;
+  }
+  return 0;
 }
 
-WrChoice choose_write_read(const sdm_shape *sh, int sm_count) {
-  std::vector<int> cands;
-  cw_candidates(sh, cands);
-  const int64_t streams = sh->B * sh->H;
-  int cw = cands.empty() ? 0 : cands.back();
-  const int forced = env_int("SDM_WR_CW", 0);
-  bool picked = false;
-  for (int c : cands) {
-    if (forced > 0 && c == forced) { cw = c; picked = true; break; }
+WrChoice configure(const sdm_shape *sh, int ncw, bool two_per_sm, int forced_g) {
+  WrChoice c;
+  c.NCW = ncw;
+  if (ncw == 8) two_per_sm = false;                  // 512 threads: one CTA per SM
+  const int RB = 32 * ncw;
+  c.slices = (int)((row_bytes_of(sh) + RB - 1) / RB);
+  int G = two_per_sm ? stage_tokens(sh, RB, kSmemTwoCta) : 0;
+  if (G == 0) {                                      // one CTA per SM (the only choice for NCW = 8)
+    two_per_sm = false;
+    G = stage_tokens(sh, RB, kSmemOneCta);
   }
-  if (!picked) {
-    for (int c : cands) {
-      if (streams * (sh->d_v / c) * 10 >= (int64_t)sm_count * 8) { cw = c; break; }
+  c.LW = two_per_sm ? 4 : 8;
+  if (forced_g > 0 && forced_g < G) G = forced_g;
+  G = std::max(G, 1);
+  c.lay = plan_layout(G, sh->W, sh->R, sh->T, RB);
+  c.smem = write_read_smem_bytes(c.lay, (int)elem_bytes(sh->bank_dtype), (int)elem_bytes(sh->act_dtype));
+  return c;
+}
+
+// The widest slice (most compute warps per CTA) that still gives at least 0.8 CTAs per
+// SM; two CTAs per SM (four loader warps each) when there are more CTAs than SMs.
+WrChoice choose_write_read(const sdm_shape *sh, int sm_count) {
+  const int64_t streams = sh->B * sh->H, rb = row_bytes_of(sh);
+  int ncw = 1;
+  const int forced = g_test_slice_bytes.load();
+  if (forced == 32 || forced == 128 || forced == 256) {
+    ncw = forced / 32;
+  } else {
+    for (int n : kNcwChoices) {
+      if (n > 1 && 32 * n > rb) continue;
+      const int64_t ctas = streams * ((rb + 32 * n - 1) / (32 * n));
+      if (ctas * 10 >= (int64_t)sm_count * 8) {
+        ncw = n;
+        break;
+      }
     }
   }
-  const int64_t ctas = streams * (sh->d_v / std::max(cw, 1));
-  const int64_t budget = ctas > sm_count ? kSmemTwoCta : kSmemOneCta;
-  WrChoice c = stage_for(sh, cw, budget);
-  c.two_per_sm = budget == kSmemTwoCta;
-  const int forced_g = env_int("SDM_WR_G", 0);
-  if (forced_g > 0 && forced_g < c.lay.G) {
-    c.lay = plan_layout(forced_g, sh->W, sh->R, sh->T);
-    c.smem = write_read_smem_bytes(cw, (int)elem_bytes(sh->bank_dtype), (int)elem_bytes(sh->act_dtype),
-                                   forced_g, sh->W, sh->R, c.lay.rec_bytes);
+  for (;;) {
+    const int64_t ctas = streams * ((rb + 32 * ncw - 1) / (32 * ncw));
+    const WrChoice c = configure(sh, ncw, ctas > sm_count, g_test_stage_tokens.load());
+    if (c.smem <= kSmemOneCta || ncw == 1) return c;
+    ncw = ncw == 8 ? 4 : 1;                          // not even one token fits: a narrower slice
   }
-  return c;
 }
 
 // ---------------------------------------------------------------- workspace layout
@@ -332,7 +339,7 @@ int64_t a256(int64_t x) { return (x + 255) & ~int64_t(255); }
 struct WsLayout {
   int64_t idx_w, wt_w, idx_r, wt_r;  // selection outputs kept here when the caller passes NULL
   int64_t scores;                    // factor scores [2, B*T*H, sum n_f] float32
-  int64_t uniq, nuniq, written, records;
+  int64_t uniq, nuniq, uo, written, lrecs, crecs;
   int64_t total;
 };
 
@@ -350,24 +357,24 @@ WsLayout ws_layout(const sdm_shape *sh, const PlanLayout &lay) {
   w.scores = o; o = a256(o + 2 * rows * ntot * 4);
   w.uniq = o;  o = a256(o + stages * lay.L * 4);
   w.nuniq = o; o = a256(o + stages * 4);
+  w.uo = o;    o = a256(o + stages * lay.L * 2);
   w.written = o; o = a256(o + stages * lay.L);
-  w.records = o; o = a256(o + stages * lay.rec_bytes);
+  w.lrecs = o; o = a256(o + stages * lay.lrec_bytes);
+  w.crecs = o; o = a256(o + stages * lay.crec_bytes);
   w.total = o;
   return w;
 }
 
-// The size depends only on the shape: the maximum over every slice and stage length the
-// launch may pick on any device.
+// The size depends only on the shape: the maximum over every slice width and stage
+// length the launch may pick on any device (stage lengths forced down by the test hook
+// included).
 int64_t write_read_ws_bytes(const sdm_shape *sh) {
-  std::vector<int> cands;
-  cw_candidates(sh, cands);
   int64_t best = kHeaderBytes;
-  for (int cw : cands)
-    for (int64_t budget : {kSmemOneCta, kSmemTwoCta}) {
-      const WrChoice c = stage_for(sh, cw, budget);
-      best = std::max(best, ws_layout(sh, c.lay).total);
-      for (int g = 1; g <= c.lay.G; ++g)   // stage lengths forced down for tuning
-        best = std::max(best, ws_layout(sh, plan_layout(g, sh->W, sh->R, sh->T)).total);
+  for (int ncw : kNcwChoices)
+    for (bool two : {false, true}) {
+      const WrChoice c = configure(sh, ncw, two, 0);
+      for (int g = 1; g <= c.lay.G; ++g)
+        best = std::max(best, ws_layout(sh, plan_layout(g, sh->W, sh->R, sh->T, 32 * ncw)).total);
     }
   return best;
 }
@@ -408,9 +415,9 @@ sdm_status sm_count(int *out) {
 }
 
 // The tensor-core scorer takes bfloat16 inputs whose d_sub is a multiple of 64 and whose
-// factor widths are multiples of 16; SDM_SCORE_SIMT=1 forces the CUDA-core scorer.
+// factor widths are multiples of 16 (sdm_test_force_simt_scorer forces the CUDA-core one).
 bool use_tensor_cores(const Derived &d, const sdm_shape *sh) {
-  if (env_int("SDM_SCORE_SIMT", 0)) return false;
+  if (g_test_simt_scorer.load()) return false;
   int maxnf = 0;
   for (int f = 0; f < d.g.F; ++f) maxnf = std::max(maxnf, d.g.nf[f]);
   const int64_t n_tiles = (maxnf + 255) / 256;
@@ -583,16 +590,22 @@ sdm_status write_read_impl(const sdm_shape *sh, const void *q_w, const void *q_r
   PlanArgs pa{};
   pa.idx[0] = iw;
   pa.idx[1] = ir;
+  pa.wt[0] = ww;
+  pa.wt[1] = wr;
+  pa.gates = gates;
   pa.uniq = reinterpret_cast<int32_t *>(ws + wl.uniq);
   pa.nuniq = reinterpret_cast<int32_t *>(ws + wl.nuniq);
+  pa.uo = reinterpret_cast<uint16_t *>(ws + wl.uo);
   pa.written = ws + wl.written;
-  pa.records = ws + wl.records;
+  pa.lrecs = ws + wl.lrecs;
+  pa.crecs = ws + wl.crecs;
   pa.err = err;
   pa.T = sh->T;
   pa.H = (int32_t)sh->H;
   pa.W = sh->W;
   pa.R = sh->R;
   pa.N = d.N;
+  pa.pitch16 = (uint32_t)(sh->d_v * sb / 16);
   pa.lay = wc.lay;
   const int P = pow2_at_least(wc.lay.L);
   if ((st = run_kernel(SDM_KERNEL_PLAN_SORT, cs, "plan_sort", [&] { return launch_plan_sort(pa, streams, P, cs); })) != SDM_OK)
@@ -603,10 +616,8 @@ sdm_status write_read_impl(const sdm_shape *sh, const void *q_w, const void *q_r
   // 3. fused gather / delta update / read
   WriteReadArgs wa{};
   wa.k_val = k_val;
-  wa.gates = gates;
-  wa.wt[0] = ww;
-  wa.wt[1] = wr;
-  wa.records = ws + wl.records;
+  wa.lrecs = ws + wl.lrecs;
+  wa.crecs = ws + wl.crecs;
   wa.bank = bank;
   wa.y = y;
   wa.err = err;
@@ -616,16 +627,16 @@ sdm_status write_read_impl(const sdm_shape *sh, const void *q_w, const void *q_r
   wa.H = (int32_t)sh->H;
   wa.W = sh->W;
   wa.R = sh->R;
-  wa.slices = (int32_t)(sh->d_v / wc.CW);
-  wa.tok_bulk = (sh->W % 4 == 0 && sh->R % 4 == 0 && aligned(ww, 16) && aligned(wr, 16)) ? 1 : 0;
-  wa.two_per_sm = wc.two_per_sm ? 1 : 0;
+  wa.slices = wc.slices;
+  wa.row_bytes = (int32_t)(sh->d_v * sb);
   wa.lay = wc.lay;
+  const WriteReadLaunch wl_launch{wc.NCW, wc.LW, wc.smem};
   if (side) {                                          // the bank copy must land first
     ce = cudaStreamWaitEvent(cs, side->join, 0);
     if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "side stream join: %s", cudaGetErrorString(ce));
   }
   if ((st = run_kernel(SDM_KERNEL_WRITE_READ, cs, "write_read", [&] {
-         return launch_write_read(wa, streams, sh->bank_dtype, sh->act_dtype, wc.CW, wc.smem, cs);
+         return launch_write_read(wa, streams, sh->bank_dtype, sh->act_dtype, wl_launch, cs);
        })) != SDM_OK)
     return st;
   return ok();
@@ -794,6 +805,19 @@ uint64_t sdm_launch_count(void) { return g_launches.load(); }
 
 sdm_status sdm_test_stall_decode_copy(int on) {
   g_test_stall_decode_copy.store(on ? 1 : 0);
+  return SDM_OK;
+}
+
+sdm_status sdm_test_force_write_read_layout(int slice_bytes, int stage_tokens) {
+  if (!(slice_bytes == 0 || slice_bytes == 32 || slice_bytes == 128 || slice_bytes == 256) || stage_tokens < 0)
+    return fail(SDM_ERR_INVALID_ARG, "slice_bytes must be 0, 32, 128 or 256 and stage_tokens >= 0");
+  g_test_slice_bytes.store(slice_bytes);
+  g_test_stage_tokens.store(stage_tokens);
+  return ok();
+}
+
+sdm_status sdm_test_force_simt_scorer(int on) {
+  g_test_simt_scorer.store(on ? 1 : 0);
   return SDM_OK;
 }
 

@@ -213,11 +213,19 @@ __device__ __forceinline__ void store_vec16(T *p, const float (&in)[Vec16<T>::N]
   *reinterpret_cast<uint4 *>(p) = u;
 }
 
-// Loads / stores NV consecutive elements of T (NV * sizeof(T) in {8, 16} bytes, or a
-// single element) as one access.
+// Loads / stores NV consecutive elements of T as 16-byte accesses (NV * sizeof(T) of 16
+// or 32 bytes), one 8-byte access, or element by element.
 template <typename T, int NV>
 __device__ __forceinline__ void load_vec(const T *p, float (&out)[NV]) {
-  if constexpr (NV * sizeof(T) == 16) {
+  if constexpr (NV * sizeof(T) == 32) {
+    const uint4 u0 = *reinterpret_cast<const uint4 *>(p), u1 = *reinterpret_cast<const uint4 *>(p + NV / 2);
+    const T *e0 = reinterpret_cast<const T *>(&u0), *e1 = reinterpret_cast<const T *>(&u1);
+#pragma unroll
+    for (int i = 0; i < NV / 2; ++i) {
+      out[i] = to_f32(e0[i]);
+      out[NV / 2 + i] = to_f32(e1[i]);
+    }
+  } else if constexpr (NV * sizeof(T) == 16) {
     const uint4 u = *reinterpret_cast<const uint4 *>(p);
     const T *e = reinterpret_cast<const T *>(&u);
 #pragma unroll
@@ -235,7 +243,17 @@ __device__ __forceinline__ void load_vec(const T *p, float (&out)[NV]) {
 
 template <typename T, int NV>
 __device__ __forceinline__ void store_vec(T *p, const float (&in)[NV]) {
-  if constexpr (NV * sizeof(T) == 16) {
+  if constexpr (NV * sizeof(T) == 32) {
+    uint4 u0, u1;
+    T *e0 = reinterpret_cast<T *>(&u0), *e1 = reinterpret_cast<T *>(&u1);
+#pragma unroll
+    for (int i = 0; i < NV / 2; ++i) {
+      e0[i] = from_f32<T>(in[i]);
+      e1[i] = from_f32<T>(in[NV / 2 + i]);
+    }
+    *reinterpret_cast<uint4 *>(p) = u0;
+    *reinterpret_cast<uint4 *>(p + NV / 2) = u1;
+  } else if constexpr (NV * sizeof(T) == 16) {
     uint4 u;
     T *e = reinterpret_cast<T *>(&u);
 #pragma unroll

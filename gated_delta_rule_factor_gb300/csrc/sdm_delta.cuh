@@ -17,7 +17,7 @@
 //     increasing j; the RG partial sums are combined by an xor butterfly.  Each lane
 //     fetches all of its rows into shared memory with cp.async at once (one memory round
 //     trip per sum) and reads back only what it fetched.
-//   * token_blocks2 (the write/read kernel, rows in shared memory), below.
+//   * piece_token (the write/read kernel, rows in shared memory), below.
 #pragma once
 
 #include "sdm_common.cuh"
@@ -115,196 +115,167 @@ __device__ __forceinline__ void weighted_read_staged(int R, const float *r, bool
 }
 
 // ------------------------------------------------------------------------------------
-// Block-ordered token step of the write/read kernel, two warps per row slice.
+// Token step of the write/read kernel: one warp per 32-byte piece of every row.
 //
-// Summation order.  The n rows of a sum (n = W for the prediction p, n = R for the
-// read y) are cut into 8 consecutive blocks of B8 = ceil(n / 8) rows; block k is summed
-// in increasing j into a_k and the block sums are combined as
-//   ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)).
-// The order depends on n alone: not on the stage length, nor on the column slicing.
+// Columns are independent, so each compute warp of the write/read kernel owns a 32-byte
+// piece of every row of its CTA's column slice and runs the tokens on it alone: no two
+// compute warps ever wait for each other.  Lane = 2*rg + c: c picks the 16-byte half of
+// the piece (VEC = 16 / sizeof(BANK) columns), rg (0..15) a block of rows.
 //
-// Layout.  Lane % 8 owns VEC consecutive elements of the slice (the slice is 8*VEC
-// elements wide) and warp wsel's row group rg = lane / 8 owns block k = 4*wsel + rg: a
-// lane adds its block, two xor steps inside the warp give (a0+a1)+(a2+a3) in warp 0 and
-// (a4+a5)+(a6+a7) in warp 1, and the warps swap those through shared memory (xch:
-// [2 warps][8 column groups][VEC] floats) on a 64-thread named barrier `bar`.  IEEE
-// addition is commutative, so both partners of every step hold the same bits.
-// JB >= B8: register slot s holds row k*B8 + s.
-template <int BYTES>
-struct RawVec;
-template <>
-struct RawVec<16> { using T = uint4; };
-template <>
-struct RawVec<8> { using T = uint2; };
-template <>
-struct RawVec<4> { using T = uint32_t; };
-template <>
-struct RawVec<2> { using T = uint16_t; };
+// Summation order.  The n rows of a sum (n = W for the prediction p, n = R for the read
+// y) are cut into 16 consecutive blocks of B16 = ceil(n / 16) rows; lane rg sums block
+// rg in increasing j, and an xor butterfly over the rg bits (lane xor 2, 4, 8, 16)
+// combines the block sums as a balanced binary tree in block order,
+//   (((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7))) + (((s8+s9)+(s10+s11))+((s12+s13)+(s14+s15))),
+// which leaves the same bits in every lane (IEEE addition is commutative).  The order
+// depends on n alone: not on the stage length, the column slice or the warp.
+//
+// Shared-memory addresses.  rm holds, per reference, the row's offset o in the stage
+// buffer (sdm_internal.h, PlanLayout); this lane's 16 bytes of that row sit at
+// o ^ wc, wc = (warp << 5) | (c << 4).  The planner gives the rows of blocks 4q..4q+3
+// four different colors (bits 5-6 of o), so the eight lanes of a quarter-warp, which
+// read block rows 4q..4q+3 at once, hit eight different 16-byte bank groups.
 
-// VEC elements of BANK <-> float32.
-template <typename BANK, int VEC>
-struct LaneRow {
-  using Raw = typename RawVec<VEC * (int)sizeof(BANK)>::T;
-  __device__ __forceinline__ static Raw load(const unsigned char *p) { return *reinterpret_cast<const Raw *>(p); }
-  __device__ __forceinline__ static void unpack(const Raw &r, float (&out)[VEC]) {
+template <typename BANK>
+struct PieceRow {
+  static constexpr int VEC = 16 / (int)sizeof(BANK);
+  __device__ __forceinline__ static void unpack(const uint4 &r, float (&out)[VEC]) {
     const BANK *e = reinterpret_cast<const BANK *>(&r);
 #pragma unroll
     for (int i = 0; i < VEC; ++i) out[i] = to_f32(e[i]);
   }
-  __device__ __forceinline__ static void store(unsigned char *p, const float (&in)[VEC]) {
-    Raw r;
+  __device__ __forceinline__ static uint4 pack(const float (&in)[VEC]) {
+    uint4 r;
     BANK *e = reinterpret_cast<BANK *>(&r);
 #pragma unroll
     for (int i = 0; i < VEC; ++i) e[i] = from_f32<BANK>(in[i]);
-    *reinterpret_cast<Raw *>(p) = r;
+    return r;
   }
 };
 
-template <int JB>
-struct BlockSlots1 {
-  int b8, j0, n;
-  __device__ __forceinline__ BlockSlots1(int n_, int k) : b8((n_ + 7) >> 3), j0(k * ((n_ + 7) >> 3)), n(n_) {}
-  __device__ __forceinline__ int ref(int s) const { return j0 + s; }
-  __device__ __forceinline__ bool has(int s) const { return s < b8 && j0 + s < n; }
-};
-
+// The butterfly over the 16 row blocks (lane bits 1-4).
 template <int VEC>
-__device__ __forceinline__ void pair_tree(const float (&a)[VEC], float (&out)[VEC], float *xch, int wsel, int bar) {
-  const int lane = threadIdx.x & 31;
-  float x[VEC];
+__device__ __forceinline__ void block_tree(float (&x)[VEC]) {
 #pragma unroll
-  for (int c = 0; c < VEC; ++c) {
-    x[c] = __fadd_rn(a[c], __shfl_xor_sync(0xffffffffu, a[c], 8));
-    x[c] = __fadd_rn(x[c], __shfl_xor_sync(0xffffffffu, x[c], 16));
-  }
-  float *mine = xch + (wsel * 8 + (lane & 7)) * VEC;
-  const float *theirs = xch + ((wsel ^ 1) * 8 + (lane & 7)) * VEC;
-  if (lane < 8) {
-    if constexpr (VEC % 4 == 0) {
+  for (int o = 2; o < 32; o <<= 1)
 #pragma unroll
-      for (int c = 0; c < VEC; c += 4)
-        *reinterpret_cast<float4 *>(mine + c) = make_float4(x[c], x[c + 1], x[c + 2], x[c + 3]);
-    } else if constexpr (VEC == 2) {
-      *reinterpret_cast<float2 *>(mine) = make_float2(x[0], x[1]);
+    for (int c = 0; c < VEC; ++c) x[c] = __fadd_rn(x[c], __shfl_xor_sync(0xffffffffu, x[c], o));
+}
+
+// Offsets and weights of this lane's rows of one sum (block rg of n references rm / wt).
+// FULL: n == 64 (B16 = 4, read as 8- and 16-byte vectors).  Rows past the block or past
+// n get offset 0 and weight 0 and are never touched (has(s) is false for them).
+template <int JB, bool FULL>
+struct BlockRows {
+  int off[JB];
+  float w[JB];
+  int nb;                                         // rows of this block
+  __device__ __forceinline__ BlockRows(int n, int rg, const uint16_t *rm, const float *wt, uint32_t wc) {
+    if constexpr (FULL) {
+      static_assert(JB == 4, "FULL blocks hold 4 rows");
+      const uint2 o4 = *reinterpret_cast<const uint2 *>(rm + 4 * rg);
+      const uint32_t wc2 = wc | (wc << 16);
+      const uint32_t x = o4.x ^ wc2, y = o4.y ^ wc2;
+      off[0] = (int)(x & 0xffffu);
+      off[1] = (int)(x >> 16);
+      off[2] = (int)(y & 0xffffu);
+      off[3] = (int)(y >> 16);
+      const float4 w4 = *reinterpret_cast<const float4 *>(wt + 4 * rg);
+      w[0] = w4.x;
+      w[1] = w4.y;
+      w[2] = w4.z;
+      w[3] = w4.w;
+      nb = 4;
     } else {
-      mine[0] = x[0];
-    }
-  }
-  named_barrier(bar, 64);
-  float o[VEC];
-  if constexpr (VEC % 4 == 0) {
+      const int b16 = (n + 15) >> 4, j0 = rg * b16;
+      nb = min(b16, max(n - j0, 0));
 #pragma unroll
-    for (int c = 0; c < VEC; c += 4) {
-      const float4 q = *reinterpret_cast<const float4 *>(theirs + c);
-      o[c] = q.x;
-      o[c + 1] = q.y;
-      o[c + 2] = q.z;
-      o[c + 3] = q.w;
-    }
-  } else if constexpr (VEC == 2) {
-    const float2 q = *reinterpret_cast<const float2 *>(theirs);
-    o[0] = q.x;
-    o[1] = q.y;
-  } else {
-    o[0] = theirs[0];
-  }
-#pragma unroll
-  for (int c = 0; c < VEC; ++c) out[c] = __fadd_rn(x[c], o[c]);
-}
-
-template <typename BANK, int VEC, int JB>
-__device__ __forceinline__ void pair_read(const BlockSlots1<JB> &rs, const uint16_t *rm_r, const float *wt_r,
-                                          const unsigned char *rows, int RB, float (&b)[VEC]) {
-  using LR = LaneRow<BANK, VEC>;
-#pragma unroll
-  for (int s0 = 0; s0 < JB; s0 += 4) {
-    typename LR::Raw raw[4];
-    float wr[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int s = s0 + q;
-      if (rs.has(s)) {
-        raw[q] = LR::load(rows + (int)rm_r[rs.ref(s)] * RB);
-        wr[q] = wt_r[rs.ref(s)];
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (rs.has(s0 + q)) {
-        float m[VEC];
-        LR::unpack(raw[q], m);
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) b[c] = __fmaf_rn(wr[q], m[c], b[c]);
+      for (int s = 0; s < JB; ++s) {
+        const bool h = s < nb;
+        off[s] = h ? (int)((uint32_t)rm[j0 + s] ^ wc) : 0;
+        w[s] = h ? wt[j0 + s] : 0.0f;
       }
     }
   }
-}
+  __device__ __forceinline__ bool has(int s) const { return FULL ? true : s < nb; }
+};
 
-// One token: the gated delta-rule write of its W rows, then the read of its R rows, with
-// the arithmetic of delta_write_staged / weighted_read_staged per element and the block order
-// above for both sums.  rm / wt: the token's row references (stage-buffer row indices)
-// and weights, W write entries then R read entries; rows: the stage buffer offset by this
-// lane's column group; RB: the row slice in bytes.  When the token reads none of the rows
-// it writes (overlap == false) the read runs before the write: those rows hold the same
-// values before and after it.  FULL: W == R == 8 * JB.  The read's exchange barrier comes
-// after the row stores, so it also orders this token's writes before the next token's
-// loads in the other warp.
-template <typename BANK, int VEC, int JB, bool FULL = false>
-__device__ __forceinline__ void token_blocks2(int W, int R, const uint16_t *rm, const float *wt, float alpha,
-                                              float beta, const float (&v)[VEC], unsigned char *rows, int RB,
-                                              bool overlap, float (&y)[VEC], float *xch_p, float *xch_y, int wsel,
-                                              int bar) {
-  using LR = LaneRow<BANK, VEC>;
-  if constexpr (FULL) W = R = 8 * JB;
-  const int k = 4 * wsel + ((threadIdx.x & 31) >> 3);
-  const BlockSlots1<JB> ws(W, k), rs(R, k);
-  int ow[JB];
-  float ww[JB];
-  typename LR::Raw rw[JB];
-#pragma unroll
-  for (int s = 0; s < JB; ++s) {
-    ow[s] = ws.has(s) ? (int)rm[ws.ref(s)] * RB : 0;
-    ww[s] = ws.has(s) ? wt[ws.ref(s)] : 0.0f;
-  }
+// One token on this warp's pieces of the stage buffer `rows`: the gated delta-rule write
+// of its W rows, then the read of its R rows (after the write: the token's own update is
+// visible).  rm / wt: the token's W write then R read references (offsets o, weights).
+// When the token reads none of the rows it writes (overlap == false) the read rows are
+// fetched before the write: those rows hold the same values before and after it.  y is
+// left in every lane.  The caller orders tokens with __syncwarp().
+template <typename BANK, int JB, bool FULL>
+__device__ __forceinline__ void piece_token(int W, int R, const uint16_t *rm, const float *wt, float alpha,
+                                            float beta, const float (&v)[PieceRow<BANK>::VEC], unsigned char *rows,
+                                            uint32_t wc, bool overlap, float (&y)[PieceRow<BANK>::VEC]) {
+  using PR = PieceRow<BANK>;
+  constexpr int VEC = PR::VEC;
+  if constexpr (FULL) W = R = 64;
+  const int rg = (threadIdx.x & 31) >> 1;
+  const BlockRows<JB, FULL> wr_(W, rg, rm, wt, wc);
+  uint4 rw[JB];
 #pragma unroll
   for (int s = 0; s < JB; ++s)
-    if (ws.has(s)) rw[s] = LR::load(rows + ow[s]);
-  float b[VEC];
+    if (wr_.has(s)) rw[s] = *reinterpret_cast<const uint4 *>(rows + wr_.off[s]);
+  const BlockRows<JB, FULL> rd(R, rg, rm + W, wt + W, wc);
+  uint4 rr[JB];
+  if (!overlap) {
 #pragma unroll
-  for (int c = 0; c < VEC; ++c) b[c] = 0.0f;
-  if (!overlap) pair_read<BANK, VEC, JB>(rs, rm + W, wt + W, rows, RB, b);
-
+    for (int s = 0; s < JB; ++s)
+      if (rd.has(s)) rr[s] = *reinterpret_cast<const uint4 *>(rows + rd.off[s]);
+  }
+  // p = sum_j w_j (alpha m_j)
+  float am[JB][VEC];
   float a[VEC];
 #pragma unroll
   for (int c = 0; c < VEC; ++c) a[c] = 0.0f;
 #pragma unroll
   for (int s = 0; s < JB; ++s) {
-    if (ws.has(s)) {
+    if (wr_.has(s)) {
       float m[VEC];
-      LR::unpack(rw[s], m);
+      PR::unpack(rw[s], m);
 #pragma unroll
-      for (int c = 0; c < VEC; ++c) a[c] = __fmaf_rn(ww[s], __fmul_rn(alpha, m[c]), a[c]);
+      for (int c = 0; c < VEC; ++c) {
+        am[s][c] = __fmul_rn(alpha, m[c]);
+        a[c] = __fmaf_rn(wr_.w[s], am[s][c], a[c]);
+      }
     }
   }
-  float p[VEC], d[VEC];
-  pair_tree<VEC>(a, p, xch_p, wsel, bar);
+  block_tree<VEC>(a);
+  // m_j <- alpha m_j + w_j beta (v - p)
+  float d[VEC];
 #pragma unroll
-  for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], p[c]));
+  for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(beta, __fsub_rn(v[c], a[c]));
 #pragma unroll
   for (int s = 0; s < JB; ++s) {
-    if (ws.has(s)) {
+    if (wr_.has(s)) {
       float m[VEC];
-      LR::unpack(rw[s], m);
 #pragma unroll
-      for (int c = 0; c < VEC; ++c) m[c] = __fmaf_rn(ww[s], d[c], __fmul_rn(alpha, m[c]));
-      LR::store(rows + ow[s], m);
+      for (int c = 0; c < VEC; ++c) m[c] = __fmaf_rn(wr_.w[s], d[c], am[s][c]);
+      *reinterpret_cast<uint4 *>(rows + wr_.off[s]) = PR::pack(m);
     }
   }
   if (overlap) {
-    named_barrier(bar, 64);
-    pair_read<BANK, VEC, JB>(rs, rm + W, wt + W, rows, RB, b);
+    __syncwarp();
+#pragma unroll
+    for (int s = 0; s < JB; ++s)
+      if (rd.has(s)) rr[s] = *reinterpret_cast<const uint4 *>(rows + rd.off[s]);
   }
-  pair_tree<VEC>(b, y, xch_y, wsel, bar);
+  // y = sum_j r_j m_j
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) y[c] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < JB; ++s) {
+    if (rd.has(s)) {
+      float m[VEC];
+      PR::unpack(rr[s], m);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) y[c] = __fmaf_rn(rd.w[s], m[c], y[c]);
+    }
+  }
+  block_tree<VEC>(y);
 }
 
 }  // namespace sdm

@@ -73,32 +73,55 @@ struct BankCopyArgs {
   int64_t H;
 };
 
-// Chunk plan (per stream s = b*H + h and stage g of G tokens, L = G*(W+R) refs):
-//   uniq[s][g][u]    sorted unique slot ids of the stage      (int32, L per stage)
+// Chunk plan (per stream s = b*H + h and stage g of G tokens, L = G*(W+R) refs).
+// The write/read kernel keeps a stage's distinct rows in one of three shared-memory
+// row buffers; row u of a stage lives at byte offset o(u) = u*RB + (color << 5) of its
+// buffer, where RB is the CTA's row slice in bytes and `color` (0..3, masked by cmask)
+// rotates which 32-byte piece of the slot each compute warp uses, so that the four
+// rows a quarter-warp reads at once sit in four different bank groups.  Every offset
+// the kernel uses is such an o (a u16: L*RB <= 65536).
+//   uniq[s][g][u]    sorted unique slot ids of the stage        (int32, L per stage)
 //   nuniq[s][g]      number of unique rows
-//   written[s][g][u] 1 if a write ref of the stage hits row u (uint8, L per stage)
-//   record[s][g]     the stage record read by the write/read kernel:
-//     int32 n_u, n_load, n_carry, n_wb, n_late, 3 x pad   (32 bytes)
-//       the last n_late loads re-read rows stage g-2 held (possibly written back late)
-//     int32  load_slot[L]; uint16 load_u[L]      rows fetched from the bank
-//     uint32 carry[L]      (u | src_u << 16)      rows copied from the previous stage
-//     int32  wb_slot[L];   uint16 wb_u[L]         rows written back after the stage
-//     uint16 refmap[L]     row u of ref (t_local*(W+R) + j)
-//     uint8  tokflag[G]    1 if the token reads a row it also writes
+//   uo[s][g][u]      o(u)                                        (uint16, L per stage)
+//   written[s][g][u] 1 if a write ref of the stage hits row u   (uint8, L per stage)
+//   lrec[s][g]       the stage's row lists, fetched three stages ahead:
+//     int32 n_u, n_load, n_c1, n_c2, n_wb, 3 x pad               (32 bytes)
+//     uint2 ent[L]     entries [0, n_load): bank rows fetched, {row offset, o}, the
+//                      row offset being slot * (d_v * elem / 16) in 16-byte units from
+//                      the stream's table; then n_c1 carries from stage g-1's buffer
+//                      and n_c2 carries from stage g-2's buffer (rows stage g-1 does
+//                      not hold), {o_dst | o_src << 16, 0}; the compute warps make those
+//                      copies at the end of stage g-1 and g-2 respectively
+//     uint2 wb[L]      rows written back after the stage, {row offset, o}: dirty ones
+//                      (written, or carried in) that neither of the next two stages holds
+//   crec[s][g]       the compute warps' per-stage data, one contiguous copy:
+//     uint16 refmap[L]    o of ref (t_local*(W+R) + j)
+//     uint8  tokflag[G]   1 if the token reads a row it also writes
+//     float  wts[L]       the weights of ref (t_local*(W+R) + j): W write, then R read
+//     float  gates[G][2]  (alpha, beta) of each token
 struct PlanLayout {
   int32_t G;             // tokens per stage
   int32_t L;             // refs per full stage = G*(W+R)
   int32_t n_stages;      // ceil(T / G)
-  int64_t rec_bytes;     // bytes per stage record (multiple of 16)
-  int64_t off_load_slot, off_load_u, off_carry, off_wb_slot, off_wb_u, off_refmap, off_tokflag;
+  int32_t RB;            // row slice bytes of one CTA (row slot stride)
+  int32_t cmask;         // color bits usable in o (3 when RB >= 128, else 0)
+  int64_t lrec_bytes;    // bytes per row-list record (multiple of 16)
+  int64_t off_ent, off_wb;
+  int64_t crec_bytes;    // bytes per compute record (multiple of 16)
+  int64_t off_refmap, off_tokflag, off_wts, off_gates;
 };
 
 struct PlanArgs {
   const int32_t *idx[2];  // idx_w [B,T,H,W], idx_r [B,T,H,R]
+  const float *wt[2];     // their weights
+  const float *gates;     // [B,T,H,2]
+  uint32_t pitch16;       // a bank row in 16-byte units (d_v * elem / 16)
   int32_t *uniq;
   int32_t *nuniq;
+  uint16_t *uo;
   uint8_t *written;
-  unsigned char *records;
+  unsigned char *lrecs;
+  unsigned char *crecs;
   int32_t *err;
   int64_t T;
   int32_t H, W, R;
@@ -108,17 +131,15 @@ struct PlanArgs {
 
 struct WriteReadArgs {
   const void *k_val;      // [B,T,H,d_v]
-  const float *gates;     // [B,T,H,2]
-  const float *wt[2];     // [B,T,H,W], [B,T,H,R]
-  const unsigned char *records;
+  const unsigned char *lrecs;
+  const unsigned char *crecs;
   void *bank;             // [B,H,N,d_v]
   void *y;                // [B,T,H,d_v]
   int32_t *err;
   int64_t T, N, d_v;
   int32_t H, W, R;
-  int32_t slices;         // d_v / CW
-  int32_t tok_bulk;       // weights and values of a token fetched by bulk copies (16-byte aligned)
-  int32_t two_per_sm;     // the launch plans for two CTAs per SM (fewer loader warps)
+  int32_t slices;         // ceil(row bytes / RB)
+  int32_t row_bytes;      // d_v * bank element bytes (the last slice may be partial)
   PlanLayout lay;
 };
 
@@ -142,13 +163,6 @@ struct DecodeArgs {
   KeyGeometry g;
 };
 
-// Column slice of the write/read kernel and its stage length.
-struct WriteReadConfig {
-  int32_t CW;             // bank columns per CTA
-  int32_t G;              // tokens per stage
-  int64_t smem_bytes;
-};
-
 // Raises a kernel's dynamic shared-memory limit to at least `smem` bytes on the current
 // device, once per (kernel, device, larger size): the attribute call is not repeated per
 // launch, so steady-state calls make only stream-ordered CUDA calls (graph capture).
@@ -164,20 +178,27 @@ cudaError_t launch_bank_copy(const BankCopyArgs &a, int sm_count, cudaStream_t s
 cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int sort_pow2,
                              cudaStream_t st);
 cudaError_t launch_plan_link(const PlanArgs &a, int64_t streams, cudaStream_t st);
+// Write/read launch: NCW compute warps (RB = 32*NCW bytes of every row per CTA), LW
+// loader warps, grid (slices, streams).
+struct WriteReadLaunch {
+  int32_t NCW;            // 1, 4 or 8
+  int32_t LW;             // 4 or 8
+  int64_t smem_bytes;
+};
 cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_dtype,
-                              int act_dtype, int CW, int64_t smem_bytes, cudaStream_t st);
+                              int act_dtype, const WriteReadLaunch &l, cudaStream_t st);
 // The instances of one (bank, activation) type pair, from sdm_write_read_<bank>_<act>.cu.
-cudaError_t launch_write_read_f32_f32(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem, cudaStream_t st);
-cudaError_t launch_write_read_f32_bf16(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem, cudaStream_t st);
-cudaError_t launch_write_read_bf16_f32(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem, cudaStream_t st);
-cudaError_t launch_write_read_bf16_bf16(const WriteReadArgs &a, int64_t streams, int CW, int64_t smem,
+cudaError_t launch_write_read_f32_f32(const WriteReadArgs &a, int64_t streams, const WriteReadLaunch &l, cudaStream_t st);
+cudaError_t launch_write_read_f32_bf16(const WriteReadArgs &a, int64_t streams, const WriteReadLaunch &l, cudaStream_t st);
+cudaError_t launch_write_read_bf16_f32(const WriteReadArgs &a, int64_t streams, const WriteReadLaunch &l, cudaStream_t st);
+cudaError_t launch_write_read_bf16_bf16(const WriteReadArgs &a, int64_t streams, const WriteReadLaunch &l,
                                         cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, const CandidateList &cl, int act_dtype,
                           int bank_dtype, int EF, int EC, int64_t smem_bytes,
                           cudaStream_t st);
 
-// Dynamic shared memory needed by the write/read kernel for a column slice and stage.
-int64_t write_read_smem_bytes(int CW, int bank_elem, int act_elem, int G, int W, int R,
-                              int64_t rec_bytes);
+// Dynamic shared memory of the write/read kernel for a plan layout (RB, G, records) and
+// the activation element size.
+int64_t write_read_smem_bytes(const PlanLayout &lay, int bank_elem, int act_elem);
 
 }  // namespace sdm

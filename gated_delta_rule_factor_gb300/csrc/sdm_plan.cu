@@ -1,19 +1,24 @@
 // Chunk planner: turns the selected slot ids of each stage (G consecutive tokens of
-// one stream) into the row movement plan the write/read kernel executes.
+// one stream) into the row movement plan the write/read kernel executes (record
+// layout in sdm_internal.h, PlanLayout).
 //
 // Tokens of a stream must see every earlier token's writes, including writes to the
 // same row inside one stage.  The write/read kernel therefore keeps each stage's rows
 // in shared memory, one copy per distinct row, and runs the tokens in order on those
 // copies.  The plan says, per stage: which distinct rows it touches (sorted slot ids),
 // where each of the stage's references lives among them, which rows come from the
-// bank and which are carried over from the previous stage's copies (the bank may
-// still hold a stale value for those), and which rows go back to the bank after the
-// stage (the ones it dirtied or carried in, unless the next stage carries them on).
+// bank and which are carried over from the copies of one of the two previous stages
+// (the bank may still hold a stale value for those), and which rows go back to the
+// bank after the stage (the ones it dirtied or carried in, unless one of the next two
+// stages carries them on).
 // Everything is integer work with fixed orders (bitonic sort of (slot, ref) keys,
 // ordered prefix sums), so plans are bitwise repeatable and no float atomics exist.
 //
-// plan_sort: per stage, sort and deduplicate its G*(W+R) references.
-// plan_link: per stage, compare with the neighbouring stages and emit the record.
+// plan_sort: per stage, sort and deduplicate its G*(W+R) references; give every
+//            distinct row its shared-memory offset o (slot u, bank color) and every
+//            reference the offset of its row.
+// plan_link: per stage, compare with the two stages before and after it and emit the
+//            row lists (bank loads, carries, write-backs).
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -58,12 +63,22 @@ __device__ __forceinline__ int find_sorted(const int32_t *a, int n, int32_t key)
   return (lo < n && a[lo] == key) ? lo : -1;
 }
 
+// Bank color of a reference: the write/read kernel's lane rg reads the rows of block rg
+// (16 consecutive blocks of ceil(n/16) references of the token's write or read list),
+// and the lanes of blocks 4q..4q+3 read at the same time, so block k's rows get color
+// k mod 4.  A row referenced several times takes the color of its first reference.
+__device__ __forceinline__ int ref_color(int j, int W, int R) {
+  if (j < W) return (j / ((W + 15) >> 4)) & 3;
+  return ((j - W) / ((R + 15) >> 4)) & 3;
+}
+
 __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_constant__ PlanArgs a, int P) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint64_t *keys = reinterpret_cast<uint64_t *>(smem);            // [P]
   uint8_t *wr = reinterpret_cast<uint8_t *>(keys + P);              // [P], 4-byte aligned
   const int P4 = (P + 3) & ~3;                                      // wr is updated by words
-  uint8_t *tokflag = wr + P4;                                       // [G]
+  uint16_t *uo_s = reinterpret_cast<uint16_t *>(wr + P4);           // [P]
+  uint8_t *tokflag = reinterpret_cast<uint8_t *>(uo_s + P);         // [G]
   __shared__ int warp_sums[kThreads / 32];
 
   const PlanLayout &lay = a.lay;
@@ -113,25 +128,28 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
   for (int i = i0; i < i1; ++i)
     nfirst += (i == 0 || (keys[i] >> 16) != (keys[i - 1] >> 16)) ? 1 : 0;
   int n_u;
-  int u = block_scan_exclusive(nfirst, warp_sums, &n_u) - 1;
+  const int u_before = block_scan_exclusive(nfirst, warp_sums, &n_u) - 1;
 
   const int64_t stage = s * lay.n_stages + g;
   int32_t *uniq = a.uniq + stage * lay.L;
-  uint16_t *refmap = reinterpret_cast<uint16_t *>(a.records + stage * lay.rec_bytes + lay.off_refmap);
+  uint16_t *uo = a.uo + stage * lay.L;
+  unsigned char *crec = a.crecs + stage * lay.crec_bytes;
+  uint16_t *refmap = reinterpret_cast<uint16_t *>(crec + lay.off_refmap);
+  // pass 1: each distinct row's slot, offset and written flag; per-token overlap flags
+  int u = u_before;
   for (int i = i0; i < i1; ++i) {
     const uint32_t slot = (uint32_t)(keys[i] >> 16);
+    const int ref = (int)(keys[i] & 0xffffu);
     if (i == 0 || slot != (uint32_t)(keys[i - 1] >> 16)) {
       ++u;
       uniq[u] = (int32_t)slot;
+      const int o = u * lay.RB + ((ref_color(ref % WR, a.W, a.R) & lay.cmask) << 5);
+      uo_s[u] = (uint16_t)o;
+      uo[u] = (uint16_t)o;
     }
-    const int ref = (int)(keys[i] & 0xffffu);
-    refmap[ref] = (uint16_t)u;
     if (ref % WR < a.W) {
-      // bit 0: written in this stage; bit 1: written by the stage's last token (such rows
-      // can only be written back once the whole stage is done).  A row's refs may be
-      // split between threads, hence the word-wide atomic OR.
-      const uint32_t bits = (ref / WR == nt - 1) ? 3u : 1u;
-      atomicOr(reinterpret_cast<unsigned int *>(wr + (u & ~3)), bits << (8 * (u & 3)));
+      // a row's refs may be split between threads, hence the word-wide atomic OR
+      atomicOr(reinterpret_cast<unsigned int *>(wr + (u & ~3)), 1u << (8 * (u & 3)));
       // a token's refs to one row are adjacent in (slot, ref) order, its write before its
       // read: a read ref of the same token right after this write ref means overlap
       if (i + 1 < L && (keys[i + 1] >> 16) == slot) {
@@ -141,8 +159,24 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
     }
   }
   __syncthreads();
-  uint8_t *tf = a.records + stage * lay.rec_bytes + lay.off_tokflag;
+  // pass 2: every reference gets its row's offset
+  u = u_before;
+  for (int i = i0; i < i1; ++i) {
+    if (i == 0 || (keys[i] >> 16) != (keys[i - 1] >> 16)) ++u;
+    refmap[keys[i] & 0xffffu] = uo_s[u];
+  }
+  uint8_t *tf = crec + lay.off_tokflag;
   for (int i = tid; i < nt; i += kThreads) tf[i] = tokflag[i];
+  // the stage's weights and gates, next to the offsets, so that the write/read kernel
+  // fetches everything its compute warps read per stage with one contiguous copy
+  float *wts = reinterpret_cast<float *>(crec + lay.off_wts);
+  for (int i = tid; i < L; i += kThreads) {
+    const int64_t row = (b * a.T + t0 + i / WR) * a.H + h;
+    const int j = i % WR;
+    wts[i] = j < a.W ? a.wt[0][row * a.W + j] : a.wt[1][row * a.R + (j - a.W)];
+  }
+  float *gts = reinterpret_cast<float *>(crec + lay.off_gates);
+  for (int i = tid; i < 2 * nt; i += kThreads) gts[i] = a.gates[((b * a.T + t0 + i / 2) * a.H + h) * 2 + (i & 1)];
   uint8_t *written = a.written + stage * lay.L;
   for (int i = tid; i < n_u; i += kThreads) written[i] = wr[i];
   if (tid == 0) a.nuniq[stage] = n_u;
@@ -151,9 +185,12 @@ __global__ void __launch_bounds__(kThreads) plan_sort_kernel(const __grid_consta
 __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_constant__ PlanArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const PlanLayout &lay = a.lay;
-  int32_t *prev = reinterpret_cast<int32_t *>(smem);       // [L]
-  int32_t *next = prev + lay.L;                             // [L]
-  int32_t *prev2 = next + lay.L;                            // [L]
+  int32_t *prev = reinterpret_cast<int32_t *>(smem);       // [L] slots of stage g-1
+  int32_t *prev2 = prev + lay.L;                            // [L] g-2
+  int32_t *next = prev2 + lay.L;                            // [L] g+1
+  int32_t *next2 = next + lay.L;                            // [L] g+2
+  uint16_t *uo_prev = reinterpret_cast<uint16_t *>(next2 + lay.L);   // [L]
+  uint16_t *uo_prev2 = uo_prev + lay.L;                              // [L]
   __shared__ int warp_sums[kThreads / 32];
 
   const int g = blockIdx.x;
@@ -162,78 +199,75 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
   const int64_t stage = s * S + g;
   const int tid = threadIdx.x;
   const int n_prev = g > 0 ? a.nuniq[stage - 1] : 0;
+  const int n_prev2 = g > 1 ? a.nuniq[stage - 2] : 0;
   const int n_cur = a.nuniq[stage];
   const int n_next = g + 1 < S ? a.nuniq[stage + 1] : 0;
-  const int n_prev2 = g > 1 ? a.nuniq[stage - 2] : 0;
-  for (int i = tid; i < n_prev2; i += kThreads) prev2[i] = a.uniq[(stage - 2) * lay.L + i];
-  for (int i = tid; i < n_prev; i += kThreads) prev[i] = a.uniq[(stage - 1) * lay.L + i];
+  const int n_next2 = g + 2 < S ? a.nuniq[stage + 2] : 0;
+  for (int i = tid; i < n_prev; i += kThreads) {
+    prev[i] = a.uniq[(stage - 1) * lay.L + i];
+    uo_prev[i] = a.uo[(stage - 1) * lay.L + i];
+  }
+  for (int i = tid; i < n_prev2; i += kThreads) {
+    prev2[i] = a.uniq[(stage - 2) * lay.L + i];
+    uo_prev2[i] = a.uo[(stage - 2) * lay.L + i];
+  }
   for (int i = tid; i < n_next; i += kThreads) next[i] = a.uniq[(stage + 1) * lay.L + i];
+  for (int i = tid; i < n_next2; i += kThreads) next2[i] = a.uniq[(stage + 2) * lay.L + i];
   __syncthreads();
 
   const int32_t *cur = a.uniq + stage * lay.L;
+  const uint16_t *uo_cur = a.uo + stage * lay.L;
   const uint8_t *written = a.written + stage * lay.L;
   const int ept = (n_cur + kThreads - 1) / kThreads;
   const int u0 = min(n_cur, tid * ept), u1 = min(n_cur, u0 + ept);
-  // A row loaded here that stage g-2 also held may have been written back at the end of
-  // stage g-2, which the write/read kernel only waits for late: such loads go last.
-  // Write-backs are listed rows-the-last-token-did-not-write first: the kernel stores
-  // those while the stage's last token still runs, the rest ("wb late") after it.
-  int c_load = 0, c_late = 0, c_carry = 0, c_wb = 0, c_wbl = 0;
+  // The bank may be stale for a row that one of the two previous stages holds (their
+  // write-backs come later), so such a row is copied from that stage's buffer: from
+  // stage g-1's if it holds the row (carry 1), else from stage g-2's (carry 2).  Any
+  // other row is read from the bank, after every older stage's write-back.  A row goes
+  // back to the bank after this stage if it is dirty here (written, or carried in) and
+  // neither of the next two stages carries it on.
+  int c_load = 0, c_c1 = 0, c_c2 = 0, c_wb = 0;
   for (int u = u0; u < u1; ++u) {
     const int32_t slot = cur[u];
-    const int src = find_sorted(prev, n_prev, slot);
-    const bool out = find_sorted(next, n_next, slot) >= 0;
-    const bool late = src < 0 && find_sorted(prev2, n_prev2, slot) >= 0;
-    c_load += src < 0 && !late;
-    c_late += late;
-    c_carry += src >= 0;
-    const bool wb = (written[u] || src >= 0) && !out;
-    c_wb += wb && !(written[u] & 2);
-    c_wbl += wb && (written[u] & 2);
+    const bool in1 = find_sorted(prev, n_prev, slot) >= 0;
+    const bool in2 = !in1 && find_sorted(prev2, n_prev2, slot) >= 0;
+    const bool out = find_sorted(next, n_next, slot) >= 0 || find_sorted(next2, n_next2, slot) >= 0;
+    c_load += !in1 && !in2;
+    c_c1 += in1;
+    c_c2 += in2;
+    c_wb += (written[u] || in1 || in2) && !out;
   }
-  int n_load, n_late, n_carry, n_wb_early, n_wb_late;
+  int n_load, n_c1, n_c2, n_wb;
   int o_load = block_scan_exclusive(c_load, warp_sums, &n_load);
-  int o_late = n_load + block_scan_exclusive(c_late, warp_sums, &n_late);
-  int o_carry = block_scan_exclusive(c_carry, warp_sums, &n_carry);
-  int o_wb = block_scan_exclusive(c_wb, warp_sums, &n_wb_early);
-  int o_wbl = n_wb_early + block_scan_exclusive(c_wbl, warp_sums, &n_wb_late);
-  const int n_wb = n_wb_early + n_wb_late;
+  int o_c1 = n_load + block_scan_exclusive(c_c1, warp_sums, &n_c1);
+  int o_c2 = n_load + n_c1 + block_scan_exclusive(c_c2, warp_sums, &n_c2);
+  int o_wb = block_scan_exclusive(c_wb, warp_sums, &n_wb);
 
-  unsigned char *rec = a.records + stage * lay.rec_bytes;
-  int32_t *load_slot = reinterpret_cast<int32_t *>(rec + lay.off_load_slot);
-  uint16_t *load_u = reinterpret_cast<uint16_t *>(rec + lay.off_load_u);
-  uint32_t *carry = reinterpret_cast<uint32_t *>(rec + lay.off_carry);
-  int32_t *wb_slot = reinterpret_cast<int32_t *>(rec + lay.off_wb_slot);
-  uint16_t *wb_u = reinterpret_cast<uint16_t *>(rec + lay.off_wb_u);
+  unsigned char *lrec = a.lrecs + stage * lay.lrec_bytes;
+  uint2 *ent = reinterpret_cast<uint2 *>(lrec + lay.off_ent);
+  uint2 *wb = reinterpret_cast<uint2 *>(lrec + lay.off_wb);
   for (int u = u0; u < u1; ++u) {
     const int32_t slot = cur[u];
-    const int src = find_sorted(prev, n_prev, slot);
-    const bool out = find_sorted(next, n_next, slot) >= 0;
-    if (src < 0) {
-      const bool late = find_sorted(prev2, n_prev2, slot) >= 0;
-      int &o = late ? o_late : o_load;
-      load_slot[o] = slot;
-      load_u[o] = (uint16_t)u;
-      ++o;
+    const uint32_t row16 = (uint32_t)slot * a.pitch16;     // < 2^32 (checked on the host)
+    const int src1 = find_sorted(prev, n_prev, slot);
+    const int src2 = src1 < 0 ? find_sorted(prev2, n_prev2, slot) : -1;
+    const bool out = find_sorted(next, n_next, slot) >= 0 || find_sorted(next2, n_next2, slot) >= 0;
+    if (src1 >= 0) {
+      ent[o_c1++] = make_uint2((uint32_t)uo_cur[u] | ((uint32_t)uo_prev[src1] << 16), 0u);
+    } else if (src2 >= 0) {
+      ent[o_c2++] = make_uint2((uint32_t)uo_cur[u] | ((uint32_t)uo_prev2[src2] << 16), 0u);
     } else {
-      carry[o_carry] = (uint32_t)u | ((uint32_t)src << 16);
-      ++o_carry;
+      ent[o_load++] = make_uint2(row16, uo_cur[u]);
     }
-    if ((written[u] || src >= 0) && !out) {
-      int &o = (written[u] & 2) ? o_wbl : o_wb;
-      wb_slot[o] = slot;
-      wb_u[o] = (uint16_t)u;
-      ++o;
-    }
+    if ((written[u] || src1 >= 0 || src2 >= 0) && !out) wb[o_wb++] = make_uint2(row16, uo_cur[u]);
   }
   if (tid == 0) {
-    int32_t *hdr = reinterpret_cast<int32_t *>(rec);
+    int32_t *hdr = reinterpret_cast<int32_t *>(lrec);
     hdr[0] = n_cur;
-    hdr[1] = n_load + n_late;
-    hdr[2] = n_carry;
-    hdr[3] = n_wb;
-    hdr[4] = n_late;
-    hdr[5] = n_wb_late;
+    hdr[1] = n_load;
+    hdr[2] = n_c1;
+    hdr[3] = n_c2;
+    hdr[4] = n_wb;
   }
 }
 
@@ -241,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
 
 cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int P, cudaStream_t st) {
   if (streams == 0 || a.lay.n_stages == 0) return cudaSuccess;
-  const int64_t smem = (int64_t)P * 8 + ((P + 3) & ~3) + a.lay.G;
+  const int64_t smem = (int64_t)P * 8 + ((P + 3) & ~3) + (int64_t)P * 2 + a.lay.G;
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(plan_sort_kernel), smem);
   if (e != cudaSuccess) return e;
   plan_sort_kernel<<<dim3((unsigned)a.lay.n_stages, (unsigned)streams), kThreads, smem, st>>>(a, P);
@@ -250,7 +284,7 @@ cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int P, cudaStre
 
 cudaError_t launch_plan_link(const PlanArgs &a, int64_t streams, cudaStream_t st) {
   if (streams == 0 || a.lay.n_stages == 0) return cudaSuccess;
-  const int64_t smem = (int64_t)a.lay.L * 12;
+  const int64_t smem = (int64_t)a.lay.L * 20;
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(plan_link_kernel), smem);
   if (e != cudaSuccess) return e;
   plan_link_kernel<<<dim3((unsigned)a.lay.n_stages, (unsigned)streams), kThreads, smem, st>>>(a);

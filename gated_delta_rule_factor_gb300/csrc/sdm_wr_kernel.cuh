@@ -3,24 +3,36 @@
 //
 // Parallel axes: streams (b, h) are independent, and so is every bank column (the
 // update of a column reads only that column, see sdm_delta.cuh).  One CTA owns one
-// stream and a slice of CW columns (CW * elem = 16..128 bytes of every row) and runs
-// the stream's tokens in order.  Tokens are staged G at a time; the chunk plan
-// (sdm_plan.cu) lists the distinct rows of each stage.
+// stream and a slice of RB = 32*NCW bytes of every row; each of its NCW compute warps
+// owns a 32-byte piece of that slice and runs the stream's tokens in order on it, with
+// no synchronisation between compute warps.  Tokens are staged G at a time; the chunk
+// plan (sdm_plan.cu) lists the distinct rows of each stage.
 //
-// Warp roles (one CTA):
-//   2 compute warps: the tokens of the current stage on the shared-memory rows, with the
-//               block-ordered token step (sdm_delta.cuh token_blocks2);
-//   8 loader warps (4 when two CTAs share an SM): fetch the next stage's rows, its token data and the stage record
-//               after it, all with 16-byte cp.async on the LSU path (a bulk/TMA copy per
-//               row slice costs more than it saves at this granularity); once the compute
-//               warps signal (barrier 5) that the current stage's next-to-last token is
-//               done, write back the current stage's dirty rows its last token leaves
-//               alone, and after the stage the rest of them, while the next stage's rows
-//               are still landing.  More loader warps keep more row requests in flight.
-//   every warp copies the rows carried over from the previous stage.
-// Two row buffers alternate between stages; rows shared by consecutive stages are
-// copied across buffers instead of re-read, because the bank copy may be stale.  Stage
-// records use three buffers (in use / rows being fetched / record being fetched).
+// Pipeline.  Three row buffers (stage g uses buffer g % 3), each with the stage's
+// per-reference offsets and token data (weights, gates, value slice); a ring of five
+// row-list records (stages g-1 .. g+3 of loader iteration g).  Three mbarriers per
+// buffer:
+//   full[b]  stage g's bank rows, offsets and token data have landed (issued two stages
+//            ahead; every loader waits for its own copies, then one thread arrives);
+//   recs[b]  loader iteration g has made the row lists of stages g+1 and g+2 visible
+//            and finished reading stage g-1's buffer for its write-back (one arrival,
+//            after the loaders' barrier);
+//   done[b]  every compute warp has finished stage g and copied out of buffer g the
+//            rows stages g+1 and g+2 carry over (one arrival per warp, after __syncwarp).
+// mbarrier arrivals are shared-memory atomics that serialize, so each is made once per
+// group of threads that a barrier or __syncwarp has already ordered.
+// Loader iteration g: fetch the row lists of stage g+3; wait done[g-1] and write stage
+// g-1's dirty rows back; arrive on recs; fetch stage g+2's bank rows into buffer
+// (g+2) % 3 (stage g-1's, now free); wait until stage g+1's rows have landed and
+// arrive on full.  (A cp.async-tracked mbarrier arrival per thread measured as costly
+// as waiting for the copies.)  Compute warps, stage g: wait full[g], run the
+// tokens, wait recs(g), copy this stage's rows that stage g+1 (carry 1) or stage g+2
+// (carry 2, rows g+1 does not hold) needs into their buffers, arrive on done.  The
+// bank is never read stale: a row one of the two previous stages holds is carried in
+// shared memory, and any older row was written back before the fetch.  No memory round
+// trip lies between one stage's end and the next stage's start.  Every wait is bounded
+// (2 s of %globaltimer); a wait that runs out records SDM_DEVERR_TIMEOUT and sets a
+// shared abort flag that every other wait also watches.
 #pragma once
 
 #include "sdm_common.cuh"
@@ -30,280 +42,376 @@
 namespace sdm {
 namespace wr {
 
+constexpr int kRowBufs = 3;      // row / compute-record / token-data buffers
+constexpr int kLoaderRecs = 5;   // loader records: stages g-1 .. g+3 of loader iteration g
 
-struct TokLayout {
-  int64_t wts, gates, v, bytes;  // offsets inside one token-data buffer
-};
-
+// Value slice of a stage's tokens (the only per-CTA token data; weights and gates come
+// with the compute record).  cols: the CTA's bank columns (RB / bank element bytes).
 __host__ __device__ inline int64_t align16(int64_t x) { return (x + 15) & ~int64_t(15); }
-
-__host__ __device__ inline TokLayout tok_layout(int G, int W, int R, int CW, int act_elem) {
-  TokLayout t;
-  t.wts = 0;
-  t.gates = align16((int64_t)G * (W + R) * 4);
-  t.v = t.gates + align16((int64_t)G * 2 * 4);
-  t.bytes = t.v + align16((int64_t)G * CW * act_elem);
-  return t;
+__host__ __device__ inline int64_t vals_bytes(int G, int cols, int act_elem) {
+  return align16((int64_t)G * cols * act_elem);
 }
 
-// A CTA owns a slice of CW columns (CW * elem = 16..128 bytes of every row): two compute
-// warps and LW loader warps (8 when one CTA runs per SM, 4 when two share an SM, so that
-// their registers fit).  Lane % 8 of a compute warp owns VB = CW / 8 consecutive columns.
-template <typename BANK, int CW, int LW_ = 8>
-struct WrGeometry {
-  static constexpr int VB = CW / 8;                   // columns per compute lane
-  static constexpr int RB = CW * (int)sizeof(BANK);   // row slice bytes
-  static constexpr int NCW = 2;                       // compute warps (rows split)
-  static constexpr int LW = LW_;                      // loader warps
-  static constexpr int NTHR = 32 * (NCW + LW);
-  static_assert(CW % 8 == 0 && RB >= 16 && RB <= 128 && (RB & (RB - 1)) == 0, "column slice");
+struct SmemLayout {
+  int64_t rows, crec, tok, lrec, bars, bytes;
 };
 
-// JB = the most rows a compute lane holds (one of the 8 row blocks of a token);
-// FULL: W == R == 8 * JB, fixed at compile time.
-template <typename BANK, typename ACT, int CW, int JB, bool FULL = false, int LW = 8>
-__global__ void __launch_bounds__(WrGeometry<BANK, CW, LW>::NTHR)
-    write_read_kernel(const __grid_constant__ WriteReadArgs a) {
-  using Geo = WrGeometry<BANK, CW, LW>;
-  constexpr int kLoaderThreads = 32 * Geo::LW;
-  constexpr int VB = Geo::VB, NCW = Geo::NCW, NTHR = Geo::NTHR, RB = Geo::RB;
-  constexpr int CPR = RB / 16;                        // 16-byte chunks per row slice
+__host__ __device__ inline SmemLayout smem_layout(const PlanLayout &lay, int bank_elem, int act_elem) {
+  SmemLayout m;
+  m.rows = 0;
+  m.crec = m.rows + (int64_t)kRowBufs * lay.L * lay.RB;
+  m.tok = m.crec + kRowBufs * lay.crec_bytes;
+  m.lrec = m.tok + kRowBufs * vals_bytes(lay.G, lay.RB / bank_elem, act_elem);
+  m.bars = m.lrec + kLoaderRecs * lay.lrec_bytes;
+  m.bytes = m.bars + 3 * kRowBufs * 8 + 16;           // full[3], recs[3], done[3], flags
+  return m;
+}
 
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ __align__(16) float xch[2 * 2 * 8 * VB];  // the two compute warps' partial sums
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Arrives on `bar` once every cp.async this thread issued so far has completed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// cp.async without a compiler memory clobber, for the loaders' row copies: the compiler
+// may then batch the row-list reads around them.  The destination is read only after a
+// cp.async.wait_group and a barrier (both with memory clobbers), so no access that the
+// clobber would order is affected.
+__device__ __forceinline__ void cp_async16_rows(uint32_t dst_smem, const void *src_gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst_smem), "l"(src_gmem));
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pending() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Bounded wait for the phase of `bar` with the given parity that also gives up as soon
+// as another warp has set the abort flag.  false: gave up.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int32_t *abort_flag) {
+  const uint32_t addr = smem_addr(bar);
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 63) == 63) {
+      if (*abort_flag) return false;
+      const uint64_t now = global_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+template <int NCW, int LW>
+struct WrGeometry {
+  static constexpr int RB = 32 * NCW;                 // row slice bytes of the CTA
+  static constexpr int CPR = RB / 16;                 // 16-byte chunks per row slice
+  static constexpr int NL = 32 * LW;                  // loader threads
+  static constexpr int NTHR = 32 * (NCW + LW);
+  static_assert(NL % CPR == 0, "loader threads cover whole row slices");
+};
+
+// JB: the most rows a lane holds per sum (ceil(max(W, R) / 16)); FULL: W == R == 64.
+template <typename BANK, typename ACT, int NCW, int JB, bool FULL, int LW>
+__global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR)
+    write_read_kernel(const __grid_constant__ WriteReadArgs a) {
+  using Geo = WrGeometry<NCW, LW>;
+  constexpr int RB = Geo::RB, CPR = Geo::CPR, NL = Geo::NL;
+  constexpr int VEC = PieceRow<BANK>::VEC;            // columns per lane
+  constexpr int PC = 2 * VEC;                         // columns per warp piece
+  constexpr int COLS = NCW * PC;                      // columns per CTA
+  extern __shared__ __align__(128) unsigned char smem[];
+
   const PlanLayout &lay = a.lay;
   const int L = lay.L, G = lay.G, S = lay.n_stages;
   const int W = a.W, R = a.R, WR = W + R;
   const int64_t s = blockIdx.y;
   const int slice = blockIdx.x;
   const int64_t b = s / a.H, h = s % a.H;
-  const int64_t c0 = (int64_t)slice * CW;
+  const int64_t c0 = (int64_t)slice * COLS;                   // first column of the slice
+  const int valid_chunks = min(CPR, (a.row_bytes - slice * RB) / 16);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool is_loader = warp >= NCW;
 
-  // Buffer addresses are computed, not kept in an indexed array, so that they stay
-  // shared-memory addresses for the compiler.
-  auto rowbuf = [&](int i) -> unsigned char * { return smem + (int64_t)(i & 1) * L * RB; };
-  unsigned char *plans = smem + 2 * (int64_t)L * RB;
-  const TokLayout tl = tok_layout(G, W, R, CW, (int)sizeof(ACT));
-  auto tokbuf = [&](int i) -> unsigned char * { return plans + 3 * lay.rec_bytes + (int64_t)(i & 1) * tl.bytes; };
+  const SmemLayout sl = smem_layout(lay, (int)sizeof(BANK), (int)sizeof(ACT));
+  const int64_t vbytes = vals_bytes(G, COLS, (int)sizeof(ACT));
+  auto rowbuf = [&](int g) -> unsigned char * { return smem + sl.rows + (int64_t)(g % kRowBufs) * L * RB; };
+  auto crecbuf = [&](int g) -> unsigned char * { return smem + sl.crec + (int64_t)(g % kRowBufs) * lay.crec_bytes; };
+  auto tokbuf = [&](int g) -> unsigned char * { return smem + sl.tok + (int64_t)(g % kRowBufs) * vbytes; };
+  auto lrecbuf = [&](int g) -> unsigned char * { return smem + sl.lrec + (int64_t)(g % kLoaderRecs) * lay.lrec_bytes; };
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + sl.bars);
+  uint64_t *recs = full + kRowBufs;
+  uint64_t *done = recs + kRowBufs;
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(done + kRowBufs);
+  volatile int32_t *loader_go = abort_flag + 1;                 // written by loader thread 0 only
 
   BANK *bank = static_cast<BANK *>(a.bank) + s * a.N * a.d_v;   // this stream's table
-  const ACT *kv = static_cast<const ACT *>(a.k_val);
-  ACT *y = static_cast<ACT *>(a.y);
-  const unsigned char *records = a.records + s * (int64_t)S * lay.rec_bytes;
-
-  auto plan_of = [&](int g) -> unsigned char * { return plans + (int64_t)(g % 3) * lay.rec_bytes; };
-  auto hdr_ok = [&](const int32_t *hdr) -> bool {
-    return hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[1] <= L && hdr[2] >= 0 && hdr[2] <= L &&
-           hdr[3] >= 0 && hdr[3] <= L && hdr[4] >= 0 && hdr[4] <= hdr[1] && hdr[5] >= 0 && hdr[5] <= hdr[3];
-  };
-
-  constexpr int VBYTES = CW * (int)sizeof(ACT);      // value bytes per token (>= 16)
-
-  // ---- loader helpers (threads of the loader warps).  Every copy is a 16-byte cp.async
-  // (or 8/4-byte for the gates and unaligned weights) on the LSU path: CPR lanes take
-  // one row slice, so one warp request covers whole 128-byte lines.
-  const int ltid = tid - 32 * NCW;
-  const int sub = ltid % CPR, grp = ltid / CPR;       // chunk of a row, row group
-  constexpr int GRP = kLoaderThreads / CPR;           // row slices per loader pass
+  const unsigned char *lrecs = a.lrecs + s * (int64_t)S * lay.lrec_bytes;
+  const unsigned char *crecs = a.crecs + s * (int64_t)S * lay.crec_bytes;
   const int64_t row_pitch = a.d_v * (int64_t)sizeof(BANK);
-  auto fetch_record = [&](int g) {
-    const unsigned char *src = records + (int64_t)g * lay.rec_bytes;
-    unsigned char *dst = plan_of(g);
-    for (int64_t i = ltid; i < lay.rec_bytes / 16; i += kLoaderThreads) cp_async16(dst + i * 16, src + i * 16);
-  };
-  // Rows of stage g's load list with index in [lo, hi) (the last hdr[4] entries are the
-  // rows of stage g-2, which must wait for that stage's write-back).
-  auto fetch_rows = [&](int g, bool early, bool late) {
-    const unsigned char *rec = plan_of(g);
-    const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
-    const int n_load = hdr_ok(hdr) ? hdr[1] : 0;
-    const int n_late = hdr_ok(hdr) ? hdr[4] : 0;
-    const int lo = early ? 0 : n_load - n_late, hi = late ? n_load : n_load - n_late;
-    const int32_t *load_slot = reinterpret_cast<const int32_t *>(rec + lay.off_load_slot);
-    const uint16_t *load_u = reinterpret_cast<const uint16_t *>(rec + lay.off_load_u);
-    unsigned char *dst = rowbuf(g & 1) + sub * 16;
-    const unsigned char *src = reinterpret_cast<const unsigned char *>(bank + c0) + sub * 16;
-#pragma unroll 4
-    for (int e = lo + grp; e < hi; e += GRP) {
-      const int32_t slot = load_slot[e];
-      const int u = load_u[e];
-      if (u >= L || slot < 0 || slot >= a.N) {
-        raise_error(a.err, SDM_DEVERR_PLAN);
-        continue;
-      }
-      cp_async16(dst + (int64_t)u * RB, src + (int64_t)slot * row_pitch);
-    }
-  };
-  auto fetch_tokens = [&](int g) {
-    const int64_t t0 = (int64_t)g * G;
-    const int nt = (int)min((int64_t)G, a.T - t0);
-    unsigned char *tb = tokbuf(g & 1);
-    float *wts = reinterpret_cast<float *>(tb + tl.wts);
-    if (a.tok_bulk) {                                  // weights in 16-byte pieces
-      const int wq = W / 4, rq = R / 4;
-      for (int i = ltid; i < nt * (wq + rq); i += kLoaderThreads) {
-        const int t = i / (wq + rq), q = i % (wq + rq);
-        const int64_t row = (b * a.T + t0 + t) * a.H + h;
-        if (q < wq) cp_async16(wts + t * WR + 4 * q, a.wt[0] + row * W + 4 * q);
-        else cp_async16(wts + t * WR + W + 4 * (q - wq), a.wt[1] + row * R + 4 * (q - wq));
-      }
-    } else {
-      for (int i = ltid; i < nt * WR; i += kLoaderThreads) {
-        const int t = i / WR, j = i % WR;
-        const int64_t row = (b * a.T + t0 + t) * a.H + h;
-        const float *src_w = (j < W) ? a.wt[0] + row * W + j : a.wt[1] + row * R + (j - W);
-        cp_async4(wts + i, src_w);
-      }
-    }
-    float *gt = reinterpret_cast<float *>(tb + tl.gates);
-    for (int i = ltid; i < nt; i += kLoaderThreads) {
-      const int64_t row = (b * a.T + t0 + i) * a.H + h;
-      cp_async8(gt + 2 * i, a.gates + row * 2);
-    }
-    unsigned char *vb = tb + tl.v;
-    for (int i = ltid; i < nt * (VBYTES / 16); i += kLoaderThreads) {
-      const int t = i / (VBYTES / 16), c = i % (VBYTES / 16);
-      const int64_t row = (b * a.T + t0 + t) * a.H + h;
-      cp_async16(vb + (int64_t)t * VBYTES + c * 16,
-                 reinterpret_cast<const unsigned char *>(kv + row * a.d_v + c0) + c * 16);
-    }
-  };
-  // Dirty rows of stage g back to the bank (CPR lanes per row slice, 16-byte stores).
-  // Dirty rows of stage g back to the bank: early = the rows its last token does not
-  // write (stored while that token runs), late = the rest (stored after the stage).
-  auto write_back = [&](int g, bool early) {
-    const unsigned char *rec = plan_of(g);
-    const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
-    const bool ok = hdr_ok(hdr);
-    const int n_all = ok ? hdr[3] : 0, n_late = ok ? hdr[5] : 0;
-    const int lo = early ? 0 : n_all - n_late, n_wb = early ? n_all - n_late : n_all;
-    const int32_t *wb_slot = reinterpret_cast<const int32_t *>(rec + lay.off_wb_slot);
-    const uint16_t *wb_u = reinterpret_cast<const uint16_t *>(rec + lay.off_wb_u);
-    const unsigned char *src = rowbuf(g & 1) + sub * 16;
-    unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + sub * 16;
-#pragma unroll 4
-    for (int e = lo + grp; e < n_wb; e += GRP) {
-      const int32_t slot = wb_slot[e];
-      const int u = wb_u[e];
-      if (u >= L || slot < 0 || slot >= a.N) {
-        raise_error(a.err, SDM_DEVERR_PLAN);
-        continue;
-      }
-      *reinterpret_cast<uint4 *>(dst + (int64_t)slot * row_pitch) = *reinterpret_cast<const uint4 *>(src + (int64_t)u * RB);
-    }
-  };
+  const int64_t row_limit = (int64_t)L * RB;                    // offsets o must stay below
 
-  auto fetch_stage = [&](int g) {
-    fetch_rows(g, true, true);
-    fetch_tokens(g);
-  };
-  // ---- prologue: record 0, then stage 0 and record 1
-  if (is_loader) {
-    fetch_record(0);
-    cp_async_commit();
-    cp_async_wait_all();
-    named_barrier(1, kLoaderThreads);
-    fetch_stage(0);
-    if (S > 1) fetch_record(1);
-    cp_async_commit();
+  if (tid == 0) {
+    for (int i = 0; i < kRowBufs; ++i) {
+      mbar_init(&full[i], 1);      // loader thread 0, after the loaders' copies landed
+      mbar_init(&recs[i], 1);      // loader thread 0, after the loader barrier
+      mbar_init(&done[i], NCW);    // lane 0 of each compute warp, after __syncwarp
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
   }
+  __syncthreads();
+  if (S == 0) return;
 
-  for (int g = 0; g < S; ++g) {
-    if (is_loader) cp_async_wait_all();
-    named_barrier(2, NTHR);                                      // stage g resident
-    const unsigned char *rec = plan_of(g);
-    {
-      // rows shared with stage g-1 come from its buffer (the bank may still be stale);
-      // every warp of the CTA copies
+  if (is_loader) {
+    // ------------------------------------------------------------------ loaders
+    const int lt = tid - 32 * NCW;
+    const int sub = lt % CPR, grp = lt / CPR;          // chunk of a row slice, row group
+    constexpr int GRP = NL / CPR;                      // row slices per loader pass
+    const unsigned char *bank_slice = reinterpret_cast<const unsigned char *>(bank + c0) + sub * 16;
+    auto loader_bar = [&] { named_barrier(1, NL); };
+    const int lrec_chunks = (int)(lay.lrec_bytes / 16), crec_chunks = (int)(lay.crec_bytes / 16);
+    auto fetch_lrec = [&](int g) {
+      const unsigned char *src = lrecs + (int64_t)g * lay.lrec_bytes;
+      unsigned char *dst = lrecbuf(g);
+      for (int i = lt; i < lrec_chunks; i += NL) cp_async16(dst + i * 16, src + i * 16);
+    };
+    auto hdr_ok = [&](const int32_t *hdr) {
+      return hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[2] >= 0 && hdr[3] >= 0 &&
+             hdr[1] + hdr[2] + hdr[3] == hdr[0] && hdr[4] >= 0 && hdr[4] <= L;
+    };
+    // Row offsets (16-byte units) must stay inside the stream's table, shared-memory
+    // offsets inside the stage buffer; a bad entry is skipped and reported.
+    const uint32_t lim16 = (uint32_t)((uint64_t)a.N * (uint64_t)row_pitch / 16);
+    const uint32_t olim = (uint32_t)row_limit;
+    const uint32_t sub16 = (uint32_t)sub << 4;
+    // stage g's bank rows (the first n_load row-list entries)
+    auto fetch_rows = [&](int g) {
+      const unsigned char *rec = lrecbuf(g);
       const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
       const bool ok = hdr_ok(hdr);
-      if (!ok && tid == 0) raise_error(a.err, SDM_DEVERR_PLAN);
-      const int n_carry = ok ? hdr[2] : 0;
-      const uint32_t *carry = reinterpret_cast<const uint32_t *>(rec + lay.off_carry);
-      const unsigned char *from = rowbuf((g + 1) & 1);
-      unsigned char *to = rowbuf(g & 1);
-      for (int i = tid; i < n_carry * CPR; i += NTHR) {
-        const int e = i / CPR, c = i % CPR;
-        const int u = carry[e] & 0xffff, src = carry[e] >> 16;
-        if (u >= L || src >= L) {
-          raise_error(a.err, SDM_DEVERR_PLAN);
-          continue;
-        }
-        *reinterpret_cast<uint4 *>(to + (int64_t)u * RB + c * 16) =
-            *reinterpret_cast<const uint4 *>(from + (int64_t)src * RB + c * 16);
+      if (!ok && lt == 0) raise_error(a.err, SDM_DEVERR_PLAN);
+      const int n_load = ok ? hdr[1] : 0;
+      const uint2 *ent = reinterpret_cast<const uint2 *>(rec + lay.off_ent);
+      const uint32_t dst = smem_addr(rowbuf(g));
+      if (sub >= valid_chunks) return;
+#pragma unroll 4
+      for (int e = grp; e < n_load; e += GRP) {
+        const uint2 v = ent[e];
+        if (v.x < lim16 && v.y < olim) cp_async16_rows(dst + (v.y ^ sub16), bank_slice + (size_t)v.x * 16);
+        else raise_error(a.err, SDM_DEVERR_PLAN);
       }
-    }
-    named_barrier(3, NTHR);                                      // carries in place
-
-    if (!is_loader) {
-      // ---- compute: tokens of stage g in order; both compute warps work on the same
-      // column groups, the token's row blocks split between them (token_blocks2); warp 0
-      // stores y
-      const uint16_t *refmap = reinterpret_cast<const uint16_t *>(rec + lay.off_refmap);
-      const uint8_t *tokflag = rec + lay.off_tokflag;
-      const unsigned char *tb = tokbuf(g);
-      const float *wts = reinterpret_cast<const float *>(tb + tl.wts);
-      const float *gt = reinterpret_cast<const float *>(tb + tl.gates);
-      const ACT *vv = reinterpret_cast<const ACT *>(tb + tl.v);
-      const int cl = lane & 7;                                 // column group in the slice
-      unsigned char *rows = rowbuf(g) + cl * VB * (int)sizeof(BANK);
+    };
+    // stage g's compute record (offsets, flags, weights, gates: one contiguous copy) and
+    // this slice's values of its tokens.  Each thread's share of the values is the same
+    // every stage: worked out once.
+    constexpr int VCH = COLS * (int)sizeof(ACT) / 16;                      // value chunks per token
+    const int vch = (int)min((int64_t)VCH, (a.d_v - c0) * (int64_t)sizeof(ACT) / 16);
+    const int tv_t = lt / VCH, tv_c = lt % VCH;
+    const ACT *kv = static_cast<const ACT *>(a.k_val);
+    auto fetch_stage_data = [&](int g) {
+      const unsigned char *src = crecs + (int64_t)g * lay.crec_bytes;
+      unsigned char *dst = crecbuf(g);
+      for (int i = lt; i < crec_chunks; i += NL) cp_async16(dst + i * 16, src + i * 16);
       const int64_t t0 = (int64_t)g * G;
       const int nt = (int)min((int64_t)G, a.T - t0);
-      ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + cl * VB;
-      const int64_t ystep = (int64_t)a.H * a.d_v;
-      if (nt <= 1) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);
-      for (int t = 0; t < nt; ++t) {
-        float v[VB], out[VB];
-        load_vec<ACT, VB>(vv + t * CW + cl * VB, v);
-        token_blocks2<BANK, VB, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, gt[2 * t], gt[2 * t + 1], v, rows,
-                                          RB, tokflag[t] != 0, out, xch, xch + 2 * 8 * VB, warp, 6);
-        if (warp == 0 && lane < 8) store_vec<ACT, VB>(ybase + t * ystep, out);
-        __syncwarp();
-        if (t == nt - 2) named_barrier_arrive(5, kLoaderThreads + 32 * NCW);  // rows the last token leaves alone are final
+      if (tv_c < vch) {
+        unsigned char *vb = tokbuf(g) + tv_c * 16;
+        const unsigned char *kvs = reinterpret_cast<const unsigned char *>(kv + c0) + tv_c * 16;
+        const int64_t tstep = (int64_t)a.H * a.d_v * (int64_t)sizeof(ACT);
+        const unsigned char *src_t = kvs + ((b * a.T + t0) * a.H + h) * a.d_v * (int64_t)sizeof(ACT);
+        for (int t = tv_t; t < nt; t += NL / VCH)
+          cp_async16(vb + (int64_t)t * COLS * sizeof(ACT), src_t + (int64_t)t * tstep);
       }
-    } else {
-      // ---- loaders: fetch stage g+1 into its buffer (stage g-1's, fully written back at
-      // the end of that stage) and record g+2, then store the rows of stage g its last
-      // token leaves alone once the compute warps are past its next-to-last token
-      if (g + 1 < S) fetch_stage(g + 1);
-      if (g + 2 < S) fetch_record(g + 2);
+    };
+    auto write_back = [&](int g) {
+      const unsigned char *rec = lrecbuf(g);
+      const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+      const int n_wb = hdr_ok(hdr) ? hdr[4] : 0;
+      const uint2 *wb = reinterpret_cast<const uint2 *>(rec + lay.off_wb);
+      const unsigned char *src = rowbuf(g);
+      unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + sub * 16;
+      if (sub >= valid_chunks) return;
+#pragma unroll 4
+      for (int e = grp; e < n_wb; e += GRP) {
+        const uint2 v = wb[e];
+        if (v.x < lim16 && v.y < olim)
+          *reinterpret_cast<uint4 *>(dst + (size_t)v.x * 16) = *reinterpret_cast<const uint4 *>(src + (v.y ^ sub16));
+        else raise_error(a.err, SDM_DEVERR_PLAN);
+      }
+    };
+    // Waits for the compute warps to finish stage g (one thread waits, all loaders learn
+    // the outcome at the loader barrier); false: give up.
+    // (The decision is published in loader_go, which only this thread writes, so that
+    // every loader reads the same value even if a compute warp raises the abort flag
+    // meanwhile; the next write of loader_go comes after another loader barrier.)
+    auto wait_done = [&](int g) -> bool {
+      if (lt == 0) {
+        bool ok = !*abort_flag && wait_phase(&done[g % kRowBufs], (uint32_t)(g / kRowBufs) & 1u, abort_flag);
+        if (!ok && !*abort_flag) {
+          raise_error(a.err, SDM_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        *loader_go = ok ? 1 : 0;
+      }
+      loader_bar();
+      return *loader_go != 0;
+    };
+
+    // prologue: row lists 0..2, then the bank rows of stages 0 and 1
+    for (int g = 0; g < 3 && g < S; ++g) fetch_lrec(g);
+    cp_async_commit();
+    cp_async_wait_all();
+    loader_bar();
+    for (int g = 0; g < 2; ++g) {
+      if (g < S) {
+        fetch_rows(g);
+        fetch_stage_data(g);
+      }
       cp_async_commit();
-      named_barrier(5, kLoaderThreads + 32 * NCW);             // stage g's next-to-last token done
-      write_back(g, true);
     }
-    named_barrier(4, NTHR);                                      // stage g computed
-    // the rest of stage g's dirty rows go back while the next stage's rows land; the next
-    // stage barrier orders these stores before any later load of the same rows
-    if (is_loader) write_back(g, false);
+    cp_async_wait_pending<1>();                                  // stage 0 landed
+    loader_bar();
+    if (lt == 0) mbar_arrive(&full[0]);
+
+    // Iteration g.  Group order: A(g) = row lists of stage g+3, R(g) = stage g+2's rows.
+    bool alive = true;
+    for (int g = 0; g < S; ++g) {
+      if (g + 3 < S) fetch_lrec(g + 3);
+      cp_async_commit();                                         // A(g)
+      if (g >= 1) {
+        alive = wait_done(g - 1);
+        if (!alive) break;
+        write_back(g - 1);
+      }
+      cp_async_wait_pending<2>();                                // A(g-1): row lists of stage g+2
+      loader_bar();                                              // write-back reads done; lists visible
+      if (g + 1 < S && lt == 0) mbar_arrive(&recs[g % kRowBufs]);
+      if (g + 2 < S) {
+        fetch_rows(g + 2);
+        fetch_stage_data(g + 2);
+      }
+      cp_async_commit();                                         // R(g)
+      cp_async_wait_pending<1>();                                // R(g-1): stage g+1 landed
+      loader_bar();
+      if (g + 1 < S && lt == 0) mbar_arrive(&full[(g + 1) % kRowBufs]);
+    }
+    if (alive && wait_done(S - 1)) write_back(S - 1);
+    cp_async_wait_all();
+    return;
+  }
+
+  // -------------------------------------------------------------------- compute warps
+  const int rg = lane >> 1, c = lane & 1;
+  const uint32_t wc = ((uint32_t)warp << 5) | ((uint32_t)c << 4);
+  const int col = warp * PC + c * VEC;                           // this lane's first column in the slice
+  const bool lane_valid = (2 * warp + c) < valid_chunks;
+  ACT *y = static_cast<ACT *>(a.y);
+  const int64_t ystep = (int64_t)a.H * a.d_v;
+  // every lane waits (and acquires what the barrier publishes); the warp gives up as one.
+  // (Letting lane 0 spin alone and the others check once measured ten times slower token
+  // steps afterwards on GB300, so every lane spins.)
+  auto wait_bar = [&](uint64_t *bar, int g) -> bool {
+    const bool ok = __all_sync(0xffffffffu, wait_phase(&bar[g % kRowBufs], (uint32_t)(g / kRowBufs) & 1u,
+                                                       abort_flag));
+    if (!ok && lane == 0) {
+      if (!*abort_flag) raise_error(a.err, SDM_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    return ok;
+  };
+  // copies of this warp's pieces: row-list entries [e0, e1), {o_dst | o_src << 16, 0}
+  auto carry = [&](const uint2 *ent, int e0, int e1, unsigned char *to, const unsigned char *from) {
+    for (int e = e0 + rg; e < e1; e += 16) {
+      const uint32_t cv = ent[e].x;
+      const uint32_t od = (cv & 0xffffu) ^ wc, os = (cv >> 16) ^ wc;
+      if (od >= (uint32_t)row_limit || os >= (uint32_t)row_limit) {
+        raise_error(a.err, SDM_DEVERR_PLAN);
+        continue;
+      }
+      *reinterpret_cast<uint4 *>(to + od) = *reinterpret_cast<const uint4 *>(from + os);
+    }
+  };
+  auto list_counts = [&](int g, int &n_load, int &n_c1, int &n_c2) -> const uint2 * {
+    const unsigned char *rec = lrecbuf(g);
+    const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+    const bool ok = hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[2] >= 0 && hdr[3] >= 0 &&
+                    hdr[1] + hdr[2] + hdr[3] == hdr[0];
+    n_load = ok ? hdr[1] : 0;
+    n_c1 = ok ? hdr[2] : 0;
+    n_c2 = ok ? hdr[3] : 0;
+    return reinterpret_cast<const uint2 *>(rec + lay.off_ent);
+  };
+  for (int g = 0; g < S; ++g) {
+    if (!wait_bar(full, g)) return;
+    const unsigned char *cr = crecbuf(g);
+    const uint16_t *refmap = reinterpret_cast<const uint16_t *>(cr + lay.off_refmap);
+    const uint8_t *tokflag = cr + lay.off_tokflag;
+    const float *wts = reinterpret_cast<const float *>(cr + lay.off_wts);
+    const float *gt = reinterpret_cast<const float *>(cr + lay.off_gates);
+    const ACT *vv = reinterpret_cast<const ACT *>(tokbuf(g));
+    unsigned char *rows = rowbuf(g);
+    const int64_t t0 = (int64_t)g * G;
+    const int nt = (int)min((int64_t)G, a.T - t0);
+    ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + col;
+    for (int t = 0; t < nt; ++t) {
+      float v[VEC], out[VEC];
+      load_vec<ACT, VEC>(vv + t * COLS + col, v);
+      const float2 ab = *reinterpret_cast<const float2 *>(gt + 2 * t);
+      piece_token<BANK, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, ab.x, ab.y, v, rows, wc, tokflag[t] != 0,
+                                  out);
+      if (rg == 0 && lane_valid) store_vec<ACT, VEC>(ybase + t * ystep, out);
+      __syncwarp();
+    }
+    // rows the next two stages carry over: copy this warp's pieces out of buffer g
+    if (g + 1 < S) {
+      if (!wait_bar(recs, g)) return;
+      int n_load, n_c1, n_c2;
+      const uint2 *ent = list_counts(g + 1, n_load, n_c1, n_c2);
+      carry(ent, n_load, n_load + n_c1, rowbuf(g + 1), rows);
+      if (g + 2 < S) {
+        ent = list_counts(g + 2, n_load, n_c1, n_c2);
+        carry(ent, n_load + n_c1, n_load + n_c1 + n_c2, rowbuf(g + 2), rows);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&done[g % kRowBufs]);
   }
 }
 
-// Launches the instance for the shape: W = R = 64 fixed at compile time, else the
-// smallest JB >= ceil(max(W, R) / 8); 4 loader warps when two CTAs share an SM.
-template <typename BANK, typename ACT, int CW, int LW>
-cudaError_t launch_cw_lw(const WriteReadArgs &a, int64_t streams, int64_t smem, cudaStream_t st) {
+// Launches the instance for the shape: W = R = 64 fixed at compile time, else up to 8
+// rows per lane and sum (W, R <= 128).
+template <typename BANK, typename ACT, int NCW, int LW>
+cudaError_t launch_ncw_lw(const WriteReadArgs &a, int64_t streams, int64_t smem, cudaStream_t st) {
   const dim3 grid((unsigned)a.slices, (unsigned)streams);
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, WrGeometry<BANK, CW, LW>::NTHR, smem, st>>>(a);
+    kern<<<grid, WrGeometry<NCW, LW>::NTHR, smem, st>>>(a);
     return cudaGetLastError();
   };
-  const int n = a.W > a.R ? a.W : a.R;
-  const int per_lane = (n + 7) / 8;
-  if (a.W == 64 && a.R == 64) return go(write_read_kernel<BANK, ACT, CW, 8, true, LW>);
-  if (per_lane <= 4) return go(write_read_kernel<BANK, ACT, CW, 4, false, LW>);
-  if (per_lane <= 8) return go(write_read_kernel<BANK, ACT, CW, 8, false, LW>);
-  if (per_lane <= 16) return go(write_read_kernel<BANK, ACT, CW, 16, false, LW>);
+  if (a.W == 64 && a.R == 64) return go(write_read_kernel<BANK, ACT, NCW, 4, true, LW>);
+  if (a.W <= 128 && a.R <= 128) return go(write_read_kernel<BANK, ACT, NCW, 8, false, LW>);
   return cudaErrorInvalidValue;
 }
 
-template <typename BANK, typename ACT, int CW>
-cudaError_t launch_cw(const WriteReadArgs &a, int64_t streams, int64_t smem, cudaStream_t st) {
-  if (a.two_per_sm) return launch_cw_lw<BANK, ACT, CW, 4>(a, streams, smem, st);
-  return launch_cw_lw<BANK, ACT, CW, 8>(a, streams, smem, st);
+template <typename BANK, typename ACT>
+cudaError_t launch_types(const WriteReadArgs &a, int64_t streams, const WriteReadLaunch &l, cudaStream_t st) {
+  if (l.NCW == 4 && l.LW == 8) return launch_ncw_lw<BANK, ACT, 4, 8>(a, streams, l.smem_bytes, st);
+  if (l.NCW == 4 && l.LW == 4) return launch_ncw_lw<BANK, ACT, 4, 4>(a, streams, l.smem_bytes, st);
+  if (l.NCW == 8 && l.LW == 8) return launch_ncw_lw<BANK, ACT, 8, 8>(a, streams, l.smem_bytes, st);
+  if (l.NCW == 1 && l.LW == 8) return launch_ncw_lw<BANK, ACT, 1, 8>(a, streams, l.smem_bytes, st);
+  if (l.NCW == 1 && l.LW == 4) return launch_ncw_lw<BANK, ACT, 1, 4>(a, streams, l.smem_bytes, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace wr

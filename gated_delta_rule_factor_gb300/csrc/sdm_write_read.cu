@@ -8,9 +8,6 @@ namespace sdm {
 
 namespace {
 
-using wr::tok_layout;
-using wr::TokLayout;
-
 // Learned table [H, N, d_v] -> every stream's bank [B, H, N, d_v]: each 16-byte chunk
 // of the source is read once and written B times.
 __global__ void __launch_bounds__(kThreads) bank_copy_kernel(const __grid_constant__ BankCopyArgs a) {
@@ -28,22 +25,19 @@ __global__ void __launch_bounds__(kThreads) bank_copy_kernel(const __grid_consta
 
 }  // namespace
 
-int64_t write_read_smem_bytes(int CW, int bank_elem, int act_elem, int G, int W, int R,
-                              int64_t rec_bytes) {
-  const int64_t L = (int64_t)G * (W + R);
-  const TokLayout t = tok_layout(G, W, R, CW, act_elem);
-  return 2 * L * CW * bank_elem + 3 * rec_bytes + 2 * t.bytes;
+int64_t write_read_smem_bytes(const PlanLayout &lay, int bank_elem, int act_elem) {
+  return wr::smem_layout(lay, bank_elem, act_elem).bytes;
 }
 
-cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_dtype,
-                              int act_dtype, int CW, int64_t smem, cudaStream_t st) {
+cudaError_t launch_write_read(const WriteReadArgs &a, int64_t streams, int bank_dtype, int act_dtype,
+                              const WriteReadLaunch &l, cudaStream_t st) {
   if (streams == 0 || a.slices == 0) return cudaSuccess;
   if (bank_dtype == SDM_F32) {
-    if (act_dtype == SDM_F32) return launch_write_read_f32_f32(a, streams, CW, smem, st);
-    return launch_write_read_f32_bf16(a, streams, CW, smem, st);
+    if (act_dtype == SDM_F32) return launch_write_read_f32_f32(a, streams, l, st);
+    return launch_write_read_f32_bf16(a, streams, l, st);
   }
-  if (act_dtype == SDM_F32) return launch_write_read_bf16_f32(a, streams, CW, smem, st);
-  return launch_write_read_bf16_bf16(a, streams, CW, smem, st);
+  if (act_dtype == SDM_F32) return launch_write_read_bf16_f32(a, streams, l, st);
+  return launch_write_read_bf16_bf16(a, streams, l, st);
 }
 
 cudaError_t launch_bank_copy(const BankCopyArgs &a, int sm_count, cudaStream_t st) {

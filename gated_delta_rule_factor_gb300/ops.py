@@ -240,6 +240,18 @@ def test_stall_decode_copy(on: bool) -> None:
     _abi.check(_abi.load().sdm_test_stall_decode_copy(1 if on else 0), "sdm_test_stall_decode_copy")
 
 
+def test_force_write_read_layout(slice_bytes: int = 0, stage_tokens: int = 0) -> None:
+    """Test hook: force the write/read kernel's row slice per CTA (32, 128 or 256 bytes)
+    and cap its stage length; 0 restores the automatic choice (sdm.h)."""
+    _abi.check(_abi.load().sdm_test_force_write_read_layout(int(slice_bytes), int(stage_tokens)),
+               "sdm_test_force_write_read_layout")
+
+
+def test_force_simt_scorer(on: bool) -> None:
+    """Test hook: score bfloat16 queries on the CUDA-core scorer (sdm.h)."""
+    _abi.check(_abi.load().sdm_test_force_simt_scorer(1 if on else 0), "sdm_test_force_simt_scorer")
+
+
 def profile_begin() -> None:
     _abi.check(_abi.load().sdm_profile_begin(), "sdm_profile_begin")
 

@@ -242,6 +242,18 @@ const char *sdm_kernel_name(int32_t kind);
  * context stays usable.  Process-wide; returns SDM_OK. */
 sdm_status sdm_test_stall_decode_copy(int on);
 
+/* Test hooks of the write/read launch choice; not for production use.  Results are
+ * bitwise the same for every choice (the per-element arithmetic and its order depend on
+ * W and R only); only speed changes.  Process-wide; 0 restores the automatic choice.
+ *   sdm_test_force_write_read_layout  slice_bytes: bytes of every row one CTA owns (32,
+ *       128 or 256, i.e. 1, 4 or 8 compute warps of 32 bytes each); stage_tokens: an
+ *       upper bound on the tokens staged together (>= 1).  SDM_ERR_INVALID_ARG for
+ *       other values.  Applies to calls made after it.
+ *   sdm_test_force_simt_scorer  on != 0: score bfloat16 queries on the CUDA-core scorer
+ *       instead of the tensor cores. */
+sdm_status sdm_test_force_write_read_layout(int slice_bytes, int stage_tokens);
+sdm_status sdm_test_force_simt_scorer(int on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,10 +1,12 @@
-"""The write/read kernel on 128-byte row slices (block-ordered token step) at small sizes.
+"""The write/read kernel at every launch geometry, at sizes the oracle checks in full.
 
-The launch picks 128-byte slices on its own only when a shape has enough columns to
-fill the GPU (the full-size layer and training shapes); SDM_WR_CW forces the slice so
-that these shapes, which the oracle checks on every stream and token, run the same
-kernel: parity with the oracle, chunk-size independence, bitwise repeatability and the
-same bits as narrower slices.
+The launch picks the row slice per CTA (32, 128 or 256 bytes: 1, 4 or 8 compute warps
+of 32 bytes each) and the stage length from the shape and the GPU; the wide slices are
+picked on their own only for shapes large enough to fill the GPU.  A test hook
+(sdm_test_force_write_read_layout) forces them here, so that small shapes run the same
+kernel instances as the full-size workloads: parity with the oracle, chunk-size
+independence, bitwise repeatability, and the same bits for every slice and stage length
+(the per-element arithmetic and its summation order depend on W and R only).
 """
 
 import pytest
@@ -17,25 +19,24 @@ from sdm_testlib import compare_stream, gpu_write_read
 pytestmark = pytest.mark.gpu
 
 
-def _slice_cols(cfg) -> int:
-    return 128 // (4 if cfg.bank_dtype == "f32" else 2)
-
-
 @pytest.fixture
-def blocks(monkeypatch):
-    def force(cfg):
-        monkeypatch.setenv("SDM_WR_CW", str(_slice_cols(cfg)))
-    return force
+def layout():
+    import gated_delta_rule_factor_gb300 as sdm
+
+    def force(slice_bytes, stage_tokens=0):
+        sdm.test_force_write_read_layout(slice_bytes, stage_tokens)
+    yield force
+    sdm.test_force_write_read_layout(0, 0)
 
 
-BLOCK_VARIANTS = {
+VARIANTS = {
     "tiny": dict(),
     "w64_r64": dict(W=64, R=64, T=40),
     "w48_r64_ragged": dict(W=48, R=64, T=37, chunk_size=5),
-    "w128_r96": dict(factor_dims=(64, 64), W=128, R=96, T=40, d_v=32),
+    "w128_r96": dict(factor_dims=(64, 64), W=128, R=96, T=40, d_v=64),
     "w3_r5": dict(W=3, R=5, T=30),
     "one_write_one_read": dict(W=1, R=1),
-    "bf16_bank": dict(act_dtype="bf16", bank_dtype="bf16", W=64, R=32, T=40),
+    "bf16_bank": dict(act_dtype="bf16", bank_dtype="bf16", W=64, R=32, T=40, d_v=128),
     "f32_acts_bf16_bank": dict(bank_dtype="bf16", d_v=128, T=32),
     "bf16_acts": dict(act_dtype="bf16", d_v=96, W=24, R=40, T=40),
     "chunk_1": dict(T=40, chunk_size=1, W=32, R=32),
@@ -43,53 +44,56 @@ BLOCK_VARIANTS = {
     "three_factors": dict(factor_dims=(8, 8, 8), d_sub=16, W=16, R=12),
     "many_streams": dict(B=3, H=2, T=50, W=64, R=64),
     "long_head": dict(d_v=2048, T=24, W=64, R=64),
+    "partial_last_slice": dict(d_v=40, T=30, W=64, R=64),
+    "partial_last_slice_bf16": dict(d_v=72, bank_dtype="bf16", act_dtype="bf16", T=30),
 }
 
 
-@pytest.mark.parametrize("name", sorted(BLOCK_VARIANTS))
-def test_block_layout_matches_oracle(blocks, name):
-    kw = dict(BLOCK_VARIANTS[name])
+@pytest.mark.parametrize("slice_bytes", [128, 256])
+@pytest.mark.parametrize("name", sorted(VARIANTS))
+def test_wide_slices_match_oracle(layout, name, slice_bytes):
+    kw = dict(VARIANTS[name])
     chunk = kw.pop("chunk_size", None)
     cfg = CONFIGS["tiny"].replace(**kw)
-    assert cfg.d_v * (4 if cfg.bank_dtype == "f32" else 2) % 128 == 0
-    blocks(cfg)
+    layout(slice_bytes)
     d = sdm_inputs.make_inputs(cfg)
     gpu = gpu_write_read(cfg, d, chunk_size=chunk)
-    streams = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
-    res = [compare_stream(cfg, d, gpu, b, h) for (b, h) in streams]
-    assert sum(r["near_ties"] for r in res) <= 1
+    res = [compare_stream(cfg, d, gpu, b, h) for b in range(cfg.B) for h in range(cfg.H)]
+    assert sum(r["near_ties"] for r in res) <= 1, res
 
 
-def test_block_layout_chunk_size_changes_nothing(blocks):
+@pytest.mark.parametrize("slice_bytes", [32, 128, 256])
+def test_chunk_size_changes_nothing(layout, slice_bytes):
     cfg = CONFIGS["tiny"].replace(W=64, R=64, B=2, H=2, T=200)
-    blocks(cfg)
+    layout(slice_bytes)
     d = sdm_inputs.make_inputs(cfg)
     ref = gpu_write_read(cfg, d, chunk_size=64)
-    for c in (1, 3, 17, 128, 256):
+    for c in (1, 2, 3, 17, 128, 256):
         out = gpu_write_read(cfg, d, chunk_size=c)
         for k in ref:
             assert torch.equal(ref[k], out[k]), (c, k)
 
 
-def test_block_layout_bitwise_repeatable(blocks):
+def test_bitwise_repeatable_at_every_slice(layout):
     cfg = CONFIGS["tiny"].replace(W=64, R=64, B=2, H=2, T=120, d_v=256)
-    blocks(cfg)
     d = sdm_inputs.make_inputs(cfg)
-    first = gpu_write_read(cfg, d)
-    for _ in range(2):
+    for sb in (32, 128, 256):
+        layout(sb)
+        first = gpu_write_read(cfg, d)
+        for _ in range(2):
+            out = gpu_write_read(cfg, d)
+            for k in first:
+                assert torch.equal(first[k], out[k]), (sb, k)
+
+
+@pytest.mark.parametrize("bank_dtype", ["f32", "bf16"])
+def test_results_do_not_depend_on_the_slice_or_the_stage_length(layout, bank_dtype):
+    cfg = CONFIGS["tiny"].replace(W=64, R=64, B=2, H=2, T=60, d_v=256, bank_dtype=bank_dtype)
+    d = sdm_inputs.make_inputs(cfg)
+    layout(0)
+    ref = gpu_write_read(cfg, d)
+    for sb, g in ((32, 0), (128, 0), (256, 0), (128, 1), (256, 2), (32, 5)):
+        layout(sb, g)
         out = gpu_write_read(cfg, d)
-        for k in first:
-            assert torch.equal(first[k], out[k]), k
-
-
-def test_results_do_not_depend_on_the_slice_width(monkeypatch):
-    # every slice width runs the same block-ordered step: an element's sums depend on
-    # W and R only, so 128-byte and 32-byte slices give the same bits
-    cfg = CONFIGS["tiny"].replace(W=64, R=64, B=2, H=2, T=60, d_v=128)
-    d = sdm_inputs.make_inputs(cfg)
-    monkeypatch.setenv("SDM_WR_CW", str(_slice_cols(cfg)))
-    wide = gpu_write_read(cfg, d)
-    monkeypatch.setenv("SDM_WR_CW", "8")
-    narrow = gpu_write_read(cfg, d)
-    for k in wide:
-        assert torch.equal(wide[k], narrow[k]), k
+        for k in ref:
+            assert torch.equal(ref[k], out[k]), (sb, g, k)
