@@ -243,6 +243,7 @@ PlanLayout plan_layout(int G, int W, int R, int64_t T, int RB) {
   const int64_t L = p.L;
   int64_t o = 32;                                    // n_u, n_load, n_c1, n_c2, n_wb
   p.off_ent = o;       o = a16(o + 8 * L);
+  p.off_out = o;       o = a16(o + 8 * L);
   p.off_wb = o;        o = a16(o + 8 * L);
   p.lrec_bytes = o;
   o = 0;

@@ -85,13 +85,14 @@ struct BankCopyArgs {
 //   uo[s][g][u]      o(u)                                        (uint16, L per stage)
 //   written[s][g][u] 1 if a write ref of the stage hits row u   (uint8, L per stage)
 //   lrec[s][g]       the stage's row lists, fetched three stages ahead:
-//     int32 n_u, n_load, n_c1, n_c2, n_wb, 3 x pad               (32 bytes)
-//     uint2 ent[L]     entries [0, n_load): bank rows fetched, {row offset, o}, the
-//                      row offset being slot * (d_v * elem / 16) in 16-byte units from
-//                      the stream's table; then n_c1 carries from stage g-1's buffer
-//                      and n_c2 carries from stage g-2's buffer (rows stage g-1 does
-//                      not hold), {o_dst | o_src << 16, 0}; the compute warps make those
-//                      copies at the end of stage g-1 and g-2 respectively
+//     int32 n_u, n_load, n_out1, n_out2, n_wb, 3 x pad           (32 bytes)
+//     uint2 ent[L]     the n_load bank rows fetched, {row offset, o}, the row offset
+//                      being slot * (d_v * elem / 16) in 16-byte units from the
+//                      stream's table
+//     uint2 out[L]     n_out1 rows this stage hands to stage g+1, then n_out2 rows it
+//                      hands to stage g+2 (rows g+1 does not hold), {o_dst | o_src << 16,
+//                      0}: the compute warps copy them out of this stage's buffer at its
+//                      end (the bank may be stale for them)
 //     uint2 wb[L]      rows written back after the stage, {row offset, o}: dirty ones
 //                      (written, or carried in) that neither of the next two stages holds
 //   crec[s][g]       the compute warps' per-stage data, one contiguous copy:
@@ -106,7 +107,7 @@ struct PlanLayout {
   int32_t RB;            // row slice bytes of one CTA (row slot stride)
   int32_t cmask;         // color bits usable in o (3 when RB >= 128, else 0)
   int64_t lrec_bytes;    // bytes per row-list record (multiple of 16)
-  int64_t off_ent, off_wb;
+  int64_t off_ent, off_out, off_wb;
   int64_t crec_bytes;    // bytes per compute record (multiple of 16)
   int64_t off_refmap, off_tokflag, off_wts, off_gates;
 };

@@ -189,8 +189,8 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
   int32_t *prev2 = prev + lay.L;                            // [L] g-2
   int32_t *next = prev2 + lay.L;                            // [L] g+1
   int32_t *next2 = next + lay.L;                            // [L] g+2
-  uint16_t *uo_prev = reinterpret_cast<uint16_t *>(next2 + lay.L);   // [L]
-  uint16_t *uo_prev2 = uo_prev + lay.L;                              // [L]
+  uint16_t *uo_next = reinterpret_cast<uint16_t *>(next2 + lay.L);   // [L]
+  uint16_t *uo_next2 = uo_next + lay.L;                              // [L]
   __shared__ int warp_sums[kThreads / 32];
 
   const int g = blockIdx.x;
@@ -203,16 +203,16 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
   const int n_cur = a.nuniq[stage];
   const int n_next = g + 1 < S ? a.nuniq[stage + 1] : 0;
   const int n_next2 = g + 2 < S ? a.nuniq[stage + 2] : 0;
-  for (int i = tid; i < n_prev; i += kThreads) {
-    prev[i] = a.uniq[(stage - 1) * lay.L + i];
-    uo_prev[i] = a.uo[(stage - 1) * lay.L + i];
+  for (int i = tid; i < n_prev; i += kThreads) prev[i] = a.uniq[(stage - 1) * lay.L + i];
+  for (int i = tid; i < n_prev2; i += kThreads) prev2[i] = a.uniq[(stage - 2) * lay.L + i];
+  for (int i = tid; i < n_next; i += kThreads) {
+    next[i] = a.uniq[(stage + 1) * lay.L + i];
+    uo_next[i] = a.uo[(stage + 1) * lay.L + i];
   }
-  for (int i = tid; i < n_prev2; i += kThreads) {
-    prev2[i] = a.uniq[(stage - 2) * lay.L + i];
-    uo_prev2[i] = a.uo[(stage - 2) * lay.L + i];
+  for (int i = tid; i < n_next2; i += kThreads) {
+    next2[i] = a.uniq[(stage + 2) * lay.L + i];
+    uo_next2[i] = a.uo[(stage + 2) * lay.L + i];
   }
-  for (int i = tid; i < n_next; i += kThreads) next[i] = a.uniq[(stage + 1) * lay.L + i];
-  for (int i = tid; i < n_next2; i += kThreads) next2[i] = a.uniq[(stage + 2) * lay.L + i];
   __syncthreads();
 
   const int32_t *cur = a.uniq + stage * lay.L;
@@ -221,52 +221,51 @@ __global__ void __launch_bounds__(kThreads) plan_link_kernel(const __grid_consta
   const int ept = (n_cur + kThreads - 1) / kThreads;
   const int u0 = min(n_cur, tid * ept), u1 = min(n_cur, u0 + ept);
   // The bank may be stale for a row that one of the two previous stages holds (their
-  // write-backs come later), so such a row is copied from that stage's buffer: from
-  // stage g-1's if it holds the row (carry 1), else from stage g-2's (carry 2).  Any
-  // other row is read from the bank, after every older stage's write-back.  A row goes
-  // back to the bank after this stage if it is dirty here (written, or carried in) and
-  // neither of the next two stages carries it on.
-  int c_load = 0, c_c1 = 0, c_c2 = 0, c_wb = 0;
+  // write-backs come later): such a row arrives by a copy in shared memory from the
+  // latest stage that holds it, made at that stage's end, so this stage fetches from
+  // the bank only rows neither previous stage holds.  It hands its own rows on the same
+  // way: to stage g+1 the rows g+1 holds, to stage g+2 the rows g+2 holds and g+1 does
+  // not.  A row goes back to the bank after this stage if it is dirty here (written, or
+  // handed in) and is not handed on.
+  int c_load = 0, c_o1 = 0, c_o2 = 0, c_wb = 0;
   for (int u = u0; u < u1; ++u) {
     const int32_t slot = cur[u];
     const bool in1 = find_sorted(prev, n_prev, slot) >= 0;
     const bool in2 = !in1 && find_sorted(prev2, n_prev2, slot) >= 0;
-    const bool out = find_sorted(next, n_next, slot) >= 0 || find_sorted(next2, n_next2, slot) >= 0;
+    const bool out1 = find_sorted(next, n_next, slot) >= 0;
+    const bool out2 = !out1 && find_sorted(next2, n_next2, slot) >= 0;
     c_load += !in1 && !in2;
-    c_c1 += in1;
-    c_c2 += in2;
-    c_wb += (written[u] || in1 || in2) && !out;
+    c_o1 += out1;
+    c_o2 += out2;
+    c_wb += (written[u] || in1 || in2) && !out1 && !out2;
   }
-  int n_load, n_c1, n_c2, n_wb;
+  int n_load, n_o1, n_o2, n_wb;
   int o_load = block_scan_exclusive(c_load, warp_sums, &n_load);
-  int o_c1 = n_load + block_scan_exclusive(c_c1, warp_sums, &n_c1);
-  int o_c2 = n_load + n_c1 + block_scan_exclusive(c_c2, warp_sums, &n_c2);
+  int o_o1 = block_scan_exclusive(c_o1, warp_sums, &n_o1);
+  int o_o2 = n_o1 + block_scan_exclusive(c_o2, warp_sums, &n_o2);
   int o_wb = block_scan_exclusive(c_wb, warp_sums, &n_wb);
 
   unsigned char *lrec = a.lrecs + stage * lay.lrec_bytes;
   uint2 *ent = reinterpret_cast<uint2 *>(lrec + lay.off_ent);
+  uint2 *out = reinterpret_cast<uint2 *>(lrec + lay.off_out);
   uint2 *wb = reinterpret_cast<uint2 *>(lrec + lay.off_wb);
   for (int u = u0; u < u1; ++u) {
     const int32_t slot = cur[u];
     const uint32_t row16 = (uint32_t)slot * a.pitch16;     // < 2^32 (checked on the host)
-    const int src1 = find_sorted(prev, n_prev, slot);
-    const int src2 = src1 < 0 ? find_sorted(prev2, n_prev2, slot) : -1;
-    const bool out = find_sorted(next, n_next, slot) >= 0 || find_sorted(next2, n_next2, slot) >= 0;
-    if (src1 >= 0) {
-      ent[o_c1++] = make_uint2((uint32_t)uo_cur[u] | ((uint32_t)uo_prev[src1] << 16), 0u);
-    } else if (src2 >= 0) {
-      ent[o_c2++] = make_uint2((uint32_t)uo_cur[u] | ((uint32_t)uo_prev2[src2] << 16), 0u);
-    } else {
-      ent[o_load++] = make_uint2(row16, uo_cur[u]);
-    }
-    if ((written[u] || src1 >= 0 || src2 >= 0) && !out) wb[o_wb++] = make_uint2(row16, uo_cur[u]);
+    const bool in = find_sorted(prev, n_prev, slot) >= 0 || find_sorted(prev2, n_prev2, slot) >= 0;
+    const int dst1 = find_sorted(next, n_next, slot);
+    const int dst2 = dst1 < 0 ? find_sorted(next2, n_next2, slot) : -1;
+    if (!in) ent[o_load++] = make_uint2(row16, uo_cur[u]);
+    if (dst1 >= 0) out[o_o1++] = make_uint2((uint32_t)uo_next[dst1] | ((uint32_t)uo_cur[u] << 16), 0u);
+    if (dst2 >= 0) out[o_o2++] = make_uint2((uint32_t)uo_next2[dst2] | ((uint32_t)uo_cur[u] << 16), 0u);
+    if ((written[u] || in) && dst1 < 0 && dst2 < 0) wb[o_wb++] = make_uint2(row16, uo_cur[u]);
   }
   if (tid == 0) {
     int32_t *hdr = reinterpret_cast<int32_t *>(lrec);
     hdr[0] = n_cur;
     hdr[1] = n_load;
-    hdr[2] = n_c1;
-    hdr[3] = n_c2;
+    hdr[2] = n_o1;
+    hdr[3] = n_o2;
     hdr[4] = n_wb;
   }
 }
@@ -284,7 +283,7 @@ cudaError_t launch_plan_sort(const PlanArgs &a, int64_t streams, int P, cudaStre
 
 cudaError_t launch_plan_link(const PlanArgs &a, int64_t streams, cudaStream_t st) {
   if (streams == 0 || a.lay.n_stages == 0) return cudaSuccess;
-  const int64_t smem = (int64_t)a.lay.L * 20;
+  const int64_t smem = (int64_t)a.lay.L * 20;   // four slot lists and two offset lists
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(plan_link_kernel), smem);
   if (e != cudaSuccess) return e;
   plan_link_kernel<<<dim3((unsigned)a.lay.n_stages, (unsigned)streams), kThreads, smem, st>>>(a);

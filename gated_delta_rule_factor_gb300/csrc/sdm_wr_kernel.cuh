@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR)
       for (int i = lt; i < lrec_chunks; i += NL) cp_async16(dst + i * 16, src + i * 16);
     };
     auto hdr_ok = [&](const int32_t *hdr) {
-      return hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[2] >= 0 && hdr[3] >= 0 &&
-             hdr[1] + hdr[2] + hdr[3] == hdr[0] && hdr[4] >= 0 && hdr[4] <= L;
+      return hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[1] <= hdr[0] && hdr[2] >= 0 && hdr[3] >= 0 &&
+             hdr[2] + hdr[3] <= hdr[0] && hdr[4] >= 0 && hdr[4] <= hdr[0];
     };
     // Row offsets (16-byte units) must stay inside the stream's table, shared-memory
     // offsets inside the stage buffer; a bad entry is skipped and reported.
@@ -329,30 +329,45 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR)
     }
     return ok;
   };
-  // copies of this warp's pieces: row-list entries [e0, e1), {o_dst | o_src << 16, 0}
-  auto carry = [&](const uint2 *ent, int e0, int e1, unsigned char *to, const unsigned char *from) {
-    for (int e = e0 + rg; e < e1; e += 16) {
-      const uint32_t cv = ent[e].x;
-      const uint32_t od = (cv & 0xffffu) ^ wc, os = (cv >> 16) ^ wc;
-      if (od >= (uint32_t)row_limit || os >= (uint32_t)row_limit) {
-        raise_error(a.err, SDM_DEVERR_PLAN);
-        continue;
-      }
-      *reinterpret_cast<uint4 *>(to + od) = *reinterpret_cast<const uint4 *>(from + os);
-    }
+  // Rows this stage hands on (its own record's out list, visible since the end of stage
+  // g-1): {o_dst | o_src << 16}; the first 32 entries are read into registers at the
+  // stage's start, two per lane pair, so the copies at its end cost one round trip.
+  struct Handoff {
+    int n1 = 0, n2 = 0;
+    uint32_t e[2] = {0, 0};
   };
-  auto list_counts = [&](int g, int &n_load, int &n_c1, int &n_c2) -> const uint2 * {
+  auto handoff_of = [&](int g) -> Handoff {
+    Handoff hf;
     const unsigned char *rec = lrecbuf(g);
     const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
-    const bool ok = hdr[0] >= 0 && hdr[0] <= L && hdr[1] >= 0 && hdr[2] >= 0 && hdr[3] >= 0 &&
-                    hdr[1] + hdr[2] + hdr[3] == hdr[0];
-    n_load = ok ? hdr[1] : 0;
-    n_c1 = ok ? hdr[2] : 0;
-    n_c2 = ok ? hdr[3] : 0;
-    return reinterpret_cast<const uint2 *>(rec + lay.off_ent);
+    const bool ok = hdr[0] >= 0 && hdr[0] <= L && hdr[2] >= 0 && hdr[3] >= 0 && hdr[2] + hdr[3] <= hdr[0];
+    if (!ok) return hf;
+    hf.n1 = hdr[2];
+    hf.n2 = hdr[3];
+    const uint2 *out = reinterpret_cast<const uint2 *>(rec + lay.off_out);
+    if (rg < hf.n1 + hf.n2) hf.e[0] = out[rg].x;
+    if (rg + 16 < hf.n1 + hf.n2) hf.e[1] = out[rg + 16].x;
+    return hf;
+  };
+  auto copy_piece = [&](uint32_t cv, unsigned char *to, const unsigned char *from) {
+    const uint32_t od = (cv & 0xffffu) ^ wc, os = (cv >> 16) ^ wc;
+    if (od >= (uint32_t)row_limit || os >= (uint32_t)row_limit) {
+      raise_error(a.err, SDM_DEVERR_PLAN);
+      return;
+    }
+    *reinterpret_cast<uint4 *>(to + od) = *reinterpret_cast<const uint4 *>(from + os);
+  };
+  auto hand_on = [&](int g, const Handoff &hf) {
+    const unsigned char *rows = rowbuf(g);
+    const uint2 *out = reinterpret_cast<const uint2 *>(lrecbuf(g) + lay.off_out);
+    for (int e = rg, k = 0; e < hf.n1 + hf.n2; e += 16, ++k) {
+      const uint32_t cv = k < 2 ? hf.e[k] : out[e].x;
+      copy_piece(cv, e < hf.n1 ? rowbuf(g + 1) : rowbuf(g + 2), rows);
+    }
   };
   for (int g = 0; g < S; ++g) {
     if (!wait_bar(full, g)) return;
+    const Handoff hf = handoff_of(g);
     const unsigned char *cr = crecbuf(g);
     const uint16_t *refmap = reinterpret_cast<const uint16_t *>(cr + lay.off_refmap);
     const uint8_t *tokflag = cr + lay.off_tokflag;
@@ -372,16 +387,11 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR)
       if (rg == 0 && lane_valid) store_vec<ACT, VEC>(ybase + t * ystep, out);
       __syncwarp();
     }
-    // rows the next two stages carry over: copy this warp's pieces out of buffer g
+    // rows the next two stages take over: copy this warp's pieces out of buffer g (into
+    // buffer g+2 only once the loaders have written back stage g-1 from it: recs(g))
     if (g + 1 < S) {
       if (!wait_bar(recs, g)) return;
-      int n_load, n_c1, n_c2;
-      const uint2 *ent = list_counts(g + 1, n_load, n_c1, n_c2);
-      carry(ent, n_load, n_load + n_c1, rowbuf(g + 1), rows);
-      if (g + 2 < S) {
-        ent = list_counts(g + 2, n_load, n_c1, n_c2);
-        carry(ent, n_load + n_c1, n_load + n_c1 + n_c2, rowbuf(g + 2), rows);
-      }
+      hand_on(g, hf);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&done[g % kRowBufs]);
