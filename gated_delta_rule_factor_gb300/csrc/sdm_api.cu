@@ -199,6 +199,34 @@ sdm_status check_shape(const sdm_shape *sh, bool decode, Derived *d) {
   return SDM_OK;
 }
 
+// Boxes of at least k position tuples, by corner: the first F-1 sides run over powers of
+// two (and the full width kf), the last side is the least that reaches k tuples.
+void enumerate_boxes(int F, const int32_t *kf, int k, std::vector<uint32_t> &out) {
+  out.clear();
+  int a[SDM_MAX_FACTORS] = {1, 1, 1, 1};
+  struct Rec {
+    static void go(int f, int F, const int32_t *kf, int k, int64_t prod, int *a, std::vector<uint32_t> &o) {
+      if (o.size() >= 32) return;
+      if (f == F - 1) {
+        const int64_t last = (k + prod - 1) / prod;
+        if (last < 1 || last > kf[f]) return;
+        a[f] = (int)last;
+        uint32_t t = 0;
+        for (int i = 0; i < F; ++i) t |= (uint32_t)(a[i] - 1) << (8 * i);
+        if (std::find(o.begin(), o.end(), t) == o.end()) o.push_back(t);
+        return;
+      }
+      for (int x = 1;; x <<= 1) {
+        const int side = x < kf[f] ? x : kf[f];
+        a[f] = side;
+        go(f + 1, F, kf, k, prod * side, a, o);
+        if (side == kf[f]) break;
+      }
+    }
+  };
+  Rec::go(0, F, kf, k, 1, a, out);
+}
+
 sdm_status build_candidates(const Derived &d, CandidateList *cl) {
   std::vector<uint32_t> v;
   for (int q = 0; q < 2; ++q) {
@@ -207,6 +235,9 @@ sdm_status build_candidates(const Derived &d, CandidateList *cl) {
       return fail(SDM_ERR_UNSUPPORTED, "k = %d has more than %d product-key candidates", d.g.k[q], SDM_MAX_CANDIDATES);
     cl->n[q] = (int32_t)v.size();
     std::copy(v.begin(), v.end(), cl->tup[q]);
+    enumerate_boxes(d.g.F, d.g.kf[q], d.g.k[q], v);
+    cl->nbox[q] = (int32_t)v.size();
+    std::copy(v.begin(), v.end(), cl->box[q]);
   }
   return SDM_OK;
 }

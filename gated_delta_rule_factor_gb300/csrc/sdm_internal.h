@@ -33,6 +33,11 @@ inline int64_t decode_region_bytes(int64_t W, int64_t R, bool copy) {
 struct CandidateList {
   int32_t n[2];
   uint32_t tup[2][SDM_MAX_CANDIDATES];
+  // Boxes {p_f < a_f for every f} holding at least k tuples, by their corner (a_f - 1 in
+  // byte f): every slot of such a box scores at least the corner's slot, so the k-th
+  // best slot score is at least the best corner score (the selection's pruning bound).
+  int32_t nbox[2];
+  uint32_t box[2][32];
 };
 
 // Geometry of the product keys, shared by the top-k and decode kernels.

@@ -1,6 +1,6 @@
 // Exact product-key top-k of every query row from its factor scores: one warp per row
-// (row_topk in sdm_topk.cuh), CTAs looping over rows so that the candidate lists are
-// staged into shared memory once per CTA.
+// (row_topk in sdm_topk.cuh), CTAs looping over rows so that the candidate lists and
+// pruning boxes are staged into shared memory once per CTA.
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 #include "sdm_topk.cuh"
@@ -13,10 +13,12 @@ template <int EF, int EC>
 __global__ void __launch_bounds__(kThreads, 3)
     select_kernel(const __grid_constant__ SelectArgs a, const __grid_constant__ CandidateList cl) {
   __shared__ uint32_t cand[2 * SDM_MAX_CANDIDATES];
+  __shared__ uint32_t boxes[2][32];
   __shared__ RowScratch rs[kThreads / 32];
   const int tid = threadIdx.x, warp = tid >> 5;
   for (int i = tid; i < cl.n[0]; i += kThreads) cand[i] = cl.tup[0][i];
   for (int i = tid; i < cl.n[1]; i += kThreads) cand[cl.n[0] + i] = cl.tup[1][i];
+  if (tid < 64) boxes[tid >> 5][tid & 31] = cl.box[tid >> 5][tid & 31];
   __syncthreads();
   const KeyGeometry &g = a.g;
   const int64_t total = 2 * a.rows;
@@ -25,8 +27,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int qsel = r >= a.rows ? 1 : 0;
     const int64_t row = r - qsel * a.rows;
     const int k = g.k[qsel];
-    row_topk<EF, EC>(a.scores + r * g.ntot, g, qsel, cand + (qsel ? cl.n[0] : 0), cl.n[qsel], rs[warp],
-                     a.idx[qsel] + row * k, a.wt[qsel] + row * k);
+    row_topk<EF, EC>(a.scores + r * g.ntot, g, qsel, cand + (qsel ? cl.n[0] : 0), cl.n[qsel], boxes[qsel],
+                     cl.nbox[qsel], rs[warp], a.idx[qsel] + row * k, a.wt[qsel] + row * k);
   }
 }
 

@@ -27,10 +27,13 @@
 
 namespace sdm {
 
-// Per-warp scratch: best-first factor scores and indices, [F][SDM_MAX_K] each.
+// Per-warp scratch: best-first factor scores and indices, [F][SDM_MAX_K] each, and the
+// keys of the candidates that pass the pruning bound.
+constexpr int kSurvivorCap = 2 * SDM_MAX_K;
 struct RowScratch {
   float fs[SDM_MAX_FACTORS * SDM_MAX_K];
   int32_t fi[SDM_MAX_FACTORS * SDM_MAX_K];
+  uint64_t surv[kSurvivorCap];
 };
 
 // The 32*E best keys of a list of n keys, best first: chunks of 32*E keys (made by
@@ -97,6 +100,24 @@ __device__ __forceinline__ void factor_topk(const float *scores, const KeyGeomet
   }
 }
 
+// Slot score of a position tuple (byte f = p_f): the float32 sum of its factor scores,
+// left to right.
+__device__ __forceinline__ float tuple_score(uint32_t t, const KeyGeometry &g, const RowScratch &sc) {
+  float S = sc.fs[t & 255];
+  if (g.F > 1) S = __fadd_rn(S, sc.fs[SDM_MAX_K + ((t >> 8) & 255)]);
+  if (g.F > 2) S = __fadd_rn(S, sc.fs[2 * SDM_MAX_K + ((t >> 16) & 255)]);
+  if (g.F > 3) S = __fadd_rn(S, sc.fs[3 * SDM_MAX_K + (t >> 24)]);
+  return S;
+}
+
+// The 64-bit key of a position tuple with score S (layout above).
+__device__ __forceinline__ uint64_t tuple_key(uint32_t t, float S) {
+  const uint32_t p0 = t & 255, p1 = (t >> 8) & 255, p2 = (t >> 16) & 255, p3 = t >> 24;
+  const uint32_t sum = p0 + p1 + p2 + p3;
+  const uint32_t low = ((255u - sum) << 24) | ((255u - p0) << 16) | ((255u - p1) << 8) | (255u - p2);
+  return ((uint64_t)ordered_bits(S) << 32) | low;
+}
+
 // Candidate tuples cand[c0, c1), keyed and kept best first (k <= 32 * EC); an empty
 // range gives all-zero keys, which order after every real key.
 template <int EC>
@@ -114,20 +135,58 @@ __device__ __forceinline__ void candidate_topk(const uint32_t *cand, int c0, int
       const int c = c0 + b0 + lane * EC + e;
       if (c < c1) {
         const uint32_t t = cand[c];
-        const int p0 = t & 255, p1 = (t >> 8) & 255, p2 = (t >> 16) & 255, p3 = t >> 24;
-        float S = sc.fs[p0];
-        if (g.F > 1) S = __fadd_rn(S, sc.fs[SDM_MAX_K + p1]);
-        if (g.F > 2) S = __fadd_rn(S, sc.fs[2 * SDM_MAX_K + p2]);
-        if (g.F > 3) S = __fadd_rn(S, sc.fs[3 * SDM_MAX_K + p3]);
-        const uint32_t sum = p0 + p1 + p2 + p3;
-        const uint32_t low = ((255u - sum) << 24) | ((255u - p0) << 16) | ((255u - p1) << 8) |
-                             (255u - p2);
-        kk[e] = ((uint64_t)ordered_bits(S) << 32) | low;
+        kk[e] = tuple_key(t, tuple_score(t, g, sc));
       } else {
         kk[e] = 0ull;
       }
     }
   }, ck);
+}
+
+// candidate_topk over all ncand tuples, sorting only those that can be among the k
+// best.  Every slot of a box of at least k tuples scores at least the box's corner
+// (float addition is monotone in each operand), so the k-th best slot score is at
+// least tau, the best corner score of `boxes`; a tuple scoring below tau cannot be
+// selected.  The others are gathered (up to kSurvivorCap of them; past that, all
+// tuples are sorted) and sorted with the same keys, so the result is the same.
+template <int EC>
+__device__ __forceinline__ void candidate_topk_pruned(const uint32_t *cand, int ncand, const uint32_t *boxes,
+                                                      int nbox, const KeyGeometry &g, RowScratch &sc,
+                                                      uint64_t (&ck)[EC]) {
+  const int lane = threadIdx.x & 31;
+  float tau = -INFINITY;
+  if (lane < nbox) tau = tuple_score(boxes[lane], g, sc);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tau = fmaxf(tau, __shfl_xor_sync(0xffffffffu, tau, o));
+  int cnt = 0;
+  for (int c0 = 0; c0 < ncand; c0 += 32) {
+    const int c = c0 + lane;
+    uint64_t key = 0ull;
+    bool keep = false;
+    if (c < ncand) {
+      const uint32_t t = cand[c];
+      const float S = tuple_score(t, g, sc);
+      keep = S >= tau;
+      key = tuple_key(t, S);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+    if (keep && pos < kSurvivorCap) sc.surv[pos] = key;
+    cnt += __popc(m);
+  }
+  __syncwarp();
+  if (cnt > kSurvivorCap) {
+    candidate_topk<EC>(cand, 0, ncand, g, sc, ck);
+    return;
+  }
+  top_of_chunks<EC>(cnt, [&](int b0, uint64_t(&kk)[EC]) {
+#pragma unroll
+    for (int e = 0; e < EC; ++e) {
+      const int i = b0 + lane * EC + e;
+      kk[e] = i < cnt ? sc.surv[i] : 0ull;
+    }
+  }, ck);
+  __syncwarp();
 }
 
 // Softmax weights of the k best keys (fixed summation order) and their slot ids.
@@ -178,12 +237,12 @@ __device__ __forceinline__ void finish_topk(const uint64_t (&ck)[EC], const KeyG
 // ids (best first) to idx_out and their softmax weights to wt_out.
 template <int EF, int EC>
 __device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry &g, int qsel,
-                                         const uint32_t *cand, int ncand, RowScratch &sc,
-                                         int32_t *idx_out, float *wt_out) {
+                                         const uint32_t *cand, int ncand, const uint32_t *boxes, int nbox,
+                                         RowScratch &sc, int32_t *idx_out, float *wt_out) {
   for (int f = 0; f < g.F; ++f) factor_topk<EF>(scores, g, qsel, f, sc);
   __syncwarp();
   uint64_t ck[EC];
-  candidate_topk<EC>(cand, 0, ncand, g, sc, ck);
+  candidate_topk_pruned<EC>(cand, ncand, boxes, nbox, g, sc, ck);
   finish_topk<EC>(ck, g, qsel, sc, idx_out, wt_out);
 }
 
