@@ -278,155 +278,4 @@ __device__ __forceinline__ void piece_token(int W, int R, const uint16_t *rm, co
   block_tree<VEC>(y);
 }
 
-// ------------------------------------------------------------------------------------
-// The same token step for W = R = 64 (four rows per lane and sum), software-pipelined
-// over the tokens of a stage.  A token's offsets, weights, gates and value slice do not
-// depend on the rows, so they are read one token ahead; its rows are read right after
-// the previous token's update (the only ordering the rows need).  When a token reads
-// none of the rows it writes, its read sum is formed before the write and both sums
-// share one butterfly.  The arithmetic of every element is that of piece_token.
-template <typename BANK, typename ACT>
-struct PieceTok64 {
-  static constexpr int VEC = PieceRow<BANK>::VEC;
-  int ow[4], orr[4];
-  float ww[4], wr[4];
-  float alpha, beta;
-  float v[VEC];
-  bool overlap;
-  // token t of the stage: refs rm, weights wt (64 write then 64 read each), gates gt,
-  // values vv (this lane's columns), flags
-  __device__ __forceinline__ void load(const uint16_t *rm, const float *wt, const float *gt, const ACT *vv,
-                                       const uint8_t *flags, uint32_t wc) {
-    const int rg = (threadIdx.x & 31) >> 1;
-    const uint32_t wc2 = wc | (wc << 16);
-    const uint2 a = *reinterpret_cast<const uint2 *>(rm + 4 * rg);
-    const uint2 b = *reinterpret_cast<const uint2 *>(rm + 64 + 4 * rg);
-    const float4 w4 = *reinterpret_cast<const float4 *>(wt + 4 * rg);
-    const float4 r4 = *reinterpret_cast<const float4 *>(wt + 64 + 4 * rg);
-    const uint32_t ax = a.x ^ wc2, ay = a.y ^ wc2, bx = b.x ^ wc2, by = b.y ^ wc2;
-    ow[0] = (int)(ax & 0xffffu);
-    ow[1] = (int)(ax >> 16);
-    ow[2] = (int)(ay & 0xffffu);
-    ow[3] = (int)(ay >> 16);
-    orr[0] = (int)(bx & 0xffffu);
-    orr[1] = (int)(bx >> 16);
-    orr[2] = (int)(by & 0xffffu);
-    orr[3] = (int)(by >> 16);
-    ww[0] = w4.x;
-    ww[1] = w4.y;
-    ww[2] = w4.z;
-    ww[3] = w4.w;
-    wr[0] = r4.x;
-    wr[1] = r4.y;
-    wr[2] = r4.z;
-    wr[3] = r4.w;
-    const float2 g2 = *reinterpret_cast<const float2 *>(gt);
-    alpha = g2.x;
-    beta = g2.y;
-    load_vec<ACT, VEC>(vv, v);
-    overlap = *flags != 0;
-  }
-};
-
-template <int VEC>
-__device__ __forceinline__ void block_tree2(float (&x)[VEC], float (&y)[VEC]) {
-#pragma unroll
-  for (int o = 2; o < 32; o <<= 1)
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) {
-      x[c] = __fadd_rn(x[c], __shfl_xor_sync(0xffffffffu, x[c], o));
-      y[c] = __fadd_rn(y[c], __shfl_xor_sync(0xffffffffu, y[c], o));
-    }
-}
-
-// Runs tokens [0, nt) of a stage on this warp's pieces of `rows`.  rm / wt: the stage's
-// refs and weights (128 per token), gt: gates (2 per token), vv: the value slice (COLS
-// per token, this lane's columns at +col), flags: per token; y(t, out) stores token t's
-// read (every lane holds it).
-template <typename BANK, typename ACT, int COLS, class StoreY>
-__device__ __forceinline__ void run_tokens64(int nt, const uint16_t *rm, const float *wt, const float *gt,
-                                             const ACT *vv, int col, const uint8_t *flags, unsigned char *rows,
-                                             uint32_t wc, StoreY store_y) {
-  using PR = PieceRow<BANK>;
-  constexpr int VEC = PR::VEC;
-  if (nt <= 0) return;
-  PieceTok64<BANK, ACT> cur, nxt;
-  cur.load(rm, wt, gt, vv + col, flags, wc);
-  uint4 rw[4], rr[4];
-#pragma unroll
-  for (int s = 0; s < 4; ++s) rw[s] = *reinterpret_cast<const uint4 *>(rows + cur.ow[s]);
-  if (!cur.overlap) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) rr[s] = *reinterpret_cast<const uint4 *>(rows + cur.orr[s]);
-  }
-  for (int t = 0; t < nt; ++t) {
-    const bool more = t + 1 < nt;
-    if (more) nxt.load(rm + (t + 1) * 128, wt + (t + 1) * 128, gt + 2 * (t + 1), vv + (t + 1) * COLS + col,
-                       flags + t + 1, wc);
-    // p = sum_j w_j (alpha m_j), and y = sum_j r_j m_j when the read rows are final
-    float am[4][VEC], a[VEC], b[VEC];
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) {
-      a[c] = 0.0f;
-      b[c] = 0.0f;
-    }
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      float m[VEC];
-      PR::unpack(rw[s], m);
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) {
-        am[s][c] = __fmul_rn(cur.alpha, m[c]);
-        a[c] = __fmaf_rn(cur.ww[s], am[s][c], a[c]);
-      }
-    }
-    if (!cur.overlap) {
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        float m[VEC];
-        PR::unpack(rr[s], m);
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) b[c] = __fmaf_rn(cur.wr[s], m[c], b[c]);
-      }
-      block_tree2<VEC>(a, b);
-    } else {
-      block_tree<VEC>(a);
-    }
-    float d[VEC];
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) d[c] = __fmul_rn(cur.beta, __fsub_rn(cur.v[c], a[c]));
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      float m[VEC];
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) m[c] = __fmaf_rn(cur.ww[s], d[c], am[s][c]);
-      *reinterpret_cast<uint4 *>(rows + cur.ow[s]) = PR::pack(m);
-    }
-    __syncwarp();
-    if (cur.overlap) {        // the read follows the token's own write
-#pragma unroll
-      for (int s = 0; s < 4; ++s) rr[s] = *reinterpret_cast<const uint4 *>(rows + cur.orr[s]);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        float m[VEC];
-        PR::unpack(rr[s], m);
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) b[c] = __fmaf_rn(cur.wr[s], m[c], b[c]);
-      }
-      block_tree<VEC>(b);
-    }
-    if (more) {               // the next token's rows, after this token's update
-#pragma unroll
-      for (int s = 0; s < 4; ++s) rw[s] = *reinterpret_cast<const uint4 *>(rows + nxt.ow[s]);
-      if (!nxt.overlap) {
-#pragma unroll
-        for (int s = 0; s < 4; ++s) rr[s] = *reinterpret_cast<const uint4 *>(rows + nxt.orr[s]);
-      }
-    }
-    store_y(t, b);
-    __syncwarp();             // every lane's reads of this token before the next token's writes
-    cur = nxt;
-  }
-}
-
 }  // namespace sdm

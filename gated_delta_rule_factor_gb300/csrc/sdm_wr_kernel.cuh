@@ -379,20 +379,14 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
     const int64_t t0 = (int64_t)g * G;
     const int nt = (int)min((int64_t)G, a.T - t0);
     ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + col;
-    if constexpr (FULL) {
-      run_tokens64<BANK, ACT, COLS>(nt, refmap, wts, gt, vv, col, tokflag, rows, wc, [&](int t, float(&out)[VEC]) {
-        if (rg == 0 && lane_valid) store_vec<ACT, VEC>(ybase + t * ystep, out);
-      });
-    } else {
-      for (int t = 0; t < nt; ++t) {
-        float v[VEC], out[VEC];
-        load_vec<ACT, VEC>(vv + t * COLS + col, v);
-        const float2 ab = *reinterpret_cast<const float2 *>(gt + 2 * t);
-        piece_token<BANK, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, ab.x, ab.y, v, rows, wc, tokflag[t] != 0,
-                                    out);
-        if (rg == 0 && lane_valid) store_vec<ACT, VEC>(ybase + t * ystep, out);
-        __syncwarp();
-      }
+    for (int t = 0; t < nt; ++t) {
+      float v[VEC], out[VEC];
+      load_vec<ACT, VEC>(vv + t * COLS + col, v);
+      const float2 ab = *reinterpret_cast<const float2 *>(gt + 2 * t);
+      piece_token<BANK, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, ab.x, ab.y, v, rows, wc, tokflag[t] != 0,
+                                  out);
+      if (rg == 0 && lane_valid) store_vec<ACT, VEC>(ybase + t * ystep, out);
+      __syncwarp();
     }
     // rows the next two stages take over: copy this warp's pieces out of buffer g (into
     // buffer g+2 only once the loaders have written back stage g-1 from it: recs(g))
