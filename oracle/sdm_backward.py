@@ -43,14 +43,14 @@ y = sum_j r_j M'[i^r_j], given G = dL/dM' (all rows) and dy:
 
 from __future__ import annotations
 
-from typing import Iterable, Optional
+from typing import Callable, Iterable, Optional
 
 import numpy as np
 
 from .sdm_oracle import (_f64, factor_ranks, round_to, slot_scores, softmax_weights,
                          topk_slots)
 
-__all__ = ["select_record", "stream_forward", "stream_backward", "sdm_write_read_backward"]
+__all__ = ["select_record", "record_of", "stream_forward", "stream_backward", "sdm_write_read_backward"]
 
 
 def _factor_scores(q: np.ndarray, subkeys: np.ndarray, factor_dims, d_sub: int, exact: bool) -> list:
@@ -84,16 +84,26 @@ def select_record(q: np.ndarray, subkeys: np.ndarray, factor_dims, d_sub: int, k
     return {"idx": idx, "digits": digits, "w": softmax_weights(S[idx]), "S": S[idx]}
 
 
+def record_of(q: np.ndarray, subkeys: np.ndarray, factor_dims, d_sub: int, idx) -> dict:
+    """select_record for slots a caller supplies (in its order), scored as the forward does."""
+    idx = np.asarray(idx, dtype=np.int64)
+    S = slot_scores(_factor_scores(q, subkeys, factor_dims, d_sub, False)).astype(np.float64)
+    digits = np.stack(np.unravel_index(idx, tuple(int(n) for n in factor_dims)), axis=1)
+    return {"idx": idx, "digits": digits, "w": softmax_weights(S[idx]), "S": S[idx]}
+
+
 def stream_forward(M: np.ndarray, q_w, q_r, k_val, gates, subkeys, *, factor_dims, d_sub: int, W: int,
                    R: int, act_dtype: str = "f32", bank_dtype: str = "f32", exact: bool = False,
-                   snapshot_dtype: Optional[str] = None) -> dict:
+                   snapshot_dtype: Optional[str] = None, pick: Optional[Callable] = None) -> dict:
     """The forward of one stream (M advances in place), keeping the backward's record.
 
     Same arithmetic as sdm_oracle.run_stream; additionally stores per token the write
     and read selections and the snapshot of the W rows before the write: exact, or
     rounded to ``snapshot_dtype`` (the forward itself uses the rows as they are).
     ``exact``: float64 scores (bank_dtype / act_dtype "f64" then make the whole forward
-    float64).
+    float64).  ``pick(t, which, idx, w)``: as in sdm_oracle.run_stream, may return other
+    slot ids (a different valid top-k at a near tie) whose weights are then the softmax
+    of their own slot scores.
     """
     T, d_v = q_w.shape[0], M.shape[1]
     y = np.zeros((T, d_v))
@@ -101,6 +111,13 @@ def stream_forward(M: np.ndarray, q_w, q_r, k_val, gates, subkeys, *, factor_dim
     for t in range(T):
         sw = select_record(q_w[t], subkeys, factor_dims, d_sub, W, exact)
         sr = select_record(q_r[t], subkeys, factor_dims, d_sub, R, exact)
+        if pick is not None:
+            alt = pick(t, 0, sw["idx"], sw["w"])
+            if alt is not None:
+                sw = record_of(q_w[t], subkeys, factor_dims, d_sub, alt)
+            alt = pick(t, 1, sr["idx"], sr["w"])
+            if alt is not None:
+                sr = record_of(q_r[t], subkeys, factor_dims, d_sub, alt)
         alpha, beta = float(gates[t, 0]), float(gates[t, 1])
         X = M[sw["idx"]].copy()
         m = alpha * X
@@ -173,14 +190,15 @@ def stream_backward(M: np.ndarray, fwd: dict, dy: np.ndarray, dM: np.ndarray, q_
 
 def sdm_write_read_backward(q_w, q_r, k_val, gates, subkeys, bank, dy, dbank, *, factor_dims, W: int, R: int,
                             act_dtype: str = "f32", bank_dtype: str = "f32", snapshot_dtype: Optional[str] = None,
-                            streams: Optional[Iterable] = None) -> dict:
+                            streams: Optional[Iterable] = None, pick: Optional[Callable] = None) -> dict:
     """Gradients of the write/read op over all (or the listed) streams.
 
     Inputs as sdm_oracle.sdm_write_read (bank [B,H,N,d_v] per stream); dy [B,T,H,d_v] and
     dbank [B,H,N,d_v]: the loss gradients with respect to y and the final bank.  Runs the
     forward with its record, then the reverse sweep, stream by stream.  Sub-key gradients
     of one head are summed over batch elements in increasing b.  Returns float64 arrays
-    shaped like the inputs.
+    shaped like the inputs.  ``pick(b, h)``, if given, returns the per-stream pick
+    passed to stream_forward (or None).
     """
     q_w, q_r, k_val, gates, subkeys = _f64(q_w), _f64(q_r), _f64(k_val), _f64(gates), _f64(subkeys)
     bank, dy, dbank = _f64(bank), _f64(dy), _f64(dbank)
@@ -194,7 +212,8 @@ def sdm_write_read_backward(q_w, q_r, k_val, gates, subkeys, bank, dy, dbank, *,
         M = bank[b, h].copy()
         fwd = stream_forward(M, q_w[b, :, h], q_r[b, :, h], k_val[b, :, h], gates[b, :, h], subkeys[h],
                              factor_dims=factor_dims, d_sub=d_sub, W=W, R=R, act_dtype=act_dtype,
-                             bank_dtype=bank_dtype, snapshot_dtype=snapshot_dtype)
+                             bank_dtype=bank_dtype, snapshot_dtype=snapshot_dtype,
+                             pick=None if pick is None else pick(b, h))
         g = stream_backward(M, fwd, dy[b, :, h], dbank[b, h], q_w[b, :, h], q_r[b, :, h], k_val[b, :, h],
                             gates[b, :, h], subkeys[h], factor_dims=factor_dims, d_sub=d_sub)
         out["bank"][b, h] = g["bank"]

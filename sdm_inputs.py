@@ -171,3 +171,25 @@ def make_decode_inputs(cfg: SdmConfig, steps: int, *, seed: Optional[int] = None
     bank = d.pop("bank_init")
     d["bank"] = bank.unsqueeze(0).expand(cfg.B, *bank.shape).contiguous()
     return d
+
+
+def make_grad_inputs(cfg: SdmConfig, *, seed: Optional[int] = None, T: Optional[int] = None,
+                     B: Optional[int] = None, dbank: bool = True) -> dict:
+    """Loss gradients for the backward of one ``make_inputs`` batch (CPU tensors).
+
+      dy     [B, T, H, d_v]  act dtype, N(0, 1): dL/dy
+      dbank  [B, H, N, d_v]  float32, N(0, 0.01^2): dL/d(final bank), or zeros when
+             ``dbank`` is False (y the only output that matters)
+    Drawn from a generator of its own (seed + 500), so the forward's inputs are the same
+    whether or not gradients are drawn.
+    """
+    seed = (cfg.seed if seed is None else seed) + 500
+    B = cfg.B if B is None else B
+    T = cfg.T if T is None else T
+    g = _gen(seed)
+    dy = torch.randn(B, T, cfg.H, cfg.d_v, generator=g).to(_TORCH_DTYPE[cfg.act_dtype]).contiguous()
+    if dbank:
+        db = 0.01 * torch.randn(B, cfg.H, cfg.N, cfg.d_v, generator=g)
+    else:
+        db = torch.zeros(B, cfg.H, cfg.N, cfg.d_v)
+    return {"dy": dy, "dbank": db.to(torch.float32).contiguous()}

@@ -112,6 +112,40 @@ def test_recording_forward_is_the_oracle_forward():
         assert np.array_equal(r["w"]["idx"], b["idx_w"][t]) and np.array_equal(r["r"]["idx"], b["idx_r"][t])
 
 
+def test_supplied_slots_follow_the_forward_oracle():
+    """A pick that hands back slots (its own, then a reordered and a substituted set) gives
+    the records run_stream computes for the same picks: same weights, y and bank."""
+    p = _problem(6)
+
+    def swap(t, which, idx, w):
+        if t % 3 == 0:
+            return None
+        alt = np.array(idx, dtype=np.int64)
+        if t % 3 == 1:
+            alt[[0, 1]] = alt[[1, 0]]
+        else:
+            others = np.setdiff1d(np.arange(int(np.prod(p["factor_dims"]))), alt)
+            alt[-1] = others[0]
+        return alt
+
+    M1 = p["bank"].astype(np.float32).astype(np.float64)
+    M2 = M1.copy()
+    a = bwd.stream_forward(M1, p["q_w"], p["q_r"], p["k_val"], p["gates"], p["subkeys"],
+                           factor_dims=p["factor_dims"], d_sub=p["d_sub"], W=p["W"], R=p["R"], pick=swap)
+    b = fwd_oracle.run_stream(M2, p["q_w"], p["q_r"], p["k_val"], p["gates"], p["subkeys"],
+                              factor_dims=p["factor_dims"], d_sub=p["d_sub"], W=p["W"], R=p["R"],
+                              act_dtype="f32", bank_dtype="f32", pick=swap)
+    assert np.array_equal(a["y"], b["y"]) and np.array_equal(M1, M2)
+    for t, r in enumerate(a["rec"]):
+        assert np.array_equal(r["w"]["idx"], b["idx_w"][t]) and np.array_equal(r["w"]["w"], b["wt_w"][t])
+        assert np.array_equal(r["r"]["idx"], b["idx_r"][t]) and np.array_equal(r["r"]["w"], b["wt_r"][t])
+        dig = np.stack(np.unravel_index(r["w"]["idx"], p["factor_dims"]), axis=1)
+        assert np.array_equal(r["w"]["digits"], dig)
+    own = bwd.record_of(p["q_w"][0], p["subkeys"], p["factor_dims"], p["d_sub"], a["rec"][0]["w"]["idx"])
+    for k in ("idx", "digits", "w", "S"):
+        assert np.array_equal(own[k], a["rec"][0]["w"][k]), k
+
+
 def test_identity_write_closed_form():
     # alpha = 1, beta = 0: the bank never changes; y_t = sum_j r_j M[i^r_j].  Then
     # dL/dM = c_M + sum_t scatter(i^r_t, r_t dy_t); the write passes nothing to the bank.
