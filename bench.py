@@ -37,7 +37,7 @@ import sdm_inputs  # noqa: E402
 METRIC = "SDM write/read tokens/s per layer on 1 GB300; achieved HBM GB/s vs roofline"
 UNIT = "tokens/s"
 WORKLOADS = {"layer": "layer", "train_fwd": "train_fwd", "three_factor": "three_factor",
-             "decode": "decode", "tiny": "tiny"}
+             "decode": "decode", "tiny": "tiny", "train": "train_fwd"}
 KERNEL_SOURCES = ("sdm_write_read.cu", "sdm_write_read_f32_f32.cu", "sdm_write_read_f32_bf16.cu",
                   "sdm_write_read_bf16_f32.cu", "sdm_write_read_bf16_bf16.cu", "sdm_wr_kernel.cuh",
                   "sdm_delta.cuh", "sdm_common.cuh", "sdm_internal.h")
@@ -308,6 +308,8 @@ def main():
 
     if cfg.T == 1:
         return bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg)
+    if args.workload == "train":
+        return bench_train(args, cfg, sdm, dev, rank, world, barrier, pg)
 
     d = sdm_inputs.make_inputs(cfg, seed=rank_seed(cfg, rank))
     g = {k: v.to(dev) for k, v in d.items()}
@@ -459,6 +461,104 @@ def main():
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+    return 0
+
+
+def bench_train(args, cfg, sdm, dev, rank, world, barrier, pg):
+    """Training step of the 32K-token shape: the forward with a snapshot of the rows each
+    token overwrites (sdm_write_read_train, bank reset from the learned table), then the
+    deterministic sparse backward (sdm_write_read_backward) with dL/dy drawn once and
+    dL/d(final bank) = 0 (a torch fill of the gradient table each step)."""
+    d = sdm_inputs.make_inputs(cfg, seed=rank_seed(cfg, rank))
+    gr = sdm_inputs.make_grad_inputs(cfg, seed=rank_seed(cfg, rank), dbank=False)
+    g = {k: v.to(dev) for k, v in d.items()}
+    dy = gr["dy"].to(dev)
+    B, T, H = cfg.B, cfg.T, cfg.H
+    bank = torch.empty((B, H, cfg.N, cfg.d_v), dtype=g["bank_init"].dtype, device=dev)
+    dbank = torch.zeros((B, H, cfg.N, cfg.d_v), dtype=torch.float32, device=dev)
+    shape = sdm.make_shape(B=B, T=T, H=H, factor_dims=cfg.factor_dims, d_sub=cfg.d_sub, d_v=cfg.d_v,
+                           W=cfg.W, R=cfg.R, chunk_size=cfg.chunk_size,
+                           act_dtype=0 if cfg.act_dtype == "f32" else 1,
+                           bank_dtype=0 if cfg.bank_dtype == "f32" else 1)
+    ws = torch.empty(sdm.write_read_workspace_size(shape), dtype=torch.uint8, device=dev)
+    bws = torch.empty(sdm.backward_workspace_size(shape), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    # a bfloat16 snapshot holds a bfloat16 bank exactly (half the bytes of a float32 one)
+    snap_dt = torch.bfloat16 if cfg.bank_dtype == "bf16" else torch.float32
+    saved = None
+    grads = None
+
+    def step():
+        nonlocal saved, grads
+        saved = sdm.sdm_write_read_train(g["q_w"], g["q_r"], g["k_val"], g["gates"], g["subkeys"], bank,
+                                         cfg.chunk_size, cfg.W, cfg.R, factor_dims=cfg.factor_dims,
+                                         bank_init=g["bank_init"], snapshot_dtype=snap_dt, saved=saved,
+                                         workspace=ws, stream=stream)
+        dbank.zero_()
+        grads = sdm.sdm_write_read_backward(g["q_w"], g["q_r"], g["k_val"], g["gates"], g["subkeys"], bank, dy,
+                                            saved, cfg.W, cfg.R, factor_dims=cfg.factor_dims, dbank=dbank,
+                                            grads=grads, workspace=bws, stream=stream)
+        grads.pop("workspace", None)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    assert sdm.last_device_error(ws) == 0 and sdm.last_device_error(bws) == 0
+
+    launches0 = sdm.launch_count()
+    sdm.profile_begin()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+    kt = sdm.profile_end()
+    launches = sdm.launch_count() - launches0
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
+    value = whole_job_rate(B * T * args.steps, world, ms)
+
+    sb = 4 if cfg.bank_dtype == "f32" else 2
+    se = 2 if snap_dt == torch.bfloat16 else 4
+    rows = B * T * H
+    # per token and column: forward W+R rows (+ the W snapshot rows written); backward
+    # reads the R read rows and the W snapshot rows, reads and writes the float32 gradient
+    # rows of both lists and writes the W restored rows
+    fwd_bytes = rows * cfg.d_v * ((cfg.W + cfg.R) * sb + cfg.W * se)
+    sweep_bytes = rows * cfg.d_v * (cfg.R * sb + 2 * 4 * (cfg.W + cfg.R) + cfg.W * se + cfg.W * sb)
+    peak, peak_kind = peaks()
+    per = {}
+    for name, nbytes in (("write_read", fwd_bytes), ("bwd_sweep", sweep_bytes)):
+        n, t = kt[name]
+        avg = t / max(n, 1) / 1e3
+        per[name] = {"bound": "hbm", "kernel": name, "achieved": nbytes / avg / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": nbytes / avg / 1e9 / peak, "traffic": None, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": nbytes, "launch_ms": avg * 1e3}
+    dominant = max(per, key=lambda k: per[k]["launch_ms"])
+    if rank != 0:
+        return 0
+    line = {
+        "metric": "SDM training step (forward with snapshot + deterministic sparse backward) tokens/s per layer "
+                  "on 1 GB300", "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg) + ", forward + backward",
+                   "snapshot_dtype": "bf16" if se == 2 else "f32",
+                   "l2": "inputs larger than L2: the bank is rewritten from the learned table every step",
+                   "step": "bank copy + scoring/top-k + chunk plan + write/read with snapshot + backward "
+                           "(flags, reverse sweep, column sums + softmax + dq, sub-key gradient); dL/d(final bank) "
+                           "zeroed by a torch fill"},
+        "roofline": per[dominant],
+        "rooflines": per,
+        "kernels_ms_per_step": {k: v[1] / max(v[0], 1) * (v[0] / args.steps) for k, v in kt.items() if v[0]},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": None,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 

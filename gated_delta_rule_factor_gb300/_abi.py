@@ -11,19 +11,21 @@ MAX_FACTORS = 4
 MAX_K = 128
 MAX_CANDIDATES = 1024
 MAX_CHUNK = 256
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 SDM_OK, SDM_ERR_INVALID_ARG, SDM_ERR_UNSUPPORTED, SDM_ERR_ALIAS, SDM_ERR_WORKSPACE, \
     SDM_ERR_CUDA, SDM_ERR_DEVICE = range(7)
 SDM_F32, SDM_BF16, SDM_F16 = 0, 1, 2
-KERNEL_KINDS = ("bank_copy", "score", "select", "plan_sort", "plan_link", "write_read", "decode")
+KERNEL_KINDS = ("bank_copy", "score", "select", "plan_sort", "plan_link", "write_read", "decode",
+                "bwd_flags", "bwd_sweep", "bwd_reduce", "bwd_subkeys")
 
 # Every function include/sdm.h declares, in header order.
 EXPORTS = (
     "sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
-    "sdm_decode_step", "sdm_last_device_error", "sdm_status_string", "sdm_last_error_message",
+    "sdm_write_read_static", "sdm_snapshot_bytes", "sdm_write_read_train",
+    "sdm_write_read_backward_workspace_size", "sdm_write_read_backward", "sdm_decode_step", "sdm_last_device_error", "sdm_status_string", "sdm_last_error_message",
     "sdm_abi_version", "sdm_launch_count", "sdm_profile_begin", "sdm_profile_end",
-    "sdm_kernel_name", "sdm_write_read_static", "sdm_test_stall_decode_copy",
+    "sdm_kernel_name", "sdm_test_stall_decode_copy",
     "sdm_test_force_write_read_layout", "sdm_test_force_simt_scorer",
 )
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -85,6 +87,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.sdm_write_read.argtypes = [sp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    ctypes.c_size_t, _P]
     lib.sdm_write_read_static.argtypes = [sp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.sdm_snapshot_bytes.argtypes = [sp, ctypes.c_int32, szp]
+    lib.sdm_write_read_train.argtypes = [sp] + [_P] * 13 + [ctypes.c_size_t, ctypes.c_int32, _P,
+                                                            ctypes.c_size_t, _P]
+    lib.sdm_write_read_backward_workspace_size.argtypes = [sp, szp]
+    lib.sdm_write_read_backward.argtypes = [sp] + [_P] * 10 + [ctypes.c_size_t, ctypes.c_int32] + \
+        [_P] * 9 + [ctypes.c_size_t, _P]
     lib.sdm_decode_step.argtypes = [sp, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _P,
                                     _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     lib.sdm_last_device_error.argtypes = [_P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int32), _P]
@@ -102,7 +110,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.sdm_test_force_write_read_layout.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.sdm_test_force_simt_scorer.argtypes = [ctypes.c_int]
     for name in ("sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
-                 "sdm_write_read_static", "sdm_decode_step", "sdm_last_device_error", "sdm_profile_begin", "sdm_profile_end"):
+                 "sdm_write_read_static", "sdm_decode_step", "sdm_last_device_error", "sdm_profile_begin", "sdm_profile_end",
+                 "sdm_snapshot_bytes", "sdm_write_read_train", "sdm_write_read_backward_workspace_size",
+                 "sdm_write_read_backward"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.sdm_abi_version() != ABI_VERSION:
         raise ImportError(f"SDM library ABI {lib.sdm_abi_version()} != binding ABI {ABI_VERSION}")

@@ -493,10 +493,25 @@ sdm_status side_stream(SideStream **out) {
 // The write/read op.  side_copy: run the learned-table copy on the library's side stream
 // of the device, concurrently with scoring, selection and planning (they touch no bank
 // row), and join it before the write/read kernel.
+// Snapshot of a training forward: where its data starts (after the header) and its type.
+struct SnapOut {
+  unsigned char *data;
+  int32_t bf16;
+};
+
+int64_t snapshot_pieces(const sdm_shape *sh) { return (sh->d_v * elem_bytes(sh->bank_dtype) + 31) / 32; }
+
+int64_t snapshot_bytes_of(const sdm_shape *sh, int32_t snap_dtype) {
+  const int64_t pc = 32 / elem_bytes(sh->bank_dtype);          // bank columns of a piece
+  return kSnapshotHeaderBytes +
+         sh->B * sh->H * sh->T * snapshot_pieces(sh) * (int64_t)sh->W * pc * elem_bytes(snap_dtype);
+}
+
 sdm_status write_read_impl(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
                            const float *gates, const void *subkeys, const void *bank_init, void *bank,
                            void *y, int32_t *idx_w, float *wt_w, int32_t *idx_r, float *wt_r,
-                           void *workspace, size_t workspace_bytes, sdm_stream_t stream, bool side_copy) {
+                           void *workspace, size_t workspace_bytes, sdm_stream_t stream, bool side_copy,
+                           const SnapOut *snap = nullptr) {
   Derived d;
   sdm_status st = check_shape(sh, false, &d);
   if (st != SDM_OK) return st;
@@ -662,6 +677,9 @@ sdm_status write_read_impl(const sdm_shape *sh, const void *q_w, const void *q_r
   wa.slices = wc.slices;
   wa.row_bytes = (int32_t)(sh->d_v * sb);
   wa.lay = wc.lay;
+  wa.snap = snap ? snap->data : nullptr;
+  wa.snap_bf16 = snap ? snap->bf16 : 0;
+  wa.pieces = (int32_t)snapshot_pieces(sh);
   const WriteReadLaunch wl_launch{wc.NCW, wc.LW, wc.smem};
   if (side) {                                          // the bank copy must land first
     ce = cudaStreamWaitEvent(cs, side->join, 0);
@@ -670,6 +688,156 @@ sdm_status write_read_impl(const sdm_shape *sh, const void *q_w, const void *q_r
   if ((st = run_kernel(SDM_KERNEL_WRITE_READ, cs, "write_read", [&] {
          return launch_write_read(wa, streams, sh->bank_dtype, sh->act_dtype, wl_launch, cs);
        })) != SDM_OK)
+    return st;
+  return ok();
+}
+
+// ---------------------------------------------------------------- backward
+
+constexpr int64_t kSubkeyChunk = 1024;        // rows of K = 2*B*T per split of the sub-key gradient
+
+struct BwdLayout {
+  int64_t flags, part, ds, dk_part, total;
+  int64_t P, PS, KS;
+};
+
+BwdLayout bwd_layout(const sdm_shape *sh, const Derived &d) {
+  BwdLayout w{};
+  const int64_t S = sh->B * sh->H, BT = sh->B * sh->T;
+  w.P = snapshot_pieces(sh);
+  w.PS = bwd_part_stride(sh->W, sh->R);
+  w.KS = (2 * BT + kSubkeyChunk - 1) / kSubkeyChunk;
+  int64_t o = kHeaderBytes;
+  w.flags = o;   o = a256(o + S * sh->T);
+  w.part = o;    o = a256(o + S * sh->T * w.P * w.PS * 4);
+  w.ds = o;      o = a256(o + sh->H * 2 * BT * (int64_t)d.ntot * 4);
+  w.dk_part = o; o = a256(o + w.KS * sh->H * (int64_t)d.ntot * sh->d_sub * 4);
+  w.total = o;
+  return w;
+}
+
+sdm_status check_snapshot_dtype(int32_t dt) {
+  if (dt == SDM_F16) return fail(SDM_ERR_UNSUPPORTED, "snapshot_dtype: float16 is not supported");
+  if (dt != SDM_F32 && dt != SDM_BF16) return fail(SDM_ERR_INVALID_ARG, "snapshot_dtype: unknown dtype %d", dt);
+  return SDM_OK;
+}
+
+sdm_status backward_impl(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
+                         const float *gates, const void *subkeys, const int32_t *idx_w, const float *wt_w,
+                         const int32_t *idx_r, const float *wt_r, void *snapshot, size_t snapshot_bytes,
+                         int32_t snap_dtype, void *bank, const void *dy, float *dbank, float *d_k_val,
+                         float *d_gates, float *d_q_w, float *d_q_r, float *d_subkeys, void *workspace,
+                         size_t workspace_bytes, sdm_stream_t stream) {
+  Derived d;
+  sdm_status st = check_shape(sh, false, &d);
+  if (st != SDM_OK) return st;
+  if ((st = check_snapshot_dtype(snap_dtype)) != SDM_OK) return st;
+  const int64_t ab = elem_bytes(sh->act_dtype), sb = elem_bytes(sh->bank_dtype);
+  const int64_t rows = sh->B * sh->T * sh->H;
+  const int64_t qbytes = rows * sh->F * sh->d_sub * ab;
+  const int64_t table = sh->B * sh->H * d.N * sh->d_v;
+  const int64_t skbytes = sh->H * d.ntot * sh->d_sub;
+  const Range r_qw{q_w, qbytes, "q_w"}, r_qr{q_r, qbytes, "q_r"}, r_kv{k_val, rows * sh->d_v * ab, "k_val"};
+  const Range r_g{gates, rows * 2 * 4, "gates"}, r_sk{subkeys, skbytes * ab, "subkeys"};
+  const Range r_iw{idx_w, rows * sh->W * 4, "idx_w"}, r_ww{wt_w, rows * sh->W * 4, "wt_w"};
+  const Range r_ir{idx_r, rows * sh->R * 4, "idx_r"}, r_wr{wt_r, rows * sh->R * 4, "wt_r"};
+  const Range r_dy{dy, rows * sh->d_v * ab, "dy"};
+  const Range r_snap{snapshot, (int64_t)snapshot_bytes, "snapshot"};
+  const Range r_b{bank, table * sb, "bank"}, r_db{dbank, table * 4, "dbank"};
+  const Range r_dkv{d_k_val, rows * sh->d_v * 4, "d_k_val"}, r_dg{d_gates, rows * 2 * 4, "d_gates"};
+  const Range r_dqw{d_q_w, rows * sh->F * sh->d_sub * 4, "d_q_w"}, r_dqr{d_q_r, rows * sh->F * sh->d_sub * 4, "d_q_r"};
+  const Range r_dsk{d_subkeys, skbytes * 4, "d_subkeys"};
+  const Range r_ws{workspace, (int64_t)workspace_bytes, "workspace"};
+  const int64_t need_snap = snapshot_bytes_of(sh, snap_dtype);
+  const BwdLayout bl = bwd_layout(sh, d);
+
+  const Range all[] = {r_qw, r_qr, r_kv, r_g, r_sk, r_iw, r_ww, r_ir, r_wr, r_dy, r_snap,
+                       r_b, r_db, r_dkv, r_dg, r_dqw, r_dqr, r_dsk};
+  if (rows > 0) {
+    for (const Range &r : all)
+      if (!r.p) return fail(SDM_ERR_INVALID_ARG, "%s is NULL", r.name);
+  } else if (!snapshot || (!d_subkeys && skbytes > 0)) {
+    return fail(SDM_ERR_INVALID_ARG, "%s is NULL", snapshot ? "d_subkeys" : "snapshot");
+  }
+  for (const Range &r : all)
+    if (r.p && !aligned(r.p, r.p == gates ? 8 : 16))
+      return fail(SDM_ERR_INVALID_ARG, "%s is not %d-byte aligned", r.name, r.p == gates ? 8 : 16);
+  if ((int64_t)snapshot_bytes < need_snap)
+    return fail(SDM_ERR_INVALID_ARG, "snapshot has %zu bytes, needs %lld", snapshot_bytes, (long long)need_snap);
+  if (!workspace) return fail(SDM_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 16)) return fail(SDM_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+  if ((int64_t)workspace_bytes < bl.total)
+    return fail(SDM_ERR_WORKSPACE, "workspace has %zu bytes, needs %lld", workspace_bytes, (long long)bl.total);
+  const Range ins[] = {r_qw, r_qr, r_kv, r_g, r_sk, r_iw, r_ww, r_ir, r_wr, r_dy};
+  const Range outs[] = {r_snap, r_b, r_db, r_dkv, r_dg, r_dqw, r_dqr, r_dsk, r_ws};
+  for (const Range &o : outs)
+    for (const Range &i : ins)
+      if (overlap(o, i)) return fail(SDM_ERR_ALIAS, "%s overlaps %s", o.name, i.name);
+  for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i)
+    for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+      if (overlap(outs[i], outs[j])) return fail(SDM_ERR_ALIAS, "%s overlaps %s", outs[i].name, outs[j].name);
+
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  int32_t *err = reinterpret_cast<int32_t *>(ws);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t ce = cudaMemsetAsync(err, 0, sizeof(int32_t), cs);
+  if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
+
+  BackwardArgs a{};
+  a.idx[0] = idx_w;
+  a.idx[1] = idx_r;
+  a.wt[0] = wt_w;
+  a.wt[1] = wt_r;
+  a.gates = gates;
+  a.q[0] = q_w;
+  a.q[1] = q_r;
+  a.k_val = k_val;
+  a.dy = dy;
+  a.subkeys = subkeys;
+  a.snap = static_cast<const unsigned char *>(snapshot) + kSnapshotHeaderBytes;
+  a.snap_hdr = static_cast<const int32_t *>(snapshot);
+  a.flags = ws + bl.flags;
+  a.bank = bank;
+  a.grad = dbank;
+  a.d_kv = d_k_val;
+  a.d_gates = d_gates;
+  a.d_q[0] = d_q_w;
+  a.d_q[1] = d_q_r;
+  a.d_subkeys = d_subkeys;
+  a.part = reinterpret_cast<float *>(ws + bl.part);
+  a.ds = reinterpret_cast<float *>(ws + bl.ds);
+  a.dk_part = reinterpret_cast<float *>(ws + bl.dk_part);
+  a.err = err;
+  a.B = sh->B;
+  a.T = sh->T;
+  a.N = d.N;
+  a.d_v = sh->d_v;
+  a.H = (int32_t)sh->H;
+  a.W = sh->W;
+  a.R = sh->R;
+  a.P = (int32_t)bl.P;
+  a.PS = (int32_t)bl.PS;
+  a.act_bf16 = sh->act_dtype == SDM_BF16;
+  a.snap_bf16 = snap_dtype == SDM_BF16;
+  a.KS = (int32_t)bl.KS;
+  a.k_chunk = kSubkeyChunk;
+  a.g = d.g;
+
+  if (rows > 0) {
+    if ((st = run_kernel(SDM_KERNEL_BWD_FLAGS, cs, "bwd_flags", [&] { return launch_bwd_flags(a, cs); })) != SDM_OK)
+      return st;
+    if ((st = run_kernel(SDM_KERNEL_BWD_SWEEP, cs, "bwd_sweep",
+                         [&] { return launch_bwd_sweep(a, sh->bank_dtype, cs); })) != SDM_OK)
+      return st;
+  }
+  // the snapshot is spent: a second backward through it is refused
+  ce = cudaMemsetAsync(snapshot, 0, sizeof(int32_t), cs);
+  if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
+  if (rows > 0 &&
+      (st = run_kernel(SDM_KERNEL_BWD_REDUCE, cs, "bwd_reduce", [&] { return launch_bwd_reduce(a, cs); })) != SDM_OK)
+    return st;
+  if ((st = run_kernel(SDM_KERNEL_BWD_SUBKEY, cs, "bwd_subkeys", [&] { return launch_bwd_subkeys(a, cs); })) !=
+      SDM_OK)
     return st;
   return ok();
 }
@@ -703,6 +871,78 @@ sdm_status sdm_write_read(const sdm_shape *sh, const void *q_w, const void *q_r,
                           void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
   return write_read_impl(sh, q_w, q_r, k_val, gates, subkeys, bank_init, bank, y, idx_w, wt_w, idx_r, wt_r,
                          workspace, workspace_bytes, stream, true);
+}
+
+sdm_status sdm_snapshot_bytes(const sdm_shape *shape, int32_t snapshot_dtype, size_t *bytes) {
+  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
+  sdm_status st = check_shape(shape, false, nullptr);
+  if (st != SDM_OK) return st;
+  if ((st = check_snapshot_dtype(snapshot_dtype)) != SDM_OK) return st;
+  *bytes = (size_t)snapshot_bytes_of(shape, snapshot_dtype);
+  return ok();
+}
+
+sdm_status sdm_write_read_train(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
+                                const float *gates, const void *subkeys, const void *bank_init, void *bank,
+                                void *y, int32_t *idx_w, float *wt_w, int32_t *idx_r, float *wt_r,
+                                void *snapshot, size_t snapshot_bytes, int32_t snapshot_dtype, void *workspace,
+                                size_t workspace_bytes, sdm_stream_t stream) {
+  sdm_status st = check_shape(sh, false, nullptr);
+  if (st != SDM_OK) return st;
+  if ((st = check_snapshot_dtype(snapshot_dtype)) != SDM_OK) return st;
+  const int64_t rows = sh->B * sh->T * sh->H;
+  if (!snapshot) return fail(SDM_ERR_INVALID_ARG, "snapshot is NULL");
+  if (!aligned(snapshot, 16)) return fail(SDM_ERR_INVALID_ARG, "snapshot is not 16-byte aligned");
+  const int64_t need = snapshot_bytes_of(sh, snapshot_dtype);
+  if ((int64_t)snapshot_bytes < need)
+    return fail(SDM_ERR_INVALID_ARG, "snapshot has %zu bytes, needs %lld", snapshot_bytes, (long long)need);
+  const Range r_snap{snapshot, (int64_t)snapshot_bytes, "snapshot"};
+  const Range sel[] = {{idx_w, rows * sh->W * 4, "idx_w"}, {wt_w, rows * sh->W * 4, "wt_w"},
+                       {idx_r, rows * sh->R * 4, "idx_r"}, {wt_r, rows * sh->R * 4, "wt_r"}};
+  for (const Range &r : sel) {
+    if (rows > 0 && !r.p) return fail(SDM_ERR_INVALID_ARG, "%s is NULL (the backward reads it)", r.name);
+    if (r.p && !aligned(r.p, 16)) return fail(SDM_ERR_INVALID_ARG, "%s is not 16-byte aligned", r.name);
+  }
+  Derived d;
+  check_shape(sh, false, &d);
+  const int64_t ab = elem_bytes(sh->act_dtype), sb = elem_bytes(sh->bank_dtype);
+  const Range others[] = {{q_w, rows * sh->F * sh->d_sub * ab, "q_w"}, {q_r, rows * sh->F * sh->d_sub * ab, "q_r"},
+                          {k_val, rows * sh->d_v * ab, "k_val"}, {gates, rows * 8, "gates"},
+                          {subkeys, sh->H * d.ntot * sh->d_sub * ab, "subkeys"},
+                          {bank_init, sh->H * d.N * sh->d_v * sb, "bank_init"},
+                          {bank, sh->B * sh->H * d.N * sh->d_v * sb, "bank"}, {y, rows * sh->d_v * ab, "y"},
+                          sel[0], sel[1], sel[2], sel[3],
+                          {workspace, (int64_t)workspace_bytes, "workspace"}};
+  for (const Range &o : others)
+    if (overlap(r_snap, o)) return fail(SDM_ERR_ALIAS, "snapshot overlaps %s", o.name);
+  const SnapOut so{static_cast<unsigned char *>(snapshot) + kSnapshotHeaderBytes, snapshot_dtype == SDM_BF16};
+  st = write_read_impl(sh, q_w, q_r, k_val, gates, subkeys, bank_init, bank, y, idx_w, wt_w, idx_r, wt_r,
+                       workspace, workspace_bytes, stream, true, &so);
+  if (st != SDM_OK) return st;
+  // armed for one backward, once the forward's kernels are done (stream order)
+  const cudaError_t ce = cudaMemsetAsync(snapshot, 0x5a, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
+  return ok();
+}
+
+sdm_status sdm_write_read_backward_workspace_size(const sdm_shape *shape, size_t *bytes) {
+  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
+  Derived d;
+  sdm_status st = check_shape(shape, false, &d);
+  if (st != SDM_OK) return st;
+  *bytes = (size_t)bwd_layout(shape, d).total;
+  return ok();
+}
+
+sdm_status sdm_write_read_backward(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
+                                   const float *gates, const void *subkeys, const int32_t *idx_w, const float *wt_w,
+                                   const int32_t *idx_r, const float *wt_r, void *snapshot, size_t snapshot_bytes,
+                                   int32_t snapshot_dtype, void *bank, const void *dy, float *dbank, float *d_k_val,
+                                   float *d_gates, float *d_q_w, float *d_q_r, float *d_subkeys, void *workspace,
+                                   size_t workspace_bytes, sdm_stream_t stream) {
+  return backward_impl(sh, q_w, q_r, k_val, gates, subkeys, idx_w, wt_w, idx_r, wt_r, snapshot, snapshot_bytes,
+                       snapshot_dtype, bank, dy, dbank, d_k_val, d_gates, d_q_w, d_q_r, d_subkeys, workspace,
+                       workspace_bytes, stream);
 }
 
 sdm_status sdm_decode_step(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
@@ -897,6 +1137,10 @@ const char *sdm_kernel_name(int32_t kind) {
     case SDM_KERNEL_PLAN_LINK: return "plan_link";
     case SDM_KERNEL_WRITE_READ: return "write_read";
     case SDM_KERNEL_DECODE: return "decode";
+    case SDM_KERNEL_BWD_FLAGS: return "bwd_flags";
+    case SDM_KERNEL_BWD_SWEEP: return "bwd_sweep";
+    case SDM_KERNEL_BWD_REDUCE: return "bwd_reduce";
+    case SDM_KERNEL_BWD_SUBKEY: return "bwd_subkeys";
   }
   return "unknown";
 }

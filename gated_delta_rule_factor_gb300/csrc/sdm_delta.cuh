@@ -169,6 +169,7 @@ template <int JB, bool FULL>
 struct BlockRows {
   int off[JB];
   float w[JB];
+  int j0;                                         // first row of this block
   int nb;                                         // rows of this block
   __device__ __forceinline__ BlockRows(int n, int rg, const uint16_t *rm, const float *wt, uint32_t wc) {
     if constexpr (FULL) {
@@ -185,9 +186,11 @@ struct BlockRows {
       w[1] = w4.y;
       w[2] = w4.z;
       w[3] = w4.w;
+      j0 = 4 * rg;
       nb = 4;
     } else {
-      const int b16 = (n + 15) >> 4, j0 = rg * b16;
+      const int b16 = (n + 15) >> 4;
+      j0 = rg * b16;
       nb = min(b16, max(n - j0, 0));
 #pragma unroll
       for (int s = 0; s < JB; ++s) {
@@ -205,11 +208,12 @@ struct BlockRows {
 // visible).  rm / wt: the token's W write then R read references (offsets o, weights).
 // When the token reads none of the rows it writes (overlap == false) the read rows are
 // fetched before the write: those rows hold the same values before and after it.  y is
-// left in every lane.  The caller orders tokens with __syncwarp().
-template <typename BANK, int JB, bool FULL>
+// left in every lane.  snap(j, raw) receives this lane's 16 bytes of write row j before
+// the write (the backward's snapshot).  The caller orders tokens with __syncwarp().
+template <typename BANK, int JB, bool FULL, class Snap>
 __device__ __forceinline__ void piece_token(int W, int R, const uint16_t *rm, const float *wt, float alpha,
                                             float beta, const float (&v)[PieceRow<BANK>::VEC], unsigned char *rows,
-                                            uint32_t wc, bool overlap, float (&y)[PieceRow<BANK>::VEC]) {
+                                            uint32_t wc, bool overlap, float (&y)[PieceRow<BANK>::VEC], Snap &&snap) {
   using PR = PieceRow<BANK>;
   constexpr int VEC = PR::VEC;
   if constexpr (FULL) W = R = 64;
@@ -226,6 +230,9 @@ __device__ __forceinline__ void piece_token(int W, int R, const uint16_t *rm, co
     for (int s = 0; s < JB; ++s)
       if (rd.has(s)) rr[s] = *reinterpret_cast<const uint4 *>(rows + rd.off[s]);
   }
+#pragma unroll
+  for (int s = 0; s < JB; ++s)
+    if (wr_.has(s)) snap(wr_.j0 + s, rw[s]);
   // p = sum_j w_j (alpha m_j)
   float am[JB][VEC];
   float a[VEC];

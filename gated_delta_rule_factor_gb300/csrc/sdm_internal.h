@@ -147,6 +147,13 @@ struct WriteReadArgs {
   int32_t slices;         // ceil(row bytes / RB)
   int32_t row_bytes;      // d_v * bank element bytes (the last slice may be partial)
   PlanLayout lay;
+  // Snapshot of the rows each token overwrites, taken before its write (NULL: none).
+  // Layout [B*H, T, P, W, PC] of the snapshot type, P = ceil(row_bytes / 32) 32-byte
+  // pieces of a bank row and PC = 32 / bank element bytes columns per piece: the rows a
+  // compute warp holds for one token are contiguous.
+  unsigned char *snap;
+  int32_t snap_bf16;      // snapshot rounded to bfloat16 (else float32, exact)
+  int32_t pieces;         // P
 };
 
 struct DecodeArgs {
@@ -168,6 +175,54 @@ struct DecodeArgs {
   int32_t test_stall_copy;  // test hook: the copy waits on a barrier nothing arrives at
   KeyGeometry g;
 };
+
+// The backward of the write/read op (sdm_backward.cu).  Stream s = b*H + h; row r of
+// a token = (b*T + t)*H + h.
+//   sweep: one warp per (stream, 32-byte piece p of every bank row) runs the tokens from
+//          last to first on its piece, with the bank (restored from the snapshot) and
+//          the gradient table G (float32) in global memory, and writes per-piece partial
+//          sums of the per-token scalars: part[s][t][p][PS], PS = align4(W + R + 2):
+//          dw_j (j < W), dr_j (W + j), dalpha (W + R), dbeta (W + R + 1).
+//   reduce: one warp per token row: sums the partials over p in increasing p, the
+//          softmax backward, the gate gradients, the dense factor-score gradients
+//          ds[h][kind][b*T + t][ntot] and the query gradients.
+//   subkey_grad: split-K tiles of dK_f = sum_k ds_f[k]^T q_f[k], then their sum in
+//          split order.
+struct BackwardArgs {
+  const int32_t *idx[2];  // idx_w [B,T,H,W], idx_r [B,T,H,R]
+  const float *wt[2];
+  const float *gates;     // [B,T,H,2]
+  const void *q[2];       // q_w, q_r [B,T,H,F*d_sub] (act)
+  const void *k_val;      // [B,T,H,d_v] (act)
+  const void *dy;         // [B,T,H,d_v] (act)
+  const void *subkeys;    // [H, ntot, d_sub] (act)
+  const unsigned char *snap;  // snapshot data (layout as WriteReadArgs::snap)
+  const int32_t *snap_hdr;    // the snapshot's header word (armed by the forward)
+  uint8_t *flags;         // [B*H*T] 1 if the token reads a row it writes
+  void *bank;             // [B,H,N,d_v] (bank type): final bank in, restored out
+  float *grad;            // [B,H,N,d_v]: dL/d(final bank) in, dL/d(initial bank) out
+  float *d_kv;            // [B,T,H,d_v]
+  float *d_gates;         // [B,T,H,2]
+  float *d_q[2];          // [B,T,H,F*d_sub]
+  float *d_subkeys;       // [H, ntot, d_sub]
+  float *part;            // [B*H, T, P, PS]
+  float *ds;              // [H, 2, B*T, ntot]
+  float *dk_part;         // [KS, H, ntot, d_sub]
+  int32_t *err;
+  int64_t B, T, N, d_v;
+  int32_t H, W, R, P, PS;
+  int32_t act_bf16, snap_bf16;
+  int32_t KS;             // split of the sub-key gradient's K = 2*B*T rows
+  int64_t k_chunk;        // rows per split (multiple of 16)
+  KeyGeometry g;
+};
+constexpr int32_t kSnapshotArmed = 0x5a5a5a5a;   // header word of a snapshot a backward may use
+constexpr int64_t kSnapshotHeaderBytes = 256;
+cudaError_t launch_bwd_flags(const BackwardArgs &a, cudaStream_t st);
+cudaError_t launch_bwd_sweep(const BackwardArgs &a, int bank_dtype, cudaStream_t st);
+cudaError_t launch_bwd_reduce(const BackwardArgs &a, cudaStream_t st);
+cudaError_t launch_bwd_subkeys(const BackwardArgs &a, cudaStream_t st);
+inline int32_t bwd_part_stride(int W, int R) { return (W + R + 2 + 3) & ~3; }
 
 // Raises a kernel's dynamic shared-memory limit to at least `smem` bytes on the current
 // device, once per (kernel, device, larger size): the attribute call is not repeated per

@@ -317,6 +317,34 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
   const int col = warp * PC + c * VEC;                           // this lane's first column in the slice
   const bool lane_valid = (2 * warp + c) < valid_chunks;
   ACT *y = static_cast<ACT *>(a.y);
+  // The snapshot of this warp's piece: rows of one token contiguous, [T][P][W][PC].
+  const bool snap_on = a.snap != nullptr;
+  const int snap_elem = a.snap_bf16 ? 2 : 4;
+  const int64_t snap_pcs = (int64_t)PC * snap_elem;                // bytes of one row piece
+  const int64_t snap_row_step = (int64_t)W * snap_pcs;             // one (token, piece)
+  const int64_t snap_tok_step = (int64_t)a.pieces * snap_row_step; // one token
+  const int piece = slice * NCW + warp;
+  const int64_t snap_lane = (int64_t)c * VEC * snap_elem;
+  auto snap_store = [&](unsigned char *dst, const uint4 &raw) {
+    dst += snap_lane;
+    if constexpr (sizeof(BANK) == 4) {
+      if (a.snap_bf16) {
+        float x[VEC];
+        PieceRow<BANK>::unpack(raw, x);
+        store_vec<__nv_bfloat16, VEC>(reinterpret_cast<__nv_bfloat16 *>(dst), x);
+      } else {
+        *reinterpret_cast<uint4 *>(dst) = raw;
+      }
+    } else {
+      if (a.snap_bf16) {
+        *reinterpret_cast<uint4 *>(dst) = raw;
+      } else {
+        float x[VEC];
+        PieceRow<BANK>::unpack(raw, x);
+        store_vec<float, VEC>(reinterpret_cast<float *>(dst), x);
+      }
+    }
+  };
   const int64_t ystep = (int64_t)a.H * a.d_v;
   // every lane waits (and acquires what the barrier publishes); the warp gives up as one.
   // (Letting lane 0 spin alone and the others check once measured ten times slower token
@@ -379,12 +407,16 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
     const int64_t t0 = (int64_t)g * G;
     const int nt = (int)min((int64_t)G, a.T - t0);
     ACT *ybase = y + ((b * a.T + t0) * a.H + h) * a.d_v + c0 + col;
+    unsigned char *snap_tok = snap_on ? a.snap + ((s * a.T + t0) * a.pieces + piece) * snap_row_step : nullptr;
     for (int t = 0; t < nt; ++t) {
       float v[VEC], out[VEC];
       load_vec<ACT, VEC>(vv + t * COLS + col, v);
       const float2 ab = *reinterpret_cast<const float2 *>(gt + 2 * t);
       piece_token<BANK, JB, FULL>(W, R, refmap + t * WR, wts + t * WR, ab.x, ab.y, v, rows, wc, tokflag[t] != 0,
-                                  out);
+                                  out, [&](int j, const uint4 &raw) {
+                                    if (snap_on && lane_valid) snap_store(snap_tok + (int64_t)j * snap_pcs, raw);
+                                  });
+      if (snap_on) snap_tok += snap_tok_step;
       if (rg == 0 && lane_valid) store_vec<ACT, VEC>(ybase + t * ystep, out);
       __syncwarp();
     }

@@ -150,6 +150,123 @@ def sdm_write_read_static(q_w: torch.Tensor, q_r: torch.Tensor, k_val: torch.Ten
     return y
 
 
+_SNAP_DT = {"f32": _abi.SDM_F32, "bf16": _abi.SDM_BF16, torch.float32: _abi.SDM_F32,
+            torch.bfloat16: _abi.SDM_BF16}
+
+
+def _snap_code(snapshot_dtype) -> int:
+    if snapshot_dtype in (_abi.SDM_F32, _abi.SDM_BF16) and isinstance(snapshot_dtype, int):
+        return snapshot_dtype
+    if snapshot_dtype not in _SNAP_DT:
+        raise TypeError(f"snapshot_dtype {snapshot_dtype!r} is not float32 or bfloat16")
+    return _SNAP_DT[snapshot_dtype]
+
+
+def snapshot_bytes(shape: _abi.SdmShape, snapshot_dtype=torch.float32) -> int:
+    n = ctypes.c_size_t(0)
+    _abi.check(_abi.load().sdm_snapshot_bytes(ctypes.byref(shape), _snap_code(snapshot_dtype), ctypes.byref(n)),
+               "sdm_snapshot_bytes")
+    return int(n.value)
+
+
+def backward_workspace_size(shape: _abi.SdmShape) -> int:
+    n = ctypes.c_size_t(0)
+    _abi.check(_abi.load().sdm_write_read_backward_workspace_size(ctypes.byref(shape), ctypes.byref(n)),
+               "sdm_write_read_backward_workspace_size")
+    return int(n.value)
+
+
+def sdm_write_read_train(q_w: torch.Tensor, q_r: torch.Tensor, k_val: torch.Tensor, gates: torch.Tensor,
+                         subkeys: torch.Tensor, bank: torch.Tensor, chunk_size: int, W: int, R: int, *,
+                         factor_dims: Sequence[int], bank_init: Optional[torch.Tensor] = None,
+                         snapshot_dtype=torch.float32, y: Optional[torch.Tensor] = None,
+                         saved: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """sdm_write_read that keeps what its backward needs: the selections and a snapshot of
+    the rows each token overwrites (float32, exact, or bfloat16).  The bank advances in
+    place.  Returns {"y", "idx_w", "wt_w", "idx_r", "wt_r", "snapshot", "snapshot_dtype"}
+    (``saved`` may pass those buffers in to be reused)."""
+    dev = q_w.device
+    shape = _shape_of(q_w, k_val, bank, factor_dims, W, R, chunk_size)
+    code = _snap_code(snapshot_dtype)
+    B, T, H = shape.B, shape.T, shape.H
+    if saved is None:
+        saved = {
+            "idx_w": torch.empty((B, T, H, W), dtype=torch.int32, device=dev),
+            "wt_w": torch.empty((B, T, H, W), dtype=torch.float32, device=dev),
+            "idx_r": torch.empty((B, T, H, R), dtype=torch.int32, device=dev),
+            "wt_r": torch.empty((B, T, H, R), dtype=torch.float32, device=dev),
+            "snapshot": torch.empty(snapshot_bytes(shape, code), dtype=torch.uint8, device=dev),
+        }
+    saved = dict(saved)
+    saved["snapshot_dtype"] = code
+    saved["y"] = torch.empty_like(k_val) if y is None else y
+    for name, t in (("q_w", q_w), ("q_r", q_r), ("k_val", k_val), ("gates", gates), ("subkeys", subkeys),
+                    ("bank", bank), ("bank_init", bank_init), ("y", saved["y"]), ("idx_w", saved["idx_w"]),
+                    ("wt_w", saved["wt_w"]), ("idx_r", saved["idx_r"]), ("wt_r", saved["wt_r"]),
+                    ("snapshot", saved["snapshot"]), ("workspace", workspace)):
+        _require_cuda_contig(name, t, dev)
+    if gates.dtype != torch.float32:
+        raise TypeError("gates must be float32")
+    if workspace is None:
+        workspace = torch.empty(write_read_workspace_size(shape), dtype=torch.uint8, device=dev)
+    snap = saved["snapshot"]
+    st = _abi.load().sdm_write_read_train(
+        ctypes.byref(shape), _ptr(q_w), _ptr(q_r), _ptr(k_val), _ptr(gates), _ptr(subkeys), _ptr(bank_init),
+        _ptr(bank), _ptr(saved["y"]), _ptr(saved["idx_w"]), _ptr(saved["wt_w"]), _ptr(saved["idx_r"]),
+        _ptr(saved["wt_r"]), _ptr(snap), snap.numel() * snap.element_size(), code, _ptr(workspace),
+        workspace.numel(), _stream_handle(stream, dev))
+    _abi.check(st, "sdm_write_read_train")
+    return saved
+
+
+def sdm_write_read_backward(q_w: torch.Tensor, q_r: torch.Tensor, k_val: torch.Tensor, gates: torch.Tensor,
+                            subkeys: torch.Tensor, bank: torch.Tensor, dy: torch.Tensor, saved: dict,
+                            W: int, R: int, *, factor_dims: Sequence[int], dbank: Optional[torch.Tensor] = None,
+                            grads: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """The backward of one sdm_write_read_train call (``saved`` is what it returned).
+
+    bank: the bank the forward left; restored in place to the bank before it.  dy:
+    dL/dy.  dbank: float32 dL/d(final bank) (zeros when None), overwritten in place with
+    dL/d(initial bank).  Returns float32 gradients {"bank", "k_val", "gates", "q_w",
+    "q_r", "subkeys"} (``grads`` may pass those buffers in).  A second backward through
+    the same ``saved`` is refused by the library (SDM_DEVERR_SNAPSHOT, bank untouched).
+    """
+    dev = q_w.device
+    shape = _shape_of(q_w, k_val, bank, factor_dims, W, R, 1)
+    f32 = dict(dtype=torch.float32, device=dev)
+    if dbank is None:
+        dbank = torch.zeros(bank.shape, **f32)
+    if grads is None:
+        grads = {"k_val": torch.empty(k_val.shape, **f32), "gates": torch.empty(gates.shape, **f32),
+                 "q_w": torch.empty(q_w.shape, **f32), "q_r": torch.empty(q_r.shape, **f32),
+                 "subkeys": torch.empty(subkeys.shape, **f32)}
+    grads = dict(grads)
+    grads["bank"] = dbank
+    snap = saved["snapshot"]
+    for name, t in (("q_w", q_w), ("q_r", q_r), ("k_val", k_val), ("gates", gates), ("subkeys", subkeys),
+                    ("bank", bank), ("dy", dy), ("dbank", dbank), ("snapshot", snap), ("workspace", workspace),
+                    ("idx_w", saved["idx_w"]), ("wt_w", saved["wt_w"]), ("idx_r", saved["idx_r"]),
+                    ("wt_r", saved["wt_r"])) + tuple((f"grads[{k}]", v) for k, v in grads.items()):
+        _require_cuda_contig(name, t, dev)
+    if dbank.dtype != torch.float32 or any(g.dtype != torch.float32 for g in grads.values()):
+        raise TypeError("gradient buffers must be float32")
+    if dy.dtype != k_val.dtype:
+        raise TypeError("dy must have the activations' dtype")
+    if workspace is None:
+        workspace = torch.empty(backward_workspace_size(shape), dtype=torch.uint8, device=dev)
+    st = _abi.load().sdm_write_read_backward(
+        ctypes.byref(shape), _ptr(q_w), _ptr(q_r), _ptr(k_val), _ptr(gates), _ptr(subkeys),
+        _ptr(saved["idx_w"]), _ptr(saved["wt_w"]), _ptr(saved["idx_r"]), _ptr(saved["wt_r"]), _ptr(snap),
+        snap.numel() * snap.element_size(), int(saved["snapshot_dtype"]), _ptr(bank), _ptr(dy), _ptr(dbank),
+        _ptr(grads["k_val"]), _ptr(grads["gates"]), _ptr(grads["q_w"]), _ptr(grads["q_r"]),
+        _ptr(grads["subkeys"]), _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    _abi.check(st, "sdm_write_read_backward")
+    grads["workspace"] = workspace
+    return grads
+
+
 def _owns_storage(t: torch.Tensor) -> bool:
     """True when writing into t cannot reach another tensor's data (the donate guards).
 

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define SDM_ABI_VERSION 1
+#define SDM_ABI_VERSION 2
 
 /* Compiled limits.  Shapes beyond them are refused with SDM_ERR_UNSUPPORTED. */
 #define SDM_MAX_FACTORS 4          /* product-key factors F                          */
@@ -85,6 +85,7 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1, SDM_F16 = 2 /* always refused */ } sdm
 #define SDM_DEVERR_SLOT_RANGE 1    /* a selected slot id outside [0, N)                */
 #define SDM_DEVERR_PLAN 2          /* a chunk plan count or row index out of range     */
 #define SDM_DEVERR_TIMEOUT 3       /* a bounded wait inside a kernel gave up             */
+#define SDM_DEVERR_SNAPSHOT 4      /* a backward found no armed snapshot (second backward) */
 
 /*
  * Shape of one call.  Tensors (row-major, contiguous):
@@ -170,6 +171,82 @@ sdm_status sdm_write_read_static(const sdm_shape *shape, const void *q_w, const 
                                  float *wt_w, int32_t *idx_r, float *wt_r, sdm_stream_t stream);
 
 /*
+ * Training: the forward with a snapshot, then the deterministic sparse backward
+ * (CHANGELOG 2.0.0 > New: "exact product-key top-k with a deterministic sparse
+ * backward"; > Deterministic: every gradient is bitwise repeatable; > Package: training
+ * saves a snapshot of the rows each step overwrites, float32 by default or bf16 at half
+ * the size; > Behavior changes: the first backward restores the bank in place and a
+ * second backward through the same forward is refused).
+ *
+ * The gradient is the chain rule through the forward above, per stream, from the last
+ * token to the first.  With X_j the token's W rows before its write, m_j = alpha X_j,
+ * u = v - sum_j w_j m_j, G = dL/d(bank after the token) and dy = dL/dy[b,t,h]:
+ *   read:    dr_j = <dy, M[i^r_j]> (the rows after the write);  G[i^r_j] += r_j dy
+ *   write:   dv = beta sum_j w_j G[i_j];  dm_j = G[i_j] - w_j dv;
+ *            dw_j = beta <G[i_j], u> - <dv, m_j>;  dbeta = sum_j w_j <G[i_j], u>;
+ *            dalpha = sum_j <dm_j, X_j>;  G[i_j] <- alpha dm_j;  M[i_j] <- X_j
+ *   weights: dS_j = w_j (dw_j - sum_k w_k dw_k) (and the same for the read weights);
+ *   scores:  the slot score is the sum of the factor scores, so dS_j flows to each
+ *            factor's score of the slot, and from s_f[a] = <q_f, K_f[a]> to the query
+ *            and the sub-key.
+ * Readings where the pages are silent: the selected slot ids are piecewise constant
+ * (no gradient flows through the choice); float32 roundings of scores, stored rows and
+ * outputs pass the gradient unchanged; the gate gradients are with respect to the
+ * post-sigmoid (alpha, beta) the op takes.
+ */
+
+/* Bytes of a snapshot buffer for `shape` (snapshot_dtype SDM_F32, exact, or SDM_BF16,
+ * rows rounded to bfloat16; on a bfloat16 bank both are exact).  The buffer holds a
+ * 256-byte header and, per stream and token, the W rows the token overwrites, in a
+ * layout private to the library. */
+sdm_status sdm_snapshot_bytes(const sdm_shape *shape, int32_t snapshot_dtype, size_t *bytes);
+
+/* sdm_write_read that also fills `snapshot` (>= sdm_snapshot_bytes bytes, 16-byte
+ * aligned) and arms it for one backward.  idx_w, wt_w, idx_r, wt_r are required here
+ * (16-byte aligned): the backward reads the selections from them.  y, the bank and
+ * the selections are bitwise those of sdm_write_read, whatever the snapshot type.
+ * Takes sdm_write_read's workspace. */
+sdm_status sdm_write_read_train(const sdm_shape *shape, const void *q_w, const void *q_r,
+                                const void *k_val, const float *gates, const void *subkeys,
+                                const void *bank_init, void *bank, void *y, int32_t *idx_w,
+                                float *wt_w, int32_t *idx_r, float *wt_r, void *snapshot,
+                                size_t snapshot_bytes, int32_t snapshot_dtype, void *workspace,
+                                size_t workspace_bytes, sdm_stream_t stream);
+
+/* Device bytes of workspace sdm_write_read_backward needs for `shape` (depends only on
+ * the shape). */
+sdm_status sdm_write_read_backward_workspace_size(const sdm_shape *shape, size_t *bytes);
+
+/*
+ * The backward of one sdm_write_read_train call.
+ *   q_w ... subkeys, idx_*, wt_*  the forward's inputs and selections, unchanged since;
+ *   snapshot   the forward's snapshot and its type; the backward disarms it.  A
+ *              snapshot that is not armed (never filled, or already used) makes the
+ *              call touch neither the bank nor dbank, record SDM_DEVERR_SNAPSHOT and
+ *              leave the other outputs unspecified;
+ *   bank       [B,H,N,d_v] in: the bank the forward left; out: the bank before the
+ *              forward (the rows the forward wrote are restored from the snapshot, so
+ *              with a bfloat16 snapshot of a float32 bank they come back rounded);
+ *   dy         [B,T,H,d_v] act_dtype: dL/dy;
+ *   dbank      [B,H,N,d_v] float32 in: dL/d(bank after the forward); out: dL/d(bank
+ *              before it) (zeros in: y is the only output that matters);
+ *   d_k_val    [B,T,H,d_v], d_gates [B,T,H,2], d_q_w / d_q_r [B,T,H,F*d_sub],
+ *   d_subkeys  [H, sum_f n_f, d_sub]: float32 outputs (sub-key gradients summed over
+ *              the batch).
+ * Every pointer is 16-byte aligned and non-NULL (when B*T*H > 0).  Outputs must not
+ * overlap inputs or each other.  Gradients are bitwise repeatable: every sum runs in a
+ * fixed order (no float atomics) that depends only on the shape.
+ */
+sdm_status sdm_write_read_backward(const sdm_shape *shape, const void *q_w, const void *q_r,
+                                   const void *k_val, const float *gates, const void *subkeys,
+                                   const int32_t *idx_w, const float *wt_w, const int32_t *idx_r,
+                                   const float *wt_r, void *snapshot, size_t snapshot_bytes,
+                                   int32_t snapshot_dtype, void *bank, const void *dy, float *dbank,
+                                   float *d_k_val, float *d_gates, float *d_q_w, float *d_q_r,
+                                   float *d_subkeys, void *workspace, size_t workspace_bytes,
+                                   sdm_stream_t stream);
+
+/*
  * One decode step (shape->T must be 1; chunk_size is ignored) for all B*H streams.
  * Tensors as above with T = 1.
  *   bank_in         the state's tables: [B, H, N, d_v], or, with bank_in_shared != 0,
@@ -222,7 +299,11 @@ enum {
   SDM_KERNEL_PLAN_LINK = 4,
   SDM_KERNEL_WRITE_READ = 5,
   SDM_KERNEL_DECODE = 6,
-  SDM_NUM_KERNEL_KINDS = 7
+  SDM_KERNEL_BWD_FLAGS = 7,   /* backward: tokens that read a row they write            */
+  SDM_KERNEL_BWD_SWEEP = 8,   /* backward: reverse sweep over the rows, bank restored   */
+  SDM_KERNEL_BWD_REDUCE = 9,  /* backward: column sums, softmax backward, dq            */
+  SDM_KERNEL_BWD_SUBKEY = 10, /* backward: sub-key gradient tiles and their sum         */
+  SDM_NUM_KERNEL_KINDS = 11
 };
 typedef struct {
   int64_t launches[SDM_NUM_KERNEL_KINDS];
