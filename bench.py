@@ -275,6 +275,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's T (smaller cases for profiler captures)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's B (smaller cases for profiler captures)")
     ap.add_argument("--wr-slice", type=int, default=0, choices=[0, 32, 128, 256],
                     help="tuning: force the write/read kernel's row slice per CTA in bytes (0 = automatic)")
     ap.add_argument("--wr-stage", type=int, default=0,
@@ -285,6 +287,8 @@ def main():
     cfg = sdm_inputs.CONFIGS[WORKLOADS[args.workload]]
     if args.seq_len > 0 and cfg.T > 1:
         cfg = dataclasses.replace(cfg, T=args.seq_len)
+    if args.batch > 0:
+        cfg = dataclasses.replace(cfg, B=args.batch)
 
     if args.impl == "reference":
         return reference_arm(args, cfg, rank, world)

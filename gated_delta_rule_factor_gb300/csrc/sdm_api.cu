@@ -704,7 +704,7 @@ struct BwdLayout {
 BwdLayout bwd_layout(const sdm_shape *sh, const Derived &d) {
   BwdLayout w{};
   const int64_t S = sh->B * sh->H, BT = sh->B * sh->T;
-  w.P = snapshot_pieces(sh);
+  w.P = (sh->d_v * elem_bytes(sh->bank_dtype) + 16 * kSweepCG - 1) / (16 * kSweepCG);
   w.PS = bwd_part_stride(sh->W, sh->R);
   w.KS = (2 * BT + kSubkeyChunk - 1) / kSubkeyChunk;
   int64_t o = kHeaderBytes;
@@ -816,6 +816,7 @@ sdm_status backward_impl(const sdm_shape *sh, const void *q_w, const void *q_r, 
   a.W = sh->W;
   a.R = sh->R;
   a.P = (int32_t)bl.P;
+  a.P32 = (int32_t)snapshot_pieces(sh);
   a.PS = (int32_t)bl.PS;
   a.act_bf16 = sh->act_dtype == SDM_BF16;
   a.snap_bf16 = snap_dtype == SDM_BF16;

@@ -27,7 +27,8 @@ namespace sdm {
 
 namespace {
 
-constexpr int kSweepWarps = 2;      // independent warps per CTA of the sweep
+constexpr int kSweepWarps = 2;      // warps per CTA of the sweep (adjacent pieces of the rows)
+constexpr bool kSweepLockstep = false;  // the CTA's warps meet at a barrier after every token
 constexpr int kReduceWarps = 4;
 constexpr int kFlagWarps = kThreads / 32;
 
@@ -83,40 +84,52 @@ __device__ __forceinline__ void load_act(const void *base, int64_t e, bool bf16,
   else load_vec<float, V>(static_cast<const float *>(base) + e, o);
 }
 
-// The sum over the 16 row blocks of a warp (lane bits 1-4), as in the forward's token step.
-template <int V>
+// The sum over the row blocks of a warp (the lane bits above the column group's), a
+// balanced tree in block order.
+template <int CG, int V>
 __device__ __forceinline__ void row_block_sum(float (&x)[V]) {
 #pragma unroll
-  for (int o = 2; o < 32; o <<= 1)
+  for (int o = CG; o < 32; o <<= 1)
 #pragma unroll
     for (int c = 0; c < V; ++c) x[c] = __fadd_rn(x[c], __shfl_xor_sync(0xffffffffu, x[c], o));
 }
 
-// This lane's rows of one selection of token row r: block rg of ceil(n/16) rows.  A slot
-// id outside [0, N) is reported and its row skipped.
-template <int JB, bool FULL>
+// This lane's rows of one selection of token row r: block rg of ceil(n / RG) rows (RG row
+// groups per warp).  FULL: n == 64, JB = 64 / RG rows read as vectors.  A slot id
+// outside [0, N) is reported and its row skipped.
+template <int RG, int JB, bool FULL>
 struct LaneRefs {
   int32_t idx[JB];
   float w[JB];
   int j0, nb;
   __device__ __forceinline__ void load(const int32_t *ids, const float *wts, int n, int rg) {
     if constexpr (FULL) {
-      j0 = 4 * rg;
-      nb = 4;
-      const int4 i4 = *reinterpret_cast<const int4 *>(ids + j0);
-      const float4 w4 = *reinterpret_cast<const float4 *>(wts + j0);
-      idx[0] = i4.x;
-      idx[1] = i4.y;
-      idx[2] = i4.z;
-      idx[3] = i4.w;
-      w[0] = w4.x;
-      w[1] = w4.y;
-      w[2] = w4.z;
-      w[3] = w4.w;
+      static_assert(JB * RG == 64 && (JB == 2 || JB == 4), "FULL lanes hold 2 or 4 rows");
+      j0 = JB * rg;
+      nb = JB;
+      if constexpr (JB == 4) {
+        const int4 i4 = *reinterpret_cast<const int4 *>(ids + j0);
+        const float4 w4 = *reinterpret_cast<const float4 *>(wts + j0);
+        idx[0] = i4.x;
+        idx[1] = i4.y;
+        idx[2] = i4.z;
+        idx[3] = i4.w;
+        w[0] = w4.x;
+        w[1] = w4.y;
+        w[2] = w4.z;
+        w[3] = w4.w;
+      } else {
+        const int2 i2 = *reinterpret_cast<const int2 *>(ids + j0);
+        const float2 w2 = *reinterpret_cast<const float2 *>(wts + j0);
+        idx[0] = i2.x;
+        idx[1] = i2.y;
+        w[0] = w2.x;
+        w[1] = w2.y;
+      }
     } else {
-      const int b16 = (n + 15) >> 4;
-      j0 = rg * b16;
-      nb = min(b16, max(n - j0, 0));
+      const int bk = (n + RG - 1) / RG;
+      j0 = rg * bk;
+      nb = min(bk, max(n - j0, 0));
 #pragma unroll
       for (int s = 0; s < JB; ++s) {
         idx[s] = s < nb ? ids[j0 + s] : 0;
@@ -129,47 +142,49 @@ struct LaneRefs {
   }
 };
 
-template <int JB, bool FULL>
+template <int RG, int JB, bool FULL>
 struct TokenRefs {
-  LaneRefs<JB, FULL> wr, rd;
+  LaneRefs<RG, JB, FULL> wr, rd;
   float2 ab;
   int flag;
 };
 
-// One warp per (stream, piece p of PC = 32 / sizeof(BANK) columns); lane = 2*rg + c: c
-// picks the 16-byte half of the piece's bank columns (VEC columns), rg a block of rows,
-// exactly as the forward's token step lays them out.  The warp runs the stream's tokens
-// from last to first on its columns alone; its global-memory traffic is ordered by
-// __syncwarp between dependent phases (the bank and G rows of one column are only ever
-// touched by this warp).
-template <typename BANK, int JB, bool FULL>
+// One warp per (stream, piece p of CG 16-byte column groups of every bank row): lane =
+// CG*rg + c, c picks the column group (VEC columns), rg (RG = 32 / CG of them) a block of
+// consecutive rows of each sum.  The warp runs the stream's tokens from last to first on
+// its columns alone; its global-memory traffic is ordered by __syncwarp between
+// dependent phases (the bank and G entries of one column are only ever touched by this
+// warp).  The snapshot is read in the forward's layout (32-byte pieces).
+template <typename BANK, int CG, int JB, bool FULL>
 __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __grid_constant__ BackwardArgs a) {
   constexpr int VEC = 16 / (int)sizeof(BANK);
-  constexpr int PC = 2 * VEC;
+  constexpr int RG = 32 / CG;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p = blockIdx.x * kSweepWarps + warp;
   const int64_t s = blockIdx.y;
-  if (p >= a.P) return;
   if (*a.snap_hdr != kSnapshotArmed) {          // no snapshot to undo: touch nothing
     if (lane == 0 && p == 0) raise_error(a.err, SDM_DEVERR_SNAPSHOT);
-    return;
+    return;                                     // (the whole CTA reads the same word)
   }
+  if (!kSweepLockstep && p >= a.P) return;
   const int W = FULL ? 64 : a.W, R = FULL ? 64 : a.R;
-  const int rg = lane >> 1, c = lane & 1;
-  const int64_t col = (int64_t)p * PC + c * VEC;
-  const bool valid = col < a.d_v;
+  const int rg = lane / CG, c = lane % CG;
+  const int64_t col = ((int64_t)p * CG + c) * VEC;
+  const bool valid = col < a.d_v;               // false for a whole warp past the last piece
   const int64_t b = s / a.H, h = s % a.H;
   const int64_t N = a.N, d_v = a.d_v;
   BANK *bank = static_cast<BANK *>(a.bank) + s * N * d_v + col;
   float *grad = a.grad + s * N * d_v + col;
   const bool sbf = a.snap_bf16 != 0;
-  const int64_t pcs = (int64_t)PC * (sbf ? 2 : 4);                 // snapshot bytes of a row piece
-  const unsigned char *snap_sp = a.snap + ((s * a.T) * a.P + p) * (int64_t)W * pcs + c * VEC * (sbf ? 2 : 4);
-  const int64_t snap_tstep = (int64_t)a.P * W * pcs;
+  const int se = sbf ? 2 : 4;
+  const int64_t pcs = 2 * VEC * se;                  // snapshot bytes of a row's 32-byte piece
+  const int64_t p32 = col / (2 * VEC), half = (col / VEC) & 1;
+  const unsigned char *snap_sp = a.snap + ((s * a.T) * a.P32 + p32) * (int64_t)W * pcs + half * VEC * se;
+  const int64_t snap_tstep = (int64_t)a.P32 * W * pcs;
   const bool abf = a.act_bf16 != 0;
 
   auto refs_of = [&](int64_t t) {
-    TokenRefs<JB, FULL> k;
+    TokenRefs<RG, JB, FULL> k;
     const int64_t r = (b * a.T + t) * a.H + h;
     k.wr.load(a.idx[0] + r * W, a.wt[0] + r * W, W, rg);
     k.rd.load(a.idx[1] + r * R, a.wt[1] + r * R, R, rg);
@@ -178,11 +193,11 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
     return k;
   };
 
-  TokenRefs<JB, FULL> cur = refs_of(a.T - 1);
+  TokenRefs<RG, JB, FULL> cur = refs_of(a.T - 1);
   for (int64_t t = a.T - 1; t >= 0; --t) {
-    const TokenRefs<JB, FULL> nxt = t > 0 ? refs_of(t - 1) : cur;
+    const TokenRefs<RG, JB, FULL> nxt = t > 0 ? refs_of(t - 1) : cur;
     const int64_t r = (b * a.T + t) * a.H + h;
-    const LaneRefs<JB, FULL> &wr_ = cur.wr, &rd = cur.rd;
+    const LaneRefs<RG, JB, FULL> &wr_ = cur.wr, &rd = cur.rd;
     bool bad = false;
     float dyv[VEC], vv[VEC];
 #pragma unroll
@@ -251,8 +266,8 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
         sg[i] = __fmaf_rn(wr_.w[q], gw[q][i], sg[i]);
       }
     }
-    row_block_sum<VEC>(sp_);
-    row_block_sum<VEC>(sg);
+    row_block_sum<CG, VEC>(sp_);
+    row_block_sum<CG, VEC>(sg);
     float dv[VEC], u[VEC];
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
@@ -285,31 +300,39 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
     // partial column sums of this piece: the row sums over its two halves, dalpha and
     // dbeta over the whole warp (a fixed butterfly)
 #pragma unroll
-    for (int q = 0; q < JB; ++q) {
-      dwp[q] = __fadd_rn(dwp[q], __shfl_xor_sync(0xffffffffu, dwp[q], 1));
-      drp[q] = __fadd_rn(drp[q], __shfl_xor_sync(0xffffffffu, drp[q], 1));
-    }
+    for (int o = 1; o < CG; o <<= 1)
+#pragma unroll
+      for (int q = 0; q < JB; ++q) {
+        dwp[q] = __fadd_rn(dwp[q], __shfl_xor_sync(0xffffffffu, dwp[q], o));
+        drp[q] = __fadd_rn(drp[q], __shfl_xor_sync(0xffffffffu, drp[q], o));
+      }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       dap = __fadd_rn(dap, __shfl_xor_sync(0xffffffffu, dap, o));
       dbp = __fadd_rn(dbp, __shfl_xor_sync(0xffffffffu, dbp, o));
     }
-    float *pp = a.part + ((s * a.T + t) * a.P + p) * (int64_t)a.PS;
-    if constexpr (FULL) {
+    float *pp = a.part + ((s * a.T + t) * a.P + min(p, a.P - 1)) * (int64_t)a.PS;
+    const bool own = p < a.P;                       // (a lockstep CTA's warps past the last piece write nothing)
+    if (!own) {
+    } else if constexpr (FULL && JB == 4) {
       if (c == 0) *reinterpret_cast<float4 *>(pp + wr_.j0) = make_float4(dwp[0], dwp[1], dwp[2], dwp[3]);
-      else *reinterpret_cast<float4 *>(pp + W + rd.j0) = make_float4(drp[0], drp[1], drp[2], drp[3]);
+      if (c == CG - 1) *reinterpret_cast<float4 *>(pp + W + rd.j0) = make_float4(drp[0], drp[1], drp[2], drp[3]);
+    } else if constexpr (FULL && JB == 2) {
+      if (c == 0) *reinterpret_cast<float2 *>(pp + wr_.j0) = make_float2(dwp[0], dwp[1]);
+      if (c == CG - 1) *reinterpret_cast<float2 *>(pp + W + rd.j0) = make_float2(drp[0], drp[1]);
     } else {
       if (c == 0) {
 #pragma unroll
         for (int q = 0; q < JB; ++q)
           if (q < wr_.nb) pp[wr_.j0 + q] = dwp[q];
-      } else {
+      }
+      if (c == CG - 1) {
 #pragma unroll
         for (int q = 0; q < JB; ++q)
           if (q < rd.nb) pp[W + rd.j0 + q] = drp[q];
       }
     }
-    if (lane == 0) {
+    if (lane == 0 && own) {
       pp[W + R] = dap;
       pp[W + R + 1] = dbp;
     }
@@ -318,7 +341,8 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
       for (int q = 0; q < JB; ++q) bad |= !wr_.has(q, N) || !rd.has(q, N);
     }
     if (bad) raise_error(a.err, SDM_DEVERR_SLOT_RANGE);
-    __syncwarp();                                   // this token's stores before the next one's loads
+    if constexpr (kSweepLockstep) __syncthreads();
+    else __syncwarp();                              // this token's stores before the next one's loads
     cur = nxt;
   }
 }
@@ -335,25 +359,32 @@ __device__ __forceinline__ float load_act1(const void *base, int64_t e, bool bf1
   return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[e]) : static_cast<const float *>(base)[e];
 }
 
+// Eight consecutive elements of an activation row (16 bytes of bfloat16, 32 of float32).
+__device__ __forceinline__ void load_act8(const void *base, int64_t e, bool bf16, float (&o)[8]) {
+  if (bf16) load_vec<__nv_bfloat16, 8>(static_cast<const __nv_bfloat16 *>(base) + e, o);
+  else load_vec<float, 8>(static_cast<const float *>(base) + e, o);
+}
+
 // One warp per token row r = (b*T + t)*H + h.
-__global__ void __launch_bounds__(32 * kReduceWarps) bwd_reduce_kernel(const __grid_constant__ BackwardArgs a) {
+__global__ void __launch_bounds__(32 * kReduceWarps, 4) bwd_reduce_kernel(const __grid_constant__ BackwardArgs a) {
   __shared__ float tot[kReduceWarps][2 * SDM_MAX_K + 4];
-  __shared__ float dS[kReduceWarps][SDM_MAX_K];
-  __shared__ int32_t dig[kReduceWarps][SDM_MAX_K];
   __shared__ float dsrow[kReduceWarps][SDM_MAX_FACTOR_DIM];
   __shared__ int32_t nz[kReduceWarps][SDM_MAX_K];
+  constexpr int kJ = SDM_MAX_K / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rows = a.B * a.T * a.H, BT = a.B * a.T;
   const int W = a.W, R = a.R, n_tot = W + R + 2;
   const KeyGeometry &g = a.g;
   const int d_sub = g.d_sub;
   const bool abf = a.act_bf16 != 0;
+  const bool vec8 = (d_sub % 8) == 0;
   for (int64_t r = (int64_t)blockIdx.x * kReduceWarps + warp; r < rows; r += (int64_t)gridDim.x * kReduceWarps) {
     const int64_t h = r % a.H, bt = r / a.H, b = bt / a.T, t = bt % a.T, s = b * a.H + h;
     // 1. the per-piece partial sums, added in piece order
     const float *pp = a.part + (s * a.T + t) * (int64_t)a.P * a.PS;
     for (int v = lane; v < n_tot; v += 32) {
       float acc = 0.0f;
+#pragma unroll 8
       for (int p = 0; p < a.P; ++p) acc = __fadd_rn(acc, pp[(int64_t)p * a.PS + v]);
       tot[warp][v] = acc;
     }
@@ -367,50 +398,79 @@ __global__ void __launch_bounds__(32 * kReduceWarps) bwd_reduce_kernel(const __g
       const float *wts = a.wt[kind] + r * k;
       const int32_t *ids = a.idx[kind] + r * k;
       const float *dw = tot[warp] + (kind ? W : 0);
-      // 2. softmax backward: dS_j = w_j (dw_j - sum_k w_k dw_k)
+      // 2. softmax backward: dS_j = w_j (dw_j - sum_k w_k dw_k); lane holds j = 32 i + lane
       float sw = 0.0f;
       for (int j = lane; j < k; j += 32) sw = __fmaf_rn(wts[j], dw[j], sw);
       sw = warp_sum(sw);
-      for (int j = lane; j < k; j += 32) dS[warp][j] = __fmul_rn(wts[j], __fsub_rn(dw[j], sw));
-      __syncwarp();
+      float dSj[kJ];
+      int32_t idj[kJ];
+#pragma unroll
+      for (int i = 0; i < kJ; ++i) {
+        const int j = lane + 32 * i;
+        dSj[i] = j < k ? __fmul_rn(wts[j], __fsub_rn(dw[j], sw)) : 0.0f;
+        idj[i] = j < k ? ids[j] : -1;
+      }
       int64_t stride = 1;
       for (int f = g.F - 1; f >= 0; --f) {
         const int n = g.nf[f];
-        // 3. ds_f[a] = sum of dS_j over the slots whose factor-f index is a (in j order)
-        for (int j = lane; j < k; j += 32) {
-          const int32_t id = ids[j];
-          dig[warp][j] = (id >= 0 && (int64_t)id < a.N) ? (int32_t)(((int64_t)id / stride) % n) : -1;
-        }
+        float *drow = dsrow[warp];
+        for (int x = lane; x < n; x += 32) drow[x] = 0.0f;
         __syncwarp();
+        // 3. ds_f[x] = sum of dS_j over the slots whose factor-f index is x, in a fixed
+        // order: within each group of 32 slots (j = 32 i + lane) the slots sharing x are
+        // added in lane order by the first of them, and the groups in increasing i.
+#pragma unroll
+        for (int i = 0; i < kJ; ++i) {
+          if (32 * i < k) {
+            const int32_t id = idj[i];
+            const bool in = id >= 0 && (int64_t)id < a.N;
+            const int x = in ? (int)(((int64_t)id / stride) % n) : -1 - lane;   // a bad slot stays alone
+            const unsigned grp = __match_any_sync(0xffffffffu, x);
+            float sum = 0.0f;
+            for (unsigned m = grp; m; m &= m - 1) sum = __fadd_rn(sum, __shfl_sync(grp, dSj[i], __ffs(m) - 1));
+            if (in && __ffs(grp) - 1 == lane) drow[x] = __fadd_rn(drow[x], sum);
+            __syncwarp();
+          }
+        }
+        // the dense row for the sub-key gradient, and the indices with a nonzero ds, ascending
         float *dsg = a.ds + ((h * 2 + kind) * BT + bt) * (int64_t)g.ntot + g.off[f];
-        for (int x = lane; x < n; x += 32) {
-          float acc = 0.0f;
-          for (int j = 0; j < k; ++j)
-            if (dig[warp][j] == x) acc = __fadd_rn(acc, dS[warp][j]);
-          dsrow[warp][x] = acc;
-          dsg[x] = acc;
-        }
-        __syncwarp();
-        // the indices with a nonzero ds, ascending
         int nnz = 0;
         for (int x0 = 0; x0 < n; x0 += 32) {
           const int x = x0 + lane;
-          const bool on = x < n && dsrow[warp][x] != 0.0f;
-          const unsigned m = __ballot_sync(0xffffffffu, on);
-          if (on) nz[warp][nnz + __popc(m & ((1u << lane) - 1u))] = x;
-          nnz += __popc(m);                          // at most k: only selected indices are nonzero
+          const float v = x < n ? drow[x] : 0.0f;
+          if (x < n) dsg[x] = v;
+          const unsigned m = __ballot_sync(0xffffffffu, v != 0.0f);
+          if (v != 0.0f) nz[warp][nnz + __popc(m & ((1u << lane) - 1u))] = x;
+          nnz += __popc(m);                         // at most k: only selected indices are nonzero
         }
         __syncwarp();
-        // 4. dq_f[d] = sum over those indices (ascending) of ds_f[a] K_f[a][d]
+        // 4. dq_f[d] = sum over those indices (ascending) of ds_f[x] K_f[x][d]
         const int64_t krow0 = (h * g.ntot + g.off[f]) * (int64_t)d_sub;
         float *dq = a.d_q[kind] + r * (int64_t)g.F * d_sub + (int64_t)f * d_sub;
-        for (int d = lane; d < d_sub; d += 32) {
-          float acc = 0.0f;
-          for (int i = 0; i < nnz; ++i) {
-            const int x = nz[warp][i];
-            acc = __fmaf_rn(dsrow[warp][x], load_act1(a.subkeys, krow0 + (int64_t)x * d_sub + d, abf), acc);
+        if (vec8) {
+          for (int d = 8 * lane; d < d_sub; d += 256) {
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+            for (int q = 0; q < nnz; ++q) {
+              const int x = nz[warp][q];
+              const float dx = drow[x];
+              float kv[8];
+              load_act8(a.subkeys, krow0 + (int64_t)x * d_sub + d, abf, kv);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[e] = __fmaf_rn(dx, kv[e], acc[e]);
+            }
+            store_f32v<8>(dq + d, acc);
           }
-          dq[d] = acc;
+        } else {
+          for (int d = lane; d < d_sub; d += 32) {
+            float acc = 0.0f;
+            for (int q = 0; q < nnz; ++q) {
+              const int x = nz[warp][q];
+              acc = __fmaf_rn(drow[x], load_act1(a.subkeys, krow0 + (int64_t)x * d_sub + d, abf), acc);
+            }
+            dq[d] = acc;
+          }
         }
         __syncwarp();
         stride *= n;
@@ -513,12 +573,12 @@ __global__ void __launch_bounds__(kThreads) bwd_subkey_sum_kernel(const __grid_c
   }
 }
 
+// W = R = 64 fixed at compile time (two rows per lane and sum), else up to four.
 template <typename BANK>
 cudaError_t launch_sweep_t(const BackwardArgs &a, cudaStream_t st) {
   const dim3 grid((unsigned)((a.P + kSweepWarps - 1) / kSweepWarps), (unsigned)(a.B * a.H));
-  if (a.W == 64 && a.R == 64) bwd_sweep_kernel<BANK, 4, true><<<grid, 32 * kSweepWarps, 0, st>>>(a);
-  else if (a.W <= 64 && a.R <= 64) bwd_sweep_kernel<BANK, 4, false><<<grid, 32 * kSweepWarps, 0, st>>>(a);
-  else bwd_sweep_kernel<BANK, 8, false><<<grid, 32 * kSweepWarps, 0, st>>>(a);
+  if (a.W == 64 && a.R == 64) bwd_sweep_kernel<BANK, kSweepCG, 64 / (32 / kSweepCG), true><<<grid, 32 * kSweepWarps, 0, st>>>(a);
+  else bwd_sweep_kernel<BANK, kSweepCG, SDM_MAX_K / (32 / kSweepCG), false><<<grid, 32 * kSweepWarps, 0, st>>>(a);
   return cudaGetLastError();
 }
 

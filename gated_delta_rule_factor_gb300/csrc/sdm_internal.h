@@ -210,7 +210,8 @@ struct BackwardArgs {
   float *dk_part;         // [KS, H, ntot, d_sub]
   int32_t *err;
   int64_t B, T, N, d_v;
-  int32_t H, W, R, P, PS;
+  int32_t H, W, R, P, PS;  // P: column pieces of the sweep (partials); PS: partial stride
+  int32_t P32;            // 32-byte pieces of a row (the snapshot's layout)
   int32_t act_bf16, snap_bf16;
   int32_t KS;             // split of the sub-key gradient's K = 2*B*T rows
   int64_t k_chunk;        // rows per split (multiple of 16)
@@ -223,6 +224,9 @@ cudaError_t launch_bwd_sweep(const BackwardArgs &a, int bank_dtype, cudaStream_t
 cudaError_t launch_bwd_reduce(const BackwardArgs &a, cudaStream_t st);
 cudaError_t launch_bwd_subkeys(const BackwardArgs &a, cudaStream_t st);
 inline int32_t bwd_part_stride(int W, int R) { return (W + R + 2 + 3) & ~3; }
+// 16-byte column groups per warp of the backward's reverse sweep (the piece is
+// 16 * kSweepCG bytes of every bank row).
+constexpr int kSweepCG = 2;
 
 // Raises a kernel's dynamic shared-memory limit to at least `smem` bytes on the current
 // device, once per (kernel, device, larger size): the attribute call is not repeated per
