@@ -28,6 +28,10 @@ namespace sdm {
 namespace {
 
 constexpr int kSweepWarps = 2;      // warps per CTA of the sweep (adjacent pieces of the rows)
+constexpr bool kSweepStage = true;  // rows gathered with cp.async through shared memory
+// 16-byte stage slots per lane: JB snapshot rows (two slots each), JB read rows and the
+// float32 G of the read and write rows (VEC / 4 slots each)
+__host__ __device__ constexpr int sweep_slots(int JB, int VEC) { return JB * (3 + 2 * (VEC / 4)); }
 constexpr bool kSweepLockstep = false;  // the CTA's warps meet at a barrier after every token
 constexpr int kReduceWarps = 4;
 constexpr int kFlagWarps = kThreads / 32;
@@ -182,6 +186,15 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
   const unsigned char *snap_sp = a.snap + ((s * a.T) * a.P32 + p32) * (int64_t)W * pcs + half * VEC * se;
   const int64_t snap_tstep = (int64_t)a.P32 * W * pcs;
   const bool abf = a.act_bf16 != 0;
+  // stage slots of a lane (16-byte chunks): snapshot rows (2 each), read rows, their G
+  // (GC each), write rows' G (GC each)
+  constexpr int GC = VEC / 4;
+  extern __shared__ __align__(16) unsigned char sweep_smem[];
+  unsigned char *stg = sweep_smem + ((int64_t)warp * sweep_slots(JB, VEC) * 32 + lane) * 16;
+  auto sx = [&](int q, int hh) { return (int64_t)(2 * q + hh) * 512; };
+  auto sm_ = [&](int q) { return (int64_t)(2 * JB + q) * 512; };
+  auto sgr = [&](int q, int hh) { return (int64_t)(3 * JB + GC * q + hh) * 512; };
+  auto sgw = [&](int q, int hh) { return (int64_t)((3 + GC) * JB + GC * q + hh) * 512; };
 
   auto refs_of = [&](int64_t t) {
     TokenRefs<RG, JB, FULL> k;
@@ -210,17 +223,81 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
     float xw[JB][VEC], mr[JB][VEC], gr[JB][VEC], gw[JB][VEC];
     const unsigned char *snap_t = snap_sp + t * snap_tstep;
 #pragma unroll
-    for (int q = 0; q < JB; ++q) {
+    for (int q = 0; q < JB; ++q)
 #pragma unroll
       for (int i = 0; i < VEC; ++i) xw[q][i] = mr[q][i] = gr[q][i] = gw[q][i] = 0.0f;
-      if (valid && wr_.has(q, N)) {
-        const unsigned char *sp = snap_t + (int64_t)(wr_.j0 + q) * pcs;
-        if (sbf) load_vec<__nv_bfloat16, VEC>(reinterpret_cast<const __nv_bfloat16 *>(sp), xw[q]);
-        else load_vec<float, VEC>(reinterpret_cast<const float *>(sp), xw[q]);
+    if constexpr (kSweepStage) {
+      // the token's rows come in through cp.async into this lane's slots of the stage
+      // area ([slot][lane] 16-byte chunks), then into registers
+      const int xbytes = VEC * se;
+#pragma unroll
+      for (int q = 0; q < JB; ++q) {
+        if (valid && wr_.has(q, N)) {
+          const unsigned char *sp = snap_t + (int64_t)(wr_.j0 + q) * pcs;
+          if (xbytes == 8) cp_async8(stg + sx(q, 0), sp);
+          else {
+            cp_async16(stg + sx(q, 0), sp);
+            if (xbytes == 32) cp_async16(stg + sx(q, 1), sp + 16);
+          }
+          if (!cur.flag)
+#pragma unroll
+            for (int hh = 0; hh < GC; ++hh) cp_async16(stg + sgw(q, hh), grad + (int64_t)wr_.idx[q] * d_v + 4 * hh);
+        }
+        if (valid && rd.has(q, N)) {
+          cp_async16(stg + sm_(q), bank + (int64_t)rd.idx[q] * d_v);
+#pragma unroll
+          for (int hh = 0; hh < GC; ++hh) cp_async16(stg + sgr(q, hh), grad + (int64_t)rd.idx[q] * d_v + 4 * hh);
+        }
       }
-      if (valid && rd.has(q, N)) {
-        load_vec<BANK, VEC>(bank + (int64_t)rd.idx[q] * d_v, mr[q]);
-        load_f32v<VEC>(grad + (int64_t)rd.idx[q] * d_v, gr[q]);
+      cp_async_commit();
+      cp_async_wait_all();
+#pragma unroll
+      for (int q = 0; q < JB; ++q) {
+        if (valid && wr_.has(q, N)) {
+          if (sbf) load_vec<__nv_bfloat16, VEC>(reinterpret_cast<const __nv_bfloat16 *>(stg + sx(q, 0)), xw[q]);
+          else if (VEC == 4) load_vec<float, VEC>(reinterpret_cast<const float *>(stg + sx(q, 0)), xw[q]);
+          else {
+            float lo[4], hi[4];
+            load_vec<float, 4>(reinterpret_cast<const float *>(stg + sx(q, 0)), lo);
+            load_vec<float, 4>(reinterpret_cast<const float *>(stg + sx(q, 1)), hi);
+#pragma unroll
+            for (int i = 0; i < 4 && i + 4 < VEC + 4; ++i) {
+              xw[q][i] = lo[i];
+              if (i + 4 < VEC) xw[q][i + 4] = hi[i];
+            }
+          }
+          if (!cur.flag)
+#pragma unroll
+            for (int hh = 0; hh < GC; ++hh) {
+              float x4[4];
+              load_vec<float, 4>(reinterpret_cast<const float *>(stg + sgw(q, hh)), x4);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) gw[q][4 * hh + i] = x4[i];
+            }
+        }
+        if (valid && rd.has(q, N)) {
+          load_vec<BANK, VEC>(reinterpret_cast<const BANK *>(stg + sm_(q)), mr[q]);
+#pragma unroll
+          for (int hh = 0; hh < GC; ++hh) {
+            float x4[4];
+            load_vec<float, 4>(reinterpret_cast<const float *>(stg + sgr(q, hh)), x4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) gr[q][4 * hh + i] = x4[i];
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < JB; ++q) {
+        if (valid && wr_.has(q, N)) {
+          const unsigned char *sp = snap_t + (int64_t)(wr_.j0 + q) * pcs;
+          if (sbf) load_vec<__nv_bfloat16, VEC>(reinterpret_cast<const __nv_bfloat16 *>(sp), xw[q]);
+          else load_vec<float, VEC>(reinterpret_cast<const float *>(sp), xw[q]);
+        }
+        if (valid && rd.has(q, N)) {
+          load_vec<BANK, VEC>(bank + (int64_t)rd.idx[q] * d_v, mr[q]);
+          load_f32v<VEC>(grad + (int64_t)rd.idx[q] * d_v, gr[q]);
+        }
       }
     }
     auto load_write_grads = [&] {
@@ -228,7 +305,7 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
       for (int q = 0; q < JB; ++q)
         if (valid && wr_.has(q, N)) load_f32v<VEC>(grad + (int64_t)wr_.idx[q] * d_v, gw[q]);
     };
-    if (!cur.flag) load_write_grads();             // no row in both lists: independent
+    if (!kSweepStage && !cur.flag) load_write_grads();   // no row in both lists: independent
     // read: dr_j = <dy, M'[i^r_j]>, G[i^r_j] += r_j dy
     float drp[JB];
 #pragma unroll
@@ -574,12 +651,23 @@ __global__ void __launch_bounds__(kThreads) bwd_subkey_sum_kernel(const __grid_c
 }
 
 // W = R = 64 fixed at compile time (two rows per lane and sum), else up to four.
+template <typename BANK, int JB, bool FULL>
+cudaError_t launch_sweep_jb(const BackwardArgs &a, cudaStream_t st) {
+  const dim3 grid((unsigned)((a.P + kSweepWarps - 1) / kSweepWarps), (unsigned)(a.B * a.H));
+  const int64_t smem = kSweepStage ? (int64_t)kSweepWarps * sweep_slots(JB, 16 / (int)sizeof(BANK)) * 32 * 16 : 0;
+  auto kern = bwd_sweep_kernel<BANK, kSweepCG, JB, FULL>;
+  if (smem > 0) {
+    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kern), smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<grid, 32 * kSweepWarps, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename BANK>
 cudaError_t launch_sweep_t(const BackwardArgs &a, cudaStream_t st) {
-  const dim3 grid((unsigned)((a.P + kSweepWarps - 1) / kSweepWarps), (unsigned)(a.B * a.H));
-  if (a.W == 64 && a.R == 64) bwd_sweep_kernel<BANK, kSweepCG, 64 / (32 / kSweepCG), true><<<grid, 32 * kSweepWarps, 0, st>>>(a);
-  else bwd_sweep_kernel<BANK, kSweepCG, SDM_MAX_K / (32 / kSweepCG), false><<<grid, 32 * kSweepWarps, 0, st>>>(a);
-  return cudaGetLastError();
+  if (a.W == 64 && a.R == 64) return launch_sweep_jb<BANK, 64 / (32 / kSweepCG), true>(a, st);
+  return launch_sweep_jb<BANK, SDM_MAX_K / (32 / kSweepCG), false>(a, st);
 }
 
 unsigned grid_for(int64_t items, int per_block) {
