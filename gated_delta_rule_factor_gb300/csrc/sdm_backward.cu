@@ -28,11 +28,9 @@ namespace sdm {
 namespace {
 
 constexpr int kSweepWarps = 2;      // warps per CTA of the sweep (adjacent pieces of the rows)
-constexpr bool kSweepStage = true;  // rows gathered with cp.async through shared memory
 // 16-byte stage slots per lane: JB snapshot rows (two slots each), JB read rows and the
 // float32 G of the read and write rows (VEC / 4 slots each)
 __host__ __device__ constexpr int sweep_slots(int JB, int VEC) { return JB * (3 + 2 * (VEC / 4)); }
-constexpr bool kSweepLockstep = false;  // the CTA's warps meet at a barrier after every token
 constexpr int kReduceWarps = 4;
 constexpr int kFlagWarps = kThreads / 32;
 
@@ -168,9 +166,9 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
   const int64_t s = blockIdx.y;
   if (*a.snap_hdr != kSnapshotArmed) {          // no snapshot to undo: touch nothing
     if (lane == 0 && p == 0) raise_error(a.err, SDM_DEVERR_SNAPSHOT);
-    return;                                     // (the whole CTA reads the same word)
+    return;
   }
-  if (!kSweepLockstep && p >= a.P) return;
+  if (p >= a.P) return;
   const int W = FULL ? 64 : a.W, R = FULL ? 64 : a.R;
   const int rg = lane / CG, c = lane % CG;
   const int64_t col = ((int64_t)p * CG + c) * VEC;
@@ -219,93 +217,81 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
       load_act<VEC>(a.dy, r * d_v + col, abf, dyv);
       load_act<VEC>(a.k_val, r * d_v + col, abf, vv);
     }
-    // rows before the write (the snapshot), and the read rows after it with their G
+    // rows before the write (the snapshot), and the read rows after it with their G: in
+    // through cp.async into this lane's stage slots ([slot][lane] 16-byte chunks; plain
+    // 16-byte register gathers measured slower, held back by how many a warp keeps in
+    // flight), then into registers
     float xw[JB][VEC], mr[JB][VEC], gr[JB][VEC], gw[JB][VEC];
     const unsigned char *snap_t = snap_sp + t * snap_tstep;
 #pragma unroll
     for (int q = 0; q < JB; ++q)
 #pragma unroll
       for (int i = 0; i < VEC; ++i) xw[q][i] = mr[q][i] = gr[q][i] = gw[q][i] = 0.0f;
-    if constexpr (kSweepStage) {
-      // the token's rows come in through cp.async into this lane's slots of the stage
-      // area ([slot][lane] 16-byte chunks), then into registers
-      const int xbytes = VEC * se;
+    // the token's rows come in through cp.async into this lane's slots of the stage
+    // area ([slot][lane] 16-byte chunks), then into registers
+    const int xbytes = VEC * se;
 #pragma unroll
-      for (int q = 0; q < JB; ++q) {
-        if (valid && wr_.has(q, N)) {
-          const unsigned char *sp = snap_t + (int64_t)(wr_.j0 + q) * pcs;
-          if (xbytes == 8) cp_async8(stg + sx(q, 0), sp);
-          else {
-            cp_async16(stg + sx(q, 0), sp);
-            if (xbytes == 32) cp_async16(stg + sx(q, 1), sp + 16);
-          }
-          if (!cur.flag)
-#pragma unroll
-            for (int hh = 0; hh < GC; ++hh) cp_async16(stg + sgw(q, hh), grad + (int64_t)wr_.idx[q] * d_v + 4 * hh);
+    for (int q = 0; q < JB; ++q) {
+      if (valid && wr_.has(q, N)) {
+        const unsigned char *sp = snap_t + (int64_t)(wr_.j0 + q) * pcs;
+        if (xbytes == 8) cp_async8(stg + sx(q, 0), sp);
+        else {
+          cp_async16(stg + sx(q, 0), sp);
+          if (xbytes == 32) cp_async16(stg + sx(q, 1), sp + 16);
         }
-        if (valid && rd.has(q, N)) {
-          cp_async16(stg + sm_(q), bank + (int64_t)rd.idx[q] * d_v);
+        if (!cur.flag)
 #pragma unroll
-          for (int hh = 0; hh < GC; ++hh) cp_async16(stg + sgr(q, hh), grad + (int64_t)rd.idx[q] * d_v + 4 * hh);
-        }
+          for (int hh = 0; hh < GC; ++hh) cp_async16(stg + sgw(q, hh), grad + (int64_t)wr_.idx[q] * d_v + 4 * hh);
       }
-      cp_async_commit();
-      cp_async_wait_all();
+      if (valid && rd.has(q, N)) {
+        cp_async16(stg + sm_(q), bank + (int64_t)rd.idx[q] * d_v);
 #pragma unroll
-      for (int q = 0; q < JB; ++q) {
-        if (valid && wr_.has(q, N)) {
-          if (sbf) load_vec<__nv_bfloat16, VEC>(reinterpret_cast<const __nv_bfloat16 *>(stg + sx(q, 0)), xw[q]);
-          else if (VEC == 4) load_vec<float, VEC>(reinterpret_cast<const float *>(stg + sx(q, 0)), xw[q]);
-          else {
-            float lo[4], hi[4];
-            load_vec<float, 4>(reinterpret_cast<const float *>(stg + sx(q, 0)), lo);
-            load_vec<float, 4>(reinterpret_cast<const float *>(stg + sx(q, 1)), hi);
+        for (int hh = 0; hh < GC; ++hh) cp_async16(stg + sgr(q, hh), grad + (int64_t)rd.idx[q] * d_v + 4 * hh);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait_all();
 #pragma unroll
-            for (int i = 0; i < 4 && i + 4 < VEC + 4; ++i) {
-              xw[q][i] = lo[i];
-              if (i + 4 < VEC) xw[q][i + 4] = hi[i];
-            }
+    for (int q = 0; q < JB; ++q) {
+      if (valid && wr_.has(q, N)) {
+        if (sbf) load_vec<__nv_bfloat16, VEC>(reinterpret_cast<const __nv_bfloat16 *>(stg + sx(q, 0)), xw[q]);
+        else if (VEC == 4) load_vec<float, VEC>(reinterpret_cast<const float *>(stg + sx(q, 0)), xw[q]);
+        else {
+          float lo[4], hi[4];
+          load_vec<float, 4>(reinterpret_cast<const float *>(stg + sx(q, 0)), lo);
+          load_vec<float, 4>(reinterpret_cast<const float *>(stg + sx(q, 1)), hi);
+#pragma unroll
+          for (int i = 0; i < 4 && i + 4 < VEC + 4; ++i) {
+            xw[q][i] = lo[i];
+            if (i + 4 < VEC) xw[q][i + 4] = hi[i];
           }
-          if (!cur.flag)
-#pragma unroll
-            for (int hh = 0; hh < GC; ++hh) {
-              float x4[4];
-              load_vec<float, 4>(reinterpret_cast<const float *>(stg + sgw(q, hh)), x4);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) gw[q][4 * hh + i] = x4[i];
-            }
         }
-        if (valid && rd.has(q, N)) {
-          load_vec<BANK, VEC>(reinterpret_cast<const BANK *>(stg + sm_(q)), mr[q]);
+        if (!cur.flag)
 #pragma unroll
           for (int hh = 0; hh < GC; ++hh) {
             float x4[4];
-            load_vec<float, 4>(reinterpret_cast<const float *>(stg + sgr(q, hh)), x4);
+            load_vec<float, 4>(reinterpret_cast<const float *>(stg + sgw(q, hh)), x4);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) gr[q][4 * hh + i] = x4[i];
+            for (int i = 0; i < 4; ++i) gw[q][4 * hh + i] = x4[i];
           }
-        }
       }
-    } else {
+      if (valid && rd.has(q, N)) {
+        load_vec<BANK, VEC>(reinterpret_cast<const BANK *>(stg + sm_(q)), mr[q]);
 #pragma unroll
-      for (int q = 0; q < JB; ++q) {
-        if (valid && wr_.has(q, N)) {
-          const unsigned char *sp = snap_t + (int64_t)(wr_.j0 + q) * pcs;
-          if (sbf) load_vec<__nv_bfloat16, VEC>(reinterpret_cast<const __nv_bfloat16 *>(sp), xw[q]);
-          else load_vec<float, VEC>(reinterpret_cast<const float *>(sp), xw[q]);
-        }
-        if (valid && rd.has(q, N)) {
-          load_vec<BANK, VEC>(bank + (int64_t)rd.idx[q] * d_v, mr[q]);
-          load_f32v<VEC>(grad + (int64_t)rd.idx[q] * d_v, gr[q]);
+        for (int hh = 0; hh < GC; ++hh) {
+          float x4[4];
+          load_vec<float, 4>(reinterpret_cast<const float *>(stg + sgr(q, hh)), x4);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) gr[q][4 * hh + i] = x4[i];
         }
       }
     }
+
     auto load_write_grads = [&] {
 #pragma unroll
       for (int q = 0; q < JB; ++q)
         if (valid && wr_.has(q, N)) load_f32v<VEC>(grad + (int64_t)wr_.idx[q] * d_v, gw[q]);
     };
-    if (!kSweepStage && !cur.flag) load_write_grads();   // no row in both lists: independent
     // read: dr_j = <dy, M'[i^r_j]>, G[i^r_j] += r_j dy
     float drp[JB];
 #pragma unroll
@@ -388,10 +374,8 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
       dap = __fadd_rn(dap, __shfl_xor_sync(0xffffffffu, dap, o));
       dbp = __fadd_rn(dbp, __shfl_xor_sync(0xffffffffu, dbp, o));
     }
-    float *pp = a.part + ((s * a.T + t) * a.P + min(p, a.P - 1)) * (int64_t)a.PS;
-    const bool own = p < a.P;                       // (a lockstep CTA's warps past the last piece write nothing)
-    if (!own) {
-    } else if constexpr (FULL && JB == 4) {
+    float *pp = a.part + ((s * a.T + t) * a.P + p) * (int64_t)a.PS;
+    if constexpr (FULL && JB == 4) {
       if (c == 0) *reinterpret_cast<float4 *>(pp + wr_.j0) = make_float4(dwp[0], dwp[1], dwp[2], dwp[3]);
       if (c == CG - 1) *reinterpret_cast<float4 *>(pp + W + rd.j0) = make_float4(drp[0], drp[1], drp[2], drp[3]);
     } else if constexpr (FULL && JB == 2) {
@@ -409,7 +393,7 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
           if (q < rd.nb) pp[W + rd.j0 + q] = drp[q];
       }
     }
-    if (lane == 0 && own) {
+    if (lane == 0) {
       pp[W + R] = dap;
       pp[W + R + 1] = dbp;
     }
@@ -418,8 +402,7 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
       for (int q = 0; q < JB; ++q) bad |= !wr_.has(q, N) || !rd.has(q, N);
     }
     if (bad) raise_error(a.err, SDM_DEVERR_SLOT_RANGE);
-    if constexpr (kSweepLockstep) __syncthreads();
-    else __syncwarp();                              // this token's stores before the next one's loads
+    __syncwarp();                                   // this token's stores before the next one's loads
     cur = nxt;
   }
 }
@@ -654,12 +637,10 @@ __global__ void __launch_bounds__(kThreads) bwd_subkey_sum_kernel(const __grid_c
 template <typename BANK, int JB, bool FULL>
 cudaError_t launch_sweep_jb(const BackwardArgs &a, cudaStream_t st) {
   const dim3 grid((unsigned)((a.P + kSweepWarps - 1) / kSweepWarps), (unsigned)(a.B * a.H));
-  const int64_t smem = kSweepStage ? (int64_t)kSweepWarps * sweep_slots(JB, 16 / (int)sizeof(BANK)) * 32 * 16 : 0;
+  const int64_t smem = (int64_t)kSweepWarps * sweep_slots(JB, 16 / (int)sizeof(BANK)) * 32 * 16;
   auto kern = bwd_sweep_kernel<BANK, kSweepCG, JB, FULL>;
-  if (smem > 0) {
-    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kern), smem);
-    if (e != cudaSuccess) return e;
-  }
+  const cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kern), smem);
+  if (e != cudaSuccess) return e;
   kern<<<grid, 32 * kSweepWarps, smem, st>>>(a);
   return cudaGetLastError();
 }

@@ -299,6 +299,12 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
+// Waits until at most N of this thread's committed cp.async groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pending() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- mbarriers and bulk copies
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

@@ -71,22 +71,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Arrives on `bar` once every cp.async this thread issued so far has completed.
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // cp.async without a compiler memory clobber, for the loaders' row copies: the compiler
 // may then batch the row-list reads around them.  The destination is read only after a
 // cp.async.wait_group and a barrier (both with memory clobbers), so no access that the
 // clobber would order is affected.
 __device__ __forceinline__ void cp_async16_rows(uint32_t dst_smem, const void *src_gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst_smem), "l"(src_gmem));
-}
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait_pending() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
 // Bounded wait for the phase of `bar` with the given parity that also gives up as soon
