@@ -155,9 +155,11 @@ sdm_status sdm_write_read(const sdm_shape *shape, const void *q_w, const void *q
  *              has to start at zero: the one word the kernels read before writing (the
  *              device error code) is cleared on `stream` at the start of every call.
  *   set-up     the first call on a device, with that device current, looks up the
- *              array's address (cudaGetSymbolAddress) and keeps it; make that first
- *              call before any stream capture begins.  A failed lookup returns
- *              SDM_ERR_CUDA.
+ *              array's address (cudaGetSymbolAddress) and keeps it for the life of the
+ *              process; make that first call before any stream capture begins.  A
+ *              failed lookup returns SDM_ERR_CUDA.  A device reset (cudaDeviceReset, or a
+ *              framework that destroys and recreates the primary context) invalidates the
+ *              kept address: do not use this entry after one.
  *   races      every call on a device shares the one array: calls whose work may
  *              overlap on the device (other streams, other host threads) corrupt each
  *              other's scratch.  Order them on one stream.
