@@ -55,6 +55,13 @@ def rank_seed(cfg, rank: int) -> int:
     return cfg.seed + 7919 * rank
 
 
+def rank_streams(B: int, H: int, rank: int, world: int) -> list:
+    """The global streams (b, h) rank ``rank`` runs: the job's batch is world*B elements and
+    rank r holds elements r*B .. r*B + B - 1, every head of each (its inputs are drawn with
+    rank_seed, so they are that slice of the global batch)."""
+    return [(rank * B + b, h) for b in range(B) for h in range(H)]
+
+
 def max_over_ranks(x: float, pg, device) -> float:
     """The largest of the ranks' values (a time): the whole job is as slow as its slowest rank."""
     if pg is None:
@@ -443,6 +450,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "parallelism": f"streams sharded, {world} independent ranks",
+                   "global_batch": B * world,
                    "l2": "inputs larger than L2: the 1 GiB bank is rewritten from the learned table every step",
                    "step": "bank copy + scoring/top-k + chunk plan + fused write/read",
                    "chunk_collision_rate": collision},

@@ -3,8 +3,8 @@
 Streams are independent, so under torchrun every rank runs its own streams (weak
 scaling) with no collective on the data path; the only collectives are the barrier and
 the max-over-ranks of the timed region.  Checked here: the ranks draw different inputs,
-every rank sees the slowest rank's time, and the whole-job rate counts the units of all
-ranks over that time.
+their streams partition the global batch (each (b, h) exactly once), every rank sees the
+slowest rank's time, and the whole-job rate counts the units of all ranks over that time.
 """
 
 import os
@@ -33,7 +33,13 @@ def _rank_main(rank: int, world: int, port: int, out) -> None:
         cfg = sdm_inputs.CONFIGS["tiny"]
         ms = bench.max_over_ranks(10.0 + 5.0 * rank, dist, torch.device("cpu"))
         d = sdm_inputs.make_inputs(cfg, seed=bench.rank_seed(cfg, rank))
-        out.put((rank, ms, float(d["q_w"].double().sum()), float(d["k_val"].double().sum())))
+        # every rank's share of the global streams, gathered on every rank
+        B, H = 3, 2
+        mine = torch.tensor(bench.rank_streams(B, H, rank, world), dtype=torch.int64)
+        parts = [torch.empty_like(mine) for _ in range(world)]
+        dist.all_gather(parts, mine)
+        allst = sorted(tuple(x) for p_ in parts for x in p_.tolist())
+        out.put((rank, ms, float(d["q_w"].double().sum()), float(d["k_val"].double().sum()), allst))
         dist.barrier()
     finally:
         dist.destroy_process_group()
@@ -52,8 +58,10 @@ def test_two_gloo_ranks_time_and_shard_like_the_bench():
         for p in procs:
             p.join(timeout=60)
     assert [p.exitcode for p in procs] == [0, 0]
-    (r0, ms0, qw0, kv0), (r1, ms1, qw1, kv1) = got
+    (r0, ms0, qw0, kv0, st0), (r1, ms1, qw1, kv1, st1) = got
     assert (r0, r1) == (0, 1)
+    # the two ranks' streams cover the global batch's (b, h) exactly once
+    assert st0 == st1 == [(b, h) for b in range(2 * 3) for h in range(2)]
     assert ms0 == ms1 == 15.0                      # the slowest rank's time, on every rank
     assert qw0 != qw1 and kv0 != kv1               # each rank runs its own streams
 
