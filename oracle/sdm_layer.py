@@ -1,0 +1,75 @@
+"""CPU oracle of the SDM layer forward around the write/read op.
+
+TEST INFRASTRUCTURE ONLY, like sdm_oracle.py: nothing in the product path imports it.
+
+What the pages fix (page title > section): sparse-delta-memory README > usage example: a
+layer built from dim, num_heads, slots_per_head, num_writes, num_reads and chunk_size
+maps x [batch, tokens, dim] to y of the same shape, and the bank advances in place.
+Readings where the pages are silent (the plainest layer that the op's inputs imply):
+  * four input projections of x without bias: the write and read queries
+    [H*F*d_sub], the values [H*d_v], and two gate logits per head whose sigmoids are
+    (alpha, beta); weights stored [out, in];
+  * an output projection of the heads' reads [H*d_v] back to dim, without bias;
+  * projections accumulate exactly (float64 here) and round once to the activation
+    type; the gates round once to float32.
+"""
+
+from __future__ import annotations
+
+from typing import Iterable, Optional
+
+import numpy as np
+
+from .sdm_oracle import _f64, round_to, sdm_write_read
+
+__all__ = ["project", "gates_of", "layer_forward"]
+
+
+def project(x: np.ndarray, w: np.ndarray, act_dtype: str) -> np.ndarray:
+    """x [rows, in] times w [out, in] transposed, rounded once to the activation type."""
+    return round_to(_f64(x) @ _f64(w).T, act_dtype)
+
+
+def gates_of(x: np.ndarray, w_g: np.ndarray) -> np.ndarray:
+    """sigmoid(x w_g^T) [rows, 2H] in float64, rounded once to float32."""
+    z = _f64(x) @ _f64(w_g).T
+    return round_to(1.0 / (1.0 + np.exp(-z)), "f32")
+
+
+def layer_forward(x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank_init, *, factor_dims, W: int, R: int,
+                  chunk_size: int = 64, act_dtype: str = "f32", bank_dtype: str = "f32",
+                  streams: Optional[Iterable] = None, given: Optional[dict] = None) -> dict:
+    """The layer forward of x [B, T, dim]: projections, the op (sdm_oracle.sdm_write_read,
+    every stream starting from the learned table bank_init [H, N, d_v]) and the output
+    projection.
+
+    ``given`` may hold the op's inputs "q_w", "q_r", "k_val", "gates" ([B,T,H,...]) to use
+    instead of the oracle's own projections (to check the op and the output projection
+    on another path's projections); the oracle's own projections are returned either way.
+    Returns float64 arrays: q_w, q_r, k_val, gates, y [B,T,H,d_v], out [B,T,dim] (out and
+    y only for the listed streams' heads when ``streams`` is given: other entries zero),
+    and the per-stream op results under "op".
+    """
+    x = _f64(x)
+    B, T, dim = x.shape
+    H, _, d_sub = np.shape(subkeys)
+    F = len(factor_dims)
+    d_v = np.shape(bank_init)[-1]
+    X = x.reshape(B * T, dim)
+    own = {
+        "q_w": project(X, w_qw, act_dtype).reshape(B, T, H, F * d_sub),
+        "q_r": project(X, w_qr, act_dtype).reshape(B, T, H, F * d_sub),
+        "k_val": project(X, w_v, act_dtype).reshape(B, T, H, d_v),
+        "gates": gates_of(X, w_g).reshape(B, T, H, 2),
+    }
+    src = dict(own)
+    if given:
+        src.update({k: _f64(v) for k, v in given.items()})
+    op = sdm_write_read(src["q_w"], src["q_r"], src["k_val"], src["gates"], subkeys, bank_init,
+                        factor_dims=factor_dims, W=W, R=R, chunk_size=chunk_size, act_dtype=act_dtype,
+                        bank_dtype=bank_dtype, streams=streams)
+    y = np.zeros((B, T, H, d_v))
+    for (b, h), res in op.items():
+        y[b, :, h] = res["y"]
+    out = project(y.reshape(B * T, H * d_v), w_o, act_dtype).reshape(B, T, dim)
+    return dict(own, y=y, out=out, op=op)

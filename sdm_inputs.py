@@ -193,3 +193,38 @@ def make_grad_inputs(cfg: SdmConfig, *, seed: Optional[int] = None, T: Optional[
     else:
         db = torch.zeros(B, cfg.H, cfg.N, cfg.d_v)
     return {"dy": dy, "dbank": db.to(torch.float32).contiguous()}
+
+
+def make_layer_inputs(cfg: SdmConfig, dim: int, *, seed: Optional[int] = None, T: Optional[int] = None,
+                      B: Optional[int] = None) -> dict:
+    """Inputs of the layer around the op, for ``cfg``'s op shape and model width ``dim``
+    (CPU tensors, activation dtype unless noted).
+
+      x      [B, T, dim]            N(0, 1)
+      w_qw, w_qr [H*F*d_sub, dim]   N(0, 1/dim): projected queries ~ N(0, 1)
+      w_v    [H*d_v, dim]           N(0, 1/dim)
+      w_g    [2H, dim]              N(0, 1/dim): gate logits ~ N(0, 1), as the op's gates
+      w_o    [dim, H*d_v]           N(0, 1/(H*d_v))
+      subkeys, bank_init            as make_inputs
+    Drawn from a generator of its own (seed + 900).
+    """
+    base = make_inputs(cfg, seed=seed, T=1, B=1)
+    seed = (cfg.seed if seed is None else seed) + 900
+    B = cfg.B if B is None else B
+    T = cfg.T if T is None else T
+    g = _gen(seed)
+    act = _TORCH_DTYPE[cfg.act_dtype]
+    H, dq, dv = cfg.H, cfg.H * cfg.F * cfg.d_sub, cfg.H * cfg.d_v
+    s = 1.0 / math.sqrt(dim)
+    out = {
+        "x": torch.randn(B, T, dim, generator=g),
+        "w_qw": s * torch.randn(dq, dim, generator=g),
+        "w_qr": s * torch.randn(dq, dim, generator=g),
+        "w_v": s * torch.randn(dv, dim, generator=g),
+        "w_g": s * torch.randn(2 * H, dim, generator=g),
+        "w_o": torch.randn(dim, dv, generator=g) / math.sqrt(dv),
+    }
+    out = {k: v.to(act).contiguous() for k, v in out.items()}
+    out["subkeys"] = base["subkeys"]
+    out["bank_init"] = base["bank_init"]
+    return out
