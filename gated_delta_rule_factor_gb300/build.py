@@ -83,7 +83,7 @@ def build(force: bool = False, jobs: int = 0, verbose: bool = False, extra_flags
                     print(msg, file=sys.stderr)
     if force or todo or _stale(LIB_PATH, objs):
         tmp = LIB_PATH + ".tmp"
-        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
+        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static", "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -99,6 +99,19 @@ sdm_status run_kernel(int kind, cudaStream_t st, const char *name, Launch &&laun
   return SDM_OK;
 }
 
+// A launch of library code (cuBLASLt): timed like the library's kernels, not counted by
+// sdm_launch_count.  launch() returns nullptr or the reason it failed.
+template <class Launch>
+sdm_status run_library(int kind, cudaStream_t st, const char *name, Launch &&launch) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  const bool prof = prof_acquire(kind, &e0, &e1);
+  if (prof) cudaEventRecord(e0, st);
+  const char *why = launch();
+  if (prof) cudaEventRecord(e1, st);
+  if (why) return fail(SDM_ERR_CUDA, "%s: %s", name, why);
+  return SDM_OK;
+}
+
 // ---------------------------------------------------------------- shape checks
 
 int64_t elem_bytes(int32_t dt) { return dt == SDM_BF16 ? 2 : 4; }
@@ -843,6 +856,107 @@ sdm_status backward_impl(const sdm_shape *sh, const void *q_w, const void *q_r, 
   return ok();
 }
 
+// ---------------------------------------------------------------- the layer around the op
+
+struct LayerLayout {
+  int64_t op_ws, q_w, q_r, k_val, gates, y, gemm, total;
+};
+
+LayerLayout layer_layout(const sdm_shape *sh, const Derived &d) {
+  LayerLayout w{};
+  const int64_t rows = sh->B * sh->T * sh->H, ab = elem_bytes(sh->act_dtype);
+  int64_t o = 0;
+  w.op_ws = o;  o = a256(o + write_read_ws_bytes(sh));
+  w.q_w = o;    o = a256(o + rows * d.g.F * sh->d_sub * ab);
+  w.q_r = o;    o = a256(o + rows * d.g.F * sh->d_sub * ab);
+  w.k_val = o;  o = a256(o + rows * sh->d_v * ab);
+  w.gates = o;  o = a256(o + rows * 2 * 4);
+  w.y = o;      o = a256(o + rows * sh->d_v * ab);
+  w.gemm = o;   o = a256(o + kLayerGemmWorkspace);
+  w.total = o;
+  return w;
+}
+
+sdm_status layer_impl(const sdm_shape *sh, int64_t dim, const void *x, const void *w_qw, const void *w_qr,
+                      const void *w_v, const void *w_g, const void *w_o, const void *subkeys,
+                      const void *bank_init, void *bank, void *out, void *q_w, void *q_r, void *k_val,
+                      float *gates, void *y, void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+  Derived d;
+  sdm_status st = check_shape(sh, false, &d);
+  if (st != SDM_OK) return st;
+  if (dim < 1) return fail(SDM_ERR_INVALID_ARG, "dim must be >= 1");
+  const int64_t ab = elem_bytes(sh->act_dtype), BT = sh->B * sh->T, rows = BT * sh->H;
+  const int64_t dq = (int64_t)d.g.F * sh->d_sub * sh->H;            // query width of a token
+  const int64_t dv = sh->d_v * sh->H;
+  const LayerLayout ll = layer_layout(sh, d);
+  const Range r_x{x, BT * dim * ab, "x"}, r_out{out, BT * dim * ab, "out"};
+  const Range r_wqw{w_qw, dq * dim * ab, "w_qw"}, r_wqr{w_qr, dq * dim * ab, "w_qr"};
+  const Range r_wv{w_v, dv * dim * ab, "w_v"}, r_wg{w_g, 2 * sh->H * dim * ab, "w_g"}, r_wo{w_o, dim * dv * ab, "w_o"};
+  const Range r_ws{workspace, (int64_t)workspace_bytes, "workspace"};
+  if (rows > 0) {
+    const Range req[] = {r_x, r_out, r_wqw, r_wqr, r_wv, r_wg, r_wo};
+    for (const Range &r : req)
+      if (!r.p) return fail(SDM_ERR_INVALID_ARG, "%s is NULL", r.name);
+  }
+  const Range al[] = {r_x, r_out, r_wqw, r_wqr, r_wv, r_wg, r_wo, {q_w, 1, "q_w"}, {q_r, 1, "q_r"},
+                      {k_val, 1, "k_val"}, {gates, 1, "gates"}, {y, 1, "y"}};
+  for (const Range &r : al)
+    if (r.p && !aligned(r.p, 16)) return fail(SDM_ERR_INVALID_ARG, "%s is not 16-byte aligned", r.name);
+  if (!workspace) return fail(SDM_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256)) return fail(SDM_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  if ((int64_t)workspace_bytes < ll.total)
+    return fail(SDM_ERR_WORKSPACE, "workspace has %zu bytes, needs %lld", workspace_bytes, (long long)ll.total);
+  const Range ins[] = {r_x, r_wqw, r_wqr, r_wv, r_wg, r_wo};
+  const Range outs[] = {r_out, r_ws, {q_w, rows * d.g.F * sh->d_sub * ab, "q_w"},
+                        {q_r, rows * d.g.F * sh->d_sub * ab, "q_r"}, {k_val, rows * sh->d_v * ab, "k_val"},
+                        {gates, rows * 8, "gates"}, {y, rows * sh->d_v * ab, "y"}};
+  for (const Range &o : outs)
+    for (const Range &i : ins)
+      if (overlap(o, i)) return fail(SDM_ERR_ALIAS, "%s overlaps %s", o.name, i.name);
+  for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i)
+    for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+      if (overlap(outs[i], outs[j])) return fail(SDM_ERR_ALIAS, "%s overlaps %s", outs[i].name, outs[j].name);
+
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  void *qw = q_w ? q_w : ws + ll.q_w, *qr = q_r ? q_r : ws + ll.q_r, *kv = k_val ? k_val : ws + ll.k_val;
+  float *gt = gates ? gates : reinterpret_cast<float *>(ws + ll.gates);
+  void *yy = y ? y : ws + ll.y;
+  void *gws = ws + ll.gemm;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((st = sm_count(&sms)) != SDM_OK) return st;
+  const int adt = sh->act_dtype;
+  if (rows > 0) {
+    // input projections, then the gates
+    if ((st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer q_w projection", [&] {
+           return layer_gemm(w_qw, x, qw, dq, BT, dim, adt, gws, kLayerGemmWorkspace, cs);
+         })) != SDM_OK)
+      return st;
+    if ((st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer q_r projection", [&] {
+           return layer_gemm(w_qr, x, qr, dq, BT, dim, adt, gws, kLayerGemmWorkspace, cs);
+         })) != SDM_OK)
+      return st;
+    if ((st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer value projection", [&] {
+           return layer_gemm(w_v, x, kv, dv, BT, dim, adt, gws, kLayerGemmWorkspace, cs);
+         })) != SDM_OK)
+      return st;
+    if ((st = run_kernel(SDM_KERNEL_LAYER_GATES, cs, "layer_gates", [&] {
+           return launch_layer_gates(x, w_g, gt, BT, dim, (int32_t)(2 * sh->H), adt, sms, cs);
+         })) != SDM_OK)
+      return st;
+  }
+  // the op
+  if ((st = write_read_impl(sh, qw, qr, kv, gt, subkeys, bank_init, bank, yy, nullptr, nullptr, nullptr, nullptr,
+                            ws + ll.op_ws, (size_t)(ll.q_w - ll.op_ws), stream, true)) != SDM_OK)
+    return st;
+  if (rows > 0 &&
+      (st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer output projection", [&] {
+         return layer_gemm(w_o, yy, out, dim, BT, dv, adt, gws, kLayerGemmWorkspace, cs);
+       })) != SDM_OK)
+    return st;
+  return ok();
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -944,6 +1058,24 @@ sdm_status sdm_write_read_backward(const sdm_shape *sh, const void *q_w, const v
   return backward_impl(sh, q_w, q_r, k_val, gates, subkeys, idx_w, wt_w, idx_r, wt_r, snapshot, snapshot_bytes,
                        snapshot_dtype, bank, dy, dbank, d_k_val, d_gates, d_q_w, d_q_r, d_subkeys, workspace,
                        workspace_bytes, stream);
+}
+
+sdm_status sdm_layer_workspace_size(const sdm_shape *shape, int64_t dim, size_t *bytes) {
+  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
+  Derived d;
+  sdm_status st = check_shape(shape, false, &d);
+  if (st != SDM_OK) return st;
+  if (dim < 1) return fail(SDM_ERR_INVALID_ARG, "dim must be >= 1");
+  *bytes = (size_t)layer_layout(shape, d).total;
+  return ok();
+}
+
+sdm_status sdm_layer_forward(const sdm_shape *sh, int64_t dim, const void *x, const void *w_qw, const void *w_qr,
+                             const void *w_v, const void *w_g, const void *w_o, const void *subkeys,
+                             const void *bank_init, void *bank, void *out, void *q_w, void *q_r, void *k_val,
+                             float *gates, void *y, void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+  return layer_impl(sh, dim, x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank_init, bank, out, q_w, q_r, k_val, gates,
+                    y, workspace, workspace_bytes, stream);
 }
 
 sdm_status sdm_decode_step(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
@@ -1142,6 +1274,8 @@ const char *sdm_kernel_name(int32_t kind) {
     case SDM_KERNEL_BWD_SWEEP: return "bwd_sweep";
     case SDM_KERNEL_BWD_REDUCE: return "bwd_reduce";
     case SDM_KERNEL_BWD_SUBKEY: return "bwd_subkeys";
+    case SDM_KERNEL_LAYER_GATES: return "layer_gates";
+    case SDM_KERNEL_LAYER_GEMM: return "layer_gemm";
   }
   return "unknown";
 }

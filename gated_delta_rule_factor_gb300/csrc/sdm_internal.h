@@ -228,6 +228,15 @@ inline int32_t bwd_part_stride(int W, int R) { return (W + R + 2 + 3) & ~3; }
 // 16 * kSweepCG bytes of every bank row).
 constexpr int kSweepCG = 2;
 
+// The layer around the op (sdm_layer.cu).  layer_gemm: out[n][m] = sum_k a[m][k] b[n][k]
+// (row-major weights a [m, k], activations b [n, k]) by cuBLASLt, loaded on first use;
+// returns nullptr or the reason it failed.
+const char *layer_gemm(const void *a, const void *b, void *out, int64_t m, int64_t n, int64_t k, int act_dtype,
+                       void *ws, size_t ws_bytes, cudaStream_t st);
+cudaError_t launch_layer_gates(const void *x, const void *w_g, float *gates, int64_t rows, int64_t dim,
+                               int32_t n_gates, int act_dtype, int sm_count, cudaStream_t st);
+constexpr int64_t kLayerGemmWorkspace = (int64_t)32 << 20;   // cuBLASLt's share of a layer workspace
+
 // Raises a kernel's dynamic shared-memory limit to at least `smem` bytes on the current
 // device, once per (kernel, device, larger size): the attribute call is not repeated per
 // launch, so steady-state calls make only stream-ordered CUDA calls (graph capture).

@@ -267,6 +267,56 @@ def sdm_write_read_backward(q_w: torch.Tensor, q_r: torch.Tensor, k_val: torch.T
     return grads
 
 
+def layer_workspace_size(shape: _abi.SdmShape, dim: int) -> int:
+    n = ctypes.c_size_t(0)
+    _abi.check(_abi.load().sdm_layer_workspace_size(ctypes.byref(shape), int(dim), ctypes.byref(n)),
+               "sdm_layer_workspace_size")
+    return int(n.value)
+
+
+def sdm_layer_forward(x: torch.Tensor, w_qw: torch.Tensor, w_qr: torch.Tensor, w_v: torch.Tensor,
+                      w_g: torch.Tensor, w_o: torch.Tensor, subkeys: torch.Tensor, bank: torch.Tensor,
+                      chunk_size: int, W: int, R: int, *, factor_dims: Sequence[int],
+                      bank_init: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                      keep: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The SDM layer forward around the op: x [B,T,dim] -> out [B,T,dim]; the bank advances in
+    place (bank_init, if given, is copied into it first).  Weights are [out, in]: w_qw, w_qr
+    [H*F*d_sub, dim], w_v [H*d_v, dim], w_g [2H, dim] (rows: alpha, beta of each head), w_o
+    [dim, H*d_v].  ``keep``: optional dict of buffers receiving the intermediates "q_w",
+    "q_r", "k_val", "gates" (float32) and "y"."""
+    dev = x.device
+    B, T, dim = x.shape
+    H, d_sub = subkeys.shape[0], subkeys.shape[2]
+    F = len(factor_dims)
+    d_v = bank.shape[-1]
+    sh = make_shape(B=B, T=T, H=H, factor_dims=factor_dims, d_sub=d_sub, d_v=d_v, W=W, R=R,
+                    chunk_size=chunk_size, act_dtype=_dtype_code(x, "x"), bank_dtype=_dtype_code(bank, "bank"))
+    keep = keep or {}
+    if out is None:
+        out = torch.empty_like(x)
+    for name, t in (("x", x), ("w_qw", w_qw), ("w_qr", w_qr), ("w_v", w_v), ("w_g", w_g), ("w_o", w_o),
+                    ("subkeys", subkeys), ("bank", bank), ("bank_init", bank_init), ("out", out),
+                    ("workspace", workspace)) + tuple((f"keep[{k}]", v) for k, v in keep.items()):
+        _require_cuda_contig(name, t, dev)
+    for name, t, rows in (("w_qw", w_qw, H * F * d_sub), ("w_qr", w_qr, H * F * d_sub), ("w_v", w_v, H * d_v),
+                          ("w_g", w_g, 2 * H), ("w_o", w_o, dim)):
+        cols = H * d_v if name == "w_o" else dim
+        if tuple(t.shape) != (rows, cols):
+            raise ValueError(f"{name} must be [{rows}, {cols}], got {tuple(t.shape)}")
+        if t.dtype != x.dtype:
+            raise TypeError(f"{name} must have x's dtype")
+    if workspace is None:
+        workspace = torch.empty(layer_workspace_size(sh, dim), dtype=torch.uint8, device=dev)
+    st = _abi.load().sdm_layer_forward(
+        ctypes.byref(sh), int(dim), _ptr(x), _ptr(w_qw), _ptr(w_qr), _ptr(w_v), _ptr(w_g), _ptr(w_o),
+        _ptr(subkeys), _ptr(bank_init), _ptr(bank), _ptr(out), _ptr(keep.get("q_w")), _ptr(keep.get("q_r")),
+        _ptr(keep.get("k_val")), _ptr(keep.get("gates")), _ptr(keep.get("y")), _ptr(workspace),
+        workspace.numel(), _stream_handle(stream, dev))
+    _abi.check(st, "sdm_layer_forward")
+    return out
+
+
 def _owns_storage(t: torch.Tensor) -> bool:
     """True when writing into t cannot reach another tensor's data (the donate guards).
 

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define SDM_ABI_VERSION 2
+#define SDM_ABI_VERSION 3
 
 /* Compiled limits.  Shapes beyond them are refused with SDM_ERR_UNSUPPORTED. */
 #define SDM_MAX_FACTORS 4          /* product-key factors F                          */
@@ -249,6 +249,34 @@ sdm_status sdm_write_read_backward(const sdm_shape *shape, const void *q_w, cons
                                    sdm_stream_t stream);
 
 /*
+ * The SDM layer forward around the op (sparse-delta-memory README, usage example: a layer
+ * of model width dim with num_heads heads, slots_per_head slots, num_writes / num_reads and
+ * chunk_size; y = layer(x) with the bank advancing in place).  With X = x as [B*T, dim] and
+ * row-major weights [out, in]:
+ *   q_w = X w_qw^T, q_r = X w_qr^T   [B,T,H,F*d_sub]   w_qw, w_qr: [H*F*d_sub, dim]
+ *   k_val = X w_v^T                  [B,T,H,d_v]       w_v: [H*d_v, dim]
+ *   gates = sigmoid(X w_g^T)         [B,T,H,2] float32 w_g: [2H, dim], row 2h = alpha of
+ *                                                      head h, row 2h+1 = beta
+ *   y = the write/read op (sdm_write_read) on them, bank_init copied into bank first
+ *   out = Y w_o^T                    [B,T,dim]         w_o: [dim, H*d_v]
+ * x, the weights, subkeys, the intermediates and out are in the activation dtype (the
+ * gates float32); products accumulate in float32.  The dense projections are cuBLASLt
+ * GEMMs (loaded on first use; unavailable -> SDM_ERR_CUDA) run on the caller's workspace
+ * with split-K reductions excluded; the gate projection and its sigmoid are a kernel of
+ * this library.  Results are bitwise repeatable on one device.
+ *   q_w, q_r, k_val, gates, y  NULL, or buffers that receive those intermediates (else
+ *              they live in the workspace).
+ * Every pointer is 16-byte aligned.  Refusals as for sdm_write_read, plus dim < 1
+ * (INVALID).  The layer has no counterpart of the backward here (forward only).
+ */
+sdm_status sdm_layer_workspace_size(const sdm_shape *shape, int64_t dim, size_t *bytes);
+sdm_status sdm_layer_forward(const sdm_shape *shape, int64_t dim, const void *x, const void *w_qw,
+                             const void *w_qr, const void *w_v, const void *w_g, const void *w_o,
+                             const void *subkeys, const void *bank_init, void *bank, void *out,
+                             void *q_w, void *q_r, void *k_val, float *gates, void *y,
+                             void *workspace, size_t workspace_bytes, sdm_stream_t stream);
+
+/*
  * One decode step (shape->T must be 1; chunk_size is ignored) for all B*H streams.
  * Tensors as above with T = 1.
  *   bank_in         the state's tables: [B, H, N, d_v], or, with bank_in_shared != 0,
@@ -305,7 +333,10 @@ enum {
   SDM_KERNEL_BWD_SWEEP = 8,   /* backward: reverse sweep over the rows, bank restored   */
   SDM_KERNEL_BWD_REDUCE = 9,  /* backward: column sums, softmax backward, dq            */
   SDM_KERNEL_BWD_SUBKEY = 10, /* backward: sub-key gradient tiles and their sum         */
-  SDM_NUM_KERNEL_KINDS = 11
+  SDM_KERNEL_LAYER_GATES = 11, /* layer: gate projection + sigmoid                      */
+  SDM_KERNEL_LAYER_GEMM = 12,  /* layer: the cuBLASLt projections (library kernels, not  */
+                               /* counted by sdm_launch_count)                            */
+  SDM_NUM_KERNEL_KINDS = 13
 };
 typedef struct {
   int64_t launches[SDM_NUM_KERNEL_KINDS];
