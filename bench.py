@@ -37,7 +37,8 @@ import sdm_inputs  # noqa: E402
 METRIC = "SDM write/read tokens/s per layer on 1 GB300; achieved HBM GB/s vs roofline"
 UNIT = "tokens/s"
 WORKLOADS = {"layer": "layer", "train_fwd": "train_fwd", "three_factor": "three_factor",
-             "decode": "decode", "tiny": "tiny", "train": "train_fwd"}
+             "decode": "decode", "tiny": "tiny", "train": "train_fwd", "readme_layer": "layer"}
+README_DIM = 2048          # the README usage example's model width (dim = num_heads * d_v)
 KERNEL_SOURCES = ("sdm_write_read.cu", "sdm_write_read_f32_f32.cu", "sdm_write_read_f32_bf16.cu",
                   "sdm_write_read_bf16_f32.cu", "sdm_write_read_bf16_bf16.cu", "sdm_wr_kernel.cuh",
                   "sdm_delta.cuh", "sdm_common.cuh", "sdm_internal.h")
@@ -321,6 +322,8 @@ def main():
         return bench_decode(args, cfg, sdm, dev, rank, world, barrier, pg)
     if args.workload == "train":
         return bench_train(args, cfg, sdm, dev, rank, world, barrier, pg)
+    if args.workload == "readme_layer":
+        return bench_readme_layer(args, cfg, sdm, dev, rank, world, barrier, pg)
 
     d = sdm_inputs.make_inputs(cfg, seed=rank_seed(cfg, rank))
     g = {k: v.to(dev) for k, v in d.items()}
@@ -565,6 +568,77 @@ def bench_train(args, cfg, sdm, dev, rank, world, barrier, pg):
         "roofline": per[dominant],
         "rooflines": per,
         "kernels_ms_per_step": {k: v[1] / max(v[0], 1) * (v[0] / args.steps) for k, v in kt.items() if v[0]},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": None,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_readme_layer(args, cfg, sdm, dev, rank, world, barrier, pg):
+    """The README call: the SDM layer forward around the op (x [B, T, dim] -> [B, T, dim],
+    dim = 2048, the bank reset from the learned table every call), through
+    sdm_layer_forward: the cuBLASLt projections, the gates kernel, the op, the output
+    projection."""
+    L = sdm_inputs.make_layer_inputs(cfg, README_DIM, seed=rank_seed(cfg, rank))
+    g = {k: v.to(dev) for k, v in L.items()}
+    B, T, H = cfg.B, cfg.T, cfg.H
+    bank = torch.empty((B, H, cfg.N, cfg.d_v), dtype=g["bank_init"].dtype, device=dev)
+    out = torch.empty_like(g["x"])
+    shape = sdm.make_shape(B=B, T=T, H=H, factor_dims=cfg.factor_dims, d_sub=cfg.d_sub, d_v=cfg.d_v,
+                           W=cfg.W, R=cfg.R, chunk_size=cfg.chunk_size,
+                           act_dtype=0 if cfg.act_dtype == "f32" else 1,
+                           bank_dtype=0 if cfg.bank_dtype == "f32" else 1)
+    ws = torch.empty(sdm.layer_workspace_size(shape, README_DIM), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        sdm.sdm_layer_forward(g["x"], g["w_qw"], g["w_qr"], g["w_v"], g["w_g"], g["w_o"], g["subkeys"], bank,
+                              cfg.chunk_size, cfg.W, cfg.R, factor_dims=cfg.factor_dims, bank_init=g["bank_init"],
+                              out=out, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    assert sdm.last_device_error(ws) == 0
+    launches0 = sdm.launch_count()
+    sdm.profile_begin()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+    kt = sdm.profile_end()
+    launches = sdm.launch_count() - launches0
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
+    value = whole_job_rate(B * T * args.steps, world, ms)
+    sb = 4 if cfg.bank_dtype == "f32" else 2
+    alg = B * T * H * (cfg.W + cfg.R) * cfg.d_v * sb
+    n, t = kt["write_read"]
+    avg = t / max(n, 1) / 1e3
+    peak, peak_kind = peaks()
+    gemm_flop = 2 * B * T * README_DIM * (2 * H * cfg.F * cfg.d_sub + 2 * H * cfg.d_v)
+    gn, gt = kt["layer_gemm"]
+    if rank != 0:
+        return 0
+    line = {
+        "metric": "SDM layer forward (README call) tokens/s on 1 GB300", "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg) + f", layer dim={README_DIM}",
+                   "step": "query/value projections (cuBLASLt) + gates kernel + bank copy + scoring/top-k + plan "
+                           "+ write/read + output projection (cuBLASLt)"},
+        "roofline": {"bound": "hbm", "kernel": "write_read", "achieved": alg / avg / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": alg / avg / 1e9 / peak, "traffic": None, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": alg, "launch_ms": avg * 1e3},
+        "projections": {"flop_per_step": gemm_flop, "ms_per_step": gt / args.steps,
+                        "tflops": gemm_flop / (gt / args.steps / 1e3) / 1e12 if gt else None},
+        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items() if v[0]},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "e2e": None,
