@@ -711,13 +711,14 @@ constexpr int64_t kSubkeyChunk = 1024;        // rows of K = 2*B*T per split of 
 
 struct BwdLayout {
   int64_t flags, part, ds, dk_part, total;
-  int64_t P, PS, KS;
+  int64_t P, PS, KS, Pw;
 };
 
 BwdLayout bwd_layout(const sdm_shape *sh, const Derived &d) {
   BwdLayout w{};
   const int64_t S = sh->B * sh->H, BT = sh->B * sh->T;
-  w.P = (sh->d_v * elem_bytes(sh->bank_dtype) + 16 * kSweepCG - 1) / (16 * kSweepCG);
+  w.Pw = (sh->d_v * elem_bytes(sh->bank_dtype) + 16 * kSweepCG - 1) / (16 * kSweepCG);
+  w.P = kSweepCtaRecord ? (w.Pw + kSweepCtaWarps - 1) / kSweepCtaWarps : w.Pw;
   w.PS = bwd_part_stride(sh->W, sh->R);
   w.KS = (2 * BT + kSubkeyChunk - 1) / kSubkeyChunk;
   int64_t o = kHeaderBytes;
@@ -829,6 +830,7 @@ sdm_status backward_impl(const sdm_shape *sh, const void *q_w, const void *q_r, 
   a.W = sh->W;
   a.R = sh->R;
   a.P = (int32_t)bl.P;
+  a.Pw = (int32_t)bl.Pw;
   a.P32 = (int32_t)snapshot_pieces(sh);
   a.PS = (int32_t)bl.PS;
   a.act_bf16 = sh->act_dtype == SDM_BF16;

@@ -27,7 +27,11 @@ namespace sdm {
 
 namespace {
 
-constexpr int kSweepWarps = 2;      // warps per CTA of the sweep (adjacent pieces of the rows)
+constexpr int kSweepWarps = kSweepCtaWarps;      // warps per CTA of the sweep (adjacent pieces of the rows)
+// The CTA's warps add their partial column sums in shared memory (in warp order, once per
+// token, behind a CTA barrier) and store one record per CTA instead of one per warp.
+constexpr bool kSweepCombine = kSweepCtaRecord;
+constexpr int kPartMax = (2 * SDM_MAX_K + 2 + 3) & ~3;   // the largest partial record (floats)
 // 16-byte stage slots per lane: JB snapshot rows (two slots each), JB read rows and the
 // float32 G of the read and write rows (VEC / 4 slots each)
 __host__ __device__ constexpr int sweep_slots(int JB, int VEC) { return JB * (3 + 2 * (VEC / 4)); }
@@ -162,13 +166,13 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
   constexpr int VEC = 16 / (int)sizeof(BANK);
   constexpr int RG = 32 / CG;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = blockIdx.x * kSweepWarps + warp;
+  const int p = blockIdx.x * kSweepWarps + warp;    // this warp's column piece
   const int64_t s = blockIdx.y;
   if (*a.snap_hdr != kSnapshotArmed) {          // no snapshot to undo: touch nothing
     if (lane == 0 && p == 0) raise_error(a.err, SDM_DEVERR_SNAPSHOT);
     return;
   }
-  if (p >= a.P) return;
+  if (!kSweepCombine && p >= a.Pw) return;       // (with the combine, idle warps add zeros)
   const int W = FULL ? 64 : a.W, R = FULL ? 64 : a.R;
   const int rg = lane / CG, c = lane % CG;
   const int64_t col = ((int64_t)p * CG + c) * VEC;
@@ -184,6 +188,7 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
   const unsigned char *snap_sp = a.snap + ((s * a.T) * a.P32 + p32) * (int64_t)W * pcs + half * VEC * se;
   const int64_t snap_tstep = (int64_t)a.P32 * W * pcs;
   const bool abf = a.act_bf16 != 0;
+  __shared__ __align__(16) float comb[2][kSweepWarps][kPartMax];
   // stage slots of a lane (16-byte chunks): snapshot rows (2 each), read rows, their G
   // (GC each), write rows' G (GC each)
   constexpr int GC = VEC / 4;
@@ -374,7 +379,9 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
       dap = __fadd_rn(dap, __shfl_xor_sync(0xffffffffu, dap, o));
       dbp = __fadd_rn(dbp, __shfl_xor_sync(0xffffffffu, dbp, o));
     }
-    float *pp = a.part + ((s * a.T + t) * a.P + p) * (int64_t)a.PS;
+    // this warp's record: its own slot of the part buffer, or its row of the CTA's
+    // shared-memory buffer (two, alternating by token, so one barrier a token suffices)
+    float *pp = kSweepCombine ? comb[t & 1][warp] : a.part + ((s * a.T + t) * a.P + p) * (int64_t)a.PS;
     if constexpr (FULL && JB == 4) {
       if (c == 0) *reinterpret_cast<float4 *>(pp + wr_.j0) = make_float4(dwp[0], dwp[1], dwp[2], dwp[3]);
       if (c == CG - 1) *reinterpret_cast<float4 *>(pp + W + rd.j0) = make_float4(drp[0], drp[1], drp[2], drp[3]);
@@ -402,7 +409,22 @@ __global__ void __launch_bounds__(32 * kSweepWarps) bwd_sweep_kernel(const __gri
       for (int q = 0; q < JB; ++q) bad |= !wr_.has(q, N) || !rd.has(q, N);
     }
     if (bad) raise_error(a.err, SDM_DEVERR_SLOT_RANGE);
-    __syncwarp();                                   // this token's stores before the next one's loads
+    if constexpr (kSweepCombine) {
+      // every warp's record is in shared memory and its global stores are ordered before
+      // the next token's loads (the barrier orders the CTA's memory traffic); the CTA's
+      // threads then add the records in warp order and store the CTA's one
+      named_barrier(1, 32 * kSweepWarps);
+      const int n_tot = W + R + 2;
+      float *dst = a.part + ((s * a.T + t) * a.P + blockIdx.x) * (int64_t)a.PS;
+      for (int v = threadIdx.x; v < n_tot; v += 32 * kSweepWarps) {
+        float acc = comb[t & 1][0][v];
+#pragma unroll
+        for (int w = 1; w < kSweepWarps; ++w) acc = __fadd_rn(acc, comb[t & 1][w][v]);
+        dst[v] = acc;
+      }
+    } else {
+      __syncwarp();                                 // this token's stores before the next one's loads
+    }
     cur = nxt;
   }
 }
@@ -636,7 +658,7 @@ __global__ void __launch_bounds__(kThreads) bwd_subkey_sum_kernel(const __grid_c
 // W = R = 64 fixed at compile time (two rows per lane and sum), else up to four.
 template <typename BANK, int JB, bool FULL>
 cudaError_t launch_sweep_jb(const BackwardArgs &a, cudaStream_t st) {
-  const dim3 grid((unsigned)((a.P + kSweepWarps - 1) / kSweepWarps), (unsigned)(a.B * a.H));
+  const dim3 grid((unsigned)((a.Pw + kSweepWarps - 1) / kSweepWarps), (unsigned)(a.B * a.H));
   const int64_t smem = (int64_t)kSweepWarps * sweep_slots(JB, 16 / (int)sizeof(BANK)) * 32 * 16;
   auto kern = bwd_sweep_kernel<BANK, kSweepCG, JB, FULL>;
   const cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kern), smem);

@@ -210,7 +210,8 @@ struct BackwardArgs {
   float *dk_part;         // [KS, H, ntot, d_sub]
   int32_t *err;
   int64_t B, T, N, d_v;
-  int32_t H, W, R, P, PS;  // P: column pieces of the sweep (partials); PS: partial stride
+  int32_t H, W, R, P, PS;  // P: partial records per token; PS: their stride (floats)
+  int32_t Pw;             // column pieces of the sweep (one warp each)
   int32_t P32;            // 32-byte pieces of a row (the snapshot's layout)
   int32_t act_bf16, snap_bf16;
   int32_t KS;             // split of the sub-key gradient's K = 2*B*T rows
@@ -225,8 +226,11 @@ cudaError_t launch_bwd_reduce(const BackwardArgs &a, cudaStream_t st);
 cudaError_t launch_bwd_subkeys(const BackwardArgs &a, cudaStream_t st);
 inline int32_t bwd_part_stride(int W, int R) { return (W + R + 2 + 3) & ~3; }
 // 16-byte column groups per warp of the backward's reverse sweep (the piece is
-// 16 * kSweepCG bytes of every bank row).
+// 16 * kSweepCG bytes of every bank row), warps per sweep CTA, and whether a CTA's warps
+// store one combined record of partial column sums per token (else one each).
 constexpr int kSweepCG = 2;
+constexpr int kSweepCtaWarps = 2;
+constexpr bool kSweepCtaRecord = true;
 
 // The layer around the op (sdm_layer.cu).  layer_gemm: out[n][m] = sum_k a[m][k] b[n][k]
 // (row-major weights a [m, k], activations b [n, k]) by cuBLASLt, loaded on first use;
