@@ -144,3 +144,86 @@ def test_decode_copy_form_captures(sdm):
     torch.cuda.synchronize()
     assert torch.equal(out, out_e) and torch.equal(y, y_e)
     assert sdm.last_device_error(ws) == 0
+
+
+def _capture_and_compare(call, outputs, check):
+    """Warm up off the capture, capture one call, zero the outputs, replay: the replay
+    gives the eager results bit for bit."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    want = {k: v.clone() for k, v in outputs.items()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for v in outputs.values():
+        v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    check()
+    for k, v in outputs.items():
+        assert torch.equal(v, want[k]), k
+    return graph
+
+
+def test_training_step_graph_replay_is_bitwise_eager(sdm):
+    """The training pair (forward with snapshot, dL/d(final bank) = 0, backward) captured as
+    one graph: every replay arms and spends the snapshot, restores the bank and gives the
+    eager gradients bit for bit."""
+    cfg = CONFIGS["tiny"].replace(W=64, R=64, T=96, d_v=128, act_dtype="bf16", bank_dtype="bf16")
+    g = to_device(sdm_inputs.make_inputs(cfg))
+    gr = to_device(sdm_inputs.make_grad_inputs(cfg, dbank=False))
+    bank, y, ws = _write_read_buffers(sdm, cfg, g)
+    shape = sdm.make_shape(B=cfg.B, T=cfg.T, H=cfg.H, factor_dims=cfg.factor_dims, d_sub=cfg.d_sub, d_v=cfg.d_v,
+                           W=cfg.W, R=cfg.R, chunk_size=cfg.chunk_size, act_dtype=1, bank_dtype=1)
+    bws = torch.empty(sdm.backward_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    dbank = torch.zeros((cfg.B, cfg.H, cfg.N, cfg.d_v), dtype=torch.float32, device="cuda")
+    saved = sdm.sdm_write_read_train(g["q_w"], g["q_r"], g["k_val"], g["gates"], g["subkeys"], bank, cfg.chunk_size,
+                                     cfg.W, cfg.R, factor_dims=cfg.factor_dims, bank_init=g["bank_init"],
+                                     snapshot_dtype=torch.bfloat16, y=y, workspace=ws)
+    grads = sdm.sdm_write_read_backward(g["q_w"], g["q_r"], g["k_val"], g["gates"], g["subkeys"], bank, gr["dy"],
+                                        saved, cfg.W, cfg.R, factor_dims=cfg.factor_dims, dbank=dbank,
+                                        workspace=bws)
+    grads.pop("workspace")
+
+    def call():
+        sdm.sdm_write_read_train(g["q_w"], g["q_r"], g["k_val"], g["gates"], g["subkeys"], bank, cfg.chunk_size,
+                                 cfg.W, cfg.R, factor_dims=cfg.factor_dims, bank_init=g["bank_init"],
+                                 snapshot_dtype=torch.bfloat16, saved=saved, y=y, workspace=ws)
+        dbank.zero_()
+        sdm.sdm_write_read_backward(g["q_w"], g["q_r"], g["k_val"], g["gates"], g["subkeys"], bank, gr["dy"],
+                                    saved, cfg.W, cfg.R, factor_dims=cfg.factor_dims, dbank=dbank, grads=grads,
+                                    workspace=bws)
+
+    outs = {("d_" + k): v for k, v in grads.items()}          # d_bank is the gradient table
+    outs.update(y=y, bank=bank)
+
+    def check():
+        assert sdm.last_device_error(ws) == 0 and sdm.last_device_error(bws) == 0
+
+    _capture_and_compare(call, outs, check)
+    assert torch.equal(bank, g["bank_init"].unsqueeze(0).expand_as(bank))   # restored
+
+
+def test_layer_forward_graph_replay_is_bitwise_eager(sdm):
+    """The layer forward (cuBLASLt projections included) captured and replayed."""
+    cfg = CONFIGS["tiny"].replace(act_dtype="bf16", factor_dims=(16, 16), d_sub=32, d_v=64, H=2, B=2, T=48,
+                                  W=16, R=16)
+    dim = 128
+    L = to_device(sdm_inputs.make_layer_inputs(cfg, dim))
+    bank = torch.empty((cfg.B, cfg.H, cfg.N, cfg.d_v), dtype=L["bank_init"].dtype, device="cuda")
+    out = torch.empty_like(L["x"])
+    shape = sdm.make_shape(B=cfg.B, T=cfg.T, H=cfg.H, factor_dims=cfg.factor_dims, d_sub=cfg.d_sub, d_v=cfg.d_v,
+                           W=cfg.W, R=cfg.R, chunk_size=cfg.chunk_size, act_dtype=1, bank_dtype=0)
+    ws = torch.empty(sdm.layer_workspace_size(shape, dim), dtype=torch.uint8, device="cuda")
+
+    def call():
+        sdm.sdm_layer_forward(L["x"], L["w_qw"], L["w_qr"], L["w_v"], L["w_g"], L["w_o"], L["subkeys"], bank,
+                              cfg.chunk_size, cfg.W, cfg.R, factor_dims=cfg.factor_dims, bank_init=L["bank_init"],
+                              out=out, workspace=ws)
+
+    _capture_and_compare(call, {"out": out, "bank": bank}, lambda: None)
+    assert sdm.last_device_error(ws) == 0
