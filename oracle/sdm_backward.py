@@ -190,7 +190,8 @@ def stream_backward(M: np.ndarray, fwd: dict, dy: np.ndarray, dM: np.ndarray, q_
 
 def sdm_write_read_backward(q_w, q_r, k_val, gates, subkeys, bank, dy, dbank, *, factor_dims, W: int, R: int,
                             act_dtype: str = "f32", bank_dtype: str = "f32", snapshot_dtype: Optional[str] = None,
-                            streams: Optional[Iterable] = None, pick: Optional[Callable] = None) -> dict:
+                            streams: Optional[Iterable] = None, pick: Optional[Callable] = None,
+                            exact: bool = False) -> dict:
     """Gradients of the write/read op over all (or the listed) streams.
 
     Inputs as sdm_oracle.sdm_write_read (bank [B,H,N,d_v] per stream); dy [B,T,H,d_v] and
@@ -198,7 +199,7 @@ def sdm_write_read_backward(q_w, q_r, k_val, gates, subkeys, bank, dy, dbank, *,
     forward with its record, then the reverse sweep, stream by stream.  Sub-key gradients
     of one head are summed over batch elements in increasing b.  Returns float64 arrays
     shaped like the inputs.  ``pick(b, h)``, if given, returns the per-stream pick
-    passed to stream_forward (or None).
+    passed to stream_forward (or None); ``exact`` is stream_forward's (float64 scores).
     """
     q_w, q_r, k_val, gates, subkeys = _f64(q_w), _f64(q_r), _f64(k_val), _f64(gates), _f64(subkeys)
     bank, dy, dbank = _f64(bank), _f64(dy), _f64(dbank)
@@ -212,7 +213,7 @@ def sdm_write_read_backward(q_w, q_r, k_val, gates, subkeys, bank, dy, dbank, *,
         M = bank[b, h].copy()
         fwd = stream_forward(M, q_w[b, :, h], q_r[b, :, h], k_val[b, :, h], gates[b, :, h], subkeys[h],
                              factor_dims=factor_dims, d_sub=d_sub, W=W, R=R, act_dtype=act_dtype,
-                             bank_dtype=bank_dtype, snapshot_dtype=snapshot_dtype,
+                             bank_dtype=bank_dtype, snapshot_dtype=snapshot_dtype, exact=exact,
                              pick=None if pick is None else pick(b, h))
         g = stream_backward(M, fwd, dy[b, :, h], dbank[b, h], q_w[b, :, h], q_r[b, :, h], k_val[b, :, h],
                             gates[b, :, h], subkeys[h], factor_dims=factor_dims, d_sub=d_sub)

@@ -11,7 +11,11 @@ Readings where the pages are silent (the plainest layer that the op's inputs imp
     (alpha, beta); weights stored [out, in];
   * an output projection of the heads' reads [H*d_v] back to dim, without bias;
   * projections accumulate exactly (float64 here) and round once to the activation
-    type; the gates round once to float32.
+    type; the gates round once to float32;
+  * the backward (README > usage example: backward() through the layer) is the chain rule
+    through these maps around the op's backward (sdm_backward), every rounding passing
+    the gradient unchanged; the learned table's gradient is the sum over the batch of the
+    streams' bank gradients.
 """
 
 from __future__ import annotations
@@ -20,9 +24,10 @@ from typing import Iterable, Optional
 
 import numpy as np
 
+from . import sdm_backward
 from .sdm_oracle import _f64, round_to, sdm_write_read
 
-__all__ = ["project", "gates_of", "layer_forward"]
+__all__ = ["project", "gates_of", "layer_forward", "layer_backward"]
 
 
 def project(x: np.ndarray, w: np.ndarray, act_dtype: str) -> np.ndarray:
@@ -73,3 +78,71 @@ def layer_forward(x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank_init, *, factor_di
         y[b, :, h] = res["y"]
     out = project(y.reshape(B * T, H * d_v), w_o, act_dtype).reshape(B, T, dim)
     return dict(own, y=y, out=out, op=op)
+
+
+def layer_backward(x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank_init, dout, *, factor_dims, W: int, R: int,
+                   act_dtype: str = "f32", bank_dtype: str = "f32", snapshot_dtype: Optional[str] = None,
+                   dbank=None, given: Optional[dict] = None, pick=None, exact: bool = False) -> dict:
+    """Gradients of a loss with respect to the layer's inputs, for dout = dL/d(out) [B,T,dim]
+    (and dbank = dL/d(final bank) [B,H,N,d_v], zeros when None).
+
+    ``given`` as in layer_forward (the op's inputs and its read y: the backward then runs the
+    op's backward on them and the output projection's backward on y); ``pick`` goes to
+    sdm_backward.sdm_write_read_backward; ``exact``: float64 everywhere with float64 scores
+    (for finite differences; act_dtype and bank_dtype should then be "f64").
+    Returns float64 arrays keyed x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank ([B,H,N,d_v]),
+    bank_init ([H,N,d_v]), and the op's gradients under "op".
+    """
+    x = _f64(x)
+    B, T, dim = x.shape
+    H, _, d_sub = np.shape(subkeys)
+    F = len(factor_dims)
+    d_v = np.shape(bank_init)[-1]
+    BT, dq, dv = B * T, H * F * d_sub, H * d_v
+    X = x.reshape(BT, dim)
+    w_qw, w_qr, w_v, w_g, w_o = (_f64(w) for w in (w_qw, w_qr, w_v, w_g, w_o))
+    if exact:
+        ins = {"q_w": (X @ w_qw.T).reshape(B, T, H, F * d_sub), "q_r": (X @ w_qr.T).reshape(B, T, H, F * d_sub),
+               "k_val": (X @ w_v.T).reshape(B, T, H, d_v),
+               "gates": (1.0 / (1.0 + np.exp(-(X @ w_g.T)))).reshape(B, T, H, 2)}
+    else:
+        ins = {"q_w": project(X, w_qw, act_dtype).reshape(B, T, H, F * d_sub),
+               "q_r": project(X, w_qr, act_dtype).reshape(B, T, H, F * d_sub),
+               "k_val": project(X, w_v, act_dtype).reshape(B, T, H, d_v),
+               "gates": gates_of(X, w_g).reshape(B, T, H, 2)}
+    if given:
+        ins.update({k: _f64(v) for k, v in given.items() if k != "y"})
+    if given and "y" in given:
+        Y = _f64(given["y"]).reshape(BT, dv)
+    else:
+        bank = np.broadcast_to(_f64(bank_init)[None], (B, H) + np.shape(bank_init)[1:])
+        fwd = {}
+        for b in range(B):
+            for h in range(H):
+                M = np.array(bank[b, h])
+                rec = sdm_backward.stream_forward(M, ins["q_w"][b, :, h], ins["q_r"][b, :, h], ins["k_val"][b, :, h],
+                                                  ins["gates"][b, :, h], _f64(subkeys)[h], factor_dims=factor_dims,
+                                                  d_sub=d_sub, W=W, R=R, act_dtype=act_dtype, bank_dtype=bank_dtype,
+                                                  exact=exact, pick=None if pick is None else pick(b, h))
+                fwd[(b, h)] = rec["y"]
+        Y = np.zeros((B, T, H, d_v))
+        for (b, h), yy in fwd.items():
+            Y[b, :, h] = yy
+        Y = Y.reshape(BT, dv)
+    D = _f64(dout).reshape(BT, dim)
+    dY = D @ w_o                                        # [BT, H d_v]
+    dw_o = D.T @ Y                                      # [dim, H d_v]
+    bank = np.broadcast_to(_f64(bank_init)[None], (B, H) + np.shape(bank_init)[1:])
+    db = np.zeros(bank.shape) if dbank is None else _f64(dbank)
+    g = sdm_backward.sdm_write_read_backward(ins["q_w"], ins["q_r"], ins["k_val"], ins["gates"], subkeys, bank,
+                                             dY.reshape(B, T, H, d_v), db, factor_dims=factor_dims, W=W, R=R,
+                                             act_dtype=act_dtype, bank_dtype=bank_dtype,
+                                             snapshot_dtype=snapshot_dtype, pick=pick, exact=exact)
+    z = X @ w_g.T
+    s = 1.0 / (1.0 + np.exp(-z))
+    dz = g["gates"].reshape(BT, 2 * H) * s * (1.0 - s)
+    d_qw, d_qr, d_kv = g["q_w"].reshape(BT, dq), g["q_r"].reshape(BT, dq), g["k_val"].reshape(BT, dv)
+    dx = d_qw @ w_qw + d_qr @ w_qr + d_kv @ w_v + dz @ w_g
+    return {"x": dx.reshape(B, T, dim), "w_qw": d_qw.T @ X, "w_qr": d_qr.T @ X, "w_v": d_kv.T @ X,
+            "w_g": dz.T @ X, "w_o": dw_o, "subkeys": g["subkeys"], "bank": g["bank"],
+            "bank_init": g["bank"].sum(axis=0), "op": g}

@@ -8,6 +8,7 @@ projection or a wrong head order fails); the gates' sigmoid is checked on exact 
 """
 
 import numpy as np
+import pytest
 
 from oracle import sdm_layer, sdm_oracle
 
@@ -95,3 +96,75 @@ def test_output_projection_is_linear_in_its_weight():
     b = sdm_layer.layer_forward(*args, w_o2, p["subkeys"], p["bank"], **kw)["out"]
     c = sdm_layer.layer_forward(*args, w_o1 + w_o2, p["subkeys"], p["bank"], **kw)["out"]
     assert np.allclose(a + b, c, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- the layer's backward
+
+from oracle import sdm_backward  # noqa: E402
+
+GROUPS = ("x", "w_qw", "w_qr", "w_v", "w_g", "w_o", "subkeys", "bank_init")
+
+
+def _train_problem(seed=3, B=2, T=6, H=2, factor_dims=(4, 5), d_sub=3, d_v=4, dim=9):
+    rng = np.random.default_rng(seed)
+    F = len(factor_dims)
+    N = int(np.prod(factor_dims))
+    dq = H * F * d_sub
+    p = {"x": rng.normal(0, 1, (B, T, dim)), "w_qw": rng.normal(0, 0.6, (dq, dim)),
+         "w_qr": rng.normal(0, 0.6, (dq, dim)), "w_v": rng.normal(0, 0.5, (H * d_v, dim)),
+         "w_g": rng.normal(0, 0.5, (2 * H, dim)), "w_o": rng.normal(0, 0.5, (dim, H * d_v)),
+         "subkeys": rng.normal(0, 1 / np.sqrt(d_sub), (H, sum(factor_dims), d_sub)),
+         "bank_init": rng.normal(0, 0.5, (H, N, d_v))}
+    c_out = rng.normal(0, 1, (B, T, dim))
+    c_M = rng.normal(0, 1, (B, H, N, d_v))
+    return p, c_out, c_M, dict(factor_dims=factor_dims, W=3, R=4)
+
+
+def _exact_loss(p, c_out, c_M, kw):
+    """sum(c_out * out) + sum(c_M * final banks), the layer in float64 with float64 scores."""
+    B, T, dim = p["x"].shape
+    H = p["subkeys"].shape[0]
+    X = p["x"].reshape(B * T, dim)
+    q_w = (X @ p["w_qw"].T).reshape(B, T, H, -1)
+    q_r = (X @ p["w_qr"].T).reshape(B, T, H, -1)
+    k_val = (X @ p["w_v"].T).reshape(B, T, H, -1)
+    gates = (1.0 / (1.0 + np.exp(-(X @ p["w_g"].T)))).reshape(B, T, H, 2)
+    d_v = p["bank_init"].shape[-1]
+    Y = np.zeros((B, T, H, d_v))
+    loss = 0.0
+    for b in range(B):
+        for h in range(H):
+            M = p["bank_init"][h].copy()
+            rec = sdm_backward.stream_forward(M, q_w[b, :, h], q_r[b, :, h], k_val[b, :, h], gates[b, :, h],
+                                              p["subkeys"][h], factor_dims=kw["factor_dims"], d_sub=p["subkeys"].shape[2],
+                                              W=kw["W"], R=kw["R"], act_dtype="f64", bank_dtype="f64", exact=True)
+            Y[b, :, h] = rec["y"]
+            loss += float(np.sum(c_M[b, h] * M))
+    out = Y.reshape(B * T, -1) @ p["w_o"].T
+    return loss + float(np.sum(c_out.reshape(B * T, dim) * out))
+
+
+@pytest.mark.parametrize("group", GROUPS)
+def test_layer_gradients_match_directional_differences(group):
+    """<grad, v> against the central difference of the exact layer loss along a random
+    direction v of one parameter group: a dropped term, a transposed weight or a wrong
+    sigmoid derivative moves it far beyond the difference's error."""
+    p, c_out, c_M, kw = _train_problem()
+    g = sdm_layer.layer_backward(p["x"], p["w_qw"], p["w_qr"], p["w_v"], p["w_g"], p["w_o"], p["subkeys"],
+                                 p["bank_init"], c_out, dbank=c_M, act_dtype="f64", bank_dtype="f64", exact=True, **kw)
+    rng = np.random.default_rng(11)
+    v = rng.normal(0, 1, p[group].shape)
+    eps = 1e-6
+    hi, lo = dict(p), dict(p)
+    hi[group] = p[group] + eps * v
+    lo[group] = p[group] - eps * v
+    fd = (_exact_loss(hi, c_out, c_M, kw) - _exact_loss(lo, c_out, c_M, kw)) / (2 * eps)
+    an = float(np.sum(g[group] * v))
+    assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (group, fd, an)
+
+
+def test_learned_table_gradient_is_the_batch_sum():
+    p, c_out, c_M, kw = _train_problem(4)
+    g = sdm_layer.layer_backward(p["x"], p["w_qw"], p["w_qr"], p["w_v"], p["w_g"], p["w_o"], p["subkeys"],
+                                 p["bank_init"], c_out, dbank=c_M, act_dtype="f64", bank_dtype="f64", exact=True, **kw)
+    assert np.array_equal(g["bank_init"], g["bank"].sum(axis=0))
