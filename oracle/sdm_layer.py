@@ -14,7 +14,10 @@ Readings where the pages are silent (the plainest layer that the op's inputs imp
     type; the gates round once to float32;
   * the backward (README > usage example: backward() through the layer) is the chain rule
     through these maps around the op's backward (sdm_backward), every rounding passing
-    the gradient unchanged; the learned table's gradient is the sum over the batch of the
+    the gradient unchanged; the gradients that cross between the dense products and the op
+    are held in the activation type, as the op's activations are (dy = dout w_o, and the
+    query, value and gate-logit gradients before they meet the weights), so they round
+    once to it there; the learned table's gradient is the sum over the batch of the
     streams' bank gradients.
 """
 
@@ -130,7 +133,9 @@ def layer_backward(x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank_init, dout, *, fa
             Y[b, :, h] = yy
         Y = Y.reshape(BT, dv)
     D = _f64(dout).reshape(BT, dim)
-    dY = D @ w_o                                        # [BT, H d_v]
+    dY = D @ w_o                                        # [BT, H d_v]: the op's dy
+    if not exact:
+        dY = round_to(dY, act_dtype)                    # the op takes dy in the activation type
     dw_o = D.T @ Y                                      # [dim, H d_v]
     bank = np.broadcast_to(_f64(bank_init)[None], (B, H) + np.shape(bank_init)[1:])
     db = np.zeros(bank.shape) if dbank is None else _f64(dbank)
@@ -142,6 +147,9 @@ def layer_backward(x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank_init, dout, *, fa
     s = 1.0 / (1.0 + np.exp(-z))
     dz = g["gates"].reshape(BT, 2 * H) * s * (1.0 - s)
     d_qw, d_qr, d_kv = g["q_w"].reshape(BT, dq), g["q_r"].reshape(BT, dq), g["k_val"].reshape(BT, dv)
+    if not exact:                                       # the projections' gradients meet the
+        d_qw, d_qr, d_kv, dz = (round_to(a, act_dtype)  # weights in the activation type
+                                for a in (d_qw, d_qr, d_kv, dz))
     dx = d_qw @ w_qw + d_qr @ w_qr + d_kv @ w_v + dz @ w_g
     return {"x": dx.reshape(B, T, dim), "w_qw": d_qw.T @ X, "w_qr": d_qr.T @ X, "w_v": d_kv.T @ X,
             "w_g": dz.T @ X, "w_o": dw_o, "subkeys": g["subkeys"], "bank": g["bank"],
