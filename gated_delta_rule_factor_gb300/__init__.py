@@ -11,8 +11,9 @@ and fails loudly if it has not been built (``python gated_delta_rule_factor_gb30
 from . import _abi
 from ._abi import SdmError, SdmShape
 from .ops import (backward_workspace_size, decode_workspace_size, last_device_error, launch_count,
-                  layer_workspace_size, make_shape, profile_begin, profile_end, sdm_decode_step,
-                  sdm_layer_forward, sdm_write_read,
+                  layer_backward_workspace_size, layer_workspace_size, make_shape, profile_begin, profile_end,
+                  sdm_decode_step, sdm_layer_backward, sdm_layer_forward, sdm_layer_forward_train,
+                  sdm_write_read,
                   sdm_write_read_backward, sdm_write_read_static, sdm_write_read_train,
                   snapshot_bytes, test_force_simt_scorer, test_force_write_read_layout,
                   test_stall_decode_copy, write_read_workspace_size)
@@ -21,7 +22,8 @@ lib = _abi.load()
 
 __all__ = [
     "SdmError", "SdmShape", "backward_workspace_size", "decode_workspace_size", "last_device_error",
-    "launch_count", "layer_workspace_size", "make_shape", "profile_begin", "profile_end", "sdm_decode_step", "sdm_layer_forward",
+    "launch_count", "layer_backward_workspace_size", "layer_workspace_size", "make_shape", "profile_begin", "profile_end", "sdm_decode_step", "sdm_layer_backward", "sdm_layer_forward",
+    "sdm_layer_forward_train",
     "sdm_write_read", "sdm_write_read_backward", "sdm_write_read_static", "sdm_write_read_train", "snapshot_bytes",
     "test_force_simt_scorer", "test_force_write_read_layout", "test_stall_decode_copy",
     "write_read_workspace_size", "lib",

@@ -858,6 +858,50 @@ sdm_status backward_impl(const sdm_shape *sh, const void *q_w, const void *q_r, 
   return ok();
 }
 
+// sdm_write_read_train's checks and work (also the op of the layer's training forward).
+sdm_status train_forward_impl(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
+                              const float *gates, const void *subkeys, const void *bank_init, void *bank, void *y,
+                              int32_t *idx_w, float *wt_w, int32_t *idx_r, float *wt_r, void *snapshot,
+                              size_t snapshot_bytes, int32_t snapshot_dtype, void *workspace, size_t workspace_bytes,
+                              sdm_stream_t stream) {
+  sdm_status st = check_shape(sh, false, nullptr);
+  if (st != SDM_OK) return st;
+  if ((st = check_snapshot_dtype(snapshot_dtype)) != SDM_OK) return st;
+  const int64_t rows = sh->B * sh->T * sh->H;
+  if (!snapshot) return fail(SDM_ERR_INVALID_ARG, "snapshot is NULL");
+  if (!aligned(snapshot, 16)) return fail(SDM_ERR_INVALID_ARG, "snapshot is not 16-byte aligned");
+  const int64_t need = snapshot_bytes_of(sh, snapshot_dtype);
+  if ((int64_t)snapshot_bytes < need)
+    return fail(SDM_ERR_INVALID_ARG, "snapshot has %zu bytes, needs %lld", snapshot_bytes, (long long)need);
+  const Range r_snap{snapshot, (int64_t)snapshot_bytes, "snapshot"};
+  const Range sel[] = {{idx_w, rows * sh->W * 4, "idx_w"}, {wt_w, rows * sh->W * 4, "wt_w"},
+                       {idx_r, rows * sh->R * 4, "idx_r"}, {wt_r, rows * sh->R * 4, "wt_r"}};
+  for (const Range &r : sel) {
+    if (rows > 0 && !r.p) return fail(SDM_ERR_INVALID_ARG, "%s is NULL (the backward reads it)", r.name);
+    if (r.p && !aligned(r.p, 16)) return fail(SDM_ERR_INVALID_ARG, "%s is not 16-byte aligned", r.name);
+  }
+  Derived d;
+  check_shape(sh, false, &d);
+  const int64_t ab = elem_bytes(sh->act_dtype), sb = elem_bytes(sh->bank_dtype);
+  const Range others[] = {{q_w, rows * sh->F * sh->d_sub * ab, "q_w"}, {q_r, rows * sh->F * sh->d_sub * ab, "q_r"},
+                          {k_val, rows * sh->d_v * ab, "k_val"}, {gates, rows * 8, "gates"},
+                          {subkeys, sh->H * d.ntot * sh->d_sub * ab, "subkeys"},
+                          {bank_init, sh->H * d.N * sh->d_v * sb, "bank_init"},
+                          {bank, sh->B * sh->H * d.N * sh->d_v * sb, "bank"}, {y, rows * sh->d_v * ab, "y"},
+                          sel[0], sel[1], sel[2], sel[3],
+                          {workspace, (int64_t)workspace_bytes, "workspace"}};
+  for (const Range &o : others)
+    if (overlap(r_snap, o)) return fail(SDM_ERR_ALIAS, "snapshot overlaps %s", o.name);
+  const SnapOut so{static_cast<unsigned char *>(snapshot) + kSnapshotHeaderBytes, snapshot_dtype == SDM_BF16};
+  st = write_read_impl(sh, q_w, q_r, k_val, gates, subkeys, bank_init, bank, y, idx_w, wt_w, idx_r, wt_r,
+                       workspace, workspace_bytes, stream, true, &so);
+  if (st != SDM_OK) return st;
+  // armed for one backward, once the forward's kernels are done (stream order)
+  const cudaError_t ce = cudaMemsetAsync(snapshot, 0x5a, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
+  return ok();
+}
+
 // ---------------------------------------------------------------- the layer around the op
 
 struct LayerLayout {
@@ -882,11 +926,15 @@ LayerLayout layer_layout(const sdm_shape *sh, const Derived &d) {
 sdm_status layer_impl(const sdm_shape *sh, int64_t dim, const void *x, const void *w_qw, const void *w_qr,
                       const void *w_v, const void *w_g, const void *w_o, const void *subkeys,
                       const void *bank_init, void *bank, void *out, void *q_w, void *q_r, void *k_val,
-                      float *gates, void *y, void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+                      float *gates, void *y, void *workspace, size_t workspace_bytes, sdm_stream_t stream,
+                      const sdm_layer_saved *saved = nullptr) {
   Derived d;
   sdm_status st = check_shape(sh, false, &d);
   if (st != SDM_OK) return st;
   if (dim < 1) return fail(SDM_ERR_INVALID_ARG, "dim must be >= 1");
+  if (saved && sh->B * sh->T * sh->H > 0 &&
+      !(saved->q_w && saved->q_r && saved->k_val && saved->gates && saved->y))
+    return fail(SDM_ERR_INVALID_ARG, "saved: the intermediates are required for training");
   const int64_t ab = elem_bytes(sh->act_dtype), BT = sh->B * sh->T, rows = BT * sh->H;
   const int64_t dq = (int64_t)d.g.F * sh->d_sub * sh->H;            // query width of a token
   const int64_t dv = sh->d_v * sh->H;
@@ -947,13 +995,156 @@ sdm_status layer_impl(const sdm_shape *sh, int64_t dim, const void *x, const voi
          })) != SDM_OK)
       return st;
   }
-  // the op
-  if ((st = write_read_impl(sh, qw, qr, kv, gt, subkeys, bank_init, bank, yy, nullptr, nullptr, nullptr, nullptr,
-                            ws + ll.op_ws, (size_t)(ll.q_w - ll.op_ws), stream, true)) != SDM_OK)
-    return st;
+  // the op (with the training forward's snapshot and selections when training)
+  if (saved) st = train_forward_impl(sh, qw, qr, kv, gt, subkeys, bank_init, bank, yy, saved->idx_w, saved->wt_w,
+                                     saved->idx_r, saved->wt_r, saved->snapshot, saved->snapshot_bytes,
+                                     saved->snapshot_dtype, ws + ll.op_ws, (size_t)(ll.q_w - ll.op_ws), stream);
+  else st = write_read_impl(sh, qw, qr, kv, gt, subkeys, bank_init, bank, yy, nullptr, nullptr, nullptr, nullptr,
+                            ws + ll.op_ws, (size_t)(ll.q_w - ll.op_ws), stream, true);
+  if (st != SDM_OK) return st;
   if (rows > 0 &&
       (st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer output projection", [&] {
          return layer_gemm(w_o, yy, out, dim, BT, dv, adt, gws, kLayerGemmWorkspace, cs);
+       })) != SDM_OK)
+    return st;
+  return ok();
+}
+
+// ---------------------------------------------------------------- the layer's backward
+
+struct LayerBwdLayout {
+  int64_t op_ws, dY, d_qw, d_qr, d_kv, d_g, gcat, wcat, gemm, total;
+  int64_t dq, dv, ng, K;
+};
+
+LayerBwdLayout layer_bwd_layout(const sdm_shape *sh, const Derived &d, int64_t dim) {
+  LayerBwdLayout w{};
+  const int64_t BT = sh->B * sh->T, ab = elem_bytes(sh->act_dtype);
+  w.dq = (int64_t)d.g.F * sh->d_sub * sh->H;
+  w.dv = sh->d_v * sh->H;
+  w.ng = 2 * sh->H;
+  w.K = 2 * w.dq + w.dv + w.ng;
+  int64_t o = 0;
+  w.op_ws = o; o = a256(o + bwd_layout(sh, d).total);
+  w.dY = o;    o = a256(o + BT * w.dv * ab);
+  w.d_qw = o;  o = a256(o + BT * w.dq * 4);
+  w.d_qr = o;  o = a256(o + BT * w.dq * 4);
+  w.d_kv = o;  o = a256(o + BT * w.dv * 4);
+  w.d_g = o;   o = a256(o + BT * w.ng * 4);
+  w.gcat = o;  o = a256(o + BT * w.K * ab);
+  w.wcat = o;  o = a256(o + w.K * dim * ab);
+  w.gemm = o;  o = a256(o + kLayerGemmWorkspace);
+  w.total = o;
+  return w;
+}
+
+sdm_status layer_backward_impl(const sdm_shape *sh, int64_t dim, const void *x, const void *w_qw, const void *w_qr,
+                               const void *w_v, const void *w_g, const void *w_o, const void *subkeys, void *bank,
+                               const void *dout, const sdm_layer_saved *sv, const sdm_layer_grads *gr,
+                               void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+  Derived d;
+  sdm_status st = check_shape(sh, false, &d);
+  if (st != SDM_OK) return st;
+  if (dim < 1) return fail(SDM_ERR_INVALID_ARG, "dim must be >= 1");
+  if (!sv || !gr) return fail(SDM_ERR_INVALID_ARG, "saved and grads are required");
+  const int64_t ab = elem_bytes(sh->act_dtype), BT = sh->B * sh->T;
+  const LayerBwdLayout L = layer_bwd_layout(sh, d, dim);
+  const Range need[] = {{x, BT * dim * ab, "x"}, {w_qw, L.dq * dim * ab, "w_qw"}, {w_qr, L.dq * dim * ab, "w_qr"},
+                        {w_v, L.dv * dim * ab, "w_v"}, {w_g, L.ng * dim * ab, "w_g"}, {w_o, dim * L.dv * ab, "w_o"},
+                        {dout, BT * dim * ab, "dout"}, {sv->y, BT * L.dv * ab, "saved.y"},
+                        {gr->dx, BT * dim * ab, "grads.dx"}, {gr->dw_qw, L.dq * dim * 4, "grads.dw_qw"},
+                        {gr->dw_qr, L.dq * dim * 4, "grads.dw_qr"}, {gr->dw_v, L.dv * dim * 4, "grads.dw_v"},
+                        {gr->dw_g, L.ng * dim * 4, "grads.dw_g"}, {gr->dw_o, dim * L.dv * 4, "grads.dw_o"}};
+  for (const Range &r : need) {
+    if (BT * sh->H > 0 && !r.p) return fail(SDM_ERR_INVALID_ARG, "%s is NULL", r.name);
+    if (r.p && !aligned(r.p, 16)) return fail(SDM_ERR_INVALID_ARG, "%s is not 16-byte aligned", r.name);
+  }
+  if (gr->d_bank_init && !aligned(gr->d_bank_init, 16))
+    return fail(SDM_ERR_INVALID_ARG, "grads.d_bank_init is not 16-byte aligned");
+  if (!workspace) return fail(SDM_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256)) return fail(SDM_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  if ((int64_t)workspace_bytes < L.total)
+    return fail(SDM_ERR_WORKSPACE, "workspace has %zu bytes, needs %lld", workspace_bytes, (long long)L.total);
+  // outputs written before the op's backward checks its own arguments: none may overlap
+  // an input or each other
+  const Range ins[] = {need[0], need[1], need[2], need[3], need[4], need[5], need[6], need[7],
+                       {sv->q_w, BT * L.dq * ab, "saved.q_w"}, {sv->q_r, BT * L.dq * ab, "saved.q_r"},
+                       {sv->k_val, BT * L.dv * ab, "saved.k_val"}, {sv->gates, BT * L.ng * 4, "saved.gates"}};
+  const Range outs[] = {need[8], need[9], need[10], need[11], need[12], need[13],
+                        {gr->d_bank_init, sh->H * d.N * sh->d_v * 4, "grads.d_bank_init"},
+                        {gr->dbank, sh->B * sh->H * d.N * sh->d_v * 4, "grads.dbank"},
+                        {workspace, (int64_t)workspace_bytes, "workspace"}};
+  for (const Range &o : outs)
+    for (const Range &i : ins)
+      if (overlap(o, i)) return fail(SDM_ERR_ALIAS, "%s overlaps %s", o.name, i.name);
+  for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i)
+    for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+      if (overlap(outs[i], outs[j])) return fail(SDM_ERR_ALIAS, "%s overlaps %s", outs[i].name, outs[j].name);
+
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  void *gws = ws + L.gemm;
+  void *dY = ws + L.dY, *gcat = ws + L.gcat, *wcat = ws + L.wcat;
+  float *d_qw = reinterpret_cast<float *>(ws + L.d_qw), *d_qr = reinterpret_cast<float *>(ws + L.d_qr);
+  float *d_kv = reinterpret_cast<float *>(ws + L.d_kv), *d_g = reinterpret_cast<float *>(ws + L.d_g);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int adt = sh->act_dtype;
+  int sms = 0;
+  if ((st = sm_count(&sms)) != SDM_OK) return st;
+  const size_t gwb = (size_t)kLayerGemmWorkspace;
+  if (BT > 0) {
+    // dY = dout w_o (the op's dy) and dw_o = dout^T Y
+    if ((st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer dY", [&] {
+           return lt_gemm(false, false, L.dv, BT, dim, w_o, L.dv, dout, dim, dY, L.dv, adt, adt, false, gws, gwb, cs);
+         })) != SDM_OK)
+      return st;
+    if ((st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer dw_o", [&] {
+           return lt_gemm(false, true, L.dv, dim, BT, sv->y, L.dv, dout, dim, gr->dw_o, L.dv, adt, SDM_F32, false,
+                          gws, gwb, cs);
+         })) != SDM_OK)
+      return st;
+  }
+  // the op's backward (restores the bank, disarms the snapshot)
+  if ((st = backward_impl(sh, sv->q_w, sv->q_r, sv->k_val, sv->gates, subkeys, sv->idx_w, sv->wt_w, sv->idx_r,
+                          sv->wt_r, sv->snapshot, sv->snapshot_bytes, sv->snapshot_dtype, bank, dY, gr->dbank, d_kv,
+                          d_g, d_qw, d_qr, gr->d_subkeys, ws + L.op_ws, (size_t)(L.dY - L.op_ws), stream)) != SDM_OK)
+    return st;
+  if (BT > 0) {
+    // G = [d_q_w | d_q_r | d_k_val | dz], W = [w_qw; w_qr; w_v; w_g]
+    if ((st = run_kernel(SDM_KERNEL_LAYER_GRAD, cs, "layer_grad_cat", [&] {
+           return launch_layer_grad_cat(d_qw, d_qr, d_kv, d_g, sv->gates, gcat, BT, L.dq, L.dv, L.ng, adt, sms, cs);
+         })) != SDM_OK)
+      return st;
+    const void *wsrc[] = {w_qw, w_qr, w_v, w_g};
+    const int64_t wrows[] = {L.dq, L.dq, L.dv, L.ng};
+    int64_t roff = 0;
+    for (int i = 0; i < 4; ++i) {
+      const cudaError_t ce = cudaMemcpyAsync(static_cast<unsigned char *>(wcat) + roff * dim * ab, wsrc[i],
+                                             (size_t)(wrows[i] * dim * ab), cudaMemcpyDeviceToDevice, cs);
+      if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemcpyAsync: %s", cudaGetErrorString(ce));
+      roff += wrows[i];
+    }
+    // dx = G W
+    if ((st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer dx", [&] {
+           return lt_gemm(false, false, dim, BT, L.K, wcat, dim, gcat, L.K, gr->dx, dim, adt, adt, false, gws, gwb,
+                          cs);
+         })) != SDM_OK)
+      return st;
+    // dw_* = G_*^T X, G_* the columns of G that belong to the weight
+    float *dws[] = {gr->dw_qw, gr->dw_qr, gr->dw_v, gr->dw_g};
+    int64_t coff = 0;
+    for (int i = 0; i < 4; ++i) {
+      const void *gi = static_cast<const unsigned char *>(gcat) + coff * ab;
+      if ((st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer dw", [&] {
+             return lt_gemm(false, true, dim, wrows[i], BT, x, dim, gi, L.K, dws[i], dim, adt, SDM_F32, false, gws,
+                            gwb, cs);
+           })) != SDM_OK)
+        return st;
+      coff += wrows[i];
+    }
+  }
+  if (gr->d_bank_init &&
+      (st = run_kernel(SDM_KERNEL_LAYER_GRAD, cs, "batch_sum", [&] {
+         return launch_batch_sum(gr->dbank, gr->d_bank_init, sh->B, sh->H * d.N * sh->d_v, sms, cs);
        })) != SDM_OK)
     return st;
   return ok();
@@ -1004,42 +1195,8 @@ sdm_status sdm_write_read_train(const sdm_shape *sh, const void *q_w, const void
                                 void *y, int32_t *idx_w, float *wt_w, int32_t *idx_r, float *wt_r,
                                 void *snapshot, size_t snapshot_bytes, int32_t snapshot_dtype, void *workspace,
                                 size_t workspace_bytes, sdm_stream_t stream) {
-  sdm_status st = check_shape(sh, false, nullptr);
-  if (st != SDM_OK) return st;
-  if ((st = check_snapshot_dtype(snapshot_dtype)) != SDM_OK) return st;
-  const int64_t rows = sh->B * sh->T * sh->H;
-  if (!snapshot) return fail(SDM_ERR_INVALID_ARG, "snapshot is NULL");
-  if (!aligned(snapshot, 16)) return fail(SDM_ERR_INVALID_ARG, "snapshot is not 16-byte aligned");
-  const int64_t need = snapshot_bytes_of(sh, snapshot_dtype);
-  if ((int64_t)snapshot_bytes < need)
-    return fail(SDM_ERR_INVALID_ARG, "snapshot has %zu bytes, needs %lld", snapshot_bytes, (long long)need);
-  const Range r_snap{snapshot, (int64_t)snapshot_bytes, "snapshot"};
-  const Range sel[] = {{idx_w, rows * sh->W * 4, "idx_w"}, {wt_w, rows * sh->W * 4, "wt_w"},
-                       {idx_r, rows * sh->R * 4, "idx_r"}, {wt_r, rows * sh->R * 4, "wt_r"}};
-  for (const Range &r : sel) {
-    if (rows > 0 && !r.p) return fail(SDM_ERR_INVALID_ARG, "%s is NULL (the backward reads it)", r.name);
-    if (r.p && !aligned(r.p, 16)) return fail(SDM_ERR_INVALID_ARG, "%s is not 16-byte aligned", r.name);
-  }
-  Derived d;
-  check_shape(sh, false, &d);
-  const int64_t ab = elem_bytes(sh->act_dtype), sb = elem_bytes(sh->bank_dtype);
-  const Range others[] = {{q_w, rows * sh->F * sh->d_sub * ab, "q_w"}, {q_r, rows * sh->F * sh->d_sub * ab, "q_r"},
-                          {k_val, rows * sh->d_v * ab, "k_val"}, {gates, rows * 8, "gates"},
-                          {subkeys, sh->H * d.ntot * sh->d_sub * ab, "subkeys"},
-                          {bank_init, sh->H * d.N * sh->d_v * sb, "bank_init"},
-                          {bank, sh->B * sh->H * d.N * sh->d_v * sb, "bank"}, {y, rows * sh->d_v * ab, "y"},
-                          sel[0], sel[1], sel[2], sel[3],
-                          {workspace, (int64_t)workspace_bytes, "workspace"}};
-  for (const Range &o : others)
-    if (overlap(r_snap, o)) return fail(SDM_ERR_ALIAS, "snapshot overlaps %s", o.name);
-  const SnapOut so{static_cast<unsigned char *>(snapshot) + kSnapshotHeaderBytes, snapshot_dtype == SDM_BF16};
-  st = write_read_impl(sh, q_w, q_r, k_val, gates, subkeys, bank_init, bank, y, idx_w, wt_w, idx_r, wt_r,
-                       workspace, workspace_bytes, stream, true, &so);
-  if (st != SDM_OK) return st;
-  // armed for one backward, once the forward's kernels are done (stream order)
-  const cudaError_t ce = cudaMemsetAsync(snapshot, 0x5a, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream));
-  if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
-  return ok();
+  return train_forward_impl(sh, q_w, q_r, k_val, gates, subkeys, bank_init, bank, y, idx_w, wt_w, idx_r, wt_r,
+                            snapshot, snapshot_bytes, snapshot_dtype, workspace, workspace_bytes, stream);
 }
 
 sdm_status sdm_write_read_backward_workspace_size(const sdm_shape *shape, size_t *bytes) {
@@ -1078,6 +1235,34 @@ sdm_status sdm_layer_forward(const sdm_shape *sh, int64_t dim, const void *x, co
                              float *gates, void *y, void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
   return layer_impl(sh, dim, x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank_init, bank, out, q_w, q_r, k_val, gates,
                     y, workspace, workspace_bytes, stream);
+}
+
+sdm_status sdm_layer_forward_train(const sdm_shape *sh, int64_t dim, const void *x, const void *w_qw,
+                                   const void *w_qr, const void *w_v, const void *w_g, const void *w_o,
+                                   const void *subkeys, const void *bank_init, void *bank, void *out,
+                                   const sdm_layer_saved *saved, void *workspace, size_t workspace_bytes,
+                                   sdm_stream_t stream) {
+  if (!saved) return fail(SDM_ERR_INVALID_ARG, "saved is NULL");
+  return layer_impl(sh, dim, x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank_init, bank, out, saved->q_w, saved->q_r,
+                    saved->k_val, saved->gates, saved->y, workspace, workspace_bytes, stream, saved);
+}
+
+sdm_status sdm_layer_backward_workspace_size(const sdm_shape *shape, int64_t dim, size_t *bytes) {
+  if (!bytes) return fail(SDM_ERR_INVALID_ARG, "bytes is NULL");
+  Derived d;
+  sdm_status st = check_shape(shape, false, &d);
+  if (st != SDM_OK) return st;
+  if (dim < 1) return fail(SDM_ERR_INVALID_ARG, "dim must be >= 1");
+  *bytes = (size_t)layer_bwd_layout(shape, d, dim).total;
+  return ok();
+}
+
+sdm_status sdm_layer_backward(const sdm_shape *sh, int64_t dim, const void *x, const void *w_qw, const void *w_qr,
+                              const void *w_v, const void *w_g, const void *w_o, const void *subkeys, void *bank,
+                              const void *dout, const sdm_layer_saved *saved, const sdm_layer_grads *grads,
+                              void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+  return layer_backward_impl(sh, dim, x, w_qw, w_qr, w_v, w_g, w_o, subkeys, bank, dout, saved, grads, workspace,
+                             workspace_bytes, stream);
 }
 
 sdm_status sdm_decode_step(const sdm_shape *sh, const void *q_w, const void *q_r, const void *k_val,
@@ -1278,6 +1463,7 @@ const char *sdm_kernel_name(int32_t kind) {
     case SDM_KERNEL_BWD_SUBKEY: return "bwd_subkeys";
     case SDM_KERNEL_LAYER_GATES: return "layer_gates";
     case SDM_KERNEL_LAYER_GEMM: return "layer_gemm";
+    case SDM_KERNEL_LAYER_GRAD: return "layer_grad";
   }
   return "unknown";
 }

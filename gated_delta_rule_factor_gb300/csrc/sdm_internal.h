@@ -239,6 +239,15 @@ const char *layer_gemm(const void *a, const void *b, void *out, int64_t m, int64
                        void *ws, size_t ws_bytes, cudaStream_t st);
 cudaError_t launch_layer_gates(const void *x, const void *w_g, float *gates, int64_t rows, int64_t dim,
                                int32_t n_gates, int act_dtype, int sm_count, cudaStream_t st);
+// The general column-major product D (m x n, ldd) = op(A) op(B) (+ D), A/B of type ab, D
+// of type dd, float32 accumulation; nullptr or the reason it failed.
+const char *lt_gemm(bool ta, bool tb, int64_t m, int64_t n, int64_t k, const void *A, int64_t lda, const void *B,
+                    int64_t ldb, void *D, int64_t ldd, int ab, int dd, bool accumulate, void *ws, size_t ws_bytes,
+                    cudaStream_t st);
+cudaError_t launch_layer_grad_cat(const float *d_qw, const float *d_qr, const float *d_kv, const float *d_g,
+                                  const float *gates, void *gcat, int64_t rows, int64_t dq, int64_t dv, int64_t ng,
+                                  int act_dtype, int sm_count, cudaStream_t st);
+cudaError_t launch_batch_sum(const float *in, float *out, int64_t B, int64_t n, int sm_count, cudaStream_t st);
 constexpr int64_t kLayerGemmWorkspace = (int64_t)32 << 20;   // cuBLASLt's share of a layer workspace
 
 // Raises a kernel's dynamic shared-memory limit to at least `smem` bytes on the current

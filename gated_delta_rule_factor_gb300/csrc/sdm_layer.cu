@@ -46,6 +46,41 @@ __global__ void __launch_bounds__(kThreads) layer_gates_kernel(const ACT *x, con
   }
 }
 
+// The layer backward's concatenated input gradient, one token row r at a time:
+//   gcat[r] = [d_q_w[r] | d_q_r[r] | d_k_val[r] | dz[r]]  (activation type)
+// with dz[r][j] = d_gates[r][j] * g (1 - g), g = gates[r][j] (the sigmoid's derivative).
+template <typename ACT>
+__global__ void __launch_bounds__(kThreads) layer_grad_cat_kernel(const float *d_qw, const float *d_qr,
+                                                                  const float *d_kv, const float *d_g,
+                                                                  const float *gates, ACT *gcat, int64_t rows,
+                                                                  int64_t dq, int64_t dv, int64_t ng) {
+  const int64_t K = 2 * dq + dv + ng;
+  const int64_t total = rows * K;
+  for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < total; e += (int64_t)gridDim.x * kThreads) {
+    const int64_t r = e / K, c = e - r * K;
+    float v;
+    if (c < dq) v = d_qw[r * dq + c];
+    else if (c < 2 * dq) v = d_qr[r * dq + (c - dq)];
+    else if (c < 2 * dq + dv) v = d_kv[r * dv + (c - 2 * dq)];
+    else {
+      const int64_t j = c - 2 * dq - dv;
+      const float g = gates[r * ng + j];
+      v = __fmul_rn(d_g[r * ng + j], __fmul_rn(g, __fsub_rn(1.0f, g)));
+    }
+    gcat[e] = from_f32<ACT>(v);
+  }
+}
+
+// out[i] = sum over b = 0 .. B-1, in that order, of in[b * n + i] (the learned table's
+// gradient: the streams' bank gradients summed over the batch).
+__global__ void __launch_bounds__(kThreads) batch_sum_kernel(const float *in, float *out, int64_t B, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
+    float acc = 0.0f;
+    for (int64_t b = 0; b < B; ++b) acc = __fadd_rn(acc, in[b * n + i]);
+    out[i] = acc;
+  }
+}
+
 // ---------------------------------------------------------------- cuBLASLt, loaded on demand
 
 struct Lt {
@@ -110,40 +145,78 @@ cublasLtHandle_t lt_handle(const char **why) {
 
 }  // namespace
 
-// out[n][m] = sum_k a[m][k] * b[n][k] for row-major a [m, k] (weights, out x in) and b
-// [n, k] (activations): the column-major product op(A) = a (transposed) times b.
-const char *layer_gemm(const void *a, const void *b, void *out, int64_t m, int64_t n, int64_t k, int act_dtype,
-                       void *ws, size_t ws_bytes, cudaStream_t st) {
+cudaError_t launch_layer_grad_cat(const float *d_qw, const float *d_qr, const float *d_kv, const float *d_g,
+                                  const float *gates, void *gcat, int64_t rows, int64_t dq, int64_t dv, int64_t ng,
+                                  int act_dtype, int sm_count, cudaStream_t st) {
+  const int64_t total = rows * (2 * dq + dv + ng);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + kThreads - 1) / kThreads;
+  if (blocks > (int64_t)sm_count * 32) blocks = (int64_t)sm_count * 32;
+  if (act_dtype == SDM_BF16)
+    layer_grad_cat_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, st>>>(
+        d_qw, d_qr, d_kv, d_g, gates, static_cast<__nv_bfloat16 *>(gcat), rows, dq, dv, ng);
+  else
+    layer_grad_cat_kernel<float><<<(unsigned)blocks, kThreads, 0, st>>>(d_qw, d_qr, d_kv, d_g, gates,
+                                                                        static_cast<float *>(gcat), rows, dq, dv, ng);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_batch_sum(const float *in, float *out, int64_t B, int64_t n, int sm_count, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + kThreads - 1) / kThreads;
+  if (blocks > (int64_t)sm_count * 32) blocks = (int64_t)sm_count * 32;
+  batch_sum_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(in, out, B, n);
+  return cudaGetLastError();
+}
+
+// D = op(A) op(B) (+ D when accumulate), column-major (cuBLASLt's convention): op(A) is
+// m x k, op(B) is k x n, D is m x n with leading dimension ldd.  A and B have the type ab
+// (bfloat16 or float32 activations), D the type dd; float32 accumulation.
+const char *lt_gemm(bool ta, bool tb, int64_t m, int64_t n, int64_t k, const void *A, int64_t lda, const void *B,
+                    int64_t ldb, void *D, int64_t ldd, int ab, int dd, bool accumulate, void *ws, size_t ws_bytes,
+                    cudaStream_t st) {
   if (m == 0 || n == 0) return nullptr;
   const char *why = nullptr;
   cublasLtHandle_t h = lt_handle(&why);
   if (!h) return why;
-  const cudaDataType_t t = act_dtype == SDM_BF16 ? CUDA_R_16BF : CUDA_R_32F;
+  const cudaDataType_t tab = ab == SDM_BF16 ? CUDA_R_16BF : CUDA_R_32F;
+  const cudaDataType_t tdd = dd == SDM_BF16 ? CUDA_R_16BF : CUDA_R_32F;
   cublasLtMatmulDesc_t desc = nullptr;
   cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
   cublasLtMatmulPreference_t pref = nullptr;
   const char *err = nullptr;
-  const cublasOperation_t tr = CUBLAS_OP_T, nt = CUBLAS_OP_N;
+  const cublasOperation_t opa = ta ? CUBLAS_OP_T : CUBLAS_OP_N, opb = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
   const uint32_t no_split_k = CUBLASLT_REDUCTION_SCHEME_NONE;
   cublasLtMatmulHeuristicResult_t res{};
   int found = 0;
-  const float one = 1.0f, zero = 0.0f;
+  const float one = 1.0f, beta = accumulate ? 1.0f : 0.0f;
+  // the operands' actual alignments (an operand may start inside a larger matrix)
+  auto align_of = [](const void *p) -> uint32_t {
+    const uintptr_t a = (uintptr_t)p;
+    const uintptr_t low = a & (~a + 1);
+    return (uint32_t)(low == 0 || low > 256 ? 256 : low);
+  };
+  const uint32_t al_a = align_of(A), al_b = align_of(B), al_d = align_of(D);
   if (g_lt.desc_create(&desc, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS ||
-      g_lt.desc_set(desc, CUBLASLT_MATMUL_DESC_TRANSA, &tr, sizeof(tr)) != CUBLAS_STATUS_SUCCESS ||
-      g_lt.desc_set(desc, CUBLASLT_MATMUL_DESC_TRANSB, &nt, sizeof(nt)) != CUBLAS_STATUS_SUCCESS ||
-      g_lt.layout_create(&la, t, (uint64_t)k, (uint64_t)m, k) != CUBLAS_STATUS_SUCCESS ||
-      g_lt.layout_create(&lb, t, (uint64_t)k, (uint64_t)n, k) != CUBLAS_STATUS_SUCCESS ||
-      g_lt.layout_create(&lc, t, (uint64_t)m, (uint64_t)n, m) != CUBLAS_STATUS_SUCCESS ||
+      g_lt.desc_set(desc, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof(opa)) != CUBLAS_STATUS_SUCCESS ||
+      g_lt.desc_set(desc, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof(opb)) != CUBLAS_STATUS_SUCCESS ||
+      g_lt.layout_create(&la, tab, (uint64_t)(ta ? k : m), (uint64_t)(ta ? m : k), lda) != CUBLAS_STATUS_SUCCESS ||
+      g_lt.layout_create(&lb, tab, (uint64_t)(tb ? n : k), (uint64_t)(tb ? k : n), ldb) != CUBLAS_STATUS_SUCCESS ||
+      g_lt.layout_create(&lc, tdd, (uint64_t)m, (uint64_t)n, ldd) != CUBLAS_STATUS_SUCCESS ||
       g_lt.pref_create(&pref) != CUBLAS_STATUS_SUCCESS ||
       g_lt.pref_set(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_bytes, sizeof(ws_bytes)) !=
           CUBLAS_STATUS_SUCCESS ||
       g_lt.pref_set(pref, CUBLASLT_MATMUL_PREF_REDUCTION_SCHEME_MASK, &no_split_k, sizeof(no_split_k)) !=
-          CUBLAS_STATUS_SUCCESS) {
+          CUBLAS_STATUS_SUCCESS ||
+      g_lt.pref_set(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_A_BYTES, &al_a, sizeof(al_a)) != CUBLAS_STATUS_SUCCESS ||
+      g_lt.pref_set(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_B_BYTES, &al_b, sizeof(al_b)) != CUBLAS_STATUS_SUCCESS ||
+      g_lt.pref_set(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_C_BYTES, &al_d, sizeof(al_d)) != CUBLAS_STATUS_SUCCESS ||
+      g_lt.pref_set(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_D_BYTES, &al_d, sizeof(al_d)) != CUBLAS_STATUS_SUCCESS) {
     err = "cuBLASLt descriptor set-up failed";
   } else if (g_lt.heuristic(h, desc, la, lb, lc, lc, pref, 1, &res, &found) != CUBLAS_STATUS_SUCCESS ||
              found < 1) {
-    err = "cuBLASLt found no algorithm for the projection";
-  } else if (g_lt.matmul(h, desc, &one, a, la, b, lb, &zero, out, lc, out, lc, &res.algo, ws, ws_bytes, st) !=
+    err = "cuBLASLt found no algorithm for the product";
+  } else if (g_lt.matmul(h, desc, &one, A, la, B, lb, &beta, D, lc, D, lc, &res.algo, ws, ws_bytes, st) !=
              CUBLAS_STATUS_SUCCESS) {
     err = "cublasLtMatmul failed";
   }
@@ -153,6 +226,13 @@ const char *layer_gemm(const void *a, const void *b, void *out, int64_t m, int64
   if (la) g_lt.layout_destroy(la);
   if (desc) g_lt.desc_destroy(desc);
   return err;
+}
+
+// out[n][m] = sum_k a[m][k] * b[n][k] for row-major a [m, k] (weights, out x in) and b
+// [n, k] (activations): the column-major product op(A) = a (transposed) times b.
+const char *layer_gemm(const void *a, const void *b, void *out, int64_t m, int64_t n, int64_t k, int act_dtype,
+                       void *ws, size_t ws_bytes, cudaStream_t st) {
+  return lt_gemm(true, false, m, n, k, a, k, b, k, out, m, act_dtype, act_dtype, false, ws, ws_bytes, st);
 }
 
 cudaError_t launch_layer_gates(const void *x, const void *w_g, float *gates, int64_t rows, int64_t dim,

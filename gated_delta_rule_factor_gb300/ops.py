@@ -317,6 +317,117 @@ def sdm_layer_forward(x: torch.Tensor, w_qw: torch.Tensor, w_qr: torch.Tensor, w
     return out
 
 
+def layer_backward_workspace_size(shape: _abi.SdmShape, dim: int) -> int:
+    n = ctypes.c_size_t(0)
+    _abi.check(_abi.load().sdm_layer_backward_workspace_size(ctypes.byref(shape), int(dim), ctypes.byref(n)),
+               "sdm_layer_backward_workspace_size")
+    return int(n.value)
+
+
+def _layer_shape(x, subkeys, bank, factor_dims, W, R, chunk_size):
+    B, T, _ = x.shape
+    return make_shape(B=B, T=T, H=subkeys.shape[0], factor_dims=factor_dims, d_sub=subkeys.shape[2],
+                      d_v=bank.shape[-1], W=W, R=R, chunk_size=chunk_size, act_dtype=_dtype_code(x, "x"),
+                      bank_dtype=_dtype_code(bank, "bank"))
+
+
+def _saved_struct(saved: dict) -> _abi.SdmLayerSaved:
+    sv = _abi.SdmLayerSaved()
+    for k in ("q_w", "q_r", "k_val", "gates", "y", "idx_w", "wt_w", "idx_r", "wt_r", "snapshot"):
+        setattr(sv, k, _ptr(saved[k]))
+    sv.snapshot_bytes = saved["snapshot"].numel() * saved["snapshot"].element_size()
+    sv.snapshot_dtype = int(saved["snapshot_dtype"])
+    return sv
+
+
+def sdm_layer_forward_train(x: torch.Tensor, w_qw: torch.Tensor, w_qr: torch.Tensor, w_v: torch.Tensor,
+                            w_g: torch.Tensor, w_o: torch.Tensor, subkeys: torch.Tensor, bank: torch.Tensor,
+                            chunk_size: int, W: int, R: int, *, factor_dims: Sequence[int],
+                            bank_init: Optional[torch.Tensor] = None, snapshot_dtype=torch.float32,
+                            out: Optional[torch.Tensor] = None, saved: Optional[dict] = None,
+                            workspace: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None):
+    """sdm_layer_forward that keeps what sdm_layer_backward needs.  Returns (out, saved):
+    saved holds the intermediates, the selections and the snapshot (pass it back in to
+    reuse its buffers)."""
+    dev = x.device
+    sh = _layer_shape(x, subkeys, bank, factor_dims, W, R, chunk_size)
+    B, T, dim = x.shape
+    H, F, d_sub, d_v = sh.H, len(factor_dims), sh.d_sub, sh.d_v
+    code = _snap_code(snapshot_dtype)
+    if saved is None:
+        f32, i32 = dict(dtype=torch.float32, device=dev), dict(dtype=torch.int32, device=dev)
+        saved = {"q_w": torch.empty((B, T, H, F * d_sub), dtype=x.dtype, device=dev),
+                 "q_r": torch.empty((B, T, H, F * d_sub), dtype=x.dtype, device=dev),
+                 "k_val": torch.empty((B, T, H, d_v), dtype=x.dtype, device=dev),
+                 "gates": torch.empty((B, T, H, 2), **f32), "y": torch.empty((B, T, H, d_v), dtype=x.dtype, device=dev),
+                 "idx_w": torch.empty((B, T, H, W), **i32), "wt_w": torch.empty((B, T, H, W), **f32),
+                 "idx_r": torch.empty((B, T, H, R), **i32), "wt_r": torch.empty((B, T, H, R), **f32),
+                 "snapshot": torch.empty(snapshot_bytes(sh, code), dtype=torch.uint8, device=dev)}
+    saved = dict(saved)
+    saved["snapshot_dtype"] = code
+    if out is None:
+        out = torch.empty_like(x)
+    for name, t in (("x", x), ("w_qw", w_qw), ("w_qr", w_qr), ("w_v", w_v), ("w_g", w_g), ("w_o", w_o),
+                    ("subkeys", subkeys), ("bank", bank), ("bank_init", bank_init), ("out", out),
+                    ("workspace", workspace)) + tuple((f"saved[{k}]", v) for k, v in saved.items()
+                                                      if isinstance(v, torch.Tensor)):
+        _require_cuda_contig(name, t, dev)
+    if workspace is None:
+        workspace = torch.empty(layer_workspace_size(sh, dim), dtype=torch.uint8, device=dev)
+    sv = _saved_struct(saved)
+    st = _abi.load().sdm_layer_forward_train(
+        ctypes.byref(sh), int(dim), _ptr(x), _ptr(w_qw), _ptr(w_qr), _ptr(w_v), _ptr(w_g), _ptr(w_o), _ptr(subkeys),
+        _ptr(bank_init), _ptr(bank), _ptr(out), ctypes.byref(sv), _ptr(workspace), workspace.numel(),
+        _stream_handle(stream, dev))
+    _abi.check(st, "sdm_layer_forward_train")
+    return out, saved
+
+
+def sdm_layer_backward(x: torch.Tensor, w_qw: torch.Tensor, w_qr: torch.Tensor, w_v: torch.Tensor,
+                       w_g: torch.Tensor, w_o: torch.Tensor, subkeys: torch.Tensor, bank: torch.Tensor,
+                       dout: torch.Tensor, saved: dict, chunk_size: int, W: int, R: int, *,
+                       factor_dims: Sequence[int], dbank: Optional[torch.Tensor] = None, learned_table: bool = True,
+                       grads: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """The backward of one sdm_layer_forward_train call for the loss gradient dout [B,T,dim].
+    Returns {"x" (activation dtype), "w_qw", "w_qr", "w_v", "w_g", "w_o", "subkeys", "bank" (the
+    float32 gradient table: dbank in, zeros when None), "bank_init" (its sum over the batch,
+    when learned_table)}; the bank is restored in place."""
+    dev = x.device
+    sh = _layer_shape(x, subkeys, bank, factor_dims, W, R, chunk_size)
+    dim = x.shape[-1]
+    f32 = dict(dtype=torch.float32, device=dev)
+    if dbank is None:
+        dbank = torch.zeros(bank.shape, **f32)
+    if grads is None:
+        grads = {"x": torch.empty_like(x), "w_qw": torch.empty(w_qw.shape, **f32),
+                 "w_qr": torch.empty(w_qr.shape, **f32), "w_v": torch.empty(w_v.shape, **f32),
+                 "w_g": torch.empty(w_g.shape, **f32), "w_o": torch.empty(w_o.shape, **f32),
+                 "subkeys": torch.empty(subkeys.shape, **f32)}
+        if learned_table:
+            grads["bank_init"] = torch.empty(bank.shape[1:], **f32)
+    grads = dict(grads)
+    grads["bank"] = dbank
+    for name, t in (("x", x), ("w_o", w_o), ("subkeys", subkeys), ("bank", bank), ("dout", dout),
+                    ("workspace", workspace)) + tuple((f"grads[{k}]", v) for k, v in grads.items()):
+        _require_cuda_contig(name, t, dev)
+    if workspace is None:
+        workspace = torch.empty(layer_backward_workspace_size(sh, dim), dtype=torch.uint8, device=dev)
+    gs = _abi.SdmLayerGrads()
+    gs.dx, gs.dw_qw, gs.dw_qr = _ptr(grads["x"]), _ptr(grads["w_qw"]), _ptr(grads["w_qr"])
+    gs.dw_v, gs.dw_g, gs.dw_o = _ptr(grads["w_v"]), _ptr(grads["w_g"]), _ptr(grads["w_o"])
+    gs.d_subkeys, gs.dbank, gs.d_bank_init = _ptr(grads["subkeys"]), _ptr(dbank), _ptr(grads.get("bank_init"))
+    sv = _saved_struct(saved)
+    st = _abi.load().sdm_layer_backward(
+        ctypes.byref(sh), int(dim), _ptr(x), _ptr(w_qw), _ptr(w_qr), _ptr(w_v), _ptr(w_g), _ptr(w_o),
+        _ptr(subkeys), _ptr(bank), _ptr(dout), ctypes.byref(sv), ctypes.byref(gs), _ptr(workspace),
+        workspace.numel(), _stream_handle(stream, dev))
+    _abi.check(st, "sdm_layer_backward")
+    grads["workspace"] = workspace
+    return grads
+
+
 def _owns_storage(t: torch.Tensor) -> bool:
     """True when writing into t cannot reach another tensor's data (the donate guards).
 

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define SDM_ABI_VERSION 3
+#define SDM_ABI_VERSION 4
 
 /* Compiled limits.  Shapes beyond them are refused with SDM_ERR_UNSUPPORTED. */
 #define SDM_MAX_FACTORS 4          /* product-key factors F                          */
@@ -267,7 +267,7 @@ sdm_status sdm_write_read_backward(const sdm_shape *shape, const void *q_w, cons
  *   q_w, q_r, k_val, gates, y  NULL, or buffers that receive those intermediates (else
  *              they live in the workspace).
  * Every pointer is 16-byte aligned.  Refusals as for sdm_write_read, plus dim < 1
- * (INVALID).  The layer has no counterpart of the backward here (forward only).
+ * (INVALID).  Training through the layer: sdm_layer_forward_train / sdm_layer_backward.
  */
 sdm_status sdm_layer_workspace_size(const sdm_shape *shape, int64_t dim, size_t *bytes);
 sdm_status sdm_layer_forward(const sdm_shape *shape, int64_t dim, const void *x, const void *w_qw,
@@ -275,6 +275,60 @@ sdm_status sdm_layer_forward(const sdm_shape *shape, int64_t dim, const void *x,
                              const void *subkeys, const void *bank_init, void *bank, void *out,
                              void *q_w, void *q_r, void *k_val, float *gates, void *y,
                              void *workspace, size_t workspace_bytes, sdm_stream_t stream);
+
+/*
+ * Training through the layer (README > usage example: the layer's output goes into a loss
+ * and backward() runs through it with deterministic kernels).  sdm_layer_forward_train is
+ * sdm_layer_forward that keeps what the backward needs in `saved` (every pointer required:
+ * the intermediates as in sdm_layer_forward, the selections [B,T,H,W|R], the snapshot as
+ * for sdm_write_read_train); sdm_layer_backward then gives, for a loss gradient dout
+ * [B,T,dim] (activation dtype):
+ *   dY = dout w_o;  dw_o = dout^T Y                      (cuBLASLt)
+ *   the op's backward (sdm_write_read_backward) on the saved intermediates, which
+ *   restores the bank in place and disarms the snapshot;
+ *   dz = d_gates * g (1 - g) for the gate logits (the sigmoid's derivative);
+ *   G = [d_q_w | d_q_r | d_k_val | dz] rounded to the activation dtype, then
+ *   dx = G [w_qw; w_qr; w_v; w_g] and dw_* = G_*^T X        (cuBLASLt)
+ *   d_bank_init = the sum over the batch, in increasing b, of the streams' bank gradients.
+ * Weight gradients and d_subkeys are float32; dx has the activation dtype.  dbank is the
+ * float32 gradient table of the op's backward: dL/d(final bank) in (zeros when only the
+ * layer's output enters the loss), dL/d(bank after the learned-table copy) out.
+ */
+typedef struct {
+  void *q_w, *q_r, *k_val;   /* [B,T,H,F*d_sub] x2, [B,T,H,d_v]              */
+  float *gates;              /* [B,T,H,2]                                     */
+  void *y;                   /* [B,T,H,d_v]: the op's read                    */
+  int32_t *idx_w;            /* [B,T,H,W] */
+  float *wt_w;
+  int32_t *idx_r;            /* [B,T,H,R] */
+  float *wt_r;
+  void *snapshot;            /* sdm_snapshot_bytes(shape, snapshot_dtype) bytes */
+  size_t snapshot_bytes;
+  int32_t snapshot_dtype;
+} sdm_layer_saved;
+
+typedef struct {
+  void *dx;                  /* [B,T,dim], activation dtype                   */
+  float *dw_qw, *dw_qr;      /* [H*F*d_sub, dim]                              */
+  float *dw_v;               /* [H*d_v, dim]                                  */
+  float *dw_g;               /* [2H, dim]                                     */
+  float *dw_o;               /* [dim, H*d_v]                                  */
+  float *d_subkeys;          /* [H, sum_f n_f, d_sub]                         */
+  float *dbank;              /* [B,H,N,d_v] in/out (above)                    */
+  float *d_bank_init;        /* [H,N,d_v], or NULL                            */
+} sdm_layer_grads;
+
+sdm_status sdm_layer_forward_train(const sdm_shape *shape, int64_t dim, const void *x, const void *w_qw,
+                                   const void *w_qr, const void *w_v, const void *w_g, const void *w_o,
+                                   const void *subkeys, const void *bank_init, void *bank, void *out,
+                                   const sdm_layer_saved *saved, void *workspace, size_t workspace_bytes,
+                                   sdm_stream_t stream);
+sdm_status sdm_layer_backward_workspace_size(const sdm_shape *shape, int64_t dim, size_t *bytes);
+sdm_status sdm_layer_backward(const sdm_shape *shape, int64_t dim, const void *x, const void *w_qw,
+                              const void *w_qr, const void *w_v, const void *w_g, const void *w_o,
+                              const void *subkeys, void *bank, const void *dout, const sdm_layer_saved *saved,
+                              const sdm_layer_grads *grads, void *workspace, size_t workspace_bytes,
+                              sdm_stream_t stream);
 
 /*
  * One decode step (shape->T must be 1; chunk_size is ignored) for all B*H streams.
@@ -334,9 +388,10 @@ enum {
   SDM_KERNEL_BWD_REDUCE = 9,  /* backward: column sums, softmax backward, dq            */
   SDM_KERNEL_BWD_SUBKEY = 10, /* backward: sub-key gradient tiles and their sum         */
   SDM_KERNEL_LAYER_GATES = 11, /* layer: gate projection + sigmoid                      */
-  SDM_KERNEL_LAYER_GEMM = 12,  /* layer: the cuBLASLt projections (library kernels, not  */
+  SDM_KERNEL_LAYER_GEMM = 12,  /* layer: the cuBLASLt products (library kernels, not     */
                                /* counted by sdm_launch_count)                            */
-  SDM_NUM_KERNEL_KINDS = 13
+  SDM_KERNEL_LAYER_GRAD = 13,  /* layer backward: gradient concatenation, batch sum       */
+  SDM_NUM_KERNEL_KINDS = 14
 };
 typedef struct {
   int64_t launches[SDM_NUM_KERNEL_KINDS];

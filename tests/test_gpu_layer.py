@@ -138,3 +138,108 @@ def test_readme_call_full_size():
     r = compare_stream(cfg, d, {"y": gpu["y"], "bank": gpu["bank"].cpu(), **sel}, 1, 0)
     assert r["rows"] == cfg.T
     print(f"README call: stream (1, 0) compared over {r['rows']} tokens, {r['near_ties']} near-tie picks")
+
+
+# ---------------------------------------------------------------- training through the layer
+
+GRAD_RTOL = {"f32": 1e-4, "bf16": 3e-2}
+LAYER_GRADS = ("x", "w_qw", "w_qr", "w_v", "w_g", "w_o", "subkeys", "bank", "bank_init")
+
+
+def run_layer_train(cfg, L, dim, dout, snapshot_dtype=torch.float32):
+    import gated_delta_rule_factor_gb300 as sdm
+    g = to_device(L)
+    B = g["x"].shape[0]
+    bank = torch.empty((B, cfg.H, cfg.N, cfg.d_v), dtype=g["bank_init"].dtype, device="cuda")
+    out, saved = sdm.sdm_layer_forward_train(g["x"], g["w_qw"], g["w_qr"], g["w_v"], g["w_g"], g["w_o"],
+                                             g["subkeys"], bank, cfg.chunk_size, cfg.W, cfg.R,
+                                             factor_dims=cfg.factor_dims, bank_init=g["bank_init"],
+                                             snapshot_dtype=snapshot_dtype)
+    torch.cuda.synchronize()
+    bank_after = bank.clone()
+    grads = sdm.sdm_layer_backward(g["x"], g["w_qw"], g["w_qr"], g["w_v"], g["w_g"], g["w_o"], g["subkeys"], bank,
+                                   dout.cuda(), saved, cfg.chunk_size, cfg.W, cfg.R, factor_dims=cfg.factor_dims)
+    torch.cuda.synchronize()
+    assert sdm.last_device_error(grads["workspace"]) == 0
+    res = {"out": out.cpu(), "bank_after": bank_after, "bank_restored": bank,
+           "saved": {k: v.cpu() for k, v in saved.items() if isinstance(v, torch.Tensor) and k != "snapshot"}}
+    res.update({k: grads[k].cpu() for k in LAYER_GRADS})
+    return res
+
+
+def oracle_layer_backward(cfg, L, dout, gpu):
+    """The oracle's layer gradients on the GPU's intermediates, following its near-tie picks."""
+    from oracle import sdm_layer
+    sv = gpu["saved"]
+    K = {h: _f64(L["subkeys"][h]) for h in range(cfg.H)}
+    near = []
+
+    def pick_for(b, h):
+        q = (_f64(sv["q_w"][b, :, h]), _f64(sv["q_r"][b, :, h]))
+        gi = (sv["idx_w"][b, :, h].numpy(), sv["idx_r"][b, :, h].numpy())
+        gw = (sv["wt_w"][b, :, h].numpy(), sv["wt_r"][b, :, h].numpy())
+
+        def pick(t, which, idx, w):
+            from sdm_testlib import check_selection
+            if check_selection(cfg, q[which][t], K[h], (cfg.W, cfg.R)[which], gi[which][t], gw[which][t], idx, w):
+                return None
+            near.append((b, h, t))
+            return np.asarray(gi[which][t], dtype=np.int64)
+        return pick
+
+    given = {k: sv[k] for k in ("q_w", "q_r", "k_val", "gates", "y")}
+    o = sdm_layer.layer_backward(L["x"], L["w_qw"], L["w_qr"], L["w_v"], L["w_g"], L["w_o"], L["subkeys"],
+                                 L["bank_init"], dout, factor_dims=cfg.factor_dims, W=cfg.W, R=cfg.R,
+                                 act_dtype=cfg.act_dtype, bank_dtype=cfg.bank_dtype, given=given, pick=pick_for)
+    return o, len(near)
+
+
+def compare_layer_grads(cfg, gpu, o):
+    rt = GRAD_RTOL["bf16" if "bf16" in (cfg.act_dtype, cfg.bank_dtype) else "f32"]
+    for k in LAYER_GRADS:
+        assert_close(gpu[k], o[k], rt, f"d_{k}")
+
+
+LAYER_TRAIN = {
+    "tiny_f32": (dict(), 96),
+    "small_bf16": (dict(act_dtype="bf16", factor_dims=(16, 16), d_sub=32, d_v=64, H=2, B=2, T=48, W=16, R=16), 128),
+    "bf16_bank": (dict(act_dtype="bf16", bank_dtype="bf16", d_v=128, W=64, R=64, T=40), 160),
+    "three_factors": (dict(factor_dims=(8, 8, 8), d_sub=16, W=16, R=12, T=60), 72),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LAYER_TRAIN))
+def test_layer_backward_matches_oracle(name):
+    kw, dim = LAYER_TRAIN[name]
+    cfg = CONFIGS["tiny"].replace(**kw)
+    L = sdm_inputs.make_layer_inputs(cfg, dim)
+    dout = sdm_inputs.make_grad_inputs(cfg.replace(d_v=dim, H=1), dbank=False)["dy"].reshape(cfg.B, cfg.T, dim)
+    gpu = run_layer_train(cfg, L, dim, dout)
+    assert torch.equal(gpu["bank_restored"], to_device(L)["bank_init"].unsqueeze(0).expand_as(gpu["bank_restored"]))
+    o, near = oracle_layer_backward(cfg, L, dout, gpu)
+    assert near <= 2, near
+    compare_layer_grads(cfg, gpu, o)
+
+
+def test_layer_training_is_bitwise_repeatable():
+    kw, dim = LAYER_TRAIN["small_bf16"]
+    cfg = CONFIGS["tiny"].replace(**kw)
+    L = sdm_inputs.make_layer_inputs(cfg, dim)
+    dout = sdm_inputs.make_grad_inputs(cfg.replace(d_v=dim, H=1), dbank=False)["dy"].reshape(cfg.B, cfg.T, dim)
+    a = run_layer_train(cfg, L, dim, dout)
+    b = run_layer_train(cfg, L, dim, dout)
+    for k in LAYER_GRADS + ("out",):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_readme_call_training_full_width():
+    """The README call's shapes (dim 2048, 2 heads of d_v 1024, 65536 slots per head,
+    W = R = 64, bf16) at T = 1024, forward and backward, every gradient against the oracle."""
+    cfg = CONFIGS["layer"].replace(T=1024)
+    dim = 2048
+    L = sdm_inputs.make_layer_inputs(cfg, dim)
+    dout = sdm_inputs.make_grad_inputs(cfg.replace(d_v=dim, H=1), dbank=False)["dy"].reshape(cfg.B, cfg.T, dim)
+    gpu = run_layer_train(cfg, L, dim, dout)
+    o, near = oracle_layer_backward(cfg, L, dout, gpu)
+    print(f"README call training: {near} near-tie picks followed")
+    compare_layer_grads(cfg, gpu, o)
