@@ -37,7 +37,8 @@ import sdm_inputs  # noqa: E402
 METRIC = "SDM write/read tokens/s per layer on 1 GB300; achieved HBM GB/s vs roofline"
 UNIT = "tokens/s"
 WORKLOADS = {"layer": "layer", "train_fwd": "train_fwd", "three_factor": "three_factor",
-             "decode": "decode", "tiny": "tiny", "train": "train_fwd", "readme_layer": "layer"}
+             "decode": "decode", "tiny": "tiny", "train": "train_fwd", "readme_layer": "layer",
+             "layer_train": "train_fwd"}
 README_DIM = 2048          # the README usage example's model width (dim = num_heads * d_v)
 KERNEL_SOURCES = ("sdm_write_read.cu", "sdm_write_read_f32_f32.cu", "sdm_write_read_f32_bf16.cu",
                   "sdm_write_read_bf16_f32.cu", "sdm_write_read_bf16_bf16.cu", "sdm_wr_kernel.cuh",
@@ -324,6 +325,8 @@ def main():
         return bench_train(args, cfg, sdm, dev, rank, world, barrier, pg)
     if args.workload == "readme_layer":
         return bench_readme_layer(args, cfg, sdm, dev, rank, world, barrier, pg)
+    if args.workload == "layer_train":
+        return bench_layer_train(args, cfg, sdm, dev, rank, world, barrier, pg)
 
     d = sdm_inputs.make_inputs(cfg, seed=rank_seed(cfg, rank))
     g = {k: v.to(dev) for k, v in d.items()}
@@ -638,6 +641,99 @@ def bench_readme_layer(args, cfg, sdm, dev, rank, world, barrier, pg):
                      "algorithmic_bytes_per_launch": alg, "launch_ms": avg * 1e3},
         "projections": {"flop_per_step": gemm_flop, "ms_per_step": gt / args.steps,
                         "tflops": gemm_flop / (gt / args.steps / 1e3) / 1e12 if gt else None},
+        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items() if v[0]},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": None,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_layer_train(args, cfg, sdm, dev, rank, world, barrier, pg):
+    """One SDM layer forward + backward at 32K tokens per step (the pages' layer benchmark
+    shape: dim 2048, 2 heads, 65536 slots per head, W = R = 64, bf16, B=8 T=4096): the
+    training forward (projections, gates, the op with a bf16 snapshot, output projection)
+    and the layer backward (the products, the op's backward, the gradient concatenation,
+    the learned table's batch sum), dL/dout drawn once, dL/d(final bank) = 0."""
+    L = sdm_inputs.make_layer_inputs(cfg, README_DIM, seed=rank_seed(cfg, rank))
+    g = {k: v.to(dev) for k, v in L.items()}
+    B, T, H = cfg.B, cfg.T, cfg.H
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(rank_seed(cfg, rank) + 77)
+    dout = torch.randn(B, T, README_DIM, generator=gen).to(g["x"].dtype).to(dev)
+    bank = torch.empty((B, H, cfg.N, cfg.d_v), dtype=g["bank_init"].dtype, device=dev)
+    dbank = torch.zeros((B, H, cfg.N, cfg.d_v), dtype=torch.float32, device=dev)
+    shape = sdm.make_shape(B=B, T=T, H=H, factor_dims=cfg.factor_dims, d_sub=cfg.d_sub, d_v=cfg.d_v,
+                           W=cfg.W, R=cfg.R, chunk_size=cfg.chunk_size,
+                           act_dtype=0 if cfg.act_dtype == "f32" else 1,
+                           bank_dtype=0 if cfg.bank_dtype == "f32" else 1)
+    ws = torch.empty(sdm.layer_workspace_size(shape, README_DIM), dtype=torch.uint8, device=dev)
+    bws = torch.empty(sdm.layer_backward_workspace_size(shape, README_DIM), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    snap_dt = torch.bfloat16 if cfg.bank_dtype == "bf16" else torch.float32
+    state = {"saved": None, "grads": None}
+    out = torch.empty_like(g["x"])
+
+    def step():
+        _, state["saved"] = sdm.sdm_layer_forward_train(
+            g["x"], g["w_qw"], g["w_qr"], g["w_v"], g["w_g"], g["w_o"], g["subkeys"], bank, cfg.chunk_size, cfg.W,
+            cfg.R, factor_dims=cfg.factor_dims, bank_init=g["bank_init"], snapshot_dtype=snap_dt, out=out,
+            saved=state["saved"], workspace=ws, stream=stream)
+        dbank.zero_()
+        grads = sdm.sdm_layer_backward(g["x"], g["w_qw"], g["w_qr"], g["w_v"], g["w_g"], g["w_o"], g["subkeys"],
+                                       bank, dout, state["saved"], cfg.chunk_size, cfg.W, cfg.R,
+                                       factor_dims=cfg.factor_dims, dbank=dbank, grads=state["grads"],
+                                       workspace=bws, stream=stream)
+        grads.pop("workspace", None)
+        grads.pop("bank", None)
+        state["grads"] = grads
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    assert sdm.last_device_error(ws) == 0 and sdm.last_device_error(bws) == 0
+    launches0 = sdm.launch_count()
+    sdm.profile_begin()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+    kt = sdm.profile_end()
+    launches = sdm.launch_count() - launches0
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
+    value = whole_job_rate(B * T * args.steps, world, ms)
+    sb = 4 if cfg.bank_dtype == "f32" else 2
+    se = 2 if snap_dt == torch.bfloat16 else 4
+    rows = B * T * H
+    sweep_bytes = rows * cfg.d_v * (cfg.R * sb + 2 * 4 * (cfg.W + cfg.R) + cfg.W * se + cfg.W * sb)
+    n, t = kt["bwd_sweep"]
+    avg = t / max(n, 1) / 1e3
+    peak, peak_kind = peaks()
+    dq, dv = H * cfg.F * cfg.d_sub, H * cfg.d_v
+    gemm_flop = 2 * B * T * README_DIM * (2 * dq + dv) * 3 + 2 * B * T * README_DIM * dv * 3
+    gn, gt = kt["layer_gemm"]
+    if rank != 0:
+        return 0
+    line = {
+        "metric": "SDM layer forward + backward tokens/s at 32K tokens per step on 1 GB300", "value": value,
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg) + f", layer dim={README_DIM}, forward + backward",
+                   "snapshot_dtype": "bf16" if se == 2 else "f32",
+                   "step": "training forward (projections, gates, op with snapshot, output projection) + layer "
+                           "backward (products, op backward, gradient concatenation, batch sum); dL/d(final bank) "
+                           "zeroed by a torch fill"},
+        "roofline": {"bound": "hbm", "kernel": "bwd_sweep", "achieved": sweep_bytes / avg / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": sweep_bytes / avg / 1e9 / peak, "traffic": None,
+                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": sweep_bytes, "launch_ms": avg * 1e3},
+        "products": {"flop_per_step": gemm_flop, "ms_per_step": gt / args.steps,
+                     "tflops": gemm_flop / (gt / args.steps / 1e3) / 1e12 if gt else None},
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items() if v[0]},
         "gpu_launches": launches,
         "clocks": clk.summary(),

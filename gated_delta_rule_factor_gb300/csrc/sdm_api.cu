@@ -1014,7 +1014,7 @@ sdm_status layer_impl(const sdm_shape *sh, int64_t dim, const void *x, const voi
 
 struct LayerBwdLayout {
   int64_t op_ws, dY, d_qw, d_qr, d_kv, d_g, gcat, wcat, gemm, total;
-  int64_t dq, dv, ng, K;
+  int64_t dq, dv, ng, K, Kp;
 };
 
 LayerBwdLayout layer_bwd_layout(const sdm_shape *sh, const Derived &d, int64_t dim) {
@@ -1024,6 +1024,7 @@ LayerBwdLayout layer_bwd_layout(const sdm_shape *sh, const Derived &d, int64_t d
   w.dv = sh->d_v * sh->H;
   w.ng = 2 * sh->H;
   w.K = 2 * w.dq + w.dv + w.ng;
+  w.Kp = (w.K + 7) / 8 * 8;          // row stride of G and rows of W: 16-byte multiples (zero padding)
   int64_t o = 0;
   w.op_ws = o; o = a256(o + bwd_layout(sh, d).total);
   w.dY = o;    o = a256(o + BT * w.dv * ab);
@@ -1031,8 +1032,8 @@ LayerBwdLayout layer_bwd_layout(const sdm_shape *sh, const Derived &d, int64_t d
   w.d_qr = o;  o = a256(o + BT * w.dq * 4);
   w.d_kv = o;  o = a256(o + BT * w.dv * 4);
   w.d_g = o;   o = a256(o + BT * w.ng * 4);
-  w.gcat = o;  o = a256(o + BT * w.K * ab);
-  w.wcat = o;  o = a256(o + w.K * dim * ab);
+  w.gcat = o;  o = a256(o + BT * w.Kp * ab);
+  w.wcat = o;  o = a256(o + w.Kp * dim * ab);
   w.gemm = o;  o = a256(o + kLayerGemmWorkspace);
   w.total = o;
   return w;
@@ -1111,7 +1112,8 @@ sdm_status layer_backward_impl(const sdm_shape *sh, int64_t dim, const void *x, 
   if (BT > 0) {
     // G = [d_q_w | d_q_r | d_k_val | dz], W = [w_qw; w_qr; w_v; w_g]
     if ((st = run_kernel(SDM_KERNEL_LAYER_GRAD, cs, "layer_grad_cat", [&] {
-           return launch_layer_grad_cat(d_qw, d_qr, d_kv, d_g, sv->gates, gcat, BT, L.dq, L.dv, L.ng, adt, sms, cs);
+           return launch_layer_grad_cat(d_qw, d_qr, d_kv, d_g, sv->gates, gcat, BT, L.dq, L.dv, L.ng, L.Kp, adt, sms,
+                                        cs);
          })) != SDM_OK)
       return st;
     const void *wsrc[] = {w_qw, w_qr, w_v, w_g};
@@ -1123,9 +1125,14 @@ sdm_status layer_backward_impl(const sdm_shape *sh, int64_t dim, const void *x, 
       if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemcpyAsync: %s", cudaGetErrorString(ce));
       roff += wrows[i];
     }
+    if (L.Kp > L.K) {                                 // the padding rows of W are zero
+      const cudaError_t ce = cudaMemsetAsync(static_cast<unsigned char *>(wcat) + L.K * dim * ab, 0,
+                                             (size_t)((L.Kp - L.K) * dim * ab), cs);
+      if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
+    }
     // dx = G W
     if ((st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer dx", [&] {
-           return lt_gemm(false, false, dim, BT, L.K, wcat, dim, gcat, L.K, gr->dx, dim, adt, adt, false, gws, gwb,
+           return lt_gemm(false, false, dim, BT, L.Kp, wcat, dim, gcat, L.Kp, gr->dx, dim, adt, adt, false, gws, gwb,
                           cs);
          })) != SDM_OK)
       return st;
@@ -1135,7 +1142,7 @@ sdm_status layer_backward_impl(const sdm_shape *sh, int64_t dim, const void *x, 
     for (int i = 0; i < 4; ++i) {
       const void *gi = static_cast<const unsigned char *>(gcat) + coff * ab;
       if ((st = run_library(SDM_KERNEL_LAYER_GEMM, cs, "layer dw", [&] {
-             return lt_gemm(false, true, dim, wrows[i], BT, x, dim, gi, L.K, dws[i], dim, adt, SDM_F32, false, gws,
+             return lt_gemm(false, true, dim, wrows[i], BT, x, dim, gi, L.Kp, dws[i], dim, adt, SDM_F32, false, gws,
                             gwb, cs);
            })) != SDM_OK)
         return st;

@@ -246,7 +246,7 @@ const char *lt_gemm(bool ta, bool tb, int64_t m, int64_t n, int64_t k, const voi
                     cudaStream_t st);
 cudaError_t launch_layer_grad_cat(const float *d_qw, const float *d_qr, const float *d_kv, const float *d_g,
                                   const float *gates, void *gcat, int64_t rows, int64_t dq, int64_t dv, int64_t ng,
-                                  int act_dtype, int sm_count, cudaStream_t st);
+                                  int64_t K, int act_dtype, int sm_count, cudaStream_t st);
 cudaError_t launch_batch_sum(const float *in, float *out, int64_t B, int64_t n, int sm_count, cudaStream_t st);
 constexpr int64_t kLayerGemmWorkspace = (int64_t)32 << 20;   // cuBLASLt's share of a layer workspace
 

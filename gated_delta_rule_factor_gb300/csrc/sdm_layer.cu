@@ -6,9 +6,9 @@
 //
 // cuBLASLt is loaded with dlopen when a layer call first needs it, so the op's own entry
 // points never depend on it; a missing library makes the layer call return
-// SDM_ERR_CUDA.  Its GEMMs run with the caller's workspace (no allocation) and with
-// split-K reductions excluded, so that each product is computed the same way on every
-// call (bitwise repeatable).
+// SDM_ERR_CUDA.  Its GEMMs run with the caller's workspace (no allocation); split-K is
+// allowed only with the partial products reduced in the workspace by a separate step, so
+// that each product is computed the same way on every call (bitwise repeatable).
 #include <dlfcn.h>
 
 #include <mutex>
@@ -47,27 +47,26 @@ __global__ void __launch_bounds__(kThreads) layer_gates_kernel(const ACT *x, con
 }
 
 // The layer backward's concatenated input gradient, one token row r at a time:
-//   gcat[r] = [d_q_w[r] | d_q_r[r] | d_k_val[r] | dz[r]]  (activation type)
+//   gcat[r] = [d_q_w[r] | d_q_r[r] | d_k_val[r] | dz[r] | 0 ...]  (activation type, row
+//   stride K: the zero padding keeps the rows 16-byte aligned for the products)
 // with dz[r][j] = d_gates[r][j] * g (1 - g), g = gates[r][j] (the sigmoid's derivative).
 template <typename ACT>
 __global__ void __launch_bounds__(kThreads) layer_grad_cat_kernel(const float *d_qw, const float *d_qr,
                                                                   const float *d_kv, const float *d_g,
                                                                   const float *gates, ACT *gcat, int64_t rows,
-                                                                  int64_t dq, int64_t dv, int64_t ng) {
-  const int64_t K = 2 * dq + dv + ng;
-  const int64_t total = rows * K;
-  for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < total; e += (int64_t)gridDim.x * kThreads) {
-    const int64_t r = e / K, c = e - r * K;
-    float v;
-    if (c < dq) v = d_qw[r * dq + c];
-    else if (c < 2 * dq) v = d_qr[r * dq + (c - dq)];
-    else if (c < 2 * dq + dv) v = d_kv[r * dv + (c - 2 * dq)];
-    else {
-      const int64_t j = c - 2 * dq - dv;
+                                                                  int64_t dq, int64_t dv, int64_t ng, int64_t K) {
+  const int64_t K0 = 2 * dq + dv + ng;               // K >= K0: the row stride, zero-padded
+  // one CTA per token row at a time: the row's four pieces, each with contiguous loads
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    ACT *out = gcat + r * K;
+    for (int64_t c = threadIdx.x; c < dq; c += kThreads) out[c] = from_f32<ACT>(d_qw[r * dq + c]);
+    for (int64_t c = threadIdx.x; c < dq; c += kThreads) out[dq + c] = from_f32<ACT>(d_qr[r * dq + c]);
+    for (int64_t c = threadIdx.x; c < dv; c += kThreads) out[2 * dq + c] = from_f32<ACT>(d_kv[r * dv + c]);
+    for (int64_t j = threadIdx.x; j < ng; j += kThreads) {
       const float g = gates[r * ng + j];
-      v = __fmul_rn(d_g[r * ng + j], __fmul_rn(g, __fsub_rn(1.0f, g)));
+      out[2 * dq + dv + j] = from_f32<ACT>(__fmul_rn(d_g[r * ng + j], __fmul_rn(g, __fsub_rn(1.0f, g))));
     }
-    gcat[e] = from_f32<ACT>(v);
+    for (int64_t c = K0 + threadIdx.x; c < K; c += kThreads) out[c] = from_f32<ACT>(0.0f);
   }
 }
 
@@ -147,17 +146,16 @@ cublasLtHandle_t lt_handle(const char **why) {
 
 cudaError_t launch_layer_grad_cat(const float *d_qw, const float *d_qr, const float *d_kv, const float *d_g,
                                   const float *gates, void *gcat, int64_t rows, int64_t dq, int64_t dv, int64_t ng,
-                                  int act_dtype, int sm_count, cudaStream_t st) {
-  const int64_t total = rows * (2 * dq + dv + ng);
-  if (total == 0) return cudaSuccess;
-  int64_t blocks = (total + kThreads - 1) / kThreads;
-  if (blocks > (int64_t)sm_count * 32) blocks = (int64_t)sm_count * 32;
+                                  int64_t K, int act_dtype, int sm_count, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  int64_t blocks = rows;
+  if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
   if (act_dtype == SDM_BF16)
     layer_grad_cat_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, st>>>(
-        d_qw, d_qr, d_kv, d_g, gates, static_cast<__nv_bfloat16 *>(gcat), rows, dq, dv, ng);
+        d_qw, d_qr, d_kv, d_g, gates, static_cast<__nv_bfloat16 *>(gcat), rows, dq, dv, ng, K);
   else
     layer_grad_cat_kernel<float><<<(unsigned)blocks, kThreads, 0, st>>>(d_qw, d_qr, d_kv, d_g, gates,
-                                                                        static_cast<float *>(gcat), rows, dq, dv, ng);
+                                                                        static_cast<float *>(gcat), rows, dq, dv, ng, K);
   return cudaGetLastError();
 }
 
@@ -186,7 +184,10 @@ const char *lt_gemm(bool ta, bool tb, int64_t m, int64_t n, int64_t k, const voi
   cublasLtMatmulPreference_t pref = nullptr;
   const char *err = nullptr;
   const cublasOperation_t opa = ta ? CUBLAS_OP_T : CUBLAS_OP_N, opb = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
-  const uint32_t no_split_k = CUBLASLT_REDUCTION_SCHEME_NONE;
+  // split-K only through a workspace and a separate reduction step (a fixed order); not
+  // the in-place scheme
+  const uint32_t no_split_k =
+      CUBLASLT_REDUCTION_SCHEME_NONE | CUBLASLT_REDUCTION_SCHEME_COMPUTE_TYPE | CUBLASLT_REDUCTION_SCHEME_OUTPUT_TYPE;
   cublasLtMatmulHeuristicResult_t res{};
   int found = 0;
   const float one = 1.0f, beta = accumulate ? 1.0f : 0.0f;
