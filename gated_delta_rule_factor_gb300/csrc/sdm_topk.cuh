@@ -100,6 +100,100 @@ __device__ __forceinline__ void factor_topk(const float *scores, const KeyGeomet
   }
 }
 
+// factor_topk for a factor of 129 to 256 sub-keys and kf <= 64 (the sequence path's row
+// selection, one warp per row with its own scratch): the kf-th largest key is found first
+// and only the keys at or above it are sorted, which gives the same kf keys in the same
+// order.  The score bits of the kf-th largest key are found by a radix select, 8 bits at
+// a time, over exact integer histograms in the row's scratch (the survivor buffer, free
+// until the candidate phase); the keys whose score bits reach it (every key of the top kf,
+// plus any key tied with the kf-th on score) are then sorted as before.
+__device__ __forceinline__ void factor_topk_radix(const float *scores, const KeyGeometry &g, int qsel, int f,
+                                                  RowScratch &sc) {
+  constexpr int KPL = 8;                              // keys per lane (n_f <= 256)
+  const int lane = threadIdx.x & 31;
+  const int nf = g.nf[f], kf = g.kf[qsel][f];
+  const float *s = scores + g.off[f];
+  uint32_t hi[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int a = lane + 32 * i;
+    hi[i] = a < nf ? ordered_bits(s[a]) : 0u;         // 0: below every real key's bits
+  }
+  int *hist = reinterpret_cast<int *>(sc.surv);       // 256 counters
+  uint32_t prefix = 0, pmask = 0;
+  int need = kf;                                      // keys still to take at the prefix
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < KPL; ++i)
+      if (lane + 32 * i < nf && (hi[i] & pmask) == prefix) atomicAdd(&hist[(hi[i] >> shift) & 255u], 1);
+    __syncwarp();
+    // bins from the top digit down: lane l holds digits 255 - 8l - j, j = 0..7
+    int c[8], run = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c[j] = hist[255 - 8 * lane - j];
+      run += c[j];
+    }
+    int before = run;                                 // inclusive scan of the lanes' totals
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, before, o);
+      if (lane >= o) before += v;
+    }
+    before -= run;                                    // keys in higher digits of earlier lanes
+    int digit = -1, above = 0, acc = before;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (digit < 0 && acc + c[j] >= need) {
+        digit = 255 - 8 * lane - j;
+        above = acc;
+      }
+      acc += c[j];
+    }
+    const unsigned has = __ballot_sync(0xffffffffu, digit >= 0);
+    const int src = __ffs(has) - 1;                   // the lane holding the first digit that reaches need
+    digit = __shfl_sync(0xffffffffu, digit, src);
+    above = __shfl_sync(0xffffffffu, above, src);
+    prefix |= (uint32_t)digit << shift;
+    pmask |= 255u << shift;
+    need -= above;
+    __syncwarp();
+  }
+  // the survivors: every key whose score bits are at least the kf-th largest's
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int a = lane + 32 * i;
+    const bool keep = a < nf && hi[i] >= prefix;
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+    if (keep) sc.surv[pos] = ((uint64_t)hi[i] << 32) | (uint32_t)a;
+    cnt += __popc(m);
+  }
+  __syncwarp();
+  uint64_t best[2];
+  top_of_chunks<2>(cnt, [&](int c0, uint64_t(&key)[2]) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = c0 + lane * 2 + e;
+      key[e] = i < cnt ? sc.surv[i] : 0ull;
+    }
+  }, best);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int pos = lane * 2 + e;
+    if (pos < kf) {
+      sc.fs[f * SDM_MAX_K + pos] = from_ordered_bits((uint32_t)(best[e] >> 32));
+      sc.fi[f * SDM_MAX_K + pos] = (int32_t)(uint32_t)(best[e] & 0xffffffffu);
+    }
+  }
+  __syncwarp();
+}
+
 // Slot score of a position tuple (byte f = p_f): the float32 sum of its factor scores,
 // left to right.
 __device__ __forceinline__ float tuple_score(uint32_t t, const KeyGeometry &g, const RowScratch &sc) {
@@ -239,7 +333,11 @@ template <int EF, int EC>
 __device__ __forceinline__ void row_topk(const float *scores, const KeyGeometry &g, int qsel,
                                          const uint32_t *cand, int ncand, const uint32_t *boxes, int nbox,
                                          RowScratch &sc, int32_t *idx_out, float *wt_out) {
-  for (int f = 0; f < g.F; ++f) factor_topk<EF>(scores, g, qsel, f, sc);
+  for (int f = 0; f < g.F; ++f) {
+    // (for at most 128 keys the chunk sorts are already short: the radix passes cost more)
+    if (EF == 2 && g.nf[f] > 128 && g.nf[f] <= 256) factor_topk_radix(scores, g, qsel, f, sc);
+    else factor_topk<EF>(scores, g, qsel, f, sc);
+  }
   __syncwarp();
   uint64_t ck[EC];
   candidate_topk_pruned<EC>(cand, ncand, boxes, nbox, g, sc, ck);
