@@ -100,28 +100,14 @@ __device__ __forceinline__ void factor_topk(const float *scores, const KeyGeomet
   }
 }
 
-// factor_topk for a factor of 129 to 256 sub-keys and kf <= 64 (the sequence path's row
-// selection, one warp per row with its own scratch): the kf-th largest key is found first
-// and only the keys at or above it are sorted, which gives the same kf keys in the same
-// order.  The score bits of the kf-th largest key are found by a radix select, 8 bits at
-// a time, over exact integer histograms in the row's scratch (the survivor buffer, free
-// until the candidate phase); the keys whose score bits reach it (every key of the top kf,
-// plus any key tied with the kf-th on score) are then sorted as before.
-__device__ __forceinline__ void factor_topk_radix(const float *scores, const KeyGeometry &g, int qsel, int f,
-                                                  RowScratch &sc) {
-  constexpr int KPL = 8;                              // keys per lane (n_f <= 256)
+// The need-th largest of the warp's values (v[i] of lane l is value l + 32 i; those with ok
+// false do not count), 1 <= need <= their number: a radix select over 8-bit digits, from
+// the top, with exact integer counters in hist (256 ints of the warp's scratch).
+template <int KPL>
+__device__ __forceinline__ uint32_t warp_kth_largest(const uint32_t (&v)[KPL], const bool (&ok)[KPL], int need,
+                                                     int *hist) {
   const int lane = threadIdx.x & 31;
-  const int nf = g.nf[f], kf = g.kf[qsel][f];
-  const float *s = scores + g.off[f];
-  uint32_t hi[KPL];
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const int a = lane + 32 * i;
-    hi[i] = a < nf ? ordered_bits(s[a]) : 0u;         // 0: below every real key's bits
-  }
-  int *hist = reinterpret_cast<int *>(sc.surv);       // 256 counters
   uint32_t prefix = 0, pmask = 0;
-  int need = kf;                                      // keys still to take at the prefix
 #pragma unroll 1
   for (int shift = 24; shift >= 0; shift -= 8) {
 #pragma unroll
@@ -129,7 +115,7 @@ __device__ __forceinline__ void factor_topk_radix(const float *scores, const Key
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < KPL; ++i)
-      if (lane + 32 * i < nf && (hi[i] & pmask) == prefix) atomicAdd(&hist[(hi[i] >> shift) & 255u], 1);
+      if (ok[i] && (v[i] & pmask) == prefix) atomicAdd(&hist[(v[i] >> shift) & 255u], 1);
     __syncwarp();
     // bins from the top digit down: lane l holds digits 255 - 8l - j, j = 0..7
     int c[8], run = 0;
@@ -138,13 +124,13 @@ __device__ __forceinline__ void factor_topk_radix(const float *scores, const Key
       c[j] = hist[255 - 8 * lane - j];
       run += c[j];
     }
-    int before = run;                                 // inclusive scan of the lanes' totals
+    int before = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, before, o);
-      if (lane >= o) before += v;
+      const int x = __shfl_up_sync(0xffffffffu, before, o);
+      if (lane >= o) before += x;
     }
-    before -= run;                                    // keys in higher digits of earlier lanes
+    before -= run;                                    // values in higher digits (earlier lanes)
     int digit = -1, above = 0, acc = before;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -154,8 +140,7 @@ __device__ __forceinline__ void factor_topk_radix(const float *scores, const Key
       }
       acc += c[j];
     }
-    const unsigned has = __ballot_sync(0xffffffffu, digit >= 0);
-    const int src = __ffs(has) - 1;                   // the lane holding the first digit that reaches need
+    const int src = __ffs(__ballot_sync(0xffffffffu, digit >= 0)) - 1;   // the first digit reaching need
     digit = __shfl_sync(0xffffffffu, digit, src);
     above = __shfl_sync(0xffffffffu, above, src);
     prefix |= (uint32_t)digit << shift;
@@ -163,15 +148,36 @@ __device__ __forceinline__ void factor_topk_radix(const float *scores, const Key
     need -= above;
     __syncwarp();
   }
-  // the survivors: every key whose score bits are at least the kf-th largest's
-  int cnt = 0;
+  return prefix;
+}
+
+// factor_topk for a factor of 129 to 256 sub-keys and kf <= 64 (the sequence path's row
+// selection, one warp per row with its own scratch): the score bits of the kf-th largest
+// key are found first (warp_kth_largest, its counters in the row's survivor buffer, free
+// until the candidate phase), and only the keys whose score bits reach them (every key of
+// the top kf, plus any key tied with the kf-th on score) are sorted as before: the same
+// kf keys in the same order.
+__device__ __forceinline__ void factor_topk_radix(const float *scores, const KeyGeometry &g, int qsel, int f,
+                                                  RowScratch &sc) {
+  constexpr int KPL = 8;                              // keys per lane (n_f <= 256)
+  const int lane = threadIdx.x & 31;
+  const int nf = g.nf[f], kf = g.kf[qsel][f];
+  const float *s = scores + g.off[f];
+  uint32_t hi[KPL];
+  bool ok[KPL];
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const int a = lane + 32 * i;
-    const bool keep = a < nf && hi[i] >= prefix;
+    ok[i] = a < nf;
+    hi[i] = ok[i] ? ordered_bits(s[a]) : 0u;
+  }
+  const uint32_t T = warp_kth_largest<KPL>(hi, ok, kf, reinterpret_cast<int *>(sc.surv));
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const bool keep = ok[i] && hi[i] >= T;
     const unsigned m = __ballot_sync(0xffffffffu, keep);
-    const int pos = cnt + __popc(m & ((1u << lane) - 1u));
-    if (keep) sc.surv[pos] = ((uint64_t)hi[i] << 32) | (uint32_t)a;
+    if (keep) sc.surv[cnt + __popc(m & ((1u << lane) - 1u))] = ((uint64_t)hi[i] << 32) | (uint32_t)(lane + 32 * i);
     cnt += __popc(m);
   }
   __syncwarp();
@@ -272,6 +278,33 @@ __device__ __forceinline__ void candidate_topk_pruned(const uint32_t *cand, int 
   if (cnt > kSurvivorCap) {
     candidate_topk<EC>(cand, 0, ncand, g, sc, ck);
     return;
+  }
+  if (EC == 2 && cnt > 64) {
+    // more than one chunk: keep only the keys whose score bits reach the 64th largest's
+    // (the best 64 keys are among them), as factor_topk_radix does
+    constexpr int KPL = kSurvivorCap / 32;
+    uint64_t kv[KPL];
+    uint32_t hi[KPL];
+    bool ok[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int j = lane + 32 * i;
+      ok[i] = j < cnt;
+      kv[i] = ok[i] ? sc.surv[j] : 0ull;
+      hi[i] = (uint32_t)(kv[i] >> 32);
+    }
+    __syncwarp();
+    const uint32_t T = warp_kth_largest<KPL>(hi, ok, 64, reinterpret_cast<int *>(sc.surv));
+    int kept = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const bool keep = ok[i] && hi[i] >= T;
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      if (keep) sc.surv[kept + __popc(m & ((1u << lane) - 1u))] = kv[i];
+      kept += __popc(m);
+    }
+    __syncwarp();
+    cnt = kept;
   }
   top_of_chunks<EC>(cnt, [&](int b0, uint64_t(&kk)[EC]) {
 #pragma unroll
