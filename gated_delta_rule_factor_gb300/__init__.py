@@ -15,7 +15,7 @@ from .ops import (backward_workspace_size, decode_workspace_size, last_device_er
                   sdm_decode_step, sdm_layer_backward, sdm_layer_forward, sdm_layer_forward_train,
                   sdm_write_read,
                   sdm_write_read_backward, sdm_write_read_static, sdm_write_read_train,
-                  snapshot_bytes, test_force_simt_scorer, test_force_write_read_layout,
+                  snapshot_bytes, test_factor_scores, test_force_simt_scorer, test_force_write_read_layout,
                   test_stall_decode_copy, write_read_workspace_size)
 
 lib = _abi.load()
@@ -25,6 +25,6 @@ __all__ = [
     "launch_count", "layer_backward_workspace_size", "layer_workspace_size", "make_shape", "profile_begin", "profile_end", "sdm_decode_step", "sdm_layer_backward", "sdm_layer_forward",
     "sdm_layer_forward_train",
     "sdm_write_read", "sdm_write_read_backward", "sdm_write_read_static", "sdm_write_read_train", "snapshot_bytes",
-    "test_force_simt_scorer", "test_force_write_read_layout", "test_stall_decode_copy",
+    "test_factor_scores", "test_force_simt_scorer", "test_force_write_read_layout", "test_stall_decode_copy",
     "write_read_workspace_size", "lib",
 ]

@@ -28,7 +28,7 @@ EXPORTS = (
     "sdm_decode_step", "sdm_last_device_error", "sdm_status_string", "sdm_last_error_message",
     "sdm_abi_version", "sdm_launch_count", "sdm_profile_begin", "sdm_profile_end",
     "sdm_kernel_name", "sdm_test_stall_decode_copy",
-    "sdm_test_force_write_read_layout", "sdm_test_force_simt_scorer",
+    "sdm_test_force_write_read_layout", "sdm_test_force_simt_scorer", "sdm_test_factor_scores",
 )
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -132,11 +132,13 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.sdm_test_stall_decode_copy.argtypes = [ctypes.c_int]
     lib.sdm_test_force_write_read_layout.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.sdm_test_force_simt_scorer.argtypes = [ctypes.c_int]
+    lib.sdm_test_factor_scores.argtypes = [sp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     for name in ("sdm_write_read_workspace_size", "sdm_decode_workspace_size", "sdm_write_read",
                  "sdm_write_read_static", "sdm_decode_step", "sdm_last_device_error", "sdm_profile_begin", "sdm_profile_end",
                  "sdm_snapshot_bytes", "sdm_write_read_train", "sdm_write_read_backward_workspace_size",
                  "sdm_write_read_backward", "sdm_layer_workspace_size", "sdm_layer_forward",
-                 "sdm_layer_forward_train", "sdm_layer_backward_workspace_size", "sdm_layer_backward"):
+                 "sdm_layer_forward_train", "sdm_layer_backward_workspace_size", "sdm_layer_backward",
+                 "sdm_test_factor_scores"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.sdm_abi_version() != ABI_VERSION:
         raise ImportError(f"SDM library ABI {lib.sdm_abi_version()} != binding ABI {ABI_VERSION}")

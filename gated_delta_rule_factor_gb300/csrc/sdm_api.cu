@@ -384,6 +384,7 @@ int64_t a256(int64_t x) { return (x + 255) & ~int64_t(255); }
 struct WsLayout {
   int64_t idx_w, wt_w, idx_r, wt_r;  // selection outputs kept here when the caller passes NULL
   int64_t scores;                    // factor scores [2, B*T*H, sum n_f] float32
+  int64_t split;                     // bf16 parts of float32 queries and sub-keys (scorer)
   int64_t uniq, nuniq, uo, written, lrecs, crecs;
   int64_t total;
 };
@@ -400,6 +401,11 @@ WsLayout ws_layout(const sdm_shape *sh, const PlanLayout &lay) {
   int64_t ntot = 0;
   for (int f = 0; f < sh->F && f < SDM_MAX_FACTORS; ++f) ntot += sh->factor_dims[f];
   w.scores = o; o = a256(o + 2 * rows * ntot * 4);
+  KeyGeometry kg{};
+  kg.F = (int32_t)sh->F;
+  kg.d_sub = (int32_t)sh->d_sub;
+  kg.ntot = (int32_t)ntot;
+  w.split = o; o = a256(o + score_split_bytes(kg, sh->B * sh->T, sh->H, sh->act_dtype));
   w.uniq = o;  o = a256(o + stages * lay.L * 4);
   w.nuniq = o; o = a256(o + stages * 4);
   w.uo = o;    o = a256(o + stages * lay.L * 2);
@@ -459,15 +465,12 @@ sdm_status sm_count(int *out) {
   return SDM_OK;
 }
 
-// The tensor-core scorer takes bfloat16 inputs whose d_sub is a multiple of 64 and whose
-// factor widths are multiples of 16 (sdm_test_force_simt_scorer forces the CUDA-core one).
+// The tensor-core scorer takes factor widths that are multiples of 16, and bfloat16
+// inputs whose d_sub is a multiple of 64 or float32 inputs of any d_sub
+// (sdm_test_force_simt_scorer forces the CUDA-core one).
 bool use_tensor_cores(const Derived &d, const sdm_shape *sh) {
   if (g_test_simt_scorer.load()) return false;
-  int maxnf = 0;
-  for (int f = 0; f < d.g.F; ++f) maxnf = std::max(maxnf, d.g.nf[f]);
-  const int64_t n_tiles = (maxnf + 255) / 256;
-  if (2 * sh->H * d.g.F * n_tiles > 65535) return false;
-  return score_tc_supported(d.g, sh->act_dtype);
+  return score_tc_supported(d.g, sh->H, sh->act_dtype);
 }
 
 // Per-device side stream and fork / join events of write_read_impl, created on first use
@@ -624,13 +627,14 @@ sdm_status write_read_impl(const sdm_shape *sh, const void *q_w, const void *q_r
   sa.q[1] = q_r;
   sa.subkeys = subkeys;
   sa.scores = scores;
+  sa.split = ws + wl.split;
   sa.err = err;
   sa.BT = sh->B * sh->T;
   sa.H = (int32_t)sh->H;
   sa.g = d.g;
   const bool tc = use_tensor_cores(d, sh);
   if ((st = run_kernel(SDM_KERNEL_SCORE, cs, tc ? "score_tc" : "score_simt", [&] {
-         return tc ? launch_score_tc(sa, cs) : launch_score_simt(sa, sh->act_dtype, cs);
+         return tc ? launch_score_tc(sa, sh->act_dtype, cs) : launch_score_simt(sa, sh->act_dtype, cs);
        })) != SDM_OK)
     return st;
   SelectArgs se{};
@@ -1412,6 +1416,53 @@ sdm_status sdm_test_force_write_read_layout(int slice_bytes, int stage_tokens) {
     return fail(SDM_ERR_INVALID_ARG, "slice_bytes must be 0, 32, 128 or 256 and stage_tokens >= 0");
   g_test_slice_bytes.store(slice_bytes);
   g_test_stage_tokens.store(stage_tokens);
+  return ok();
+}
+
+sdm_status sdm_test_factor_scores(const sdm_shape *sh, const void *q_w, const void *q_r, const void *subkeys,
+                                  float *scores, void *workspace, size_t workspace_bytes, sdm_stream_t stream) {
+  Derived d;
+  sdm_status st = check_shape(sh, false, &d);
+  if (st != SDM_OK) return st;
+  const int64_t ab = elem_bytes(sh->act_dtype);
+  const int64_t rows = sh->B * sh->T * sh->H;
+  const int64_t qbytes = rows * sh->F * sh->d_sub * ab;
+  const Range r_qw{q_w, qbytes, "q_w"}, r_qr{q_r, qbytes, "q_r"};
+  const Range r_sk{subkeys, sh->H * d.ntot * sh->d_sub * ab, "subkeys"};
+  const Range r_s{scores, 2 * rows * d.ntot * 4, "scores"};
+  const Range r_ws{workspace, (int64_t)workspace_bytes, "workspace"};
+  if (rows == 0) return ok();
+  for (const Range &r : {r_qw, r_qr, r_sk, r_s}) {
+    if (!r.p) return fail(SDM_ERR_INVALID_ARG, "%s is NULL", r.name);
+    if (!aligned(r.p, 16)) return fail(SDM_ERR_INVALID_ARG, "%s is not 16-byte aligned", r.name);
+  }
+  if (!workspace || !aligned(workspace, 16) || (int64_t)workspace_bytes < write_read_ws_bytes(sh))
+    return fail(SDM_ERR_WORKSPACE, "workspace is NULL, misaligned or short");
+  for (const Range &i : {r_qw, r_qr, r_sk})
+    for (const Range &o : {r_s, r_ws})
+      if (overlap(o, i)) return fail(SDM_ERR_ALIAS, "%s overlaps %s", o.name, i.name);
+  if (overlap(r_s, r_ws)) return fail(SDM_ERR_ALIAS, "scores overlaps workspace");
+  const WsLayout wl = ws_layout(sh, PlanLayout{});   // the split region does not depend on the plan
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  int32_t *err = reinterpret_cast<int32_t *>(ws);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t ce = cudaMemsetAsync(err, 0, sizeof(int32_t), cs);
+  if (ce != cudaSuccess) return fail(SDM_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
+  ScoreArgs sa{};
+  sa.q[0] = q_w;
+  sa.q[1] = q_r;
+  sa.subkeys = subkeys;
+  sa.scores = scores;
+  sa.split = ws + wl.split;
+  sa.err = err;
+  sa.BT = sh->B * sh->T;
+  sa.H = (int32_t)sh->H;
+  sa.g = d.g;
+  const bool tc = use_tensor_cores(d, sh);
+  if ((st = run_kernel(SDM_KERNEL_SCORE, cs, tc ? "score_tc" : "score_simt", [&] {
+         return tc ? launch_score_tc(sa, sh->act_dtype, cs) : launch_score_simt(sa, sh->act_dtype, cs);
+       })) != SDM_OK)
+    return st;
   return ok();
 }
 

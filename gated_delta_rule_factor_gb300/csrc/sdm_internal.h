@@ -54,6 +54,7 @@ struct ScoreArgs {
   const void *q[2];      // q_w, q_r [BT, H, F*d_sub]
   const void *subkeys;   // [H, ntot, d_sub]
   float *scores;         // [2, BT*H, ntot]
+  void *split;           // tensor-core scoring of float32 inputs: score_split_bytes of workspace
   int32_t *err;
   int64_t BT;            // B*T tokens
   int32_t H;
@@ -257,8 +258,11 @@ cudaError_t raise_smem_limit(const void *kernel, int64_t smem);
 
 // Launchers, defined next to their kernels.  Each returns the launch error.
 cudaError_t launch_score_simt(const ScoreArgs &a, int act_dtype, cudaStream_t st);
-cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t st);   // bf16, tensor cores
-bool score_tc_supported(const KeyGeometry &g, int act_dtype);
+// Tensor-core scoring: bf16 inputs directly, float32 inputs through an exact three-way
+// bf16 split kept in ScoreArgs::split (score_split_bytes bytes, 16-byte aligned).
+cudaError_t launch_score_tc(const ScoreArgs &a, int act_dtype, cudaStream_t st);
+bool score_tc_supported(const KeyGeometry &g, int64_t H, int act_dtype);
+int64_t score_split_bytes(const KeyGeometry &g, int64_t BT, int64_t H, int act_dtype);
 cudaError_t launch_select(const SelectArgs &a, const CandidateList &cl, int EF, int EC,
                           int sm_count, cudaStream_t st);
 cudaError_t launch_bank_copy(const BankCopyArgs &a, int sm_count, cudaStream_t st);

@@ -526,8 +526,32 @@ def test_force_write_read_layout(slice_bytes: int = 0, stage_tokens: int = 0) ->
 
 
 def test_force_simt_scorer(on: bool) -> None:
-    """Test hook: score bfloat16 queries on the CUDA-core scorer (sdm.h)."""
+    """Test hook: score on the CUDA-core scorer instead of the tensor cores (sdm.h)."""
     _abi.check(_abi.load().sdm_test_force_simt_scorer(1 if on else 0), "sdm_test_force_simt_scorer")
+
+
+def test_factor_scores(q_w: torch.Tensor, q_r: torch.Tensor, subkeys: torch.Tensor, *,
+                       factor_dims: Sequence[int], workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Test hook: the factor scores of step 1, [2, B*T*H, sum(factor_dims)] float32 (q_w rows,
+    then q_r rows), from the scorer sdm_write_read would use (sdm.h)."""
+    dev = q_w.device
+    for name, t in (("q_w", q_w), ("q_r", q_r), ("subkeys", subkeys)):
+        _require_cuda_contig(name, t, dev)
+    B, T, H, D = q_w.shape
+    F = len(factor_dims)
+    if F == 0 or D % F != 0:
+        raise ValueError(f"query width {D} is not a multiple of F={F}")
+    act = _dtype_code(q_w, "q_w")
+    shape = make_shape(B=B, T=T, H=H, factor_dims=factor_dims, d_sub=D // F, d_v=8, W=1, R=1, chunk_size=64,
+                       act_dtype=act, bank_dtype=act)
+    scores = torch.empty((2, B * T * H, sum(factor_dims)), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(write_read_workspace_size(shape), dtype=torch.uint8, device=dev)
+    st = _abi.load().sdm_test_factor_scores(ctypes.byref(shape), _ptr(q_w), _ptr(q_r), _ptr(subkeys), _ptr(scores),
+                                            _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    _abi.check(st, "sdm_test_factor_scores")
+    return scores
 
 
 def profile_begin() -> None:

@@ -377,7 +377,7 @@ uint64_t sdm_launch_count(void);
  * summed milliseconds.  Up to 4096 launches are recorded per session. */
 enum {
   SDM_KERNEL_BANK_COPY = 0,
-  SDM_KERNEL_SCORE = 1,      /* factor scores (tensor cores for bf16, else CUDA cores) */
+  SDM_KERNEL_SCORE = 1,      /* factor scores (tensor cores, or CUDA cores)             */
   SDM_KERNEL_SELECT = 2,     /* exact product-key top-k and weights                   */
   SDM_KERNEL_PLAN_SORT = 3,
   SDM_KERNEL_PLAN_LINK = 4,
@@ -418,10 +418,24 @@ sdm_status sdm_test_stall_decode_copy(int on);
  *       128 or 256, i.e. 1, 4 or 8 compute warps of 32 bytes each); stage_tokens: an
  *       upper bound on the tokens staged together (>= 1).  SDM_ERR_INVALID_ARG for
  *       other values.  Applies to calls made after it.
- *   sdm_test_force_simt_scorer  on != 0: score bfloat16 queries on the CUDA-core scorer
- *       instead of the tensor cores. */
+ *   sdm_test_force_simt_scorer  on != 0: score on the CUDA-core scorer (compensated
+ *       float32 sums) instead of the tensor cores.  The tensor cores score bfloat16 inputs
+ *       directly and float32 inputs through an exact three-way bfloat16 split of every
+ *       value, of which the six part products above 2^-24 relative are kept; the scores of
+ *       the two scorers may differ in the last bits. */
 sdm_status sdm_test_force_write_read_layout(int slice_bytes, int stage_tokens);
 sdm_status sdm_test_force_simt_scorer(int on);
+
+/* Test hook of step 1 (the factor scores, product-key memory as cited at the top of this
+ * file); not for production use.  Scores the queries of `shape` with the scorer that
+ * sdm_write_read would use and writes scores [2][B*T*H][sum n_f] float32: the q_w rows,
+ * then the q_r rows, row (b*T + t)*H + h, factor f's scores at column offset
+ * sum_{g<f} n_g.  q_w, q_r, subkeys and scores are device pointers, 16-byte aligned, as in
+ * sdm_write_read; workspace as for sdm_write_read (sdm_write_read_workspace_size bytes).
+ * Refusals (INVALID_ARG, WORKSPACE, ALIAS) are decided on the host before any launch. */
+sdm_status sdm_test_factor_scores(const sdm_shape *shape, const void *q_w, const void *q_r,
+                                  const void *subkeys, float *scores, void *workspace,
+                                  size_t workspace_bytes, sdm_stream_t stream);
 
 #ifdef __cplusplus
 }
