@@ -44,6 +44,7 @@ namespace wr {
 
 constexpr int kRowBufs = 3;      // row / compute-record / token-data buffers
 constexpr int kLoaderRecs = 5;   // loader records: stages g-1 .. g+3 of loader iteration g
+constexpr int kBatch = 4;        // list entries whose copies one thread issues together
 
 // Value slice of a stage's tokens (the only per-CTA token data; weights and gates come
 // with the compute record).  cols: the CTA's bank columns (RB / bank element bytes).
@@ -195,11 +196,17 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
       const uint2 *ent = reinterpret_cast<const uint2 *>(rec + lay.off_ent);
       const uint32_t dst = smem_addr(rowbuf(g));
       if (sub >= valid_chunks) return;
-#pragma unroll 4
-      for (int e = grp; e < n_load; e += GRP) {
-        const uint2 v = ent[e];
-        if (v.x < lim16 && v.y < olim) cp_async16_rows(dst + (v.y ^ sub16), bank_slice + (size_t)v.x * 16);
-        else raise_error(a.err, SDM_DEVERR_PLAN);
+      // kBatch entries read first, then their copies issued back to back
+      for (int e0 = grp; e0 < n_load; e0 += kBatch * GRP) {
+        uint2 v[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) v[k] = e0 + k * GRP < n_load ? ent[e0 + k * GRP] : make_uint2(0u, 0u);
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (e0 + k * GRP >= n_load) break;
+          if (v[k].x < lim16 && v[k].y < olim) cp_async16_rows(dst + (v[k].y ^ sub16), bank_slice + (size_t)v[k].x * 16);
+          else raise_error(a.err, SDM_DEVERR_PLAN);
+        }
       }
     };
     // stage g's compute record (offsets, flags, weights, gates: one contiguous copy) and
@@ -232,12 +239,21 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
       const unsigned char *src = rowbuf(g);
       unsigned char *dst = reinterpret_cast<unsigned char *>(bank + c0) + sub * 16;
       if (sub >= valid_chunks) return;
-#pragma unroll 4
-      for (int e = grp; e < n_wb; e += GRP) {
-        const uint2 v = wb[e];
-        if (v.x < lim16 && v.y < olim)
-          *reinterpret_cast<uint4 *>(dst + (size_t)v.x * 16) = *reinterpret_cast<const uint4 *>(src + (v.y ^ sub16));
-        else raise_error(a.err, SDM_DEVERR_PLAN);
+      // kBatch entries, then their rows out of shared memory, then the stores
+      for (int e0 = grp; e0 < n_wb; e0 += kBatch * GRP) {
+        uint2 v[kBatch];
+        uint4 r[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) v[k] = e0 + k * GRP < n_wb ? wb[e0 + k * GRP] : make_uint2(lim16, olim);
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+          if (v[k].x < lim16 && v[k].y < olim) r[k] = *reinterpret_cast<const uint4 *>(src + (v[k].y ^ sub16));
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (e0 + k * GRP >= n_wb) break;
+          if (v[k].x < lim16 && v[k].y < olim) *reinterpret_cast<uint4 *>(dst + (size_t)v[k].x * 16) = r[k];
+          else raise_error(a.err, SDM_DEVERR_PLAN);
+        }
       }
     };
     // Waits for the compute warps to finish stage g (one thread waits, all loaders learn
@@ -379,9 +395,31 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
   auto hand_on = [&](int g, const Handoff &hf) {
     const unsigned char *rows = rowbuf(g);
     const uint2 *out = reinterpret_cast<const uint2 *>(lrecbuf(g) + lay.off_out);
-    for (int e = rg, k = 0; e < hf.n1 + hf.n2; e += 16, ++k) {
-      const uint32_t cv = k < 2 ? hf.e[k] : out[e].x;
-      copy_piece(cv, e < hf.n1 ? rowbuf(g + 1) : rowbuf(g + 2), rows);
+    const int n = hf.n1 + hf.n2;
+    for (int e = rg, k = 0; e < n && k < 2; e += 16, ++k)
+      copy_piece(hf.e[k], e < hf.n1 ? rowbuf(g + 1) : rowbuf(g + 2), rows);
+    // the rest kBatch entries at a time: offsets, then the pieces, then the stores
+    for (int e0 = rg + 32; e0 < n; e0 += kBatch * 16) {
+      uint32_t cv[kBatch];
+      uint4 r[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) cv[k] = e0 + 16 * k < n ? out[e0 + 16 * k].x : 0u;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const uint32_t os = (cv[k] >> 16) ^ wc;
+        if (e0 + 16 * k < n && os < (uint32_t)row_limit) r[k] = *reinterpret_cast<const uint4 *>(rows + os);
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int e = e0 + 16 * k;
+        if (e >= n) break;
+        const uint32_t od = (cv[k] & 0xffffu) ^ wc, os = (cv[k] >> 16) ^ wc;
+        if (od >= (uint32_t)row_limit || os >= (uint32_t)row_limit) {
+          raise_error(a.err, SDM_DEVERR_PLAN);
+          continue;
+        }
+        *reinterpret_cast<uint4 *>((e < hf.n1 ? rowbuf(g + 1) : rowbuf(g + 2)) + od) = r[k];
+      }
     }
   };
   for (int g = 0; g < S; ++g) {
