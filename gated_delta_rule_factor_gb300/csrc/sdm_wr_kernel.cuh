@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool is_loader = warp >= NCW;
 
+  // One compute warp per CTA: the loaders, otherwise idle while it runs the tokens, copy
+  // the rows each stage hands on (the compute warps do it themselves when there are more).
+  constexpr bool kLoaderHandOn = NCW == 1;
   const SmemLayout sl = smem_layout(lay, (int)sizeof(BANK), (int)sizeof(ACT));
   const int64_t vbytes = vals_bytes(G, COLS, (int)sizeof(ACT));
   auto rowbuf = [&](int g) -> unsigned char * { return smem + sl.rows + (int64_t)(g % kRowBufs) * L * RB; };
@@ -274,6 +277,81 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
       return *loader_go != 0;
     };
 
+    // Loader hand-on (kLoaderHandOn): stage g's rows that stages g+1 and g+2 take over,
+    // copied out of buffer g once the compute warps are done with it, kBatch list
+    // entries per thread at a time, each thread one 16-byte chunk of a row slice.
+    auto hand_on_rows = [&](int g) {
+      const unsigned char *rec = lrecbuf(g);
+      const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
+      if (!hdr_ok(hdr)) return;
+      const int n1 = hdr[2], n = hdr[2] + hdr[3];
+      const uint2 *out = reinterpret_cast<const uint2 *>(rec + lay.off_out);
+      const unsigned char *src = rowbuf(g);
+      if (sub >= valid_chunks) return;
+      for (int e0 = grp; e0 < n; e0 += kBatch * GRP) {
+        uint32_t cv[kBatch];
+        uint4 r[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) cv[k] = e0 + k * GRP < n ? out[e0 + k * GRP].x : 0u;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const uint32_t os = cv[k] >> 16;
+          if (e0 + k * GRP < n && os < olim) r[k] = *reinterpret_cast<const uint4 *>(src + (os ^ sub16));
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int e = e0 + k * GRP;
+          if (e >= n) break;
+          const uint32_t od = cv[k] & 0xffffu, os = cv[k] >> 16;
+          if (od < olim && os < olim) *reinterpret_cast<uint4 *>((e < n1 ? rowbuf(g + 1) : rowbuf(g + 2)) + (od ^ sub16)) = r[k];
+          else raise_error(a.err, SDM_DEVERR_PLAN);
+        }
+      }
+    };
+
+    if constexpr (kLoaderHandOn) {
+      // Iteration g: wait until the compute warps are done with stage g-1, copy its
+      // hand-on rows into buffers g and g+1, wait for stage g's bank rows and arrive on
+      // full[g] (stage g is then complete); write stage g-1's dirty rows back; fetch the
+      // row lists of stage g+3 and the rows of stage g+2 into buffer g-1.
+      // Group order: A(g) = row lists of stage g+3, R(g) = stage g+2's rows.
+      for (int g = 0; g < 3 && g < S; ++g) fetch_lrec(g);
+      cp_async_commit();
+      cp_async_wait_all();
+      loader_bar();
+      for (int g = 0; g < 2; ++g) {
+        if (g < S) {
+          fetch_rows(g);
+          fetch_stage_data(g);
+        }
+        cp_async_commit();                                       // R(-2), R(-1)
+      }
+      bool alive = true;
+      for (int g = 0; g < S; ++g) {
+        if (g + 3 < S) fetch_lrec(g + 3);
+        cp_async_commit();                                       // A(g)
+        if (g >= 1) {
+          alive = wait_done(g - 1);
+          if (!alive) break;
+          hand_on_rows(g - 1);
+          cp_async_wait_pending<3>();                            // R(g-2): stage g's rows
+        } else {
+          cp_async_wait_pending<2>();                            // R(-2): stage 0's rows
+        }
+        loader_bar();                                            // carries and rows of stage g in place
+        if (lt == 0) mbar_arrive(&full[g % kRowBufs]);
+        if (g >= 1) write_back(g - 1);
+        cp_async_wait_pending<2>();                              // A(g-1): row lists of stage g+2
+        loader_bar();                                            // buffer g-1 read; lists visible
+        if (g + 2 < S) {
+          fetch_rows(g + 2);
+          fetch_stage_data(g + 2);
+        }
+        cp_async_commit();                                       // R(g)
+      }
+      if (alive && wait_done(S - 1)) write_back(S - 1);
+      cp_async_wait_all();
+    } else {
     // prologue: row lists 0..2, then the bank rows of stages 0 and 1
     for (int g = 0; g < 3 && g < S; ++g) fetch_lrec(g);
     cp_async_commit();
@@ -314,6 +392,7 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
     }
     if (alive && wait_done(S - 1)) write_back(S - 1);
     cp_async_wait_all();
+    }
     return;
   }
 
@@ -424,7 +503,7 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
   };
   for (int g = 0; g < S; ++g) {
     if (!wait_bar(full, g)) return;
-    const Handoff hf = handoff_of(g);
+    const Handoff hf = kLoaderHandOn ? Handoff{} : handoff_of(g);
     const unsigned char *cr = crecbuf(g);
     const uint16_t *refmap = reinterpret_cast<const uint16_t *>(cr + lay.off_refmap);
     const uint8_t *tokflag = cr + lay.off_tokflag;
@@ -450,7 +529,7 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
     }
     // rows the next two stages take over: copy this warp's pieces out of buffer g (into
     // buffer g+2 only once the loaders have written back stage g-1 from it: recs(g))
-    if (g + 1 < S) {
+    if (!kLoaderHandOn && g + 1 < S) {
       if (!wait_bar(recs, g)) return;
       hand_on(g, hf);
     }
