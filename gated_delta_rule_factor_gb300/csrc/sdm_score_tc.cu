@@ -137,15 +137,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// One warp per segment (a query's factor slice, or a sub-key row): the largest magnitude
-// m gives e with m in [2^e, 2^(e+1)) (e = 0 for an all-zero segment); each value scaled by
-// 2^(7-e) lies in [-256, 256] and is cut into its nearest integer n0 and three further
-// 8-bit integer digits of the remainders, each step exact in float32.
+// 2^k as a float32 for -126 <= k <= 127 (exact), else 0.
+__device__ __forceinline__ float pow2f(int k) {
+  return (k >= -126 && k <= 127) ? __uint_as_float((uint32_t)(k + 127) << 23) : 0.0f;
+}
+
+// x * 2^k, exact whenever the result is a normal float32.
+__device__ __forceinline__ float scale2(float x, int k) {
+  const float p = pow2f(k);
+  return p != 0.0f ? x * p : ldexpf(x, k);
+}
+
+// Eight lanes per segment (a query's factor slice, or a sub-key row), eight consecutive
+// values per lane and 64-wide column block: the largest magnitude m gives e with m in
+// [2^e, 2^(e+1)) (e = 0 for an all-zero segment); each value scaled by 2^(7-e) lies in
+// [-256, 256] and is cut into its nearest integer n0 and three further 8-bit integer
+// digits of the remainders, each step exact in float32; every slice is stored as eight
+// bfloat16 (16 bytes).
 __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ SplitArgs a) {
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, sub8 = lane & 7;
+  const unsigned gmask = 0xffu << (lane & 24);
   const int64_t qrows = 2 * a.BT * a.HF, total = qrows + a.krows;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < total; row += nwarps) {
+  const int64_t ngroups = ((int64_t)gridDim.x * blockDim.x) >> 3;
+  const bool vec = (a.d_sub & 7) == 0;
+  for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3; row < total; row += ngroups) {
     const float *src;
     __nv_bfloat16 *dst;
     int32_t *ex;
@@ -160,25 +175,50 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
       dst = a.ks + kr * kSplitParts * a.dp;
       ex = a.kexp + kr;
     }
-    float m = 0.0f;
-    for (int d = lane; d < a.d_sub; d += 32) m = fmaxf(m, fabsf(src[d]));
+    auto load8 = [&](int d0, float (&v)[8]) {
+      if (vec && d0 < a.d_sub) {
+        const float4 lo = *reinterpret_cast<const float4 *>(src + d0);
+        const float4 hi = *reinterpret_cast<const float4 *>(src + d0 + 4);
+        v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
+        v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+      } else {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        for (int j = 0; j < 8; ++j) v[j] = d0 + j < a.d_sub ? src[d0 + j] : 0.0f;
+      }
+    };
+    float m = 0.0f;
+    for (int d0 = 8 * sub8; d0 < a.d_sub; d0 += 64) {
+      float v[8];
+      load8(d0, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, o));
     int e = 0;
     if (m > 0.0f) {
       int E;
       frexpf(m, &E);                       // m = f 2^E, f in [0.5, 1)
       e = E - 1;
     }
-    if (lane == 0) *ex = e;
-    for (int d = lane; d < a.dp; d += 32) {
-      float r = d < a.d_sub ? ldexpf(src[d], 7 - e) : 0.0f;
+    if (sub8 == 0) *ex = e;
+    for (int d0 = 8 * sub8; d0 < a.dp; d0 += 64) {
+      float v[8];
+      load8(d0, v);
+      __align__(16) __nv_bfloat16 p[kSplitParts][8];
 #pragma unroll
-      for (int p = 0; p < kSplitParts; ++p) {
-        const float n = rintf(r);
-        dst[p * a.dp + d] = __float2bfloat16_rn(n);
-        r = (r - n) * 256.0f;
+      for (int j = 0; j < 8; ++j) {
+        float r = scale2(v[j], 7 - e);
+#pragma unroll
+        for (int q = 0; q < kSplitParts; ++q) {
+          const float n = rintf(r);
+          p[q][j] = __float2bfloat16_rn(n);
+          r = (r - n) * 256.0f;
+        }
       }
+#pragma unroll
+      for (int q = 0; q < kSplitParts; ++q)
+        *reinterpret_cast<uint4 *>(dst + q * a.dp + d0) = *reinterpret_cast<const uint4 *>(p[q]);
     }
   }
 }
@@ -307,20 +347,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
       float v[32];
       tmem_ld32(lane_base + (uint32_t)c0, v);
       if (PARTS == kSplitParts) {
-        // join the exact level sums: sum_L acc_L 2^(8 (3 - L)), one rounding, then 2^(e_q + e_k - 38)
+        // join the exact level sums X = sum_L acc_L 2^(8 (3 - L)) as a 64-bit integer (each
+        // acc_L converted to 32 bits), then X = H 2^24 + Lo with H and Lo exact in float32,
+        // so one float32 addition rounds X correctly; then the exact scale 2^(e_q + e_k - 38)
         long long tot[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) tot[i] = __float2ll_rn(v[i]) << 24;
+        for (int i = 0; i < 32; ++i) tot[i] = (long long)__float2int_rn(v[i]) << 24;
 #pragma unroll
         for (int L = 1; L < 4; ++L) {
           tmem_ld32(lane_base + (uint32_t)(L * lvl_col + c0), v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) tot[i] += __float2ll_rn(v[i]) << (8 * (3 - L));
+          for (int i = 0; i < 32; ++i) tot[i] += (long long)__float2int_rn(v[i]) << (8 * (3 - L));
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int32_t e = c0 + i < nvalid ? ek[c0 + i] : 0;
-          v[i] = ldexpf(__ll2float_rn(tot[i]), eq + e - 38);
+          const float hi = (float)(int32_t)(tot[i] >> 24), lo = (float)(int32_t)(tot[i] & 0xffffff);
+          v[i] = scale2(__fmaf_rn(hi, 16777216.0f, lo), eq + e - 38);
         }
       }
       if (m < a.BT) {
@@ -428,7 +471,7 @@ cudaError_t launch_score_tc(const ScoreArgs &s, int act_dtype, cudaStream_t st) 
     sp.ks = sp.qs + qrows * kSplitParts * (int64_t)a.dp;
     sp.qexp = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(s.split) + split_slice_bytes(g, s.BT, s.H));
     sp.kexp = sp.qexp + qrows;
-    const int64_t blocks = std::min<int64_t>((qrows + sp.krows + 7) / 8, 16384);   // 8 warps a block
+    const int64_t blocks = std::min<int64_t>((qrows + sp.krows + 31) / 32, 16384);  // 32 segments a block
     split_kernel<<<(unsigned)blocks, 256, 0, st>>>(sp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
