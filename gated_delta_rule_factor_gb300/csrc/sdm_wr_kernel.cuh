@@ -471,25 +471,28 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
     }
     *reinterpret_cast<uint4 *>(to + od) = *reinterpret_cast<const uint4 *>(from + os);
   };
+  // Entries a compute lane copies together: 1 where the launch caps registers at 128 (512
+  // threads per SM), where the batch's registers measured as spills in the token step.
+  constexpr int HB = Geo::NTHR * (LW == 4 ? 2 : 1) >= 512 ? 1 : kBatch;
   auto hand_on = [&](int g, const Handoff &hf) {
     const unsigned char *rows = rowbuf(g);
     const uint2 *out = reinterpret_cast<const uint2 *>(lrecbuf(g) + lay.off_out);
     const int n = hf.n1 + hf.n2;
     for (int e = rg, k = 0; e < n && k < 2; e += 16, ++k)
       copy_piece(hf.e[k], e < hf.n1 ? rowbuf(g + 1) : rowbuf(g + 2), rows);
-    // the rest kBatch entries at a time: offsets, then the pieces, then the stores
-    for (int e0 = rg + 32; e0 < n; e0 += kBatch * 16) {
-      uint32_t cv[kBatch];
-      uint4 r[kBatch];
+    // the rest HB entries at a time: offsets, then the pieces, then the stores
+    for (int e0 = rg + 32; e0 < n; e0 += HB * 16) {
+      uint32_t cv[HB];
+      uint4 r[HB];
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) cv[k] = e0 + 16 * k < n ? out[e0 + 16 * k].x : 0u;
+      for (int k = 0; k < HB; ++k) cv[k] = e0 + 16 * k < n ? out[e0 + 16 * k].x : 0u;
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
+      for (int k = 0; k < HB; ++k) {
         const uint32_t os = (cv[k] >> 16) ^ wc;
         if (e0 + 16 * k < n && os < (uint32_t)row_limit) r[k] = *reinterpret_cast<const uint4 *>(rows + os);
       }
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
+      for (int k = 0; k < HB; ++k) {
         const int e = e0 + 16 * k;
         if (e >= n) break;
         const uint32_t od = (cv[k] & 0xffffu) ^ wc, os = (cv[k] >> 16) ^ wc;
