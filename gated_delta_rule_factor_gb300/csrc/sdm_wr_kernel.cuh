@@ -277,18 +277,19 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
       return *loader_go != 0;
     };
 
-    // Loader hand-on (kLoaderHandOn): stage g's rows that stages g+1 and g+2 take over,
-    // copied out of buffer g once the compute warps are done with it, kBatch list
-    // entries per thread at a time, each thread one 16-byte chunk of a row slice.
-    auto hand_on_rows = [&](int g) {
+    // Loader hand-on (kLoaderHandOn): stage g's rows that stage g+1 (second == false) or
+    // stage g+2 (second == true) takes over, copied out of buffer g once the compute warps
+    // are done with it, kBatch list entries per thread at a time, each thread one 16-byte
+    // chunk of a row slice.
+    auto hand_on_rows = [&](int g, bool second) {
       const unsigned char *rec = lrecbuf(g);
       const int32_t *hdr = reinterpret_cast<const int32_t *>(rec);
       if (!hdr_ok(hdr)) return;
-      const int n1 = hdr[2], n = hdr[2] + hdr[3];
+      const int n1 = hdr[2], n = second ? hdr[2] + hdr[3] : hdr[2];
       const uint2 *out = reinterpret_cast<const uint2 *>(rec + lay.off_out);
       const unsigned char *src = rowbuf(g);
       if (sub >= valid_chunks) return;
-      for (int e0 = grp; e0 < n; e0 += kBatch * GRP) {
+      for (int e0 = (second ? n1 : 0) + grp; e0 < n; e0 += kBatch * GRP) {
         uint32_t cv[kBatch];
         uint4 r[kBatch];
 #pragma unroll
@@ -310,10 +311,11 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
     };
 
     if constexpr (kLoaderHandOn) {
-      // Iteration g: wait until the compute warps are done with stage g-1, copy its
-      // hand-on rows into buffers g and g+1, wait for stage g's bank rows and arrive on
-      // full[g] (stage g is then complete); write stage g-1's dirty rows back; fetch the
-      // row lists of stage g+3 and the rows of stage g+2 into buffer g-1.
+      // Iteration g: wait until the compute warps are done with stage g-1, copy the rows
+      // stage g takes over from it, wait for stage g's bank rows and arrive on full[g]
+      // (stage g is then complete); then copy the rows stage g+1 takes over from stage g-1
+      // (before full[g+1], in the next iteration), write stage g-1's dirty rows back, and
+      // fetch the row lists of stage g+3 and the rows of stage g+2 into buffer g-1.
       // Group order: A(g) = row lists of stage g+3, R(g) = stage g+2's rows.
       for (int g = 0; g < 3 && g < S; ++g) fetch_lrec(g);
       cp_async_commit();
@@ -333,14 +335,17 @@ __global__ void __launch_bounds__(WrGeometry<NCW, LW>::NTHR, LW == 4 ? 2 : 1)
         if (g >= 1) {
           alive = wait_done(g - 1);
           if (!alive) break;
-          hand_on_rows(g - 1);
+          hand_on_rows(g - 1, false);
           cp_async_wait_pending<3>();                            // R(g-2): stage g's rows
         } else {
           cp_async_wait_pending<2>();                            // R(-2): stage 0's rows
         }
         loader_bar();                                            // carries and rows of stage g in place
         if (lt == 0) mbar_arrive(&full[g % kRowBufs]);
-        if (g >= 1) write_back(g - 1);
+        if (g >= 1) {
+          hand_on_rows(g - 1, true);
+          write_back(g - 1);
+        }
         cp_async_wait_pending<2>();                              // A(g-1): row lists of stage g+2
         loader_bar();                                            // buffer g-1 read; lists visible
         if (g + 2 < S) {
