@@ -1,9 +1,11 @@
-"""Host-side tests of the training pair and the layer entry that need no GPU.
+"""Host-side tests of the training pair, the layer entry and the factor-score hook that
+need no GPU.
 
-Every refusal of sdm_write_read_train, sdm_write_read_backward and sdm_layer_forward is
-decided on the host before any CUDA call or launch, so these calls pass fake (never
-dereferenced) device addresses, as in test_abi_cpu.py.  Also checked: the snapshot size
-follows the documented layout, and the workspace sizes depend only on the shape.
+Every refusal of sdm_write_read_train, sdm_write_read_backward, sdm_layer_forward and
+sdm_test_factor_scores is decided on the host before any CUDA call or launch, so these
+calls pass fake (never dereferenced) device addresses, as in test_abi_cpu.py.  Also
+checked: the snapshot size follows the documented layout, the workspace sizes depend only
+on the shape, and a float32 shape's workspace holds the scorer's split of the queries.
 """
 
 import ctypes
@@ -143,4 +145,38 @@ def test_layer_refusals_enqueue_nothing(lib, over, status):
     before = lib.sdm_launch_count()
     dim = over.pop("dim", 96)
     assert call_layer(lib, shape(), dim=dim, **over) == status, lib.sdm_last_error_message()
+    assert lib.sdm_launch_count() == before
+
+
+def call_scores(lib, sh, **over):
+    p = dict(q_w=fake(1), q_r=fake(2), subkeys=fake(5), scores=fake(9), ws=fake(8), ws_bytes=ws_size(lib, sh)[1])
+    p.update(over)
+    return lib.sdm_test_factor_scores(ctypes.byref(sh), p["q_w"], p["q_r"], p["subkeys"], p["scores"], p["ws"],
+                                      p["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("act", [_abi.SDM_F32, _abi.SDM_BF16])
+def test_float32_workspace_holds_the_score_split(lib, act):
+    # float32 queries are split into four bfloat16 slices for the tensor cores (plus one
+    # exponent per segment) inside the op's workspace; bfloat16 queries need no split
+    sh = shape(act_dtype=act, d_sub=40)
+    n_f32 = ws_size(lib, shape(act_dtype=_abi.SDM_F32, d_sub=40))[1]
+    n_bf16 = ws_size(lib, shape(act_dtype=_abi.SDM_BF16, d_sub=40))[1]
+    segments = 2 * sh.B * sh.T * sh.H * 2 + sh.H * 32        # query factor slices + sub-key rows
+    assert n_f32 - n_bf16 >= segments * (4 * 64 * 2 + 4)      # d_sub 40 padded to 64
+    assert ws_size(lib, sh)[0] == _abi.SDM_OK
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q_w=None), _abi.SDM_ERR_INVALID_ARG),
+    (dict(scores=None), _abi.SDM_ERR_INVALID_ARG),
+    (dict(subkeys=fake(5) + 8), _abi.SDM_ERR_INVALID_ARG),         # misaligned
+    (dict(ws_bytes=1024), _abi.SDM_ERR_WORKSPACE),
+    (dict(ws=None), _abi.SDM_ERR_WORKSPACE),
+    (dict(scores=fake(1)), _abi.SDM_ERR_ALIAS),                    # scores over q_w
+    (dict(ws=fake(9)), _abi.SDM_ERR_ALIAS),                        # workspace over scores
+])
+def test_factor_score_hook_refusals_enqueue_nothing(lib, over, status):
+    before = lib.sdm_launch_count()
+    assert call_scores(lib, shape(), **over) == status, lib.sdm_last_error_message()
     assert lib.sdm_launch_count() == before
