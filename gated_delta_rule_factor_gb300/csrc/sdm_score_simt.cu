@@ -1,4 +1,7 @@
-// Product-key factor scores on CUDA cores (any activation type and sub-key width).
+// Product-key factor scores on CUDA cores (any activation type and sub-key width): the
+// op's scorer where the tensor-core one does not apply (a factor width that is not a
+// multiple of 16, bfloat16 queries whose d_sub is not a multiple of 64), and on request of
+// the test hook that compares the two.
 //
 // s_f[a] = <q[f*d_sub:(f+1)*d_sub], K_f[a]> for both queries of every token and head
 // (product-key memory, Lample et al., cited in the sparse-delta-memory README).  One CTA

@@ -30,9 +30,11 @@
 // (carry 2, rows g+1 does not hold) needs into their buffers, arrive on done.  The
 // bank is never read stale: a row one of the two previous stages holds is carried in
 // shared memory, and any older row was written back before the fetch.  No memory round
-// trip lies between one stage's end and the next stage's start.  Every wait is bounded
-// (2 s of %globaltimer); a wait that runs out records SDM_DEVERR_TIMEOUT and sets a
-// shared abort flag that every other wait also watches.
+// trip lies between one stage's end and the next stage's start.  With one compute warp
+// per CTA the loaders make the carries instead (kLoaderHandOn): after done[g-1] they copy
+// the rows stage g takes over, arrive on full[g], then copy those stage g+1 takes over.
+// Every wait is bounded (2 s of %globaltimer); a wait that runs out records
+// SDM_DEVERR_TIMEOUT and sets a shared abort flag that every other wait also watches.
 #pragma once
 
 #include "sdm_common.cuh"
